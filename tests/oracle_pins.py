@@ -1,0 +1,479 @@
+"""Pins of the CPU oracle to facts other than itself.
+
+Each ``pin_*`` function takes a loaded oracle library and raises
+``AssertionError`` when the oracle disagrees with:
+  * a hand-worked example (tests/golden/*.json, each with its derivation),
+  * a library routine the method reduces to in a special case
+    (cp = 1: the dense KV is ``torch.cat`` of ``index_select`` per request),
+  * brute force on small inputs (inverting a map by enumeration, counting
+    writers, tiling q tokens),
+  * closed forms (exclusive cumsum, ``np.repeat``).
+They are shared by tests/test_oracle_pins.py (the real oracle) and
+tests/test_oracle_mutants.py (copies of the oracle with a planted mistake,
+each of which must fail at least one pin).
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _load_golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _labelled_pool(cp, slab_pages, ps, R):
+    """Pool whose every row is distinct and decodable: bytes 0..5 hold
+    (owner, local page, offset) and the rest is a fixed pattern."""
+    slabs = []
+    for o in range(cp):
+        s = np.zeros((slab_pages, ps, R), np.uint8)
+        for p in range(slab_pages):
+            for r in range(ps):
+                s[p, r, 0] = 1  # tag: pool row
+                s[p, r, 1] = o
+                s[p, r, 2:4] = np.frombuffer(np.uint16(p).tobytes(), np.uint8)
+                s[p, r, 4] = r
+                s[p, r, 5:] = (o * 31 + p * 7 + r * 3) % 251
+        slabs.append(s)
+    return slabs
+
+
+def _labelled_rows(T, R):
+    rows = np.zeros((T, R), np.uint8)
+    for t in range(T):
+        rows[t, 0] = 2  # tag: current row
+        rows[t, 1:3] = np.frombuffer(np.uint16(t).tobytes(), np.uint8)
+        rows[t, 3:] = (t * 13 + 5) % 253
+    return rows
+
+
+def _label_row(kind_row, slabs, rows):
+    kind = kind_row[0]
+    if kind == "pool":
+        return slabs[kind_row[1]][kind_row[2], kind_row[3]]
+    if kind == "cur":
+        return rows[kind_row[1]]
+    return np.zeros(rows.shape[1] if rows.size else slabs[0].shape[-1], np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# golden, hand-worked
+# ---------------------------------------------------------------------------
+
+def pin_golden_compose(lib):
+    g = _load_golden("compose_worked_example.json")
+    inp, exp = g["input"], g["expected"]
+    ps, cp, P, cap = inp["page_size"], inp["cp_size"], inp["num_pool_pages"], inp["dense_cap"]
+    plan = oracle.compose_plan(inp["prefix_lens"], inp["cur_lens"], inp["prefix_pages"], inp["cur_pages"],
+                               inp["writer"], page_size=ps, cp_size=cp, num_pool_pages=P, dense_cap=cap, lib=lib)
+    assert plan["status"] == 0
+    assert (plan["T"], plan["C"], plan["D"]) == (exp["T"], exp["C"], exp["D"])
+    for k in ("prefix_spans", "cur_spans", "owner", "src", "mixed_locs", "staging_rows", "token_writer_row"):
+        assert plan[k].tolist() == exp[k], k
+    pi = np.full(P, -1, np.int32)
+    for k, v in exp["page_inverse_nonneg"].items():
+        pi[int(k)] = v
+    spi = np.zeros(P, np.int32)
+    for k, v in exp["staging_page_inverse_nonzero"].items():
+        spi[int(k)] = v
+    assert np.array_equal(plan["page_inverse"], pi)
+    assert np.array_equal(plan["staging_page_inverse"], spi)
+
+    R = 16
+    slab_pages = -(-P // cp)
+    slabs = _labelled_pool(cp, slab_pages, ps, R)
+    rows = _labelled_rows(exp["T"], R)
+    dense = oracle.compose_dense(inp["prefix_lens"], inp["cur_lens"], inp["prefix_pages"], slabs, rows,
+                                 page_size=ps, cp_size=cp, dense_cap=cap, lib=lib)
+    want = np.stack([_label_row(x, slabs, rows) for x in exp["dense_rows"]])
+    assert np.array_equal(dense, want)
+
+    # staging: defined pages only; everything else keeps its guard byte
+    stg = [np.full(((exp["C"] + 1) * ps, R), 0xA5, np.uint8) for _ in range(cp)]
+    oracle.staging(inp["cur_lens"], inp["writer"], rows, stg, page_size=ps, cp_size=cp, lib=lib)
+    defined = set()
+    for w, pages in exp["staging_defined"].items():
+        for p, prow in pages.items():
+            got = stg[int(w)][int(p) * ps:(int(p) + 1) * ps]
+            assert np.array_equal(got, np.stack([_label_row(x, slabs, rows) for x in prow]))
+            defined.add((int(w), int(p)))
+    for w in range(cp):
+        for p in range(exp["C"] + 1):
+            if (w, p) not in defined:
+                assert np.all(stg[w][p * ps:(p + 1) * ps] == 0xA5), (w, p)
+
+    # gather through the plan's descriptors reproduces the dense rows
+    table = slabs + [s.reshape(-1, ps, R) for s in stg]
+    caps = [slab_pages] * cp + [exp["C"] + 1] * cp
+    g_dense, st = oracle.gather([t.reshape(-1) for t in table], caps, plan["owner"], plan["src"],
+                                page_size=ps, row_bytes=R, dense_cap=cap, lib=lib)
+    assert st == 0
+    assert np.array_equal(g_dense, want)
+
+
+def pin_golden_ragged(lib):
+    g = _load_golden("ragged_worked_example.json")
+    inp = g["input"]
+    for case in g["cases"]:
+        got = oracle.ragged_plan(inp["prefix_lens"], inp["q_lens"], case["cp_index"], chunk=inp["chunk"],
+                                 k_align=case["k_align"], lib=lib)
+        exp = case["expected"]
+        assert got["status"] == 0
+        assert (got["S"], got["Q"]) == (exp["S"], exp["Q"]), case["cp_index"]
+        for k in ("seg_req", "q_starts", "q_lens", "kv_lens", "k_bases", "current_bases", "q_bases",
+                  "topk_offsets"):
+            assert got[k].tolist() == exp[k], (k, case["cp_index"], case["k_align"])
+
+
+# ---------------------------------------------------------------------------
+# brute force and library reductions on seeded batches
+# ---------------------------------------------------------------------------
+
+def _dense_page_sequence(batch):
+    """(kind, logical page, current index) of every dense page, by enumeration
+    of each request's page table: prefix pages, then current pages."""
+    seq = []
+    pp = 0
+    i = 0
+    ps = batch.page_size
+    for b in range(batch.B):
+        npp = int(batch.prefix_lens[b]) // ps
+        ncp = -(-int(batch.cur_lens[b]) // ps)
+        for k in range(npp):
+            seq.append(("p", int(batch.prefix_pages[pp + k]), -1))
+        for k in range(ncp):
+            seq.append(("c", int(batch.cur_pages[i + k]), i + k))
+        pp += npp
+        i += ncp
+    return seq
+
+
+def pin_plan_brute_force(lib, batch, dense_extra=0):
+    ps, cp, P = batch.page_size, batch.cp_size, batch.num_pool_pages
+    seq = _dense_page_sequence(batch)
+    D = len(seq)
+    cap = D + dense_extra
+    plan = oracle.compose_plan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages,
+                               batch.writer, page_size=ps, cp_size=cp, num_pool_pages=P, dense_cap=cap, lib=lib)
+    assert plan["status"] == 0
+    assert plan["D"] == D and plan["C"] == batch.C and plan["T"] == batch.T
+
+    # page_inverse: inverse of the dense-slot -> logical-page map (smallest slot)
+    want_pi = np.full(P, -1, np.int32)
+    for d in range(D - 1, -1, -1):
+        want_pi[seq[d][1]] = d
+    assert np.array_equal(plan["page_inverse"], want_pi)
+    for d, (_, lp, _) in enumerate(seq):
+        assert seq[plan["page_inverse"][lp]][1] == lp
+
+    # staging inverse: current page i -> i + 1 (row 0 reserved)
+    want_spi = np.zeros(P, np.int32)
+    for kind, lp, i in seq:
+        if kind == "c":
+            want_spi[lp] = i + 1
+    assert np.array_equal(plan["staging_page_inverse"], want_spi)
+
+    # descriptors: modulo owner for prefix, cp + writer / staging slot for current
+    for d, (kind, lp, i) in enumerate(seq):
+        if kind == "p":
+            assert (plan["owner"][d], plan["src"][d]) == (lp % cp, lp // cp), d
+        else:
+            assert (plan["owner"][d], plan["src"][d]) == (cp + int(batch.writer[i]), i + 1), d
+    assert np.all(plan["owner"][D:] == -1) and np.all(plan["src"][D:] == 0)
+
+    # spans tile the dense slots in request order
+    nxt = 0
+    for b in range(batch.B):
+        ds, npp = plan["prefix_spans"][b]
+        cs, ncp = plan["cur_spans"][b]
+        assert ds == nxt and cs == ds + npp
+        assert npp == batch.prefix_lens[b] // ps and ncp == -(-batch.cur_lens[b] // ps)
+        assert all(seq[d][0] == "p" for d in range(ds, ds + npp))
+        assert all(seq[d][0] == "c" for d in range(cs, cs + ncp))
+        nxt = cs + ncp
+    assert nxt == D
+
+    # per-token locations agree with the inverses (the pages' fill derives its
+    # destinations from the page inverse)
+    cur_lp = np.repeat(np.asarray(batch.cur_pages, np.int64), ps)
+    offs = np.tile(np.arange(ps, dtype=np.int64), batch.C)
+    keep = []
+    for b in range(batch.B):
+        ncp = -(-int(batch.cur_lens[b]) // ps)
+        m = np.zeros(ncp * ps, bool)
+        m[:int(batch.cur_lens[b])] = True
+        keep.append(m)
+    keep = np.concatenate(keep) if keep else np.zeros(0, bool)
+    cur_lp, offs = cur_lp[keep], offs[keep]
+    assert np.array_equal(plan["mixed_locs"], plan["page_inverse"][cur_lp].astype(np.int64) * ps + offs)
+    assert np.array_equal(plan["staging_rows"], plan["staging_page_inverse"][cur_lp].astype(np.int64) * ps + offs)
+
+    # token_writer_row: each writer's tokens, in batch order, are rows 0..T_w-1
+    tw = wl.token_writer(batch)
+    for w in range(cp):
+        assert np.array_equal(plan["token_writer_row"][tw == w], np.arange(int((tw == w).sum())))
+
+    # every current page has exactly one writer, and it is in range
+    assert np.all((batch.writer >= 0) & (batch.writer < cp))
+    return plan
+
+
+def pin_dense_token_level(lib, batch, dense_extra=0):
+    """Dense KV from logical token locations (lp * ps + off), vectorised with
+    numpy fancy indexing, must equal the oracle's row walk."""
+    ps, cp, R = batch.page_size, batch.cp_size, batch.row_bytes
+    slabs = wl.host_pool(batch)
+    rows = wl.host_current_rows(batch)
+    flat = np.concatenate([s.reshape(-1, R) for s in slabs])  # owner-major flat pool
+    slab_rows = slabs[0].shape[0] * ps
+    D = len(_dense_page_sequence(batch))
+    cap = D + dense_extra
+    want = np.zeros((cap * ps, R), np.uint8)
+    row, pp, tok = 0, 0, 0
+    for b in range(batch.B):
+        npp = int(batch.prefix_lens[b]) // ps
+        locs = np.repeat(np.asarray(batch.prefix_pages[pp:pp + npp], np.int64), ps) * ps + np.tile(np.arange(ps), npp)
+        lp, off = locs // ps, locs % ps
+        want[row:row + len(locs)] = flat[(lp % cp) * slab_rows + (lp // cp) * ps + off]
+        row += len(locs)
+        n = int(batch.cur_lens[b])
+        want[row:row + n] = rows[tok:tok + n]
+        row += -(-n // ps) * ps
+        pp += npp
+        tok += n
+    got = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                               page_size=ps, cp_size=cp, dense_cap=cap, lib=lib)
+    assert np.array_equal(got, want)
+    return got, slabs, rows
+
+
+def pin_cp1_index_select_cat(lib, seed=7):
+    """cp = 1: the whole pool is one slab and the dense KV of a request is
+    ``cat(pool_rows.index_select(prefix rows), current rows, zeros)``."""
+    rng = np.random.default_rng(seed)
+    ps, R = 8, 32
+    pfx = (rng.integers(0, 40, size=5) // ps) * ps
+    cur = rng.integers(0, 30, size=5)
+    batch = wl.make_compose_batch("cp1", seed, page_size=ps, cp_size=1, num_pool_pages=64, row_bytes=R,
+                                  prefix_lens=pfx, cur_lens=cur, row_kind="bytes")
+    slabs = wl.host_pool(batch)
+    rows = wl.host_current_rows(batch)
+    pool = torch.from_numpy(slabs[0].reshape(-1, R))
+    parts = []
+    pp, tok = 0, 0
+    for b in range(batch.B):
+        npp = int(pfx[b]) // ps
+        pages = torch.from_numpy(np.asarray(batch.prefix_pages[pp:pp + npp], np.int64))
+        idx = (pages[:, None] * ps + torch.arange(ps)[None, :]).reshape(-1)
+        n = int(cur[b])
+        pad = (-n) % ps
+        parts += [pool.index_select(0, idx), torch.from_numpy(rows[tok:tok + n]), torch.zeros(pad, R, dtype=torch.uint8)]
+        pp += npp
+        tok += n
+    want = torch.cat(parts).numpy()
+    got = oracle.compose_dense(pfx, cur, batch.prefix_pages, slabs, rows, page_size=ps, cp_size=1, lib=lib)
+    assert np.array_equal(got, want)
+
+
+def pin_staging_gather_roundtrip(lib, batch, dense_extra=0):
+    """Plan + staging + descriptor gather reproduces the plain dense KV, and
+    the current slots of the dense KV give back every current row."""
+    ps, cp, R = batch.page_size, batch.cp_size, batch.row_bytes
+    plan = oracle.compose_plan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages,
+                               batch.writer, page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages,
+                               dense_cap=None, lib=lib)
+    cap = plan["D"] + dense_extra
+    plan = oracle.compose_plan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages,
+                               batch.writer, page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages,
+                               dense_cap=cap, lib=lib)
+    slabs = wl.host_pool(batch)
+    rows = wl.host_current_rows(batch)
+    stg = [np.full(((batch.C + 1) * ps, R), 0x5A, np.uint8) for _ in range(cp)]
+    oracle.staging(batch.cur_lens, batch.writer, rows, stg, page_size=ps, cp_size=cp, lib=lib)
+    # page 0 of every staging is reserved and never written
+    for s in stg:
+        assert np.all(s[:ps] == 0x5A)
+    table = [s.reshape(-1) for s in slabs] + [s.reshape(-1) for s in stg]
+    caps = [batch.slab_pages] * cp + [batch.C + 1] * cp
+    dense_g, st = oracle.gather(table, caps, plan["owner"], plan["src"], page_size=ps, row_bytes=R,
+                                dense_cap=cap, lib=lib)
+    assert st == 0
+    dense = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                 page_size=ps, cp_size=cp, dense_cap=cap, lib=lib)
+    assert np.array_equal(dense_g, dense)
+    assert np.array_equal(dense[plan["mixed_locs"]], rows)
+    # the staging rows written by the fill are the current rows, writer by writer
+    tw = wl.token_writer(batch)
+    for t in range(0, batch.T, max(1, batch.T // 64)):
+        assert np.array_equal(stg[tw[t]][plan["staging_rows"][t]], rows[t])
+
+
+def pin_gather_sentinel_and_oob(lib):
+    rng = np.random.default_rng(3)
+    ps, R = 4, 16
+    table = [np.frombuffer(rng.bytes(5 * ps * R), np.uint8).copy() for _ in range(3)]
+    caps = [5, 5, 5]
+    owner = np.array([0, -1, 2, 1, 3, 1, -2], np.int32)
+    src = np.array([4, 9, 0, 5, 0, 2, 0], np.int32)
+    dense, st = oracle.gather(table, caps, owner, src, page_size=ps, row_bytes=R, dense_cap=7, lib=lib)
+    pb = ps * R
+    d = dense.reshape(7, pb)
+    assert np.array_equal(d[0], table[0][4 * pb:5 * pb])
+    assert np.all(d[1] == 0)  # owner -1 zero-fills
+    assert np.array_equal(d[2], table[2][0:pb])
+    assert np.all(d[3] == 0)  # src beyond capacity
+    assert np.all(d[4] == 0)  # owner beyond the table
+    assert np.array_equal(d[5], table[1][2 * pb:3 * pb])
+    assert np.all(d[6] == 0)
+    assert st == oracle.DESC_OOB
+
+
+def pin_ragged_closed_forms(lib, rb, ranks=None):
+    """q_bases is the exclusive cumsum of q_lens; topk offsets are
+    ``np.repeat(k_bases, q_lens)``; kv_lens / current_bases follow from the
+    request; the ranks' segments tile every request's q tokens once."""
+    B = rb.B
+    pfx = rb.prefix_lens.astype(np.int64)
+    q = rb.q_lens.astype(np.int64)
+    kv_aligned = -(-(pfx + q) // rb.k_align) * rb.k_align
+    kbase_req = np.concatenate([[0], np.cumsum(kv_aligned)[:-1]]) if B else np.zeros(0, np.int64)
+    cover = [np.zeros(int(n), np.int32) for n in q]
+    total_Q = 0
+    ranks = range(rb.cp_size) if ranks is None else ranks
+    for r in ranks:
+        ci = rb.cp_index(r)
+        got = oracle.ragged_plan(rb.prefix_lens, rb.q_lens, ci, chunk=rb.chunk, k_align=rb.k_align, lib=lib)
+        assert got["status"] == 0
+        S, Q = got["S"], got["Q"]
+        ql = got["q_lens"].astype(np.int64)
+        assert np.array_equal(got["q_bases"], np.concatenate([[0], np.cumsum(ql)[:-1]]).astype(np.int32)[:S])
+        assert np.array_equal(got["topk_offsets"], np.repeat(got["k_bases"], got["q_lens"]))
+        assert Q == int(ql.sum())
+        req = got["seg_req"]
+        assert np.array_equal(got["k_bases"], kbase_req[req])
+        assert np.array_equal(got["current_bases"], kbase_req[req] + pfx[req])
+        assert np.array_equal(got["kv_lens"], pfx[req] + got["q_starts"] + got["q_lens"])
+        for s in range(S):
+            b = int(req[s])
+            cover[b][got["q_starts"][s]:got["q_starts"][s] + got["q_lens"][s]] += 1
+        # segments are maximal: two adjacent segments of one request do not abut
+        for s in range(1, S):
+            if req[s] == req[s - 1]:
+                assert got["q_starts"][s] > got["q_starts"][s - 1] + got["q_lens"][s - 1]
+        total_Q += Q
+    if ranks == range(rb.cp_size):
+        assert total_Q == int(q.sum())
+        for b in range(B):
+            assert np.all(cover[b] == 1), b
+
+
+def pin_ragged_cp1(lib, rb):
+    """cp = 1 owns every chunk: one segment per non-empty request, starting at
+    0 and ending at the request's full kv length."""
+    n = rb.num_chunks
+    got = oracle.ragged_plan(rb.prefix_lens, rb.q_lens, np.arange(n, dtype=np.int32), chunk=rb.chunk,
+                             k_align=rb.k_align, lib=lib)
+    nz = np.nonzero(rb.q_lens > 0)[0]
+    assert got["S"] == len(nz)
+    assert np.array_equal(got["seg_req"], nz)
+    assert np.all(got["q_starts"] == 0)
+    assert np.array_equal(got["q_lens"], rb.q_lens[nz])
+    assert np.array_equal(got["kv_lens"], rb.prefix_lens[nz] + rb.q_lens[nz])
+
+
+def pin_errors(lib):
+    # unaligned prefix -> error code, capacity -> error code
+    try:
+        oracle.compose_plan([3], [4], [1], [2], [0], page_size=2, cp_size=1, num_pool_pages=8, lib=lib)
+        raise AssertionError("unaligned prefix accepted")
+    except oracle.OracleError as e:
+        assert "-2" in str(e)
+    try:
+        oracle.compose_plan([2], [4], [1], [2, 3], [0, 0], page_size=2, cp_size=1, num_pool_pages=8,
+                            dense_cap=2, lib=lib)
+        raise AssertionError("capacity accepted")
+    except oracle.OracleError as e:
+        assert "-3" in str(e)
+    # data violations -> status bits
+    p = oracle.compose_plan([0, 0], [2, 2], [], [3, 3], [0, 1], page_size=2, cp_size=2, num_pool_pages=8, lib=lib)
+    assert p["status"] & oracle.DUP_CURRENT_PAGE
+    p = oracle.compose_plan([2], [2], [5], [5], [0], page_size=2, cp_size=1, num_pool_pages=8, lib=lib)
+    assert p["status"] & oracle.CURRENT_IN_PREFIX
+    p = oracle.compose_plan([2], [2], [0], [5], [0], page_size=2, cp_size=1, num_pool_pages=8, lib=lib)
+    assert p["status"] & oracle.PAGE_OOB
+    p = oracle.compose_plan([0], [2], [], [5], [3], page_size=2, cp_size=2, num_pool_pages=8, lib=lib)
+    assert p["status"] & oracle.WRITER_OOB
+    # shared prefix page across two requests is allowed; the inverse keeps the smaller slot
+    p = oracle.compose_plan([2, 2], [1, 1], [4, 4], [5, 6], [0, 0], page_size=2, cp_size=1, num_pool_pages=8, lib=lib)
+    assert p["status"] == 0 and p["page_inverse"][4] == 0
+    # ragged: unsorted cp_index -> status bit
+    r = oracle.ragged_plan([0, 0], [8, 8], [2, 1], chunk=4, lib=lib)
+    assert r["status"] & oracle.CHUNK_OOB
+
+
+# ---------------------------------------------------------------------------
+# edge-case batches
+# ---------------------------------------------------------------------------
+
+def edge_batches():
+    """Seeded small batches covering the degenerate cases of the method."""
+    out = [wl.tiny_batch()]
+    R = 64
+    mk = wl.make_compose_batch
+    out.append(mk("no_prefix", 11, page_size=4, cp_size=2, num_pool_pages=64, row_bytes=R,
+                  prefix_lens=[0, 0, 0], cur_lens=[5, 8, 1], row_kind="bytes"))
+    out.append(mk("no_current", 12, page_size=4, cp_size=3, num_pool_pages=64, row_bytes=R,
+                  prefix_lens=[8, 4, 0], cur_lens=[0, 0, 0], row_kind="bytes"))
+    out.append(mk("exact_multiple", 13, page_size=4, cp_size=2, num_pool_pages=64, row_bytes=R,
+                  prefix_lens=[4, 12], cur_lens=[8, 4], row_kind="bytes"))
+    out.append(mk("one_request", 14, page_size=8, cp_size=4, num_pool_pages=64, row_bytes=R,
+                  prefix_lens=[16], cur_lens=[21], row_kind="bytes"))
+    out.append(mk("cp1", 15, page_size=4, cp_size=1, num_pool_pages=64, row_bytes=R,
+                  prefix_lens=[8, 0, 4], cur_lens=[3, 9, 4], row_kind="bytes"))
+    out.append(mk("empty_batch", 16, page_size=4, cp_size=2, num_pool_pages=16, row_bytes=R,
+                  prefix_lens=[], cur_lens=[], row_kind="bytes"))
+    # shared radix prefix: both requests reuse logical pages 9 and 17
+    out.append(mk("shared_prefix", 17, page_size=4, cp_size=2, num_pool_pages=64, row_bytes=R,
+                  prefix_lens=[8, 12], cur_lens=[3, 6], prefix_pages=[9, 17, 9, 17, 30],
+                  cur_pages=[40, 41, 42], row_kind="bytes"))
+    # chunk-shaped request: 2048-token page-aligned carried prefix + 512 extend, beside a short one
+    out.append(mk("chunk_shaped", 18, page_size=64, cp_size=8, num_pool_pages=256, row_bytes=R,
+                  prefix_lens=[2048, 64], cur_lens=[512, 37], row_kind="bytes"))
+    # writers not round-robin: all current pages on one rank, others idle
+    out.append(mk("one_writer", 19, page_size=4, cp_size=4, num_pool_pages=64, row_bytes=R,
+                  prefix_lens=[4, 8], cur_lens=[7, 6], writer=[2, 2, 2, 2], row_kind="bytes"))
+    return out
+
+
+def ragged_edge_batches():
+    out = []
+    rng = np.random.default_rng(21)
+    for cp, chunk, B, k_align in ((2, 4, 5, 1), (3, 8, 7, 1), (4, 16, 9, 16), (8, 64, 12, 64), (1, 4, 4, 1)):
+        q = rng.integers(0, 5 * chunk, size=B).astype(np.int32)
+        pfx = rng.integers(0, 100, size=B).astype(np.int32)
+        out.append(wl.RaggedBatch(f"ragged_cp{cp}", 21, cp, chunk, k_align, pfx, q))
+    return out
+
+
+ALL_PINS = [
+    ("golden_compose", lambda lib: pin_golden_compose(lib)),
+    ("golden_ragged", lambda lib: pin_golden_ragged(lib)),
+    ("cp1_index_select_cat", lambda lib: pin_cp1_index_select_cat(lib)),
+    ("gather_sentinel", lambda lib: pin_gather_sentinel_and_oob(lib)),
+    ("errors", lambda lib: pin_errors(lib)),
+    ("plan_brute_force", lambda lib: [pin_plan_brute_force(lib, b, 2) for b in edge_batches()]),
+    ("dense_token_level", lambda lib: [pin_dense_token_level(lib, b, 1) for b in edge_batches()]),
+    ("roundtrip", lambda lib: [pin_staging_gather_roundtrip(lib, b, 1) for b in edge_batches()]),
+    ("ragged_closed_forms", lambda lib: [pin_ragged_closed_forms(lib, rb) for rb in ragged_edge_batches()]),
+    ("ragged_cp1", lambda lib: [pin_ragged_cp1(lib, rb) for rb in ragged_edge_batches()]),
+]
