@@ -1,0 +1,599 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV compose on one GB300 (or N independent replicas).
+
+One step = one pass of the whole hot path over one batch: the compose plan
+(once per batch), the ragged index plan of CP rank 0 (once per batch) and, for
+each of the 78 layers, the fill of current rows into the writers' stagings
+followed by the slot-dense page gather into that layer's dense buffer.
+
+Default workload: the traced prefill batch (bs=12, 44 600 current tokens,
+page_size 64, cp 8 emulated writer regions, MLA 576 x bf16 rows) over 78
+layers, each layer with its own pool slab of 4096 pages and its own current
+rows.  ``--config fp8_nsa`` runs the fp8 NSA layout (bs=32, 131 072 tokens,
+656-byte rows, one 2^20-page pool shared by the layers).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "compose GB/s and % of HBM peak; ms per 78-layer compose at bs=12/44.6K tokens"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# accounting
+# ---------------------------------------------------------------------------
+
+def layer_bytes(prefix_lens, cur_lens, page_size, row_bytes, dense_cap_pages):
+    """Algorithmic bytes of one layer's fill + gather.
+
+    fill:   read T rows, write T rows + the pad rows of each request's last page
+    gather: read every described page (prefix and current, D pages), write
+            every dense slot (dense_cap pages; slots past D are zero-filled)
+    """
+    pl = np.asarray(prefix_lens, np.int64)
+    cl = np.asarray(cur_lens, np.int64)
+    ps, R = page_size, row_bytes
+    T = int(cl.sum())
+    pad = int(((ps - cl % ps) % ps).sum())
+    D = int((pl // ps).sum() + ((cl + ps - 1) // ps).sum())
+    fill_read, fill_write = T * R, (T + pad) * R
+    gather_read, gather_write = D * ps * R, dense_cap_pages * ps * R
+    return {
+        "fill_read": fill_read, "fill_write": fill_write, "gather_read": gather_read,
+        "gather_write": gather_write, "fill": fill_read + fill_write, "gather": gather_read + gather_write,
+        "total": fill_read + fill_write + gather_read + gather_write,
+        "single_pass_ideal": T * R + int((pl // ps).sum()) * ps * R + D * ps * R, "T": T, "D": D, "pad_rows": pad,
+    }
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if k in d:
+                    return float(d[k]), "measured", d
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback", {}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the workload on the GPU
+# ---------------------------------------------------------------------------
+
+class ComposeWorkload:
+    """Device state of one benchmark replica: batch metadata, plan, pools,
+    per-layer current rows, stagings, dense double buffer, ragged plan."""
+
+    def __init__(self, config: str = "traced_78", device="cuda"):
+        import torch
+
+        from paged_kv_cache_compose_gb300 import cpkv
+        from paged_kv_cache_compose_gb300.runtime import ComposeLayers, ComposePlan
+
+        self.torch, self.cpkv = torch, cpkv
+        self.config = config
+        self.batch = b = wl.CONFIGS[config]()
+        self.num_layers = b.num_layers
+        self.device = torch.device(device)
+        self.plan = ComposePlan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer,
+                                page_size=b.page_size, cp_size=b.cp_size, num_pool_pages=b.num_pool_pages,
+                                device=self.device)
+        self.layers = ComposeLayers(self.plan, b.row_bytes, num_dense=2)
+        # pools: one per layer (own slab) unless the config shares one pool over its layers
+        self.shared_pool = config.startswith("fp8")
+        n_pools = 1 if self.shared_pool else self.num_layers
+        self.pools = [wl.device_pool(b, layer, self.device) for layer in range(n_pools)]
+        self.rows = []
+        for layer in range(self.num_layers):
+            g = wl.device_current_rows(b, layer, self.device)
+            self.rows.append(wl.device_split_rows_by_writer(b, g))
+            del g
+        # ragged index plan of CP rank 0 over the batch's q tokens
+        self.rb = wl.ragged_from_compose(b)
+        self.cp_index = self.rb.cp_index(0)
+        S, Q = cpkv.cpkv_ragged_plan_sizes(self.rb.q_lens, self.cp_index, self.rb.chunk)
+        self.ragged_out = cpkv.ragged_buffers(max(S, 1), max(Q, 1), self.device)
+        self.d_cp_index = torch.from_numpy(self.cp_index).to(self.device)
+        self.ragged_counts = torch.zeros(2, dtype=torch.int64, device=self.device)
+        self.bytes = layer_bytes(b.prefix_lens, b.cur_lens, b.page_size, b.row_bytes, self.plan.dense_cap_pages)
+        self.graph = None
+        self.launches_per_step = 3 + 2 * self.num_layers  # plan (2) + ragged (1) + (fill + gather) per layer
+
+    def pools_of(self, layer):
+        return self.pools[0 if self.shared_pool else layer]
+
+    def step(self, stream=None, events=None):
+        """Enqueue one step on the current stream; ``events`` (optional) gets
+        (kind, start, end) event pairs around every fill and gather."""
+        torch = self.torch
+        self.plan.build(stream)
+        self.cpkv.cpkv_ragged_plan_build(self.rb.prefix_lens, self.rb.q_lens, self.d_cp_index, len(self.cp_index),
+                                         chunk=self.rb.chunk, k_align=self.rb.k_align, out=self.ragged_out,
+                                         d_counts=self.ragged_counts, d_status=self.plan.d_status, stream=stream)
+        for layer in range(self.num_layers):
+            dense = self.layers.dense[layer % 2]
+            if events is None:
+                self.layers.fill(self.rows[layer], stream)
+                self.layers.gather(self.pools_of(layer), dense, stream)
+            else:
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                e[0].record()
+                self.layers.fill(self.rows[layer], stream)
+                e[1].record()
+                e[2].record()
+                self.layers.gather(self.pools_of(layer), dense, stream)
+                e[3].record()
+                events.append(("fill", e[0], e[1]))
+                events.append(("gather", e[2], e[3]))
+
+    def capture(self):
+        """Capture one step as a CUDA graph (after a warm-up run)."""
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.step()
+        torch.cuda.synchronize()
+
+    def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.step()
+
+    def status(self) -> int:
+        return int(self.plan.d_status.item())
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(values_ms, units, ws):
+    """Max time over ranks and total units over ranks (torch.distributed when ws > 1)."""
+    if ws == 1:
+        return float(values_ms), float(units)
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(values_ms)], dtype=torch.float64, device=dev)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+def compact_pool(batch, slabs):
+    """Relabel the batch's prefix pages onto a compact pool holding only the
+    pages it references, keeping each page's owner (new id = cp * (j + 1) + owner,
+    j = rank of the page among the owner's referenced pages).  The compose reads
+    exactly the same bytes, so oracle results and work are unchanged; the host
+    only has to hold the referenced pages.  ``slabs``: the cp owner slabs
+    (torch CUDA tensors or numpy arrays) [slab_pages, ps, R]."""
+    import dataclasses
+
+    cp = batch.cp_size
+    lp = np.asarray(batch.prefix_pages, np.int64)
+    new_ids = np.empty_like(lp)
+    host = []
+    width = 1
+    for o in range(cp):
+        idx = np.nonzero(lp % cp == o)[0]
+        uniq, inv = np.unique(lp[idx] // cp, return_inverse=True)
+        new_ids[idx] = cp * (inv + 1) + o
+        s = slabs[o]
+        if hasattr(s, "index_select"):
+            import torch
+
+            pages = s.index_select(0, torch.from_numpy(uniq).to(s.device)).cpu().numpy()
+        else:
+            pages = s[uniq]
+        host.append(pages)
+        width = max(width, len(uniq) + 1)
+    ps, R = batch.page_size, batch.row_bytes
+    out = []
+    for pages in host:
+        slab = np.zeros((width, ps, R), np.uint8)
+        slab[1:1 + len(pages)] = pages
+        out.append(slab)
+    # current pages are never read from the pool: give them fresh ids past the compact range
+    cur_ids = cp * (width + 1 + np.arange(batch.C, dtype=np.int64))
+    nb = dataclasses.replace(batch, prefix_pages=new_ids.astype(np.int32), cur_pages=cur_ids.astype(np.int32),
+                             num_pool_pages=int(cp * (width + 2 + batch.C)))
+    return nb, out
+
+
+def oracle_sample(work_or_batch, n_layers: int):
+    """Host inputs for ``n_layers`` layers of the workload: copied from the
+    device replica when there is one, else generated on the host; pools are
+    compacted to the pages the batch references."""
+    b = work_or_batch.batch if hasattr(work_or_batch, "batch") else work_or_batch
+    pools, rows = [], []
+    nb = b
+    for layer in range(n_layers):
+        if hasattr(work_or_batch, "pools_of"):
+            w = work_or_batch
+            nb, slabs = compact_pool(b, w.pools_of(layer))
+            rows.append([r.cpu().numpy() for r in w.rows[layer]])
+        else:
+            nb, slabs = compact_pool(b, wl.host_pool(b, layer)) if not pools or not b.name.startswith("fp8") \
+                else (nb, pools[0])
+            rows.append(wl.split_rows_by_writer(b, wl.host_current_rows(b, layer)))
+        pools.append(slabs)
+    return nb, pools, rows
+
+
+def oracle_step(b, pools, rows_per_writer, lib=None):
+    """One bounded oracle step: plan once, then per sampled layer the staging
+    (fill) and the descriptor gather.  Returns the algorithmic bytes moved."""
+    import oracle
+
+    plan = oracle.compose_plan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer,
+                               page_size=b.page_size, cp_size=b.cp_size, num_pool_pages=b.num_pool_pages, lib=lib)
+    rb = wl.ragged_from_compose(b)
+    oracle.ragged_plan(rb.prefix_lens, rb.q_lens, rb.cp_index(0), chunk=rb.chunk, k_align=rb.k_align, lib=lib)
+    ps, R, cp = b.page_size, b.row_bytes, b.cp_size
+    stg = [np.zeros(((plan["C"] + 1) * ps, R), np.uint8) for _ in range(cp)]
+    tw = wl.token_writer(b)
+    moved = 0
+    lb = layer_bytes(b.prefix_lens, b.cur_lens, ps, R, plan["D"])
+    for layer in range(len(pools)):
+        # the oracle's staging takes batch-ordered rows: interleave the writers' rows back
+        g = np.empty((b.T, R), np.uint8)
+        for w in range(cp):
+            g[tw == w] = rows_per_writer[layer][w]
+        oracle.staging(b.cur_lens, b.writer, g, stg, page_size=ps, cp_size=cp, lib=lib)
+        table = [s.reshape(-1) for s in pools[layer]] + [s.reshape(-1) for s in stg]
+        caps = [s.shape[0] for s in pools[layer]] + [plan["C"] + 1] * cp
+        oracle.gather(table, caps, plan["owner"], plan["src"], page_size=ps, row_bytes=R, dense_cap=plan["D"], lib=lib)
+        moved += lb["total"]
+    return moved
+
+
+def time_oracle(b, pools, rows, min_seconds=10.0, max_seconds=30.0):
+    """Run oracle steps until at least ``min_seconds`` of work; GB/s of the work."""
+    import oracle
+
+    lib = oracle.load()
+    t0 = time.perf_counter()
+    moved, steps = 0, 0
+    while True:
+        moved += oracle_step(b, pools, rows, lib)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or el >= max_seconds:
+            break
+    return moved / el / 1e9, el, steps
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="traced_78", choices=["traced_78", "fp8_nsa"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true", help="launch layer by layer instead of replaying a CUDA graph")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's bounded sample")
+    a = ap.parse_args(argv)
+    a.warmup = max(a.warmup, 3)
+
+    ws, rank, local = _dist_env()
+    if a.impl == "reference":
+        return run_reference(a, ws, rank)
+
+    import torch
+
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+
+    from paged_kv_cache_compose_gb300 import build as cpkv_build
+
+    cpkv_build.build()
+    work = ComposeWorkload(a.config, device=device)
+    hbm_peak, peak_src, _ = read_peaks()
+
+    # warm-up (also the first use of every kernel), then capture
+    for _ in range(a.warmup):
+        work.run()
+    torch.cuda.synchronize()
+    if not a.no_graph:
+        work.capture()
+        for _ in range(2):
+            work.run()
+        torch.cuda.synchronize()
+    st0 = work.status()
+
+    # timed region
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.steps):
+        work.run()
+    e1.record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+    ms_max, units_all = aggregate(ms_total, work.bytes["total"] * work.num_layers * a.steps, ws)
+    ms_step = ms_max / a.steps
+    value_gbs = units_all / (ms_max / 1e3) / 1e9
+
+    # per-kernel durations with events around every fill and gather (one more pass, not graphed)
+    kern = {"fill": [], "gather": []}
+    for _ in range(2):
+        evs = []
+        work.step(events=evs)
+        torch.cuda.synchronize()
+        for kind, s, e in evs:
+            kern[kind].append(s.elapsed_time(e))
+    gather_ms = statistics.mean(kern["gather"])
+    fill_ms = statistics.mean(kern["fill"])
+    gather_gbs = work.bytes["gather"] / (gather_ms / 1e3) / 1e9
+    fill_gbs = work.bytes["fill"] / (fill_ms / 1e3) / 1e9
+    status = work.status()
+
+    traffic = None
+    prof_path = os.path.join(ROOT, "profiles", f"gather_traffic_{a.config}.json")
+    if os.path.exists(prof_path):
+        try:
+            with open(prof_path) as f:
+                traffic = json.load(f).get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not a.no_e2e:
+        e2e = run_e2e(work, a, ws)
+
+    cpu = None
+    if not a.no_cpu_baseline and rank == 0 and ws == 1:
+        b, pools, rows = oracle_sample(work, min(a.cpu_layers, work.num_layers))
+        gbs, secs, steps = time_oracle(b, pools, rows)
+        cpu = {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"plan + ragged plan + {len(pools)} of {work.num_layers} layers (staging + gather) of "
+                         f"the same batch and inputs, repeated {steps}x over {secs:.1f}s, single-threaded C"}
+
+    b = work.batch
+    line = {
+        "metric": METRIC,
+        "value": round(value_gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": a.steps,
+        "warmup": a.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "ms_per_78_layer_compose": round(ms_step * 78 / work.num_layers, 4),
+        "pct_of_hbm_peak": round(100 * value_gbs / ws / hbm_peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8",
+        "data": "synthetic",
+        "config": {
+            "workload": ("traced prefill compose, 78 layers: bs=12, 44600 current tokens (lognormal split), prefix "
+                         "U[0,16K] page-floored, page_size=64, cp=8 writer regions on one GPU, MLA 576xbf16 rows, "
+                         "4096-page pool slab per layer" if a.config == "traced_78" else
+                         "fp8 NSA compose, 78 layers: bs=32, 131072 current tokens, prefix U[0,64K], page_size=64, "
+                         "cp=8, 656-byte rows, one 2^20-page pool shared by the layers"),
+            "B": b.B, "T": b.T, "C": work.plan.C, "D": work.plan.D, "layers": work.num_layers,
+            "page_size": b.page_size, "cp_size": b.cp_size, "row_bytes": b.row_bytes,
+            "bytes_per_layer": work.bytes["total"], "single_pass_ideal_bytes_per_layer": work.bytes["single_pass_ideal"],
+            "l2": "inputs larger than L2: every layer reads its own pool slab and rows (%.1f GB per step)" % (
+                (sum(s.numel() for p in work.pools for s in p) + sum(r.numel() for rr in work.rows for r in rr)) / 1e9),
+            "cuda_graph": not a.no_graph,
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gather_pages_kernel (cpkv_compose_gather)",
+            "achieved": round(gather_gbs, 1),
+            "peak": hbm_peak,
+            "peak_source": peak_src,
+            "unit": "GB/s",
+            "frac": round(gather_gbs / hbm_peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": work.bytes["gather"],
+            "avg_launch_ms": round(gather_ms, 5),
+            "fill": {"achieved": round(fill_gbs, 1), "frac": round(fill_gbs / hbm_peak, 4),
+                     "avg_launch_ms": round(fill_ms, 5), "algorithmic_bytes_per_launch": work.bytes["fill"]},
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": work.launches_per_step * a.steps,
+        "clocks": clk,
+        "status_word": status | st0,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0 if (status | st0) == 0 else 3
+
+
+def run_e2e(work, a, ws):
+    """Same metric through the public API with host buffers: every step copies
+    the batch metadata and all layers' current rows from pinned host memory,
+    runs the step, and reads the status word and ragged counts back."""
+    torch = work.torch
+    b = work.batch
+    h_meta = [torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
+              for x in (b.prefix_pages, b.cur_pages, b.writer)]
+    d_meta = [work.plan.d_prefix_pages, work.plan.d_cur_pages, work.plan.d_writer]
+    h_rows = [[r.cpu().pin_memory() for r in layer] for layer in work.rows]
+    h_out = torch.empty(1, dtype=torch.int32).pin_memory()
+    h_cnt = torch.empty(2, dtype=torch.int64).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in h_meta) + sum(r.numel() for layer in h_rows for r in layer)
+    d2h = h_out.numel() * 4 + h_cnt.numel() * 8
+
+    def one():
+        for h, d in zip(h_meta, d_meta):
+            if h.numel():
+                d.copy_(h, non_blocking=True)
+        for layer in range(work.num_layers):
+            for h, d in zip(h_rows[layer], work.rows[layer]):
+                if h.numel():
+                    d.copy_(h, non_blocking=True)
+        work.run()
+        h_out.copy_(work.plan.d_status, non_blocking=True)
+        h_cnt.copy_(work.ragged_counts, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(2):
+        one()
+    steps = max(3, a.steps // 4)
+    if ws > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    el = time.perf_counter() - t0
+    ms_max, units_all = aggregate(el * 1e3, work.bytes["total"] * work.num_layers * steps, ws)
+    return {"value": round(units_all / (ms_max / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms_max / steps, 3), "steps": steps}
+
+
+def run_reference(a, ws, rank):
+    """The CPU oracle as the reference arm: each step is a bounded sample
+    (plan, ragged plan and ``--cpu-layers`` layers of staging + gather)."""
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    batch = wl.CONFIGS[a.config]()
+    n = min(a.cpu_layers, batch.num_layers)
+    b, pools, rows = oracle_sample(batch, n)
+    lib = oracle.load()
+    for _ in range(a.warmup):
+        oracle_step(b, pools, rows, lib)
+    t0 = time.perf_counter()
+    moved = 0
+    for _ in range(a.steps):
+        moved += oracle_step(b, pools, rows, lib)
+    el = time.perf_counter() - t0
+    gbs = moved / el / 1e9
+    ms_step = el * 1e3 / a.steps
+    sample = (f"plan + ragged plan + {n} of {batch.num_layers} layers (staging + gather) per step, "
+              f"host-generated inputs of the same batch, single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": ws,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_step, 3),
+        "ms_per_78_layer_compose": round(ms_step * 78 / n, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": a.config, "sampled_layers": n, "B": b.B, "T": b.T},
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

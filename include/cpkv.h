@@ -1,0 +1,241 @@
+/*
+ * cpkv — paged-KV compose of a context-parallel LLM prefill, for one GB300.
+ *
+ * Plain C ABI.  Every pointer argument is either a HOST pointer (prefix h_)
+ * or a DEVICE pointer (prefix d_) of the current CUDA device.  The caller
+ * owns all memory; the library allocates nothing, never synchronises the
+ * stream and never traps.  All GPU work is enqueued on `stream` and is
+ * asynchronous.  Lengths that size outputs are read from host arrays, so no
+ * call needs a device-to-host copy.
+ *
+ * Error handling (two channels):
+ *   - the return value: CPKV_OK, or a negative CPKV_ERR_* code for bad
+ *     arguments detected on the host before anything is launched (nothing is
+ *     written then), or CPKV_ERR_CUDA when a launch fails;
+ *   - `d_status`: a caller-owned int32 in device memory.  Kernels OR
+ *     CPKV_STATUS_* bits into it when they meet data that violates the
+ *     contract (a page id out of range, a duplicate current page, ...).  The
+ *     offending element is skipped or zero-filled as each call documents; all
+ *     other outputs are still produced.  The library never clears it: zero it
+ *     before a batch and read it whenever the caller synchronises anyway.
+ *
+ * Source of the method (commit-log pages of an SGLang fork):
+ *   "staging-direct compose" message of commits d63fbd4 (test/manual):
+ *     current rows are written straight into a slot-ordered staging through
+ *     a per-batch staging-remapped page inverse; one slot-dense page gather
+ *     over a concatenated 2*cp source-pointer table fills every dense page;
+ *     mixed_locs / staging rows are layer-invariant and computed once per
+ *     batch; the per-layer fill is a single index copy.
+ *   "touched-pages staging" message (same page): a staging slot is the
+ *     page's batch current index; staging is sized by current pages only.
+ *   "prefetch staging" message of commits 0d87bc5 (python): staging row 0 is
+ *     reserved, current page i sits at slot i + 1; page id 0 is the dummy.
+ *   "compose_v2" message (commits d63fbd4): an owner of -1 zero-fills.
+ *   "CPU-gap fixes" message (commits d63fbd4): the per-batch ragged index
+ *     plan of the NSA indexer.
+ *
+ * Notation: B requests, ps = page_size, cp = cp_size, R = row bytes,
+ * npp_b = prefix_len_b / ps, ncp_b = ceil(cur_len_b / ps), T = sum cur_len,
+ * C = sum ncp, D = sum (npp + ncp).  Logical page lp of the pool lives on
+ * owner lp % cp at local page lp / cp (modulo-owner placement); page 0 is the
+ * dummy page and is never a valid page id.
+ */
+#ifndef CPKV_H_
+#define CPKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CPKV_VERSION 1
+#define CPKV_MAX_CP 64       /* largest cp_size (2*cp source pointers)      */
+#define CPKV_MAX_BATCH 1024  /* largest B (host lengths travel as kernel parameters) */
+
+/* A cudaStream_t, passed as an opaque handle (0 = the legacy default stream). */
+typedef void *cpkv_stream_t;
+
+/* Return codes. */
+#define CPKV_OK 0
+#define CPKV_ERR_ARG (-1)              /* null/misaligned pointer, bad size or count   */
+#define CPKV_ERR_UNALIGNED_PREFIX (-2) /* a prefix length is not a multiple of ps      */
+#define CPKV_ERR_CAPACITY (-3)         /* an output or staging capacity is too small   */
+#define CPKV_ERR_LIMIT (-4)            /* B, cp or a size exceeds what this build takes */
+#define CPKV_ERR_CUDA (-5)             /* a kernel launch failed                        */
+
+/* Device status bits (ORed into *d_status). */
+#define CPKV_STATUS_PAGE_OOB 1            /* page id outside [1, num_pool_pages)         */
+#define CPKV_STATUS_WRITER_OOB 2          /* writer rank outside [0, cp)                 */
+#define CPKV_STATUS_DUP_CURRENT_PAGE 4    /* a current page id appears twice             */
+#define CPKV_STATUS_CURRENT_IN_PREFIX 8   /* a current page id is also a prefix page     */
+#define CPKV_STATUS_DESC_OOB 16           /* gather descriptor outside table/capacity    */
+#define CPKV_STATUS_ROW_OOB 32            /* fill row index outside its buffer           */
+#define CPKV_STATUS_CHUNK_OOB 64          /* cp_index not ascending or out of range      */
+#define CPKV_STATUS_OUT_CAPACITY 128      /* a device-sized output exceeded its capacity */
+#define CPKV_STATUS_TIMEOUT 256           /* a bounded wait gave up (should never occur) */
+
+/* Sizes of a batch, derived from host lengths. */
+typedef struct {
+  int64_t T; /* current tokens */
+  int64_t C; /* current pages  */
+  int64_t D; /* dense pages (prefix + current) */
+} cpkv_sizes;
+
+/*
+ * cpkv_plan_sizes — T, C and D of a batch (host only, no GPU work).
+ * h_prefix_lens, h_cur_lens: host int32 [B], non-negative; prefix lengths
+ * must be multiples of page_size ("a chunked prefix that is not page-aligned
+ * keeps its batch solo ... the CP page-aligned split would fail-fast",
+ * chunked-prefill message of commits 0d87bc5).
+ * Returns CPKV_ERR_UNALIGNED_PREFIX for an unaligned prefix, CPKV_ERR_ARG for
+ * B < 0, page_size <= 0, a negative length or a null pointer (B > 0),
+ * CPKV_ERR_LIMIT when T, C or D would not fit int32 indices.
+ */
+int cpkv_plan_sizes(int B, int page_size, const int32_t *h_prefix_lens, const int32_t *h_cur_lens,
+                    cpkv_sizes *out);
+
+/*
+ * cpkv_writer_token_counts — tokens each writer rank computes (host only).
+ * h_writer: host int32 [C], writer rank of each current page in batch order.
+ * h_tokens_per_writer: host int64 [cp_size], written.  Sizes the per-writer
+ * current-row buffers passed to cpkv_fill_current.  A writer outside [0, cp)
+ * returns CPKV_ERR_ARG.
+ */
+int cpkv_writer_token_counts(int B, int page_size, int cp_size, const int32_t *h_cur_lens,
+                             const int32_t *h_writer, int64_t C, int64_t *h_tokens_per_writer);
+
+/*
+ * cpkv_plan_build — the per-batch compose plan, built on the device.
+ * ("staging-direct compose": spans, descriptors, the page inverse, the
+ * staging-remapped page inverse and mixed_locs / staging row indices are
+ * layer-invariant and built once per batch.)
+ *
+ * Inputs:
+ *   h_prefix_lens, h_cur_lens  host int32 [B] (B <= CPKV_MAX_BATCH)
+ *   d_prefix_pages  device int32 [sum npp], CSR by request: the logical pages
+ *                   of request b's prefix, in token order
+ *   d_cur_pages     device int32 [C], CSR by request: the logical pages that
+ *                   hold request b's current tokens
+ *   d_writer        device int32 [C]: writer rank of each current page
+ *   num_pool_pages  P: valid page ids are [1, P)
+ *   dense_cap_pages capacity of the dense buffer in pages, >= D
+ * Outputs (device, caller-allocated, fully written):
+ *   d_prefix_spans  int32 [B][2]  (dense start, npp_b)
+ *   d_cur_spans     int32 [B][2]  (dense start + npp_b, ncp_b)
+ *   d_owner, d_src  int32 [dense_cap_pages] gather descriptors:
+ *                     prefix slot of lp:  owner = lp % cp,   src = lp / cp
+ *                     current page i:     owner = cp + w_i,  src = i + 1
+ *                     slots >= D:         owner = -1,        src = 0
+ *   d_page_inverse         int32 [P]: dense slot of lp (smallest if lp is in
+ *                          several prefixes), -1 if lp is not in the batch
+ *   d_staging_page_inverse int32 [P]: i + 1 if lp is current page i, else 0
+ *   d_mixed_locs     int64 [T]: dense row of each current token
+ *   d_staging_rows   int64 [T]: staging row (i + 1) * ps + offset
+ *   d_token_writer_row int32 [T]: row of the token in its writer's
+ *                    current-row buffer (batch order within each writer)
+ * Status bits: PAGE_OOB / WRITER_OOB (the slot gets owner -1), DUP_CURRENT_PAGE,
+ * CURRENT_IN_PREFIX.
+ */
+int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
+                    const int32_t *h_prefix_lens, const int32_t *h_cur_lens,
+                    const int32_t *d_prefix_pages, const int32_t *d_cur_pages, const int32_t *d_writer,
+                    int64_t dense_cap_pages, int32_t *d_prefix_spans, int32_t *d_cur_spans,
+                    int32_t *d_owner, int32_t *d_src, int32_t *d_page_inverse,
+                    int32_t *d_staging_page_inverse, int64_t *d_mixed_locs, int64_t *d_staging_rows,
+                    int32_t *d_token_writer_row, int32_t *d_status, cpkv_stream_t stream);
+
+/*
+ * cpkv_fill_current — per layer: write every current row into its writer's
+ * staging ("the per-layer fill collapses to a single index_copy_ into the
+ * zeroed staging span"; fp8 rows are handled as bytes, "fp8 -> uint8"
+ * message of commits 0d87bc5).
+ *
+ * For every token t with writer w = d_writer[d_staging_rows[t] / ps - 1]:
+ *   staging[w] row d_staging_rows[t]  <-  cur_rows[w] row d_token_writer_row[t]
+ * and for every request b whose current length is not a multiple of ps, the
+ * rows after its last token up to the end of that staging page are zeroed.
+ * No other staging row is written (page 0 and other writers' pages keep their
+ * bytes).
+ *
+ *   h_cur_lens        host int32 [B]
+ *   h_cur_rows        host array [cp] of device pointers: writer w's current
+ *                     rows, [h_cur_rows_cap[w]][R] bytes, 16-byte aligned
+ *   h_staging         host array [cp] of device pointers: writer w's staging,
+ *                     [staging_cap_pages * ps][R] bytes, 16-byte aligned;
+ *                     staging_cap_pages >= C + 1
+ *   d_staging_rows, d_token_writer_row: from cpkv_plan_build; d_writer [C]
+ *   row_bytes         R, a multiple of 16
+ * Status bits: ROW_OOB / WRITER_OOB (that row is skipped).
+ */
+int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
+                      const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
+                      void *const *h_staging, int64_t staging_cap_pages,
+                      const int64_t *d_staging_rows, const int32_t *d_token_writer_row,
+                      const int32_t *d_writer, int64_t num_cur_pages, int32_t *d_status,
+                      cpkv_stream_t stream);
+
+/*
+ * cpkv_compose_gather — per layer: the slot-dense page gather.  ONE call
+ * fills every dense page: prefix pages from the owners' pools, all current
+ * pages from the writers' stagings.
+ *
+ *   h_src_table      host array [2*cp] of device pointers:
+ *                    [pool_0 .. pool_{cp-1} | staging_0 .. staging_{cp-1}],
+ *                    each a page array [h_src_cap_pages[k]][ps][R], 16-byte aligned
+ *   d_owner, d_src   device int32 [dense_cap_pages] (from cpkv_plan_build)
+ *   d_dense          device [dense_cap_pages * ps][R], 16-byte aligned
+ * dense page d <- page d_src[d] of table[d_owner[d]] (ps*R contiguous bytes);
+ * owner -1 -> zeros.  A descriptor outside the table or the source's capacity
+ * raises DESC_OOB and its page is zero-filled.
+ */
+int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
+                        const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                        const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
+                        void *d_dense, int32_t *d_status, cpkv_stream_t stream);
+
+/*
+ * cpkv_ragged_plan_sizes — exact segment count S and q-token count Q_r of a
+ * rank's ragged plan, from a host copy of its cp_index (host only).
+ */
+int cpkv_ragged_plan_sizes(int B, int chunk, const int32_t *h_q_lens, const int32_t *h_cp_index,
+                           int64_t n_owned, int64_t *h_S, int64_t *h_Q);
+
+/*
+ * cpkv_ragged_plan_build — per batch: the NSA indexer's ragged index plan of
+ * one CP rank ("CPU-gap fixes" message: a topk offset list plus int32
+ * segment / kv_lens / q_starts / q_lens / k_bases / q_bases / current_bases
+ * descriptors, all from batch metadata keyed on cp_index).
+ *
+ * Request b's q tokens are cut into ceil(q_b / chunk) chunks; chunk ids run
+ * request-major over the batch.  d_cp_index (device int32 [n_owned]) lists the
+ * chunk ids this rank owns, strictly ascending.  A segment is a maximal run
+ * of owned chunks of one request with consecutive ids.  Per segment s of
+ * request b:
+ *   seg_req = b; q_starts = token offset inside request b's q; q_lens;
+ *   kv_lens = prefix_b + q_starts + q_lens;
+ *   k_bases = sum_{b' < b} align_up(prefix_b' + q_b', k_align);
+ *   current_bases = k_bases + prefix_b; q_bases = exclusive sum of q_lens.
+ * d_topk_offsets[j] = k_bases of the segment holding this rank's j-th token.
+ * Capacities: seg_cap >= S, topk_cap >= Q_r (S <= n_owned and
+ * Q_r <= n_owned * chunk always hold).  d_counts (device int64 [2]) receives
+ * (S, Q_r).  Status bits: CHUNK_OOB (bad cp_index), OUT_CAPACITY.
+ */
+int cpkv_ragged_plan_build(int B, int chunk, int k_align, const int32_t *h_prefix_lens,
+                           const int32_t *h_q_lens, const int32_t *d_cp_index, int64_t n_owned,
+                           int32_t *d_topk_offsets, int64_t topk_cap, int32_t *d_seg_req,
+                           int32_t *d_kv_lens, int32_t *d_q_starts, int32_t *d_q_lens,
+                           int32_t *d_k_bases, int32_t *d_q_bases, int32_t *d_current_bases,
+                           int64_t seg_cap, int64_t *d_counts, int32_t *d_status, cpkv_stream_t stream);
+
+/* Human-readable name of a return code. */
+const char *cpkv_error_string(int code);
+
+/* CPKV_VERSION of the loaded library. */
+int cpkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPKV_H_ */

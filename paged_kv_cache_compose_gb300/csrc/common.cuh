@@ -1,0 +1,200 @@
+// Shared helpers of the cpkv CUDA library (sm_103a): status reporting,
+// 16-byte streaming loads/stores, mbarrier + bulk-copy (TMA) wrappers,
+// block scans and host-side launch plumbing.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cpkv.h"
+
+#define CPKV_DEV __device__ __forceinline__
+
+namespace cpkv {
+
+// ---------------------------------------------------------------------------
+// status word
+// ---------------------------------------------------------------------------
+CPKV_DEV void raise_status(int32_t *status, int32_t bits) { atomicOr(status, bits); }
+
+// ---------------------------------------------------------------------------
+// 16-byte streaming memory ops
+// ---------------------------------------------------------------------------
+CPKV_DEV uint4 ld_stream16(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+CPKV_DEV void st_stream16(void *p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses, mbarriers and bulk async copies (TMA, non-tensor)
+// ---------------------------------------------------------------------------
+CPKV_DEV uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+CPKV_DEV void mbar_init(uint64_t *bar, uint32_t arrivals) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(arrivals)
+               : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA) proxy.
+CPKV_DEV void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Make generic-proxy shared-memory writes visible to the async proxy.
+CPKV_DEV void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+CPKV_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+CPKV_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+CPKV_DEV uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up (returns false) once
+// `limit_ns` nanoseconds have passed.
+CPKV_DEV bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// global -> shared bulk copy, completion signalled on `bar` (complete_tx).
+CPKV_DEV void bulk_load_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// shared -> global bulk copy, tracked by the bulk async-group mechanism.
+CPKV_DEV void bulk_store_s2g(void *gdst, const void *smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+CPKV_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N committed bulk groups still read shared memory.
+template <int N>
+CPKV_DEV void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+CPKV_DEV void bulk_wait_read_dyn(int n) {
+  switch (n) {
+    case 0: bulk_wait_read<0>(); break;
+    case 1: bulk_wait_read<1>(); break;
+    case 2: bulk_wait_read<2>(); break;
+    case 3: bulk_wait_read<3>(); break;
+    case 4: bulk_wait_read<4>(); break;
+    case 5: bulk_wait_read<5>(); break;
+    case 6: bulk_wait_read<6>(); break;
+    default: bulk_wait_read<7>(); break;
+  }
+}
+
+// Wait until every committed bulk group has completed (writes visible).
+CPKV_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+CPKV_DEV int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// ---------------------------------------------------------------------------
+// scans
+// ---------------------------------------------------------------------------
+template <typename T>
+CPKV_DEV T warp_inclusive_scan(T x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// Exclusive scan over the block (blockDim.x a multiple of 32, <= 1024).
+// `scratch` is shared memory of >= 33 elements.  Returns the exclusive
+// prefix of `v`; *total receives the block sum.  Contains __syncthreads().
+template <typename T>
+CPKV_DEV T block_exclusive_scan(T v, T *scratch, T *total) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  T inc = warp_inclusive_scan(v);
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < nwarps ? scratch[lane] : T(0);
+    w = warp_inclusive_scan(w);
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  T before = warp > 0 ? scratch[warp - 1] : T(0);
+  *total = scratch[nwarps - 1];
+  __syncthreads();
+  return before + inc - v;
+}
+
+// Largest index b in [0, n) with a[b] <= x, for non-decreasing a (a[0] <= x).
+template <typename T>
+CPKV_DEV int upper_index(const T *a, int n, T x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+// Number of SMs of the current device (cached per device ordinal).
+int device_sm_count();
+
+// Map the last launch error to CPKV_ERR_CUDA.
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? CPKV_OK : CPKV_ERR_CUDA;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace cpkv

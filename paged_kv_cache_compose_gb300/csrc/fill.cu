@@ -1,0 +1,205 @@
+// cpkv_fill_current: the per-layer fill of current rows into the writers'
+// stagings ("staging-direct compose" message of commits d63fbd4: the fill is
+// a single index copy of layer-invariant row indices; "fp8 -> uint8"
+// message of commits 0d87bc5: rows are opaque bytes).
+//
+// One launch.  Blocks [0, nRow) copy rows: one warp per token row, each lane
+// moving 16-byte vectors, ROWS rows in flight per warp (all loads issued
+// before the stores).  Blocks [nRow, nRow + B) zero the pad rows after each
+// request's last token, up to the end of its staging page.
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace cpkv {
+namespace {
+
+constexpr int kFillThreads = 256;
+constexpr int kWarpsPerBlock = kFillThreads / 32;
+constexpr int kRowsInFlight = 2;   // rows per warp per iteration
+constexpr int kVecPerLane = 4;     // 16-byte vectors per lane per row in the fast path (R <= 2048)
+
+template <int MAXB>
+struct FillParams {
+  const uint8_t *cur_rows[CPKV_MAX_CP];
+  int64_t cur_cap[CPKV_MAX_CP];
+  uint8_t *staging[CPKV_MAX_CP];
+  const int64_t *staging_rows;
+  const int32_t *token_writer_row, *writer;
+  int32_t *status;
+  int64_t T, C, staging_cap_rows, R;
+  int ps, cp, B, nRow, vpr;  // vpr = R / 16
+  int32_t cur_lens[MAXB];
+};
+
+struct RowJob {
+  const uint8_t *src;
+  uint8_t *dst;
+};
+
+// Resolve token t to (source row, staging row); nullptr src when skipped.
+template <int MAXB>
+__device__ RowJob resolve_row(const FillParams<MAXB> &p, int64_t t) {
+  RowJob j{nullptr, nullptr};
+  const int64_t sr = p.staging_rows[t];
+  const int64_t slot = sr / p.ps;
+  if (sr < p.ps || sr >= p.staging_cap_rows || slot > p.C) {
+    raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    return j;
+  }
+  const int32_t w = p.writer[slot - 1];
+  if (w < 0 || w >= p.cp) {
+    raise_status(p.status, CPKV_STATUS_WRITER_OOB);
+    return j;
+  }
+  const int32_t r = p.token_writer_row[t];
+  if (r < 0 || r >= p.cur_cap[w]) {
+    raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    return j;
+  }
+  j.src = p.cur_rows[w] + (int64_t)r * p.R;
+  j.dst = p.staging[w] + sr * p.R;
+  return j;
+}
+
+template <int MAXB>
+__device__ void copy_rows(const FillParams<MAXB> &p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)p.nRow * kWarpsPerBlock;
+  const int vpr = p.vpr;
+  if (vpr <= 32 * kVecPerLane) {
+    for (int64_t t0 = warp_id * kRowsInFlight; t0 < p.T; t0 += nwarps * kRowsInFlight) {
+      RowJob job[kRowsInFlight];
+      uint4 v[kRowsInFlight][kVecPerLane];
+#pragma unroll
+      for (int r = 0; r < kRowsInFlight; ++r) {
+        job[r] = (t0 + r < p.T) ? resolve_row(p, t0 + r) : RowJob{nullptr, nullptr};
+      }
+#pragma unroll
+      for (int r = 0; r < kRowsInFlight; ++r) {
+#pragma unroll
+        for (int k = 0; k < kVecPerLane; ++k) {
+          const int c = lane + 32 * k;
+          if (job[r].src != nullptr && c < vpr) v[r][k] = ld_stream16(job[r].src + 16 * (int64_t)c);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kRowsInFlight; ++r) {
+#pragma unroll
+        for (int k = 0; k < kVecPerLane; ++k) {
+          const int c = lane + 32 * k;
+          if (job[r].src != nullptr && c < vpr) st_stream16(job[r].dst + 16 * (int64_t)c, v[r][k]);
+        }
+      }
+    }
+  } else {
+    for (int64_t t = warp_id; t < p.T; t += nwarps) {
+      const RowJob job = resolve_row(p, t);
+      if (job.src == nullptr) continue;
+      for (int c = lane; c < vpr; c += 32) st_stream16(job.dst + 16 * (int64_t)c, ld_stream16(job.src + 16 * (int64_t)c));
+    }
+  }
+}
+
+// Zero the rows after request b's last token up to the end of its staging page.
+template <int MAXB>
+__device__ void zero_pad_rows(const FillParams<MAXB> &p, int b) {
+  __shared__ int64_t last_tok;
+  if (b >= p.B) return;
+  const int32_t rem = p.cur_lens[b] % p.ps;
+  if (rem == 0) return;
+  if (threadIdx.x == 0) {
+    int64_t s = 0;
+    for (int k = 0; k <= b; ++k) s += p.cur_lens[k];
+    last_tok = s - 1;
+  }
+  __syncthreads();
+  const int64_t sr = p.staging_rows[last_tok];
+  const int64_t slot = sr / p.ps;
+  if (sr < p.ps || sr >= p.staging_cap_rows || slot > p.C) {
+    if (threadIdx.x == 0) raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    return;
+  }
+  const int32_t w = p.writer[slot - 1];
+  if (w < 0 || w >= p.cp) {
+    if (threadIdx.x == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
+    return;
+  }
+  const int64_t first = sr + 1, end = (slot + 1) * p.ps;  // [first, end) rows to zero
+  uint8_t *base = p.staging[w] + first * p.R;
+  const int64_t nvec = (end - first) * p.vpr;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t i = threadIdx.x; i < nvec; i += kFillThreads) st_stream16(base + 16 * i, z);
+}
+
+template <int MAXB>
+__global__ void __launch_bounds__(kFillThreads) fill_current_kernel(const __grid_constant__ FillParams<MAXB> p) {
+  if ((int)blockIdx.x < p.nRow) copy_rows(p);
+  else zero_pad_rows(p, blockIdx.x - p.nRow);
+}
+
+}  // namespace
+}  // namespace cpkv
+
+extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_bytes,
+                                 const int32_t *h_cur_lens, const void *const *h_cur_rows,
+                                 const int64_t *h_cur_rows_cap, void *const *h_staging,
+                                 int64_t staging_cap_pages, const int64_t *d_staging_rows,
+                                 const int32_t *d_token_writer_row, const int32_t *d_writer,
+                                 int64_t num_cur_pages, int32_t *d_status, cpkv_stream_t stream) {
+  using namespace cpkv;
+  if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
+  if (row_bytes <= 0 || row_bytes % 16 != 0) return CPKV_ERR_ARG;
+  if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
+  if (h_cur_rows == nullptr || h_cur_rows_cap == nullptr || h_staging == nullptr || d_status == nullptr)
+    return CPKV_ERR_ARG;
+  if (B > 0 && h_cur_lens == nullptr) return CPKV_ERR_ARG;
+  int64_t T = 0, C = 0;
+  for (int b = 0; b < B; ++b) {
+    if (h_cur_lens[b] < 0) return CPKV_ERR_ARG;
+    T += h_cur_lens[b];
+    C += ceil_div(h_cur_lens[b], page_size);
+  }
+  if (num_cur_pages != C) return CPKV_ERR_ARG;
+  if (staging_cap_pages < C + 1) return CPKV_ERR_CAPACITY;
+  if (T > 0 && (d_staging_rows == nullptr || d_token_writer_row == nullptr || d_writer == nullptr))
+    return CPKV_ERR_ARG;
+  for (int w = 0; w < cp_size; ++w) {
+    if (h_staging[w] == nullptr || !aligned16(h_staging[w])) return CPKV_ERR_ARG;
+    if (h_cur_rows_cap[w] < 0) return CPKV_ERR_ARG;
+    if (h_cur_rows_cap[w] > 0 && (h_cur_rows[w] == nullptr || !aligned16(h_cur_rows[w]))) return CPKV_ERR_ARG;
+  }
+  if (T == 0 && C == 0) return CPKV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const int64_t row_warps = ceil_div(T, kRowsInFlight);
+  const int64_t row_blocks_needed = ceil_div(row_warps, kWarpsPerBlock);
+  const int64_t row_blocks_cap = (int64_t)device_sm_count() * (2048 / kFillThreads);
+  const int nRow = (int)(row_blocks_needed < row_blocks_cap ? row_blocks_needed : row_blocks_cap);
+
+#define CPKV_FILL_FILL(prm)                                                                  \
+  for (int w = 0; w < CPKV_MAX_CP; ++w) {                                                    \
+    prm.cur_rows[w] = w < cp_size ? static_cast<const uint8_t *>(h_cur_rows[w]) : nullptr;   \
+    prm.cur_cap[w] = w < cp_size ? h_cur_rows_cap[w] : 0;                                    \
+    prm.staging[w] = w < cp_size ? static_cast<uint8_t *>(h_staging[w]) : nullptr;           \
+  }                                                                                          \
+  prm.staging_rows = d_staging_rows; prm.token_writer_row = d_token_writer_row;              \
+  prm.writer = d_writer; prm.status = d_status; prm.T = T; prm.C = C;                        \
+  prm.staging_cap_rows = staging_cap_pages * page_size; prm.R = row_bytes;                   \
+  prm.ps = page_size; prm.cp = cp_size; prm.B = B; prm.nRow = nRow;                          \
+  prm.vpr = (int)(row_bytes / 16);                                                           \
+  for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
+
+  if (B <= 64) {
+    FillParams<64> prm;
+    CPKV_FILL_FILL(prm)
+    fill_current_kernel<64><<<nRow + B, kFillThreads, 0, s>>>(prm);
+    return launch_status();
+  }
+  FillParams<CPKV_MAX_BATCH> prm;
+  CPKV_FILL_FILL(prm)
+#undef CPKV_FILL_FILL
+  fill_current_kernel<CPKV_MAX_BATCH><<<nRow + B, kFillThreads, 0, s>>>(prm);
+  return launch_status();
+}

@@ -1,0 +1,187 @@
+// cpkv_compose_gather: the slot-dense page gather ("staging-direct compose"
+// message of commits d63fbd4: ONE gather covers prefix pages through pool
+// pointers and all current pages through staging pointers, via a
+// concatenated 2*cp pointer table; "compose_v2" message: owner -1 zero-fills).
+//
+// Every dense page is ps*R contiguous bytes copied from one contiguous
+// source page, so the kernel moves pages with bulk async copies (TMA,
+// non-tensor form): global -> shared with mbarrier completion, then
+// shared -> global tracked by bulk groups.  Each page is cut into `pieces`
+// equal 16-byte-multiple units; units are dealt round-robin to a persistent
+// grid of one-warp CTAs (several per SM), each running an S-stage ring:
+// while one unit is being stored the next S-1 loads are in flight.  Zero
+// units (owner -1 or an invalid descriptor) are written with plain 16-byte
+// stores by the whole warp.  Every mbarrier wait is bounded; on a timeout the
+// kernel raises CPKV_STATUS_TIMEOUT, stops issuing, drains what it issued
+// (bounded again) and returns.
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace cpkv {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kMaxPieceBytes = 24 * 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a page load takes microseconds
+
+struct GatherParams {
+  const uint8_t *table[2 * CPKV_MAX_CP];
+  int64_t cap_pages[2 * CPKV_MAX_CP];
+  const int32_t *owner, *src;
+  uint8_t *dense;
+  int32_t *status;
+  int64_t dense_cap, page_bytes, units;
+  int32_t n_table, pieces, piece_bytes;
+};
+
+struct Unit {
+  const uint8_t *src;  // nullptr: zero-fill
+  uint8_t *dst;
+  uint32_t bytes;
+};
+
+__device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, bool report) {
+  const int64_t d = u / p.pieces;
+  const int32_t k = (int32_t)(u - d * p.pieces);
+  const int64_t off = (int64_t)k * p.piece_bytes;
+  Unit x;
+  x.bytes = (uint32_t)min64(p.piece_bytes, p.page_bytes - off);
+  x.dst = p.dense + d * p.page_bytes + off;
+  x.src = nullptr;
+  const int32_t o = p.owner[d];
+  if (o == -1) return x;
+  const int32_t s = p.src[d];
+  if (o < -1 || o >= p.n_table || s < 0 || s >= p.cap_pages[o]) {
+    if (report && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
+    return x;
+  }
+  x.src = p.table[o] + (int64_t)s * p.page_bytes + off;
+  return x;
+}
+
+__global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant__ GatherParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ uint8_t *ring_dst[kStages];
+  __shared__ uint32_t ring_bytes[kStages];
+  __shared__ int ring_live[kStages];  // a load was issued into the stage
+  const int lane = threadIdx.x;
+
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  int64_t head = 0, tail = 0;  // consumed / issued copy units (uniform across the warp)
+  bool dead = false;           // a bounded wait gave up (lane 0 only)
+
+  // consume the oldest in-flight copy unit: wait for its load, store it.
+  // A load that was issued is always waited for (bounded), even after a
+  // timeout, so no copy into shared memory outlives the CTA.
+  auto consume = [&]() {
+    const int s = (int)(head % kStages);
+    if (lane == 0) {
+      const uint32_t parity = (uint32_t)((head / kStages) & 1);
+      bool landed = false;
+      if (ring_live[s]) {
+        landed = mbar_wait_bounded(&full[s], parity, kWaitLimitNs);
+        if (!landed && !dead) {
+          dead = true;
+          raise_status(p.status, CPKV_STATUS_TIMEOUT);
+        }
+      }
+      if (landed && !dead) {
+        bulk_store_s2g(ring_dst[s], smem + (size_t)s * p.piece_bytes, ring_bytes[s]);
+      }
+      bulk_commit();
+    }
+    ++head;
+  };
+
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
+    const Unit x = resolve_unit(p, u, lane == 0);
+    if (x.src == nullptr) {
+      for (uint32_t i = lane; i < x.bytes / 16; i += 32) st_stream16(x.dst + 16 * (size_t)i, z);
+      continue;
+    }
+    if (tail - head == kStages) consume();
+    const int s = (int)(tail % kStages);
+    if (lane == 0) {
+      if (tail >= kStages) bulk_wait_read_dyn((int)(head - tail + kStages - 1));  // stage's last store has read smem
+      ring_live[s] = 0;
+      if (!dead) {
+        ring_dst[s] = x.dst;
+        ring_bytes[s] = x.bytes;
+        ring_live[s] = 1;
+        mbar_arrive_expect_tx(&full[s], x.bytes);
+        bulk_load_g2s(smem + (size_t)s * p.piece_bytes, x.src, x.bytes, &full[s]);
+      }
+    }
+    ++tail;
+    __syncwarp();
+  }
+  while (head < tail) consume();
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
+}
+
+}  // namespace
+}  // namespace cpkv
+
+extern "C" int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
+                                   const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                                   const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
+                                   void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
+  using namespace cpkv;
+  if (page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
+  if (row_bytes <= 0 || row_bytes % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
+  if (h_src_table == nullptr || h_src_cap_pages == nullptr || d_status == nullptr) return CPKV_ERR_ARG;
+  if (dense_cap_pages == 0) return CPKV_OK;
+  if (d_owner == nullptr || d_src == nullptr || d_dense == nullptr || !aligned16(d_dense)) return CPKV_ERR_ARG;
+  const int n_table = 2 * cp_size;
+  for (int k = 0; k < n_table; ++k) {
+    if (h_src_cap_pages[k] < 0) return CPKV_ERR_ARG;
+    if (h_src_cap_pages[k] > 0 && (h_src_table[k] == nullptr || !aligned16(h_src_table[k]))) return CPKV_ERR_ARG;
+  }
+  const int64_t page_bytes = (int64_t)page_size * row_bytes;
+  const int64_t pieces = ceil_div(page_bytes, kMaxPieceBytes);
+  const int64_t piece_bytes = ceil_div(ceil_div(page_bytes, pieces), 16) * 16;
+  if (pieces > INT32_MAX || dense_cap_pages > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
+
+  GatherParams prm;
+  for (int k = 0; k < 2 * CPKV_MAX_CP; ++k) {
+    prm.table[k] = k < n_table ? static_cast<const uint8_t *>(h_src_table[k]) : nullptr;
+    prm.cap_pages[k] = k < n_table ? h_src_cap_pages[k] : 0;
+  }
+  prm.owner = d_owner;
+  prm.src = d_src;
+  prm.dense = static_cast<uint8_t *>(d_dense);
+  prm.status = d_status;
+  prm.dense_cap = dense_cap_pages;
+  prm.page_bytes = page_bytes;
+  prm.units = dense_cap_pages * pieces;
+  prm.n_table = n_table;
+  prm.pieces = (int32_t)pieces;
+  prm.piece_bytes = (int32_t)piece_bytes;
+
+  const size_t smem = (size_t)kStages * piece_bytes;
+  static int configured[256] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 256 && !configured[dev]) {
+    if (cudaFuncSetAttribute(gather_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStages * kMaxPieceBytes) != cudaSuccess)
+      return CPKV_ERR_CUDA;
+    configured[dev] = 1;
+  }
+  // One-warp CTAs; shared memory bounds residency (~227 KB per SM).
+  const int per_sm = (int)(220 * 1024 / (smem + 256));
+  const int64_t cap = (int64_t)device_sm_count() * (per_sm > 0 ? per_sm : 1);
+  const int grid = (int)(prm.units < cap ? prm.units : cap);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  gather_pages_kernel<<<grid, 32, smem, s>>>(prm);
+  return launch_status();
+}

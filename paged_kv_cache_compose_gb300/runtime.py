@@ -1,0 +1,85 @@
+"""Per-batch and per-layer drivers over the C ABI.
+
+``ComposePlan`` owns the device copies of one batch's metadata and the plan
+arrays, and builds the plan once per batch (``cpkv_plan_build``).
+``ComposeLayers`` owns the writers' staging regions and the dense buffers
+(two, alternated by layer parity: a dense buffer is reused two layers later)
+and runs the per-layer fill + gather.  Allocation uses torch device memory;
+every computation is a library kernel.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import cpkv
+
+
+class ComposePlan:
+    def __init__(self, prefix_lens, cur_lens, prefix_pages, cur_pages, writer, *, page_size: int, cp_size: int,
+                 num_pool_pages: int, dense_cap_pages: int | None = None, device="cuda"):
+        self.prefix_lens = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+        self.cur_lens = np.ascontiguousarray(cur_lens, dtype=np.int32)
+        self.page_size, self.cp_size, self.num_pool_pages = page_size, cp_size, num_pool_pages
+        self.T, self.C, self.D = cpkv.cpkv_plan_sizes(self.prefix_lens, self.cur_lens, page_size)
+        self.dense_cap_pages = self.D if dense_cap_pages is None else int(dense_cap_pages)
+        self.B = len(self.prefix_lens)
+        self.device = torch.device(device)
+        host_writer = np.ascontiguousarray(writer, dtype=np.int32)
+        self.tokens_per_writer = cpkv.cpkv_writer_token_counts(self.cur_lens, host_writer, page_size, cp_size)
+        self.d_prefix_pages = torch.as_tensor(np.ascontiguousarray(prefix_pages, dtype=np.int32)).to(self.device)
+        self.d_cur_pages = torch.as_tensor(np.ascontiguousarray(cur_pages, dtype=np.int32)).to(self.device)
+        self.d_writer = torch.as_tensor(host_writer).to(self.device)
+        self.bufs = cpkv.plan_buffers(self.B, self.T, self.dense_cap_pages, num_pool_pages, self.device)
+        self.d_status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def build(self, stream=None):
+        cpkv.cpkv_plan_build(self.prefix_lens, self.cur_lens, self.d_prefix_pages, self.d_cur_pages, self.d_writer,
+                             page_size=self.page_size, cp_size=self.cp_size, num_pool_pages=self.num_pool_pages,
+                             dense_cap_pages=self.dense_cap_pages, out=self.bufs, d_status=self.d_status,
+                             stream=stream)
+        return self
+
+    def __getitem__(self, k):
+        return self.bufs[k]
+
+    @property
+    def staging_cap_pages(self) -> int:
+        return self.C + 1
+
+
+class ComposeLayers:
+    """Staging regions (one per writer, C + 1 pages each, row 0 reserved) and
+    ``num_dense`` dense buffers of ``dense_cap_pages`` pages."""
+
+    def __init__(self, plan: ComposePlan, row_bytes: int, num_dense: int = 2):
+        self.plan = plan
+        self.row_bytes = row_bytes
+        ps, cp = plan.page_size, plan.cp_size
+        self.staging = [torch.empty((plan.staging_cap_pages * ps, row_bytes), dtype=torch.uint8, device=plan.device)
+                        for _ in range(cp)]
+        self.dense = [torch.empty((plan.dense_cap_pages * ps, row_bytes), dtype=torch.uint8, device=plan.device)
+                      for _ in range(num_dense)]
+
+    def fill(self, cur_rows_per_writer, stream=None):
+        p = self.plan
+        cpkv.cpkv_fill_current(p.cur_lens, cur_rows_per_writer, self.staging, page_size=p.page_size,
+                               cp_size=p.cp_size, row_bytes=self.row_bytes, staging_cap_pages=p.staging_cap_pages,
+                               d_staging_rows=p["staging_rows"], d_token_writer_row=p["token_writer_row"],
+                               d_writer=p.d_writer, num_cur_pages=p.C, d_status=p.d_status, stream=stream)
+
+    def gather(self, pools, dense, stream=None):
+        """``pools``: the cp owner slabs [slab_pages, ps, R] of this layer."""
+        p = self.plan
+        table = list(pools) + list(self.staging)
+        caps = [t.shape[0] for t in pools] + [p.staging_cap_pages] * p.cp_size
+        cpkv.cpkv_compose_gather(table, caps, p["owner"], p["src"], dense, page_size=p.page_size,
+                                 cp_size=p.cp_size, row_bytes=self.row_bytes, dense_cap_pages=p.dense_cap_pages,
+                                 d_status=p.d_status, stream=stream)
+
+    def compose_layer(self, layer: int, pools, cur_rows_per_writer, stream=None):
+        """Fill + gather of one layer into the dense buffer of its parity."""
+        dense = self.dense[layer % len(self.dense)]
+        self.fill(cur_rows_per_writer, stream)
+        self.gather(pools, dense, stream)
+        return dense

@@ -1,0 +1,120 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function
+declared in include/cpkv.h, and its host-side sizing and argument checks
+agree with the oracle.  Nothing here launches a kernel."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins as pins
+import workloads as wl
+from paged_kv_cache_compose_gb300 import build as cuda_build
+from paged_kv_cache_compose_gb300 import cpkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return cpkv.load()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"^(?:const\s+char\s*\*|int)\s*(cpkv_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("cpkv_plan_build", "cpkv_fill_current", "cpkv_compose_gather", "cpkv_ragged_plan_build"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert n in cpkv.EXPORTED, n
+    assert lib.cpkv_version() == 1
+
+
+def test_library_targets_sm103a_only():
+    so = cpkv.LIB_PATH
+    assert os.path.exists(so)
+    assert cuda_build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+@pytest.mark.parametrize("batch", pins.edge_batches() + [wl.traced_batch(), wl.fp8_nsa_batch()],
+                         ids=lambda b: b.name)
+def test_sizes_match_oracle(lib, batch):
+    assert cpkv.cpkv_plan_sizes(batch.prefix_lens, batch.cur_lens, batch.page_size) == \
+        oracle.sizes(batch.prefix_lens, batch.cur_lens, batch.page_size)
+    counts = cpkv.cpkv_writer_token_counts(batch.cur_lens, batch.writer, batch.page_size, batch.cp_size)
+    tw = wl.token_writer(batch)
+    assert counts.tolist() == [int((tw == w).sum()) for w in range(batch.cp_size)]
+
+
+@pytest.mark.parametrize("rb", pins.ragged_edge_batches() + [wl.ragged_batch()], ids=lambda r: r.name)
+def test_ragged_sizes_match_oracle(lib, rb):
+    for r in range(rb.cp_size):
+        want = oracle.ragged_plan(rb.prefix_lens, rb.q_lens, rb.cp_index(r), chunk=rb.chunk, k_align=rb.k_align)
+        assert cpkv.cpkv_ragged_plan_sizes(rb.q_lens, rb.cp_index(r), rb.chunk) == (want["S"], want["Q"])
+
+
+def test_host_errors_before_any_launch(lib):
+    pl = np.array([3], np.int32)
+    cl = np.array([4], np.int32)
+    null = None
+    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
+    assert rc == cpkv.CPKV_ERR_UNALIGNED_PREFIX
+    pl = np.array([2], np.int32)
+    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 2, *([null] * 10), null)
+    assert rc == cpkv.CPKV_ERR_CAPACITY
+    rc = lib.cpkv_plan_build(1, 2, 65, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
+    assert rc == cpkv.CPKV_ERR_ARG
+    big = np.zeros(1025, np.int32)
+    rc = lib.cpkv_plan_build(1025, 2, 1, 8, big.ctypes.data, big.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
+    assert rc == cpkv.CPKV_ERR_LIMIT
+    # missing output pointers are reported, not dereferenced
+    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
+    assert rc == cpkv.CPKV_ERR_ARG
+    # fill: row width must be a multiple of 16
+    rc = lib.cpkv_fill_current(1, 2, 1, 100, cl.ctypes.data, *([null] * 3), 5, *([null] * 3), 2, null, null)
+    assert rc == cpkv.CPKV_ERR_ARG
+    # gather: unaligned dense pointer
+    tbl = (ctypes.c_void_p * 2)(16, 32)
+    caps = np.array([1, 1], np.int64)
+    rc = lib.cpkv_compose_gather(2, 1, 64, ctypes.cast(tbl, ctypes.c_void_p), caps.ctypes.data, 64, 64, 1, 8, 64, null)
+    assert rc == cpkv.CPKV_ERR_ARG
+    # ragged: bad chunk / k_align
+    rc = lib.cpkv_ragged_plan_build(1, 0, 1, pl.ctypes.data, cl.ctypes.data, null, 0, null, 0, *([null] * 7), 0,
+                                    null, null, null)
+    assert rc == cpkv.CPKV_ERR_ARG
+
+
+def test_unaligned_prefix_raises_in_binding(lib):
+    with pytest.raises(cpkv.CpkvError) as e:
+        cpkv.cpkv_plan_sizes([5], [3], 4)
+    assert e.value.code == cpkv.CPKV_ERR_UNALIGNED_PREFIX
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.cpkv_error_string(code).startswith(b"CPKV_")
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = cpkv._lib
+    cpkv._lib = None
+    try:
+        with pytest.raises(cpkv.CpkvError):
+            cpkv.load(str(tmp_path / "absent.so"))
+    finally:
+        cpkv._lib = saved

@@ -1,0 +1,246 @@
+"""GPU parity of the compose path (plan, fill, gather) against the CPU oracle.
+
+Every comparison is byte-exact (tolerance 0: the path is integer indexing and
+byte copies).  Inputs are the seeded generators of ``workloads``; expected
+values come only from ``oracle``.  All calls go through the C ABI binding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins as pins
+import workloads as wl
+from paged_kv_cache_compose_gb300 import cpkv
+from paged_kv_cache_compose_gb300.runtime import ComposeLayers, ComposePlan
+
+pytestmark = pytest.mark.gpu
+
+PLAN_KEYS = ("prefix_spans", "cur_spans", "owner", "src", "page_inverse", "staging_page_inverse", "mixed_locs",
+             "staging_rows", "token_writer_row")
+
+
+def _plan_pair(batch, dense_extra=0):
+    T, C, D = oracle.sizes(batch.prefix_lens, batch.cur_lens, batch.page_size)
+    cap = D + dense_extra
+    want = oracle.compose_plan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                               page_size=batch.page_size, cp_size=batch.cp_size,
+                               num_pool_pages=batch.num_pool_pages, dense_cap=cap)
+    plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                       page_size=batch.page_size, cp_size=batch.cp_size, num_pool_pages=batch.num_pool_pages,
+                       dense_cap_pages=cap)
+    # poison outputs so that unwritten entries show up
+    for t in plan.bufs.values():
+        if t.numel():
+            t.fill_(-7)
+    plan.build()
+    torch.cuda.synchronize()
+    return plan, want
+
+
+def _assert_plan_equal(plan, want):
+    assert int(plan.d_status.item()) == want["status"] == 0
+    for k in PLAN_KEYS:
+        got = plan[k].cpu().numpy()
+        assert got.dtype == want[k].dtype, k
+        assert np.array_equal(got.reshape(want[k].shape), want[k]), k
+
+
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_plan_matches_oracle_edge_cases(batch):
+    plan, want = _plan_pair(batch, dense_extra=3)
+    _assert_plan_equal(plan, want)
+
+
+def test_plan_matches_oracle_traced_full_size():
+    plan, want = _plan_pair(wl.traced_batch(), dense_extra=0)
+    _assert_plan_equal(plan, want)
+
+
+def test_plan_matches_oracle_fp8_full_size():
+    plan, want = _plan_pair(wl.fp8_nsa_batch(), dense_extra=5)
+    _assert_plan_equal(plan, want)
+
+
+def test_plan_large_batch_template():
+    """B > 64 takes the 1024-request parameter block."""
+    rng = np.random.default_rng(5)
+    B, ps = 300, 16
+    batch = wl.make_compose_batch("b300", 5, page_size=ps, cp_size=5, num_pool_pages=20000, row_bytes=64,
+                                  prefix_lens=(rng.integers(0, 100, B) // ps) * ps, cur_lens=rng.integers(0, 70, B),
+                                  writer=None, row_kind="bytes")
+    plan, want = _plan_pair(batch, dense_extra=1)
+    _assert_plan_equal(plan, want)
+
+
+def _run_compose(batch, dense_extra=1, guard=0xA5, num_layers=1):
+    """Plan + fill + gather on the GPU with host-generated inputs; returns
+    (dense [host], staging list [host], plan, slabs, rows) for the last layer."""
+    plan, want = _plan_pair(batch, dense_extra)
+    _assert_plan_equal(plan, want)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    for s in layers.staging:
+        s.fill_(guard)
+    for d in layers.dense:
+        d.fill_(0xCD)
+    out = None
+    for layer in range(num_layers):
+        slabs = wl.host_pool(batch, layer)
+        rows = wl.host_current_rows(batch, layer)
+        d_slabs = [torch.from_numpy(s).cuda() for s in slabs]
+        d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+        dense = layers.compose_layer(layer, d_slabs, d_rows)
+        out = (dense, slabs, rows)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    dense, slabs, rows = out
+    return dense.cpu().numpy(), [s.cpu().numpy() for s in layers.staging], plan, slabs, rows
+
+
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_compose_matches_oracle_edge_cases(batch):
+    dense, staging, plan, slabs, rows = _run_compose(batch, dense_extra=2)
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense, want)
+    # staging: defined pages equal the oracle's, every other page keeps its guard bytes
+    ps, R = batch.page_size, batch.row_bytes
+    stg_want = [np.full_like(s, 0xA5) for s in staging]
+    oracle.staging(batch.cur_lens, batch.writer, rows, stg_want, page_size=ps, cp_size=batch.cp_size)
+    for w in range(batch.cp_size):
+        assert np.array_equal(staging[w], stg_want[w]), w
+
+
+def test_compose_tiny_78_layers():
+    """The tiny batch through 78 layers with distinct pools and rows; the two
+    parity buffers hold layers 76 and 77."""
+    batch = wl.tiny_batch()
+    batch.num_layers = 78
+    plan, want = _plan_pair(batch, dense_extra=1)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    kept = {}
+    for layer in range(78):
+        slabs = wl.host_pool(batch, layer)
+        rows = wl.host_current_rows(batch, layer)
+        d_slabs = [torch.from_numpy(s).cuda() for s in slabs]
+        d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+        layers.compose_layer(layer, d_slabs, d_rows)
+        if layer >= 76:
+            kept[layer] = (slabs, rows)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    for layer in (76, 77):
+        slabs, rows = kept[layer]
+        want_dense = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                          page_size=batch.page_size, cp_size=batch.cp_size,
+                                          dense_cap=plan.dense_cap_pages)
+        assert np.array_equal(layers.dense[layer % 2].cpu().numpy(), want_dense), layer
+
+
+def test_gather_random_descriptors_and_sentinels():
+    rng = np.random.default_rng(9)
+    ps, R, cp = 8, 1152, 3
+    caps = [int(x) for x in rng.integers(4, 40, size=2 * cp)]
+    host_tbl = [np.frombuffer(rng.bytes(c * ps * R), np.uint8).copy() for c in caps]
+    n = 500
+    owner = rng.integers(-1, 2 * cp, size=n).astype(np.int32)
+    src = np.array([rng.integers(0, caps[o]) if o >= 0 else 0 for o in owner], np.int32)
+    # a few invalid descriptors
+    owner[7], src[7] = 2 * cp, 0
+    owner[11], src[11] = 1, caps[1]
+    owner[13], src[13] = -3, 0
+    want, st = oracle.gather(host_tbl, caps, owner, src, page_size=ps, row_bytes=R, dense_cap=n)
+    assert st == oracle.DESC_OOB
+    d_tbl = [torch.from_numpy(t).cuda() for t in host_tbl]
+    dense = torch.full((n * ps, R), 0xCD, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_compose_gather(d_tbl, caps, torch.from_numpy(owner).cuda(), torch.from_numpy(src).cuda(), dense,
+                             page_size=ps, cp_size=cp, row_bytes=R, dense_cap_pages=n, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == cpkv.STATUS_DESC_OOB
+    assert np.array_equal(dense.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (1, 16), (3, 48), (128, 1152), (64, 4096)])
+def test_gather_page_geometries(ps, R):
+    """Pages that split into one or several bulk-copy pieces, odd page sizes,
+    and the 656-byte fp8 row."""
+    rng = np.random.default_rng(ps * 1000 + R)
+    cp = 2
+    caps = [9, 7, 5, 6]
+    host_tbl = [np.frombuffer(rng.bytes(c * ps * R), np.uint8).copy() for c in caps]
+    n = 41
+    owner = rng.integers(-1, 2 * cp, size=n).astype(np.int32)
+    src = np.array([rng.integers(0, caps[o]) if o >= 0 else 0 for o in owner], np.int32)
+    want, _ = oracle.gather(host_tbl, caps, owner, src, page_size=ps, row_bytes=R, dense_cap=n)
+    d_tbl = [torch.from_numpy(t).cuda() for t in host_tbl]
+    dense = torch.full((n * ps, R), 0xCD, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_compose_gather(d_tbl, caps, torch.from_numpy(owner).cuda(), torch.from_numpy(src).cuda(), dense,
+                             page_size=ps, cp_size=cp, row_bytes=R, dense_cap_pages=n, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(dense.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("case", ["dup_current", "current_in_prefix", "page_oob", "writer_oob", "page_zero"])
+def test_plan_status_matches_oracle(case):
+    mk = dict(page_size=4, cp_size=2, num_pool_pages=32)
+    if case == "dup_current":
+        args = ([0, 0], [3, 4], [], [5, 5], [0, 1])
+    elif case == "current_in_prefix":
+        args = ([4, 0], [3, 4], [6], [9, 6], [0, 1])
+    elif case == "page_oob":
+        args = ([4, 0], [3, 4], [40], [9, 6], [0, 1])
+    elif case == "writer_oob":
+        args = ([4, 0], [3, 4], [3], [9, 6], [0, 5])
+    else:
+        args = ([4, 0], [3, 4], [0], [9, 6], [0, 1])
+    want = oracle.compose_plan(*args, **mk)
+    plan = ComposePlan(*args, page_size=4, cp_size=2, num_pool_pages=32)
+    plan.build()
+    torch.cuda.synchronize()
+    assert want["status"] != 0
+    assert int(plan.d_status.item()) == want["status"]
+    # descriptors agree too (the offending slot gets owner -1)
+    assert np.array_equal(plan["owner"].cpu().numpy(), want["owner"])
+
+
+def test_fill_row_out_of_range_is_skipped_and_flagged():
+    batch = wl.tiny_batch()
+    plan, _ = _plan_pair(batch)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    rows = wl.host_current_rows(batch)
+    d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+    # writer 0's buffer claims one row fewer than it holds -> its last token is out of range
+    caps = [d_rows[0].shape[0] - 1, d_rows[1].shape[0]]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_fill_current(batch.cur_lens, d_rows, layers.staging, page_size=batch.page_size,
+                           cp_size=batch.cp_size, row_bytes=batch.row_bytes, staging_cap_pages=plan.staging_cap_pages,
+                           d_staging_rows=plan["staging_rows"], d_token_writer_row=plan["token_writer_row"],
+                           d_writer=plan.d_writer, num_cur_pages=plan.C, d_status=status, cur_rows_cap=caps)
+    torch.cuda.synchronize()
+    assert int(status.item()) == cpkv.STATUS_ROW_OOB
+
+
+def test_host_argument_errors_raise():
+    batch = wl.tiny_batch()
+    plan, _ = _plan_pair(batch)
+    with pytest.raises(cpkv.CpkvError) as e:
+        cpkv.cpkv_compose_gather([None] * 4, [1, 1, 1, 1], plan["owner"], plan["src"],
+                                 torch.empty(plan.dense_cap_pages * 16, 1152, dtype=torch.uint8, device="cuda"),
+                                 page_size=16, cp_size=2, row_bytes=1152, dense_cap_pages=plan.dense_cap_pages,
+                                 d_status=plan.d_status)
+    assert e.value.code == cpkv.CPKV_ERR_ARG
+    with pytest.raises(cpkv.CpkvError) as e:
+        cpkv.cpkv_fill_current(batch.cur_lens, [None, None], [None, None], page_size=16, cp_size=2, row_bytes=1000,
+                               staging_cap_pages=10, d_staging_rows=None, d_token_writer_row=None, d_writer=None,
+                               num_cur_pages=plan.C, d_status=plan.d_status, cur_rows_cap=[0, 0])
+    assert e.value.code == cpkv.CPKV_ERR_ARG
+    layers = ComposeLayers(plan, batch.row_bytes)
+    with pytest.raises(cpkv.CpkvError) as e:
+        cpkv.cpkv_fill_current(batch.cur_lens, [None, None], layers.staging, page_size=16, cp_size=2,
+                               row_bytes=1152, staging_cap_pages=plan.C, d_staging_rows=plan["staging_rows"],
+                               d_token_writer_row=plan["token_writer_row"], d_writer=plan.d_writer,
+                               num_cur_pages=plan.C, d_status=plan.d_status, cur_rows_cap=[0, 0])
+    assert e.value.code == cpkv.CPKV_ERR_CAPACITY

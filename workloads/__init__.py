@@ -361,3 +361,42 @@ __all__ = [
     "random_rows", "host_pool", "host_current_rows", "token_writer", "split_rows_by_writer",
     "bf16_bits", "pages_per_len", "describe", "ceil_div",
 ]
+
+
+# ---------------------------------------------------------------------------
+# device-side generation (large configs): seeded torch generators on the GPU
+# ---------------------------------------------------------------------------
+
+def device_random_rows(n_rows: int, row_bytes: int, kind: str, seed, device="cuda"):
+    """[n_rows, row_bytes] uint8 CUDA tensor: bf16 N(0,1) values or uniform bytes."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(np.random.SeedSequence(seed).generate_state(1, np.uint64)[0] & 0x7FFFFFFFFFFFFFFF))
+    if kind == "bf16":
+        x = torch.randn((n_rows, row_bytes // 2), dtype=torch.float32, device=device, generator=g)
+        return x.to(torch.bfloat16).view(torch.uint8).reshape(n_rows, row_bytes)
+    return torch.randint(0, 256, (n_rows, row_bytes), dtype=torch.uint8, device=device, generator=g)
+
+
+def device_pool(batch: ComposeBatch, layer: int = 0, device="cuda"):
+    """Pool slabs of one layer on the GPU: ``cp`` uint8 tensors [slab_pages, ps, R]."""
+    out = []
+    for o in range(batch.cp_size):
+        rows = device_random_rows(batch.slab_pages * batch.page_size, batch.row_bytes, batch.row_kind,
+                                  [batch.seed, 7, layer, o], device)
+        out.append(rows.view(batch.slab_pages, batch.page_size, batch.row_bytes))
+    return out
+
+
+def device_current_rows(batch: ComposeBatch, layer: int = 0, device="cuda"):
+    """Current-token rows of one layer on the GPU in batch order: [T, R] uint8."""
+    return device_random_rows(batch.T, batch.row_bytes, batch.row_kind, [batch.seed, 11, layer], device)
+
+
+def device_split_rows_by_writer(batch: ComposeBatch, rows):
+    """Per-writer compact row buffers (contiguous CUDA tensors), batch order within a writer."""
+    import torch
+
+    tw = torch.from_numpy(token_writer(batch)).to(rows.device)
+    return [rows[tw == w].contiguous() for w in range(batch.cp_size)]
