@@ -26,12 +26,17 @@ class ComposePlan:
         self.B = len(self.prefix_lens)
         self.device = torch.device(device)
         host_writer = np.ascontiguousarray(writer, dtype=np.int32)
-        self.tokens_per_writer = cpkv.cpkv_writer_token_counts(self.cur_lens, host_writer, page_size, cp_size)
+        self.host_writer = host_writer
         self.d_prefix_pages = torch.as_tensor(np.ascontiguousarray(prefix_pages, dtype=np.int32)).to(self.device)
         self.d_cur_pages = torch.as_tensor(np.ascontiguousarray(cur_pages, dtype=np.int32)).to(self.device)
         self.d_writer = torch.as_tensor(host_writer).to(self.device)
         self.bufs = cpkv.plan_buffers(self.B, self.T, self.dense_cap_pages, num_pool_pages, self.device)
         self.d_status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    @property
+    def tokens_per_writer(self):
+        """Rows each writer computes (sizes its current-row buffer)."""
+        return cpkv.cpkv_writer_token_counts(self.cur_lens, self.host_writer, self.page_size, self.cp_size)
 
     def build(self, stream=None):
         cpkv.cpkv_plan_build(self.prefix_lens, self.cur_lens, self.d_prefix_pages, self.d_cur_pages, self.d_writer,

@@ -1,0 +1,109 @@
+"""Full-size parity in the benchmark's launch configuration.
+
+The benchmark's own workload object (same inputs, same CUDA-graph replay of
+plan + ragged plan + 78 x (fill + gather)) is run once, then whole dense
+layers and stagings are compared byte for byte with the oracle.  The oracle
+receives a pool compacted to the pages the batch references (page ids
+relabelled with their owner kept), which leaves every output byte unchanged.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _batch_order_rows(batch, rows_per_writer):
+    tw = wl.token_writer(batch)
+    g = np.empty((batch.T, batch.row_bytes), np.uint8)
+    for w in range(batch.cp_size):
+        g[tw == w] = rows_per_writer[w].cpu().numpy()
+    return g
+
+
+def _check_layer(work, layer):
+    b = work.batch
+    nb, slabs = bench.compact_pool(b, work.pools_of(layer))
+    g = _batch_order_rows(b, work.rows[layer])
+    want = oracle.compose_dense(nb.prefix_lens, nb.cur_lens, nb.prefix_pages, slabs, g, page_size=b.page_size,
+                                cp_size=b.cp_size, dense_cap=work.plan.dense_cap_pages)
+    got = work.layers.dense[layer % 2].cpu().numpy()
+    assert np.array_equal(got, want), f"layer {layer}"
+    return g
+
+
+def _check_staging(work, g):
+    b = work.batch
+    stg = [s.cpu().numpy() for s in work.layers.staging]
+    want = [s.copy() for s in stg]  # undefined pages: whatever is there
+    oracle.staging(b.cur_lens, b.writer, g, want, page_size=b.page_size, cp_size=b.cp_size)
+    for w in range(b.cp_size):
+        assert np.array_equal(stg[w], want[w]), w
+
+
+def _check_plan(work):
+    b = work.batch
+    want = oracle.compose_plan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer,
+                               page_size=b.page_size, cp_size=b.cp_size, num_pool_pages=b.num_pool_pages,
+                               dense_cap=work.plan.dense_cap_pages)
+    for k in ("owner", "src", "page_inverse", "staging_page_inverse", "mixed_locs", "staging_rows",
+              "token_writer_row", "prefix_spans", "cur_spans"):
+        assert np.array_equal(work.plan[k].cpu().numpy().reshape(want[k].shape), want[k]), k
+    rb = work.rb
+    wr = oracle.ragged_plan(rb.prefix_lens, rb.q_lens, work.cp_index, chunk=rb.chunk, k_align=rb.k_align)
+    assert work.ragged_counts.cpu().tolist() == [wr["S"], wr["Q"]]
+    for k in ("seg_req", "kv_lens", "q_starts", "q_lens", "k_bases", "q_bases", "current_bases"):
+        assert np.array_equal(work.ragged_out[k].cpu().numpy()[:wr["S"]], wr[k]), k
+    assert np.array_equal(work.ragged_out["topk_offsets"].cpu().numpy()[:wr["Q"]], wr["topk_offsets"])
+
+
+@pytest.mark.parametrize("config", ["traced_78", "fp8_nsa"])
+def test_benchmark_workload_matches_oracle(config):
+    work = bench.ComposeWorkload(config)
+    try:
+        for d in work.layers.dense:
+            d.fill_(0xCD)
+        work.capture()  # warm-up step + capture, as the benchmark does
+        for d in work.layers.dense:
+            d.fill_(0xCD)
+        work.run()
+        torch.cuda.synchronize()
+        assert work.status() == 0
+        _check_plan(work)
+        _check_layer(work, work.num_layers - 2)
+        g = _check_layer(work, work.num_layers - 1)
+        _check_staging(work, g)
+    finally:
+        del work
+        gc.collect()
+        torch.cuda.empty_cache()
+
+
+def test_traced_single_layer_full_pool():
+    """The traced batch against its 200 000-page pool (one layer)."""
+    from paged_kv_cache_compose_gb300.runtime import ComposeLayers, ComposePlan
+
+    b = wl.traced_batch()
+    plan = ComposePlan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer, page_size=b.page_size,
+                       cp_size=b.cp_size, num_pool_pages=b.num_pool_pages, dense_cap_pages=None)
+    plan.build()
+    layers = ComposeLayers(plan, b.row_bytes)
+    pools = wl.device_pool(b, 0)
+    g_dev = wl.device_current_rows(b, 0)
+    rows = wl.device_split_rows_by_writer(b, g_dev)
+    dense = layers.compose_layer(0, pools, rows)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    nb, slabs = bench.compact_pool(b, pools)
+    want = oracle.compose_dense(nb.prefix_lens, nb.cur_lens, nb.prefix_pages, slabs, g_dev.cpu().numpy(),
+                                page_size=b.page_size, cp_size=b.cp_size)
+    assert np.array_equal(dense.cpu().numpy(), want)
+    del pools, rows, g_dev, layers, plan
+    gc.collect()
+    torch.cuda.empty_cache()
