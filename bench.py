@@ -140,7 +140,7 @@ class ComposeWorkload:
     """Device state of one benchmark replica: batch metadata, plan, pools,
     per-layer current rows, stagings, dense double buffer, ragged plan."""
 
-    def __init__(self, config: str = "traced_78", device="cuda"):
+    def __init__(self, config: str = "traced_78", device="cuda", num_layers: int | None = None):
         import torch
 
         from paged_kv_cache_compose_gb300 import cpkv
@@ -149,7 +149,7 @@ class ComposeWorkload:
         self.torch, self.cpkv = torch, cpkv
         self.config = config
         self.batch = b = wl.CONFIGS[config]()
-        self.num_layers = b.num_layers
+        self.num_layers = b.num_layers if num_layers is None else min(num_layers, b.num_layers)
         self.device = torch.device(device)
         self.plan = ComposePlan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer,
                                 page_size=b.page_size, cp_size=b.cp_size, num_pool_pages=b.num_pool_pages,
@@ -159,10 +159,20 @@ class ComposeWorkload:
         self.shared_pool = config.startswith("fp8")
         n_pools = 1 if self.shared_pool else self.num_layers
         self.pools = [wl.device_pool(b, layer, self.device) for layer in range(n_pools)]
+        # all layers' current rows in one allocation, writer-major inside a layer,
+        # so the end-to-end leg can upload them with one copy
+        counts = [int(x) for x in self.plan.tokens_per_writer]
+        self.rows_all = torch.empty((self.num_layers, b.T, b.row_bytes), dtype=torch.uint8, device=self.device)
         self.rows = []
         for layer in range(self.num_layers):
             g = wl.device_current_rows(b, layer, self.device)
-            self.rows.append(wl.device_split_rows_by_writer(b, g))
+            views, off = [], 0
+            for w, part in enumerate(wl.device_split_rows_by_writer(b, g)):
+                dst = self.rows_all[layer, off:off + counts[w]]
+                dst.copy_(part)
+                views.append(dst)
+                off += counts[w]
+            self.rows.append(views)
             del g
         # ragged index plan of CP rank 0 over the batch's q tokens
         self.rb = wl.ragged_from_compose(b)
@@ -178,29 +188,40 @@ class ComposeWorkload:
     def pools_of(self, layer):
         return self.pools[0 if self.shared_pool else layer]
 
-    def step(self, stream=None, events=None):
-        """Enqueue one step on the current stream; ``events`` (optional) gets
-        (kind, start, end) event pairs around every fill and gather."""
-        torch = self.torch
+    def step(self, stream=None):
+        """Enqueue one step on the current stream."""
         self.plan.build(stream)
         self.cpkv.cpkv_ragged_plan_build(self.rb.prefix_lens, self.rb.q_lens, self.d_cp_index, len(self.cp_index),
                                          chunk=self.rb.chunk, k_align=self.rb.k_align, out=self.ragged_out,
                                          d_counts=self.ragged_counts, d_status=self.plan.d_status, stream=stream)
         for layer in range(self.num_layers):
-            dense = self.layers.dense[layer % 2]
-            if events is None:
-                self.layers.fill(self.rows[layer], stream)
-                self.layers.gather(self.pools_of(layer), dense, stream)
-            else:
-                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-                e[0].record()
-                self.layers.fill(self.rows[layer], stream)
-                e[1].record()
-                e[2].record()
-                self.layers.gather(self.pools_of(layer), dense, stream)
-                e[3].record()
-                events.append(("fill", e[0], e[1]))
-                events.append(("gather", e[2], e[3]))
+            self.layers.fill(self.rows[layer], stream)
+            self.layers.gather(self.pools_of(layer), self.layers.dense[layer % 2], stream)
+
+    def kernel_graphs(self):
+        """Two more CUDA graphs: the step's fills alone and its gathers alone
+        (same inputs, same launch shapes), to time each kernel's launches."""
+        torch = self.torch
+        graphs = {}
+        for kind in ("fill", "gather"):
+            def body(kind=kind):
+                for layer in range(self.num_layers):
+                    if kind == "fill":
+                        self.layers.fill(self.rows[layer])
+                    else:
+                        self.layers.gather(self.pools_of(layer), self.layers.dense[layer % 2])
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                body()
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body()
+            graphs[kind] = g
+        torch.cuda.synchronize()
+        return graphs
 
     def capture(self):
         """Capture one step as a CUDA graph (after a warm-up run)."""
@@ -362,7 +383,7 @@ def time_oracle(b, pools, rows, min_seconds=10.0, max_seconds=30.0):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="traced_78", choices=["traced_78", "fp8_nsa"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -370,6 +391,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's bounded sample")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers (small cases for profiling; the headline uses all 78)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
 
@@ -390,7 +413,7 @@ def main(argv=None):
     from paged_kv_cache_compose_gb300 import build as cpkv_build
 
     cpkv_build.build()
-    work = ComposeWorkload(a.config, device=device)
+    work = ComposeWorkload(a.config, device=device, num_layers=a.layers)
     hbm_peak, peak_src, _ = read_peaks()
 
     # warm-up (also the first use of every kernel), then capture
@@ -424,16 +447,23 @@ def main(argv=None):
     ms_step = ms_max / a.steps
     value_gbs = units_all / (ms_max / 1e3) / 1e9
 
-    # per-kernel durations with events around every fill and gather (one more pass, not graphed)
-    kern = {"fill": [], "gather": []}
-    for _ in range(2):
-        evs = []
-        work.step(events=evs)
+    # per-kernel average launch durations: CUDA events around replays of a
+    # graph holding the step's 78 launches of that kernel alone
+    graphs = work.kernel_graphs()
+    kern = {}
+    for kind, g in graphs.items():
+        g.replay()
         torch.cuda.synchronize()
-        for kind, s, e in evs:
-            kern[kind].append(s.elapsed_time(e))
-    gather_ms = statistics.mean(kern["gather"])
-    fill_ms = statistics.mean(kern["fill"])
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, a.steps // 4)
+        k0.record()
+        for _ in range(reps):
+            g.replay()
+        k1.record()
+        torch.cuda.synchronize()
+        kern[kind] = k0.elapsed_time(k1) / (reps * work.num_layers)
+    gather_ms = kern["gather"]
+    fill_ms = kern["fill"]
     gather_gbs = work.bytes["gather"] / (gather_ms / 1e3) / 1e9
     fill_gbs = work.bytes["fill"] / (fill_ms / 1e3) / 1e9
     status = work.status()
@@ -526,20 +556,17 @@ def run_e2e(work, a, ws):
     h_meta = [torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
               for x in (b.prefix_pages, b.cur_pages, b.writer)]
     d_meta = [work.plan.d_prefix_pages, work.plan.d_cur_pages, work.plan.d_writer]
-    h_rows = [[r.cpu().pin_memory() for r in layer] for layer in work.rows]
+    h_rows = work.rows_all.cpu().pin_memory()
     h_out = torch.empty(1, dtype=torch.int32).pin_memory()
     h_cnt = torch.empty(2, dtype=torch.int64).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in h_meta) + sum(r.numel() for layer in h_rows for r in layer)
+    h2d = sum(x.numel() * x.element_size() for x in h_meta) + h_rows.numel()
     d2h = h_out.numel() * 4 + h_cnt.numel() * 8
 
     def one():
         for h, d in zip(h_meta, d_meta):
             if h.numel():
                 d.copy_(h, non_blocking=True)
-        for layer in range(work.num_layers):
-            for h, d in zip(h_rows[layer], work.rows[layer]):
-                if h.numel():
-                    d.copy_(h, non_blocking=True)
+        work.rows_all.copy_(h_rows, non_blocking=True)
         work.run()
         h_out.copy_(work.plan.d_status, non_blocking=True)
         h_cnt.copy_(work.ragged_counts, non_blocking=True)
