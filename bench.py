@@ -66,6 +66,32 @@ def layer_bytes(prefix_lens, cur_lens, page_size, row_bytes, dense_cap_pages):
     }
 
 
+def kernel_source_sha(files) -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_cache_compose_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def gather_traffic(config: str):
+    """DRAM bytes per gather launch from the committed ncu capture, or None
+    when there is none for this workload or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", f"gather_traffic_{config}.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_sha") != kernel_source_sha(["gather.cu", "common.cuh"]):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -468,14 +494,7 @@ def main(argv=None):
     fill_gbs = work.bytes["fill"] / (fill_ms / 1e3) / 1e9
     status = work.status()
 
-    traffic = None
-    prof_path = os.path.join(ROOT, "profiles", f"gather_traffic_{a.config}.json")
-    if os.path.exists(prof_path):
-        try:
-            with open(prof_path) as f:
-                traffic = json.load(f).get("dram_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = gather_traffic(a.config)
 
     # end to end through the public API with host buffers
     e2e = None

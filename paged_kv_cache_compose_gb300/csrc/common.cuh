@@ -34,6 +34,36 @@ CPKV_DEV void st_stream16(void *p, uint4 v) {
                : "memory");
 }
 
+// L2 eviction-priority policies (createpolicy) and 16-byte ops that carry one.
+// Data read or written exactly once is marked evict_first so it does not push
+// out lines that the next kernel still needs (the staging written by the fill
+// and read by the gather).
+CPKV_DEV uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+CPKV_DEV uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+CPKV_DEV uint4 ld_stream16_hint(const void *p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+CPKV_DEV void st16_hint(void *p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // shared-memory addresses, mbarriers and bulk async copies (TMA, non-tensor)
 // ---------------------------------------------------------------------------
@@ -103,6 +133,21 @@ CPKV_DEV void bulk_load_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, ui
 CPKV_DEV void bulk_store_s2g(void *gdst, const void *smem_src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
                "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+// The same two copies with an L2 cache policy.
+CPKV_DEV void bulk_load_g2s_hint(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+CPKV_DEV void bulk_store_s2g_hint(void *gdst, const void *smem_src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+               "r"(smem_addr(smem_src)), "r"(bytes), "l"(pol)
                : "memory");
 }
 

@@ -4,9 +4,12 @@
 // message of commits 0d87bc5: rows are opaque bytes).
 //
 // One launch.  Blocks [0, nRow) copy rows: one warp per token row, each lane
-// moving 16-byte vectors, ROWS rows in flight per warp (all loads issued
-// before the stores).  Blocks [nRow, nRow + B) zero the pad rows after each
-// request's last token, up to the end of its staging page.
+// moving 16-byte vectors, kRowsInFlight rows in flight per warp (all loads
+// issued before the stores); the grid is one resident wave.  Blocks
+// [nRow, nRow + B) zero the pad rows after each request's last token, up to
+// the end of its staging page.  Current rows are read once (L2 evict_first);
+// staging rows are written with evict_last because the gather that follows
+// reads them back.
 #include <stdint.h>
 
 #include "common.cuh"
@@ -18,6 +21,7 @@ constexpr int kFillThreads = 256;
 constexpr int kWarpsPerBlock = kFillThreads / 32;
 constexpr int kRowsInFlight = 2;   // rows per warp per iteration
 constexpr int kVecPerLane = 4;     // 16-byte vectors per lane per row in the fast path (R <= 2048)
+constexpr int kBlocksPerSm = 4;    // one resident wave (64 registers x 256 threads x 4 = 64K)
 
 template <int MAXB>
 struct FillParams {
@@ -68,6 +72,8 @@ __device__ void copy_rows(const FillParams<MAXB> &p) {
   const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)p.nRow * kWarpsPerBlock;
   const int vpr = p.vpr;
+  const uint64_t read_once = l2_policy_evict_first();
+  const uint64_t keep = l2_policy_evict_last();
   if (vpr <= 32 * kVecPerLane) {
     for (int64_t t0 = warp_id * kRowsInFlight; t0 < p.T; t0 += nwarps * kRowsInFlight) {
       RowJob job[kRowsInFlight];
@@ -81,7 +87,7 @@ __device__ void copy_rows(const FillParams<MAXB> &p) {
 #pragma unroll
         for (int k = 0; k < kVecPerLane; ++k) {
           const int c = lane + 32 * k;
-          if (job[r].src != nullptr && c < vpr) v[r][k] = ld_stream16(job[r].src + 16 * (int64_t)c);
+          if (job[r].src != nullptr && c < vpr) v[r][k] = ld_stream16_hint(job[r].src + 16 * (int64_t)c, read_once);
         }
       }
 #pragma unroll
@@ -89,7 +95,7 @@ __device__ void copy_rows(const FillParams<MAXB> &p) {
 #pragma unroll
         for (int k = 0; k < kVecPerLane; ++k) {
           const int c = lane + 32 * k;
-          if (job[r].src != nullptr && c < vpr) st_stream16(job[r].dst + 16 * (int64_t)c, v[r][k]);
+          if (job[r].src != nullptr && c < vpr) st16_hint(job[r].dst + 16 * (int64_t)c, v[r][k], keep);
         }
       }
     }
@@ -97,7 +103,8 @@ __device__ void copy_rows(const FillParams<MAXB> &p) {
     for (int64_t t = warp_id; t < p.T; t += nwarps) {
       const RowJob job = resolve_row(p, t);
       if (job.src == nullptr) continue;
-      for (int c = lane; c < vpr; c += 32) st_stream16(job.dst + 16 * (int64_t)c, ld_stream16(job.src + 16 * (int64_t)c));
+      for (int c = lane; c < vpr; c += 32)
+        st16_hint(job.dst + 16 * (int64_t)c, ld_stream16_hint(job.src + 16 * (int64_t)c, read_once), keep);
     }
   }
 }
@@ -130,7 +137,8 @@ __device__ void zero_pad_rows(const FillParams<MAXB> &p, int b) {
   uint8_t *base = p.staging[w] + first * p.R;
   const int64_t nvec = (end - first) * p.vpr;
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int64_t i = threadIdx.x; i < nvec; i += kFillThreads) st_stream16(base + 16 * i, z);
+  const uint64_t keep = l2_policy_evict_last();
+  for (int64_t i = threadIdx.x; i < nvec; i += kFillThreads) st16_hint(base + 16 * i, z, keep);
 }
 
 template <int MAXB>
@@ -175,7 +183,7 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
 
   const int64_t row_warps = ceil_div(T, kRowsInFlight);
   const int64_t row_blocks_needed = ceil_div(row_warps, kWarpsPerBlock);
-  const int64_t row_blocks_cap = (int64_t)device_sm_count() * (2048 / kFillThreads);
+  const int64_t row_blocks_cap = (int64_t)device_sm_count() * kBlocksPerSm;
   const int nRow = (int)(row_blocks_needed < row_blocks_cap ? row_blocks_needed : row_blocks_cap);
 
 #define CPKV_FILL_FILL(prm)                                                                  \

@@ -7,13 +7,18 @@
 // source page, so the kernel moves pages with bulk async copies (TMA,
 // non-tensor form): global -> shared with mbarrier completion, then
 // shared -> global tracked by bulk groups.  Each page is cut into `pieces`
-// equal 16-byte-multiple units; units are dealt round-robin to a persistent
-// grid of one-warp CTAs (several per SM), each running an S-stage ring:
-// while one unit is being stored the next S-1 loads are in flight.  Zero
-// units (owner -1 or an invalid descriptor) are written with plain 16-byte
-// stores by the whole warp.  Every mbarrier wait is bounded; on a timeout the
-// kernel raises CPKV_STATUS_TIMEOUT, stops issuing, drains what it issued
-// (bounded again) and returns.
+// equal 16-byte-multiple units (<= 24 KB); units are dealt round-robin to a
+// persistent grid of one-warp CTAs, two per SM.  Each CTA runs a ring of
+// kStages shared-memory stages with at most kLoadsInFlight loads
+// outstanding, so the remaining stages hold stores still draining: loads
+// and stores overlap instead of a stage waiting for its own store.  Every
+// copy carries an L2 evict_first policy: pool pages, staging pages and dense
+// pages are each touched once per layer, and streaming them must not evict
+// the staging the fill has just written for this gather.  Zero units (owner
+// -1 or an invalid descriptor) are written with plain 16-byte stores by the
+// whole warp.  Every mbarrier wait is bounded; on a timeout the kernel raises
+// CPKV_STATUS_TIMEOUT, stops issuing, drains what it issued (bounded again)
+// and returns.
 #include <stdint.h>
 
 #include "common.cuh"
@@ -22,6 +27,8 @@ namespace cpkv {
 namespace {
 
 constexpr int kStages = 4;
+constexpr int kLoadsInFlight = 2;
+constexpr int kCtasPerSm = 2;
 constexpr int kMaxPieceBytes = 24 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a page load takes microseconds
 
@@ -76,6 +83,7 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
 
   int64_t head = 0, tail = 0;  // consumed / issued copy units (uniform across the warp)
   bool dead = false;           // a bounded wait gave up (lane 0 only)
+  const uint64_t stream_once = l2_policy_evict_first();
 
   // consume the oldest in-flight copy unit: wait for its load, store it.
   // A load that was issued is always waited for (bounded), even after a
@@ -93,7 +101,7 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
         }
       }
       if (landed && !dead) {
-        bulk_store_s2g(ring_dst[s], smem + (size_t)s * p.piece_bytes, ring_bytes[s]);
+        bulk_store_s2g_hint(ring_dst[s], smem + (size_t)s * p.piece_bytes, ring_bytes[s], stream_once);
       }
       bulk_commit();
     }
@@ -107,7 +115,7 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
       for (uint32_t i = lane; i < x.bytes / 16; i += 32) st_stream16(x.dst + 16 * (size_t)i, z);
       continue;
     }
-    if (tail - head == kStages) consume();
+    if (tail - head == kLoadsInFlight) consume();
     const int s = (int)(tail % kStages);
     if (lane == 0) {
       if (tail >= kStages) bulk_wait_read_dyn((int)(head - tail + kStages - 1));  // stage's last store has read smem
@@ -117,7 +125,7 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
         ring_bytes[s] = x.bytes;
         ring_live[s] = 1;
         mbar_arrive_expect_tx(&full[s], x.bytes);
-        bulk_load_g2s(smem + (size_t)s * p.piece_bytes, x.src, x.bytes, &full[s]);
+        bulk_load_g2s_hint(smem + (size_t)s * p.piece_bytes, x.src, x.bytes, &full[s], stream_once);
       }
     }
     ++tail;
@@ -177,9 +185,8 @@ extern "C" int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes
       return CPKV_ERR_CUDA;
     configured[dev] = 1;
   }
-  // One-warp CTAs; shared memory bounds residency (~227 KB per SM).
-  const int per_sm = (int)(220 * 1024 / (smem + 256));
-  const int64_t cap = (int64_t)device_sm_count() * (per_sm > 0 ? per_sm : 1);
+  // One-warp CTAs, kCtasPerSm per SM (4 loads of <= 24 KB in flight per SM).
+  const int64_t cap = (int64_t)device_sm_count() * kCtasPerSm;
   const int grid = (int)(prm.units < cap ? prm.units : cap);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   gather_pages_kernel<<<grid, 32, smem, s>>>(prm);
