@@ -63,6 +63,8 @@ def layer_bytes(prefix_lens, cur_lens, page_size, row_bytes, dense_cap_pages):
         "gather_write": gather_write, "fill": fill_read + fill_write, "gather": gather_read + gather_write,
         "total": fill_read + fill_write + gather_read + gather_write,
         "single_pass_ideal": T * R + int((pl // ps).sum()) * ps * R + D * ps * R, "T": T, "D": D, "pad_rows": pad,
+        # one-pass compose: current rows and prefix pages read once, every dense slot written once
+        "fused": T * R + int((pl // ps).sum()) * ps * R + dense_cap_pages * ps * R,
     }
 
 
@@ -166,7 +168,8 @@ class ComposeWorkload:
     """Device state of one benchmark replica: batch metadata, plan, pools,
     per-layer current rows, stagings, dense double buffer, ragged plan."""
 
-    def __init__(self, config: str = "traced_78", device="cuda", num_layers: int | None = None):
+    def __init__(self, config: str = "traced_78", device="cuda", num_layers: int | None = None,
+                 variant: str = "staging"):
         import torch
 
         from paged_kv_cache_compose_gb300 import cpkv
@@ -209,7 +212,17 @@ class ComposeWorkload:
         self.ragged_counts = torch.zeros(2, dtype=torch.int64, device=self.device)
         self.bytes = layer_bytes(b.prefix_lens, b.cur_lens, b.page_size, b.row_bytes, self.plan.dense_cap_pages)
         self.graph = None
-        self.launches_per_step = 3 + 2 * self.num_layers  # plan (2) + ragged (1) + (fill + gather) per layer
+        self.variant = variant
+        if variant == "staging":
+            self.launches_per_step = 3 + 2 * self.num_layers  # plan (2) + ragged (1) + (fill + gather) per layer
+            self.layer_bytes = self.bytes["total"]
+            self.kernels = {"gather": self.bytes["gather"], "fill": self.bytes["fill"]}
+        elif variant == "fused":
+            self.launches_per_step = 3 + self.num_layers  # plan (2) + ragged (1) + one fused compose per layer
+            self.layer_bytes = self.bytes["fused"]
+            self.kernels = {"fused": self.bytes["fused"]}
+        else:
+            raise ValueError(variant)
 
     def pools_of(self, layer):
         return self.pools[0 if self.shared_pool else layer]
@@ -221,21 +234,28 @@ class ComposeWorkload:
                                          chunk=self.rb.chunk, k_align=self.rb.k_align, out=self.ragged_out,
                                          d_counts=self.ragged_counts, d_status=self.plan.d_status, stream=stream)
         for layer in range(self.num_layers):
+            self.run_kernel("all", layer, stream)
+
+    def run_kernel(self, kind, layer, stream=None):
+        """Launch one layer's work: ``all`` of it, or one kernel of it."""
+        dense = self.layers.dense[layer % 2]
+        if self.variant == "fused":
+            self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream)
+            return
+        if kind in ("all", "fill"):
             self.layers.fill(self.rows[layer], stream)
-            self.layers.gather(self.pools_of(layer), self.layers.dense[layer % 2], stream)
+        if kind in ("all", "gather"):
+            self.layers.gather(self.pools_of(layer), dense, stream)
 
     def kernel_graphs(self):
         """Two more CUDA graphs: the step's fills alone and its gathers alone
         (same inputs, same launch shapes), to time each kernel's launches."""
         torch = self.torch
         graphs = {}
-        for kind in ("fill", "gather"):
+        for kind in self.kernels:
             def body(kind=kind):
                 for layer in range(self.num_layers):
-                    if kind == "fill":
-                        self.layers.fill(self.rows[layer])
-                    else:
-                        self.layers.gather(self.pools_of(layer), self.layers.dense[layer % 2])
+                    self.run_kernel(kind, layer)
             s = torch.cuda.Stream()
             s.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(s):
@@ -413,6 +433,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="traced_78", choices=["traced_78", "fp8_nsa"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variant", default="staging", choices=["staging", "fused"],
+                    help="staging: fill + slot-dense gather per layer (the pages' method); "
+                         "fused: one-pass single-GPU compose without the staging round trip")
     ap.add_argument("--no-graph", action="store_true", help="launch layer by layer instead of replaying a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -439,7 +462,7 @@ def main(argv=None):
     from paged_kv_cache_compose_gb300 import build as cpkv_build
 
     cpkv_build.build()
-    work = ComposeWorkload(a.config, device=device, num_layers=a.layers)
+    work = ComposeWorkload(a.config, device=device, num_layers=a.layers, variant=a.variant)
     hbm_peak, peak_src, _ = read_peaks()
 
     # warm-up (also the first use of every kernel), then capture
@@ -469,7 +492,7 @@ def main(argv=None):
         torch.distributed.barrier()
     clk = clocks.stop()
     ms_total = e0.elapsed_time(e1)
-    ms_max, units_all = aggregate(ms_total, work.bytes["total"] * work.num_layers * a.steps, ws)
+    ms_max, units_all = aggregate(ms_total, work.layer_bytes * work.num_layers * a.steps, ws)
     ms_step = ms_max / a.steps
     value_gbs = units_all / (ms_max / 1e3) / 1e9
 
@@ -488,13 +511,11 @@ def main(argv=None):
         k1.record()
         torch.cuda.synchronize()
         kern[kind] = k0.elapsed_time(k1) / (reps * work.num_layers)
-    gather_ms = kern["gather"]
-    fill_ms = kern["fill"]
-    gather_gbs = work.bytes["gather"] / (gather_ms / 1e3) / 1e9
-    fill_gbs = work.bytes["fill"] / (fill_ms / 1e3) / 1e9
+    kgbs = {k: work.kernels[k] / (kern[k] / 1e3) / 1e9 for k in kern}
+    top = "fused" if work.variant == "fused" else "gather"
     status = work.status()
 
-    traffic = gather_traffic(a.config)
+    traffic = gather_traffic(a.config) if top == "gather" else None
 
     # end to end through the public API with host buffers
     e2e = None
@@ -533,7 +554,8 @@ def main(argv=None):
                          "cp=8, 656-byte rows, one 2^20-page pool shared by the layers"),
             "B": b.B, "T": b.T, "C": work.plan.C, "D": work.plan.D, "layers": work.num_layers,
             "page_size": b.page_size, "cp_size": b.cp_size, "row_bytes": b.row_bytes,
-            "bytes_per_layer": work.bytes["total"], "single_pass_ideal_bytes_per_layer": work.bytes["single_pass_ideal"],
+            "variant": work.variant,
+            "bytes_per_layer": work.layer_bytes, "single_pass_ideal_bytes_per_layer": work.bytes["single_pass_ideal"],
             "l2": "inputs larger than L2: every layer reads its own pool slab and rows (%.1f GB per step)" % (
                 (sum(s.numel() for p in work.pools for s in p) + sum(r.numel() for rr in work.rows for r in rr)) / 1e9),
             "cuda_graph": not a.no_graph,
@@ -541,17 +563,19 @@ def main(argv=None):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "gather_pages_kernel (cpkv_compose_gather)",
-            "achieved": round(gather_gbs, 1),
+            "kernel": ("gather_pages_kernel (cpkv_compose_gather)" if top == "gather"
+                       else "compose_fused_kernel (cpkv_compose_fused)"),
+            "achieved": round(kgbs[top], 1),
             "peak": hbm_peak,
             "peak_source": peak_src,
             "unit": "GB/s",
-            "frac": round(gather_gbs / hbm_peak, 4),
+            "frac": round(kgbs[top] / hbm_peak, 4),
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": work.bytes["gather"],
-            "avg_launch_ms": round(gather_ms, 5),
-            "fill": {"achieved": round(fill_gbs, 1), "frac": round(fill_gbs / hbm_peak, 4),
-                     "avg_launch_ms": round(fill_ms, 5), "algorithmic_bytes_per_launch": work.bytes["fill"]},
+            "algorithmic_bytes_per_launch": work.kernels[top],
+            "avg_launch_ms": round(kern[top], 5),
+            **{k: {"achieved": round(kgbs[k], 1), "frac": round(kgbs[k] / hbm_peak, 4),
+                   "avg_launch_ms": round(kern[k], 5), "algorithmic_bytes_per_launch": work.kernels[k]}
+               for k in kern if k != top},
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -600,7 +624,7 @@ def run_e2e(work, a, ws):
     for _ in range(steps):
         one()
     el = time.perf_counter() - t0
-    ms_max, units_all = aggregate(el * 1e3, work.bytes["total"] * work.num_layers * steps, ws)
+    ms_max, units_all = aggregate(el * 1e3, work.layer_bytes * work.num_layers * steps, ws)
     return {"value": round(units_all / (ms_max / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms_max / steps, 3), "steps": steps}
 

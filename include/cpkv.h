@@ -26,8 +26,8 @@
  *     over a concatenated 2*cp source-pointer table fills every dense page;
  *     mixed_locs / staging rows are layer-invariant and computed once per
  *     batch; the per-layer fill is a single index copy.
- *   "touched-pages staging" message (same page): a staging slot is the
- *     page's batch current index; staging is sized by current pages only.
+ *   "touched-pages staging" message (same page): a page's staging slot is
+ *     its index among the batch's current pages; staging is sized by current pages only.
  *   "prefetch staging" message of commits 0d87bc5 (python): staging row 0 is
  *     reserved, current page i sits at slot i + 1; page id 0 is the dummy.
  *   "compose_v2" message (commits d63fbd4): an owner of -1 zero-fills.
@@ -85,9 +85,9 @@ typedef struct {
 /*
  * cpkv_plan_sizes — T, C and D of a batch (host only, no GPU work).
  * h_prefix_lens, h_cur_lens: host int32 [B], non-negative; prefix lengths
- * must be multiples of page_size ("a chunked prefix that is not page-aligned
- * keeps its batch solo ... the CP page-aligned split would fail-fast",
- * chunked-prefill message of commits 0d87bc5).
+ * must be multiples of page_size (the chunked-prefill message of commits
+ * 0d87bc5 keeps unaligned prefixes out of multi-request batches because the
+ * page-aligned CP split rejects them).
  * Returns CPKV_ERR_UNALIGNED_PREFIX for an unaligned prefix, CPKV_ERR_ARG for
  * B < 0, page_size <= 0, a negative length or a null pointer (B > 0),
  * CPKV_ERR_LIMIT when T, C or D would not fit int32 indices.
@@ -147,9 +147,9 @@ int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
 
 /*
  * cpkv_fill_current — per layer: write every current row into its writer's
- * staging ("the per-layer fill collapses to a single index_copy_ into the
- * zeroed staging span"; fp8 rows are handled as bytes, "fp8 -> uint8"
- * message of commits 0d87bc5).
+ * staging.  In the "staging-direct compose" message this is one index copy
+ * per layer with layer-invariant row indices; rows are opaque bytes, so fp8
+ * needs nothing special ("fp8 -> uint8" message of commits 0d87bc5).
  *
  * For every token t with writer w = d_writer[d_staging_rows[t] / ps - 1]:
  *   staging[w] row d_staging_rows[t]  <-  cur_rows[w] row d_token_writer_row[t]
@@ -193,6 +193,33 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
                         const void *const *h_src_table, const int64_t *h_src_cap_pages,
                         const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
                         void *d_dense, int32_t *d_status, cpkv_stream_t stream);
+
+/*
+ * cpkv_compose_fused — per layer: the single-GPU compose in one pass, without
+ * the staging round trip.  The staging exchange ("staging-direct compose")
+ * carries current pages between GPUs; when every writer region is on this
+ * GPU a current page can be copied straight from its writer's current-row
+ * buffer.  Output is byte-identical to cpkv_fill_current followed by
+ * cpkv_compose_gather, with the same descriptors:
+ *   owner -1      -> zeros
+ *   owner r < cp  -> page src of h_pools[r]
+ *   owner cp + w  -> current page i = src - 1: the n_i consecutive rows of
+ *                    h_cur_rows[w] starting at d_token_writer_row of the page's
+ *                    first token, then ps - n_i zero rows
+ * A descriptor outside these ranges (or rows outside the buffer) raises
+ * DESC_OOB and its page is zero-filled.
+ *   h_cur_lens       host int32 [B]
+ *   h_pools          host array [cp] of device pointers, page arrays
+ *                    [h_pool_cap_pages[r]][ps][R], 16-byte aligned
+ *   h_cur_rows       host array [cp] of device pointers, [h_cur_rows_cap[w]][R]
+ *   d_owner, d_src, d_token_writer_row: from cpkv_plan_build
+ *   d_dense          device [dense_cap_pages * ps][R], 16-byte aligned
+ */
+int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
+                       const void *const *h_pools, const int64_t *h_pool_cap_pages,
+                       const void *const *h_cur_rows, const int64_t *h_cur_rows_cap, const int32_t *d_owner,
+                       const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
+                       void *d_dense, int32_t *d_status, cpkv_stream_t stream);
 
 /*
  * cpkv_ragged_plan_sizes — exact segment count S and q-token count Q_r of a

@@ -9,14 +9,15 @@
  * Sources (commit-log pages of an SGLang fork; no code is printed there):
  *   [A] commits d63fbd4 (test/manual), "staging-direct compose" message:
  *       current rows are written into a slot-ordered staging through a
- *       staging-remapped page inverse; ONE slot-dense gather over a
- *       concatenated 2*cp pointer table fills every dense page slot; current
- *       slots carry owner = cp_size + writer and src = staging slot;
+ *       staging-remapped page inverse; ONE slot-dense gather over one
+ *       pointer table of 2*cp sources fills every dense page slot; the
+ *       descriptor of a current page names its writer's staging (owner
+ *       cp + writer) and its slot there (src);
  *       mixed_locs / staging row indices are computed once per batch and the
  *       per-layer fill is a single index copy into the zeroed staging.
- *   [B] same page, "touched-pages staging" message: the staging holds one
- *       round of current pages in merged-span order; a page's slot is its
- *       batch current index, identical on every rank.
+ *   [B] same page, "touched-pages staging" message: the staging keeps only the
+ *       current pages of one batch, in the order of the merged spans; a
+ *       page's slot is its batch current index, the same on every rank.
  *   [D] same page, "symm counting barrier" message: under the page-aligned
  *       in-seq split every current page has exactly one writer rank.
  *   [E] same page, "compose_v2" message: a descriptor owner of -1 zero-fills

@@ -8,6 +8,7 @@ library; the first call does, and fails loudly if it has not been built.
 from . import cpkv  # noqa: F401
 from .cpkv import (  # noqa: F401
     CpkvError,
+    cpkv_compose_fused,
     cpkv_compose_gather,
     cpkv_fill_current,
     cpkv_plan_build,
@@ -21,7 +22,7 @@ from .cpkv import (  # noqa: F401
 )
 
 __all__ = [
-    "cpkv", "CpkvError", "cpkv_compose_gather", "cpkv_fill_current", "cpkv_plan_build", "cpkv_plan_sizes",
+    "cpkv", "CpkvError", "cpkv_compose_fused", "cpkv_compose_gather", "cpkv_fill_current", "cpkv_plan_build", "cpkv_plan_sizes",
     "cpkv_ragged_plan_build", "cpkv_ragged_plan_sizes", "cpkv_version", "cpkv_writer_token_counts",
     "plan_buffers", "ragged_buffers",
 ]

@@ -39,7 +39,7 @@ MAX_BATCH = 1024
 
 EXPORTED = (
     "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_fill_current",
-    "cpkv_compose_gather", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
+    "cpkv_compose_gather", "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
     "cpkv_version",
 )
 
@@ -66,6 +66,7 @@ def _declare(lib):
     lib.cpkv_plan_build.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _L] + [_P] * 11
     lib.cpkv_fill_current.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
     lib.cpkv_compose_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
     lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
     for name in EXPORTED:
@@ -206,6 +207,24 @@ def cpkv_compose_gather(src_table: Sequence, src_cap_pages, d_owner, d_src, d_de
                                     _dp(d_owner), _dp(d_src), dense_cap_pages, _dp(d_dense), _dp(d_status),
                                     _stream(stream))
     _check("cpkv_compose_gather", rc)
+
+
+def cpkv_compose_fused(cur_lens, pools: Sequence, cur_rows: Sequence, d_owner, d_src, d_token_writer_row, d_dense,
+                       *, page_size, cp_size, row_bytes, dense_cap_pages, d_status, pool_cap_pages=None,
+                       cur_rows_cap=None, stream=None):
+    """Single-GPU compose of one layer without staging (pools + writers' current rows -> dense)."""
+    cl = _host_i32(cur_lens)
+    if pool_cap_pages is None:
+        pool_cap_pages = [t.shape[0] for t in pools]
+    if cur_rows_cap is None:
+        cur_rows_cap = [t.numel() // row_bytes for t in cur_rows]
+    pcaps, rcaps = _host_i64(pool_cap_pages), _host_i64(cur_rows_cap)
+    parr, rarr = _ptr_array(pools), _ptr_array(cur_rows)
+    rc = load().cpkv_compose_fused(len(cl), page_size, cp_size, row_bytes, _hp(cl), ctypes.cast(parr, _P), _hp(pcaps),
+                                   ctypes.cast(rarr, _P), _hp(rcaps), _dp(d_owner), _dp(d_src),
+                                   _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense), _dp(d_status),
+                                   _stream(stream))
+    _check("cpkv_compose_fused", rc)
 
 
 def cpkv_ragged_plan_build(prefix_lens, q_lens, d_cp_index, n_owned: int, *, chunk, k_align, out, d_counts,

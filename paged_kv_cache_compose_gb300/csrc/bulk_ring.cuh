@@ -1,0 +1,102 @@
+// A single-warp ring of bulk async copies (TMA, non-tensor form) through
+// shared memory: global -> shared with mbarrier completion, shared -> global
+// as bulk groups.  Shared by the page gather and the fused compose.
+//
+// kStages shared-memory stages of `piece_bytes` each; at most kLoads loads in
+// flight, so kStages - kLoads stages hold stores that are still draining and
+// loads overlap stores.  Lane 0 issues every copy; the other lanes only take
+// part in the warp-uniform bookkeeping.  Every copy carries an L2
+// evict_first policy (each byte is moved once).  Waits on the mbarriers are
+// bounded by a time limit: on a timeout the ring raises
+// CPKV_STATUS_TIMEOUT, stops issuing and still waits (bounded) for every load
+// it issued before the CTA may exit.
+#pragma once
+
+#include "common.cuh"
+
+namespace cpkv {
+
+constexpr uint64_t kRingWaitLimitNs = 2000000000ull;  // 2 s; a piece lands in microseconds
+
+template <int kStages, int kLoads>
+struct BulkRing {
+  static_assert(kLoads >= 1 && kLoads <= kStages && kStages <= 8, "ring shape");
+  uint8_t *smem;          // kStages * piece_bytes of dynamic shared memory
+  uint64_t *full;         // kStages mbarriers (shared)
+  uint8_t **ring_dst;     // kStages destinations (shared)
+  uint32_t *ring_bytes;   // kStages sizes (shared)
+  int *ring_live;         // kStages flags: a load was issued into the stage (shared)
+  int32_t *status;
+  int32_t piece_bytes;
+  int64_t head, tail;     // consumed / issued (warp-uniform)
+  bool dead;              // lane 0: a bounded wait gave up
+  uint64_t policy;
+
+  CPKV_DEV void init(uint8_t *smem_, uint64_t *full_, uint8_t **dst_, uint32_t *bytes_, int *live_,
+                     int32_t *status_, int32_t piece_bytes_) {
+    smem = smem_; full = full_; ring_dst = dst_; ring_bytes = bytes_; ring_live = live_;
+    status = status_; piece_bytes = piece_bytes_;
+    head = tail = 0;
+    dead = false;
+    policy = l2_policy_evict_first();
+    if ((threadIdx.x & 31) == 0) {
+      for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+      fence_barrier_init();
+    }
+    __syncwarp();
+  }
+
+  // Wait for the oldest load and store it (warp-uniform call).
+  CPKV_DEV void consume() {
+    const int s = (int)(head % kStages);
+    if ((threadIdx.x & 31) == 0) {
+      const uint32_t parity = (uint32_t)((head / kStages) & 1);
+      bool landed = false;
+      if (ring_live[s]) {
+        landed = mbar_wait_bounded(&full[s], parity, kRingWaitLimitNs);
+        if (!landed && !dead) {
+          dead = true;
+          raise_status(status, CPKV_STATUS_TIMEOUT);
+        }
+      }
+      if (landed && !dead) bulk_store_s2g_hint(ring_dst[s], smem + (size_t)s * piece_bytes, ring_bytes[s], policy);
+      bulk_commit();
+    }
+    ++head;
+  }
+
+  // Copy `bytes` (a multiple of 16, <= piece_bytes) from src to dst (warp-uniform call).
+  CPKV_DEV void push(const void *src, void *dst, uint32_t bytes) {
+    if (tail - head == kLoads) consume();
+    const int s = (int)(tail % kStages);
+    if ((threadIdx.x & 31) == 0) {
+      // the stage's previous store must have finished reading shared memory
+      if (tail >= kStages) bulk_wait_read_dyn((int)(head - tail + kStages - 1));
+      ring_live[s] = 0;
+      if (!dead) {
+        ring_dst[s] = static_cast<uint8_t *>(dst);
+        ring_bytes[s] = bytes;
+        ring_live[s] = 1;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_load_g2s_hint(smem + (size_t)s * piece_bytes, src, bytes, &full[s], policy);
+      }
+    }
+    ++tail;
+    __syncwarp();
+  }
+
+  // Store everything in flight and wait until the stores are complete.
+  CPKV_DEV void drain() {
+    while (head < tail) consume();
+    if ((threadIdx.x & 31) == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+
+// Zero `bytes` (a multiple of 16) at dst with 16-byte stores across the warp.
+CPKV_DEV void warp_zero(uint8_t *dst, uint32_t bytes) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (uint32_t i = threadIdx.x & 31; i < bytes / 16; i += 32) st_stream16(dst + 16 * (size_t)i, z);
+}
+
+}  // namespace cpkv

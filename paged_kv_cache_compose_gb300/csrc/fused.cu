@@ -1,0 +1,211 @@
+// cpkv_compose_fused: the single-GPU compose in one pass per layer.
+//
+// The staging exchange of the pages ("staging-direct compose" message of
+// commits d63fbd4) exists because current pages are computed on other GPUs:
+// each rank fills its own current pages into its staging, and every rank
+// gathers all of them back.  When every writer region lives on this GPU the
+// round trip through staging is not needed: a current page's rows are already
+// contiguous in its writer's current-row buffer (tokens of one page are
+// consecutive in batch order and have one writer), so the dense page can be
+// copied straight from there, followed by zero pad rows.  The pages' own
+// measurements point the same way: the staging-direct design measured 62.8 ms
+// per batch against a 60.8 ms ideal, the gap being structure, not copies.
+//
+// One launch per layer moves every dense page exactly once:
+//   owner -1           -> zeros
+//   owner r < cp       -> page src of pool slab r (modulo-owner prefix page)
+//   owner cp + w       -> current page i = src - 1 of writer w: its n_i rows
+//                         from cur_rows[w] starting at token_writer_row of the
+//                         page's first token, then ps - n_i zero rows
+// The descriptors are the ones cpkv_plan_build writes for the gather.  The
+// output is byte-identical to cpkv_fill_current followed by
+// cpkv_compose_gather.  Same bulk-copy ring as the gather (bulk_ring.cuh).
+#include <stdint.h>
+
+#include "bulk_ring.cuh"
+
+namespace cpkv {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kLoadsInFlight = 2;
+constexpr int kCtasPerSm = 2;
+constexpr int kMaxPieceBytes = 24 * 1024;
+
+template <int MAXB>
+struct FusedParams {
+  const uint8_t *pool[CPKV_MAX_CP];
+  int64_t pool_cap[CPKV_MAX_CP];
+  const uint8_t *cur_rows[CPKV_MAX_CP];
+  int64_t cur_cap[CPKV_MAX_CP];
+  const int32_t *owner, *src, *token_writer_row;
+  uint8_t *dense;
+  int32_t *status;
+  int64_t dense_cap, page_bytes, units, R, C;
+  int32_t cp, ps, B, pieces, piece_bytes;
+  int32_t cur_lens[MAXB];
+};
+
+template <int MAXB>
+__global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant__ FusedParams<MAXB> p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ uint8_t *ring_dst[kStages];
+  __shared__ uint32_t ring_bytes[kStages];
+  __shared__ int ring_live[kStages];
+  __shared__ int32_t cur_page_start[MAXB + 1];  // first batch current page of request b
+  __shared__ int64_t token_start[MAXB + 1];     // first batch token of request b
+  const int lane = threadIdx.x;
+
+  // request-level exclusive scans, 32 requests per step
+  {
+    int32_t carry_pages = 0;
+    int64_t carry_tok = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      const int32_t n = b < p.B ? p.cur_lens[b] : 0;
+      const int32_t np = (n + p.ps - 1) / p.ps;
+      const int32_t inc_p = warp_inclusive_scan<int32_t>(np);
+      const int64_t inc_t = warp_inclusive_scan<int64_t>((int64_t)n);
+      if (b < p.B) {
+        cur_page_start[b] = carry_pages + inc_p - np;
+        token_start[b] = carry_tok + inc_t - n;
+      }
+      carry_pages += __shfl_sync(0xffffffffu, inc_p, 31);
+      carry_tok += __shfl_sync(0xffffffffu, inc_t, 31);
+    }
+    if (lane == 0) {
+      cur_page_start[p.B] = carry_pages;
+      token_start[p.B] = carry_tok;
+    }
+    __syncwarp();
+  }
+
+  BulkRing<kStages, kLoadsInFlight> ring;
+  ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
+  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
+    const int64_t d = u / p.pieces;
+    const int32_t k = (int32_t)(u - d * p.pieces);
+    const int64_t off = (int64_t)k * p.piece_bytes;
+    const uint32_t bytes = (uint32_t)min64(p.piece_bytes, p.page_bytes - off);
+    uint8_t *dst = p.dense + d * p.page_bytes + off;
+    const int32_t o = p.owner[d];
+    const int32_t s = p.src[d];
+    if (o >= 0 && o < p.cp && s >= 0 && s < p.pool_cap[o]) {
+      ring.push(p.pool[o] + (int64_t)s * p.page_bytes + off, dst, bytes);
+      continue;
+    }
+    int64_t copy = 0;  // bytes of this piece that come from current rows
+    const uint8_t *from = nullptr;
+    bool bad = o != -1 && !(o >= p.cp && o < 2 * p.cp);
+    if (!bad && o >= p.cp) {
+      const int32_t w = o - p.cp;
+      const int32_t i = s - 1;  // batch current page index
+      if (i < 0 || i >= p.C || p.B == 0) {
+        bad = true;
+      } else {
+        const int b = upper_index<int32_t>(cur_page_start, p.B, i);
+        const int32_t kp = i - cur_page_start[b];
+        const int64_t tok0 = token_start[b] + (int64_t)kp * p.ps;
+        const int64_t n = min64(p.ps, (int64_t)p.cur_lens[b] - (int64_t)kp * p.ps);
+        const int32_t row0 = p.token_writer_row[tok0];
+        if (n < 1 || row0 < 0 || row0 + n > p.cur_cap[w]) {
+          bad = true;
+        } else {
+          const int64_t rows_bytes = n * p.R;
+          copy = off < rows_bytes ? min64(bytes, rows_bytes - off) : 0;
+          from = p.cur_rows[w] + (int64_t)row0 * p.R + off;
+        }
+      }
+    }
+    if (bad) {
+      if (lane == 0 && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
+      copy = 0;
+    }
+    if (copy > 0) ring.push(from, dst, (uint32_t)copy);
+    if (copy < bytes) warp_zero(dst + copy, bytes - (uint32_t)copy);
+  }
+  ring.drain();
+}
+
+}  // namespace
+}  // namespace cpkv
+
+extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
+                                  const void *const *h_pools, const int64_t *h_pool_cap_pages,
+                                  const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
+                                  const int32_t *d_owner, const int32_t *d_src, const int32_t *d_token_writer_row,
+                                  int64_t dense_cap_pages, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
+  using namespace cpkv;
+  if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
+  if (row_bytes <= 0 || row_bytes % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
+  if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
+  if (h_pools == nullptr || h_pool_cap_pages == nullptr || h_cur_rows == nullptr || h_cur_rows_cap == nullptr ||
+      d_status == nullptr)
+    return CPKV_ERR_ARG;
+  if (B > 0 && h_cur_lens == nullptr) return CPKV_ERR_ARG;
+  int64_t T = 0, C = 0;
+  for (int b = 0; b < B; ++b) {
+    if (h_cur_lens[b] < 0) return CPKV_ERR_ARG;
+    T += h_cur_lens[b];
+    C += ceil_div(h_cur_lens[b], page_size);
+  }
+  if (T > INT32_MAX - 1 || C > INT32_MAX - 2) return CPKV_ERR_LIMIT;
+  if (dense_cap_pages == 0) return CPKV_OK;
+  if (d_owner == nullptr || d_src == nullptr || d_dense == nullptr || !aligned16(d_dense)) return CPKV_ERR_ARG;
+  if (T > 0 && d_token_writer_row == nullptr) return CPKV_ERR_ARG;
+  for (int k = 0; k < cp_size; ++k) {
+    if (h_pool_cap_pages[k] < 0 || h_cur_rows_cap[k] < 0) return CPKV_ERR_ARG;
+    if (h_pool_cap_pages[k] > 0 && (h_pools[k] == nullptr || !aligned16(h_pools[k]))) return CPKV_ERR_ARG;
+    if (h_cur_rows_cap[k] > 0 && (h_cur_rows[k] == nullptr || !aligned16(h_cur_rows[k]))) return CPKV_ERR_ARG;
+  }
+  const int64_t page_bytes = (int64_t)page_size * row_bytes;
+  const int64_t pieces = ceil_div(page_bytes, kMaxPieceBytes);
+  const int64_t piece_bytes = ceil_div(ceil_div(page_bytes, pieces), 16) * 16;
+  if (pieces > INT32_MAX || dense_cap_pages > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
+  const int64_t units = dense_cap_pages * pieces;
+  const size_t smem = (size_t)kStages * piece_bytes;
+  const int64_t cap = (int64_t)device_sm_count() * kCtasPerSm;
+  const int grid = (int)(units < cap ? units : cap);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+#define CPKV_FILL_FUSED(prm)                                                                        \
+  for (int k = 0; k < CPKV_MAX_CP; ++k) {                                                           \
+    prm.pool[k] = k < cp_size ? static_cast<const uint8_t *>(h_pools[k]) : nullptr;                 \
+    prm.pool_cap[k] = k < cp_size ? h_pool_cap_pages[k] : 0;                                        \
+    prm.cur_rows[k] = k < cp_size ? static_cast<const uint8_t *>(h_cur_rows[k]) : nullptr;          \
+    prm.cur_cap[k] = k < cp_size ? h_cur_rows_cap[k] : 0;                                           \
+  }                                                                                                 \
+  prm.owner = d_owner; prm.src = d_src; prm.token_writer_row = d_token_writer_row;                  \
+  prm.dense = static_cast<uint8_t *>(d_dense); prm.status = d_status; prm.dense_cap = dense_cap_pages; \
+  prm.page_bytes = page_bytes; prm.units = units; prm.R = row_bytes; prm.C = C; prm.cp = cp_size;  \
+  prm.ps = page_size; prm.B = B; prm.pieces = (int32_t)pieces; prm.piece_bytes = (int32_t)piece_bytes; \
+  for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
+
+  static int configured[256][2] = {{0}};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (B <= 64) {
+    if (dev >= 0 && dev < 256 && !configured[dev][0]) {
+      if (cudaFuncSetAttribute(compose_fused_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kStages * kMaxPieceBytes) != cudaSuccess)
+        return CPKV_ERR_CUDA;
+      configured[dev][0] = 1;
+    }
+    FusedParams<64> prm;
+    CPKV_FILL_FUSED(prm)
+    compose_fused_kernel<64><<<grid, 32, smem, s>>>(prm);
+    return launch_status();
+  }
+  if (dev >= 0 && dev < 256 && !configured[dev][1]) {
+    if (cudaFuncSetAttribute(compose_fused_kernel<CPKV_MAX_BATCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStages * kMaxPieceBytes) != cudaSuccess)
+      return CPKV_ERR_CUDA;
+    configured[dev][1] = 1;
+  }
+  FusedParams<CPKV_MAX_BATCH> prm;
+  CPKV_FILL_FUSED(prm)
+#undef CPKV_FILL_FUSED
+  compose_fused_kernel<CPKV_MAX_BATCH><<<grid, 32, smem, s>>>(prm);
+  return launch_status();
+}

@@ -8,20 +8,18 @@
 // non-tensor form): global -> shared with mbarrier completion, then
 // shared -> global tracked by bulk groups.  Each page is cut into `pieces`
 // equal 16-byte-multiple units (<= 24 KB); units are dealt round-robin to a
-// persistent grid of one-warp CTAs, two per SM.  Each CTA runs a ring of
-// kStages shared-memory stages with at most kLoadsInFlight loads
-// outstanding, so the remaining stages hold stores still draining: loads
-// and stores overlap instead of a stage waiting for its own store.  Every
-// copy carries an L2 evict_first policy: pool pages, staging pages and dense
-// pages are each touched once per layer, and streaming them must not evict
-// the staging the fill has just written for this gather.  Zero units (owner
-// -1 or an invalid descriptor) are written with plain 16-byte stores by the
-// whole warp.  Every mbarrier wait is bounded; on a timeout the kernel raises
-// CPKV_STATUS_TIMEOUT, stops issuing, drains what it issued (bounded again)
-// and returns.
+// persistent grid of one-warp CTAs, two per SM.  Each CTA runs a BulkRing of
+// 4 shared-memory stages with at most 2 loads outstanding, so the other
+// stages hold stores still draining: loads and stores overlap instead of a
+// stage waiting for its own store.  Every copy carries an L2 evict_first
+// policy: pool pages, staging pages and dense pages are each touched once per
+// layer, and streaming them must not evict the staging the fill has just
+// written for this gather.  Zero units (owner -1 or an invalid descriptor)
+// are written with plain 16-byte stores by the whole warp.  Every mbarrier
+// wait is bounded (see bulk_ring.cuh).
 #include <stdint.h>
 
-#include "common.cuh"
+#include "bulk_ring.cuh"
 
 namespace cpkv {
 namespace {
@@ -30,7 +28,6 @@ constexpr int kStages = 4;
 constexpr int kLoadsInFlight = 2;
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxPieceBytes = 24 * 1024;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a page load takes microseconds
 
 struct GatherParams {
   const uint8_t *table[2 * CPKV_MAX_CP];
@@ -72,68 +69,15 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ uint8_t *ring_dst[kStages];
   __shared__ uint32_t ring_bytes[kStages];
-  __shared__ int ring_live[kStages];  // a load was issued into the stage
-  const int lane = threadIdx.x;
-
-  if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
-
-  int64_t head = 0, tail = 0;  // consumed / issued copy units (uniform across the warp)
-  bool dead = false;           // a bounded wait gave up (lane 0 only)
-  const uint64_t stream_once = l2_policy_evict_first();
-
-  // consume the oldest in-flight copy unit: wait for its load, store it.
-  // A load that was issued is always waited for (bounded), even after a
-  // timeout, so no copy into shared memory outlives the CTA.
-  auto consume = [&]() {
-    const int s = (int)(head % kStages);
-    if (lane == 0) {
-      const uint32_t parity = (uint32_t)((head / kStages) & 1);
-      bool landed = false;
-      if (ring_live[s]) {
-        landed = mbar_wait_bounded(&full[s], parity, kWaitLimitNs);
-        if (!landed && !dead) {
-          dead = true;
-          raise_status(p.status, CPKV_STATUS_TIMEOUT);
-        }
-      }
-      if (landed && !dead) {
-        bulk_store_s2g_hint(ring_dst[s], smem + (size_t)s * p.piece_bytes, ring_bytes[s], stream_once);
-      }
-      bulk_commit();
-    }
-    ++head;
-  };
-
-  const uint4 z = make_uint4(0, 0, 0, 0);
+  __shared__ int ring_live[kStages];
+  BulkRing<kStages, kLoadsInFlight> ring;
+  ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
   for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-    const Unit x = resolve_unit(p, u, lane == 0);
-    if (x.src == nullptr) {
-      for (uint32_t i = lane; i < x.bytes / 16; i += 32) st_stream16(x.dst + 16 * (size_t)i, z);
-      continue;
-    }
-    if (tail - head == kLoadsInFlight) consume();
-    const int s = (int)(tail % kStages);
-    if (lane == 0) {
-      if (tail >= kStages) bulk_wait_read_dyn((int)(head - tail + kStages - 1));  // stage's last store has read smem
-      ring_live[s] = 0;
-      if (!dead) {
-        ring_dst[s] = x.dst;
-        ring_bytes[s] = x.bytes;
-        ring_live[s] = 1;
-        mbar_arrive_expect_tx(&full[s], x.bytes);
-        bulk_load_g2s_hint(smem + (size_t)s * p.piece_bytes, x.src, x.bytes, &full[s], stream_once);
-      }
-    }
-    ++tail;
-    __syncwarp();
+    const Unit x = resolve_unit(p, u, threadIdx.x == 0);
+    if (x.src == nullptr) warp_zero(x.dst, x.bytes);
+    else ring.push(x.src, x.dst, x.bytes);
   }
-  while (head < tail) consume();
-  if (lane == 0) bulk_wait_all();
-  __syncwarp();
+  ring.drain();
 }
 
 }  // namespace

@@ -82,6 +82,13 @@ class ComposeLayers:
                                  cp_size=p.cp_size, row_bytes=self.row_bytes, dense_cap_pages=p.dense_cap_pages,
                                  d_status=p.d_status, stream=stream)
 
+    def compose_fused(self, pools, cur_rows_per_writer, dense, stream=None):
+        """One-pass single-GPU compose of a layer (no staging round trip)."""
+        p = self.plan
+        cpkv.cpkv_compose_fused(p.cur_lens, pools, cur_rows_per_writer, p["owner"], p["src"], p["token_writer_row"],
+                                dense, page_size=p.page_size, cp_size=p.cp_size, row_bytes=self.row_bytes,
+                                dense_cap_pages=p.dense_cap_pages, d_status=p.d_status, stream=stream)
+
     def compose_layer(self, layer: int, pools, cur_rows_per_writer, stream=None):
         """Fill + gather of one layer into the dense buffer of its parity."""
         dense = self.dense[layer % len(self.dense)]

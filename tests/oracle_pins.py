@@ -446,7 +446,7 @@ def edge_batches():
     out.append(mk("shared_prefix", 17, page_size=4, cp_size=2, num_pool_pages=64, row_bytes=R,
                   prefix_lens=[8, 12], cur_lens=[3, 6], prefix_pages=[9, 17, 9, 17, 30],
                   cur_pages=[40, 41, 42], row_kind="bytes"))
-    # chunk-shaped request: 2048-token page-aligned carried prefix + 512 extend, beside a short one
+    # a request shaped like a chunked-prefill chunk (2048 prefix tokens, 512 new tokens) beside a short one
     out.append(mk("chunk_shaped", 18, page_size=64, cp_size=8, num_pool_pages=256, row_bytes=R,
                   prefix_lens=[2048, 64], cur_lens=[512, 37], row_kind="bytes"))
     # writers not round-robin: all current pages on one rank, others idle

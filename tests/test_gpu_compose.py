@@ -244,3 +244,79 @@ def test_host_argument_errors_raise():
                                d_token_writer_row=plan["token_writer_row"], d_writer=plan.d_writer,
                                num_cur_pages=plan.C, d_status=plan.d_status, cur_rows_cap=[0, 0])
     assert e.value.code == cpkv.CPKV_ERR_CAPACITY
+
+
+# ---------------------------------------------------------------------------
+# fused single-GPU compose (no staging round trip): same output as fill + gather
+# ---------------------------------------------------------------------------
+
+def _run_fused(batch, dense_extra=2, layer=0):
+    plan, want = _plan_pair(batch, dense_extra)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs = wl.host_pool(batch, layer)
+    rows = wl.host_current_rows(batch, layer)
+    d_slabs = [torch.from_numpy(s).cuda() for s in slabs]
+    d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+    dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
+                       device="cuda")
+    layers.compose_fused(d_slabs, d_rows, dense)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    return dense.cpu().numpy(), plan, slabs, rows
+
+
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_fused_matches_oracle_edge_cases(batch):
+    dense, plan, slabs, rows = _run_fused(batch)
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense, want)
+
+
+@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (3, 48), (128, 1152), (64, 4096), (7, 16)])
+def test_fused_page_geometries(ps, R):
+    """Pieces that straddle the end of a partial page's rows, several pieces per page."""
+    rng = np.random.default_rng(ps * 7 + R)
+    B = 6
+    pfx = (rng.integers(0, 6 * ps, B) // ps) * ps
+    cur = rng.integers(0, 5 * ps, B)
+    batch = wl.make_compose_batch("geo", 31, page_size=ps, cp_size=3, num_pool_pages=400, row_bytes=R,
+                                  prefix_lens=pfx, cur_lens=cur, row_kind="bytes")
+    dense, plan, slabs, rows = _run_fused(batch, dense_extra=1)
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense, want)
+
+
+def test_fused_large_batch_template():
+    rng = np.random.default_rng(8)
+    B, ps = 150, 16
+    batch = wl.make_compose_batch("b150", 8, page_size=ps, cp_size=4, num_pool_pages=20000, row_bytes=64,
+                                  prefix_lens=(rng.integers(0, 90, B) // ps) * ps, cur_lens=rng.integers(0, 50, B),
+                                  row_kind="bytes")
+    dense, plan, slabs, rows = _run_fused(batch, dense_extra=0)
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense, want)
+
+
+def test_fused_bad_descriptor_is_zeroed_and_flagged():
+    batch = wl.tiny_batch()
+    plan, _ = _plan_pair(batch, dense_extra=0)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs = [torch.from_numpy(s).cuda() for s in wl.host_pool(batch)]
+    rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, wl.host_current_rows(batch))]
+    owner = plan["owner"].clone()
+    src = plan["src"].clone()
+    owner[0] = 2 * batch.cp_size  # outside the table
+    src[1] = 10_000               # beyond the slab / current page range
+    dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
+                       device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_compose_fused(batch.cur_lens, slabs, rows, owner, src, plan["token_writer_row"], dense,
+                            page_size=batch.page_size, cp_size=batch.cp_size, row_bytes=batch.row_bytes,
+                            dense_cap_pages=plan.dense_cap_pages, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == cpkv.STATUS_DESC_OOB
+    page = batch.page_size
+    assert torch.all(dense[:page] == 0) and torch.all(dense[page:2 * page] == 0)

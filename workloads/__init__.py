@@ -10,8 +10,8 @@ computed here.  The only structure it knows is the scenario itself:
   current (extend) tokens occupy ``ceil(cur_len / page_size)`` pages;
 * under the page-aligned in-seq split each current page has one writer rank,
   and that rank computes the KV rows of the page's tokens (commit log
-  d63fbd4, "symm counting barrier + IPC gather" message: current pages are
-  single-writer at page granularity);
+  d63fbd4, "symm counting barrier + IPC gather" message: each current page is
+  written by exactly one rank);
 * the q tokens of the NSA indexer are cut into fixed-size chunks that are
   dealt to context-parallel ranks (commit log d63fbd4, "CPU-gap fixes"
   message: the ragged plan is keyed on ``cp_index``).
