@@ -78,18 +78,19 @@ def kernel_source_sha(files) -> str:
     return h.hexdigest()[:16]
 
 
-def gather_traffic(config: str):
-    """DRAM bytes per gather launch from the committed ncu capture, or None
-    when there is none for this workload or the kernel changed since."""
-    path = os.path.join(ROOT, "profiles", f"gather_traffic_{config}.json")
+def kernel_traffic(kernel: str, config: str):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu capture, or
+    None when there is none for this workload or the kernel's sources changed
+    since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{config}.json")
     if not os.path.exists(path):
         return None
     try:
         with open(path) as f:
             d = json.load(f)
+        if d.get("source_sha") != kernel_source_sha(d["sources"]):
+            return None
     except Exception:
-        return None
-    if d.get("source_sha") != kernel_source_sha(["gather.cu", "common.cuh"]):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -515,7 +516,7 @@ def main(argv=None):
     top = "fused" if work.variant == "fused" else "gather"
     status = work.status()
 
-    traffic = gather_traffic(a.config) if top == "gather" else None
+    traffic = kernel_traffic(top, a.config)
 
     # end to end through the public API with host buffers
     e2e = None
