@@ -432,7 +432,9 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="traced_78", choices=["traced_78", "fp8_nsa"])
+    ap.add_argument("--config", default="traced_78", choices=["traced_78", "fp8_nsa", "plans"],
+                    help="plans: latency of the per-batch plan builders (ragged plan config, all CP ranks and "
+                         "splits; compose plan of the traced and fp8 batches)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variant", default="staging", choices=["staging", "fused"],
                     help="staging: fill + slot-dense gather per layer (the pages' method); "
@@ -449,6 +451,8 @@ def main(argv=None):
     ws, rank, local = _dist_env()
     if a.impl == "reference":
         return run_reference(a, ws, rank)
+    if a.config == "plans":
+        return run_plans(a)
 
     import torch
 
@@ -628,6 +632,74 @@ def run_e2e(work, a, ws):
     ms_max, units_all = aggregate(el * 1e3, work.layer_bytes * work.num_layers * steps, ws)
     return {"value": round(units_all / (ms_max / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms_max / steps, 3), "steps": steps}
+
+
+def _graph_us(torch, fn, reps, per):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * per)
+
+
+def run_plans(a):
+    """Latency of the plan builders, one CUDA graph per measured set, launched
+    back to back (µs per build includes the launch inside the graph)."""
+    import torch
+
+    from paged_kv_cache_compose_gb300 import build as cpkv_build
+    from paged_kv_cache_compose_gb300 import cpkv
+    from paged_kv_cache_compose_gb300.runtime import ComposePlan
+
+    cpkv_build.build()
+    reps = max(20, a.steps)
+    out = {"metric": "plan build latency", "unit": "us per build", "n_gpus": 1, "steps": reps, "data": "synthetic",
+           "higher_is_better": False, "ragged": {}, "compose_plan": {}}
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    base = wl.ragged_batch()
+    for split in ("interleaved", "contiguous", "zigzag"):
+        rb = wl.RaggedBatch(base.name, base.seed, base.cp_size, base.chunk, base.k_align, base.prefix_lens,
+                            base.q_lens, split=split)
+        jobs = []
+        for r in range(rb.cp_size):
+            ci = rb.cp_index(r)
+            S, Q = cpkv.cpkv_ragged_plan_sizes(rb.q_lens, ci, rb.chunk)
+            jobs.append((torch.from_numpy(ci).cuda(), len(ci), cpkv.ragged_buffers(max(S, 1), max(Q, 1)),
+                         torch.zeros(2, dtype=torch.int64, device="cuda")))
+
+        def build(js):
+            for d_ci, n, buf, cnt in js:
+                cpkv.cpkv_ragged_plan_build(rb.prefix_lens, rb.q_lens, d_ci, n, chunk=rb.chunk, k_align=rb.k_align,
+                                            out=buf, d_counts=cnt, d_status=status)
+        per_rank = [_graph_us(torch, lambda j=j: build([j]), reps, 1) for j in jobs]
+        all_ranks = _graph_us(torch, lambda: build(jobs), reps, 1)
+        out["ragged"][split] = {"us_per_rank": [round(x, 2) for x in per_rank], "us_all_ranks": round(all_ranks, 2),
+                                "B": rb.B, "q_tokens": int(rb.q_lens.sum()), "cp": rb.cp_size}
+    for name, fn in (("traced", wl.traced_batch), ("traced_78_slab", wl.traced_78_layer_batch),
+                     ("fp8_nsa", wl.fp8_nsa_batch)):
+        b = fn()
+        plan = ComposePlan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer, page_size=b.page_size,
+                           cp_size=b.cp_size, num_pool_pages=b.num_pool_pages)
+        out["compose_plan"][name] = {"us": round(_graph_us(torch, lambda: plan.build(), reps, 1), 2), "B": b.B,
+                                     "T": b.T, "D": plan.D, "num_pool_pages": b.num_pool_pages}
+    torch.cuda.synchronize()
+    out["status_word"] = int(status.item())
+    print(json.dumps(out), flush=True)
+    return 0 if out["status_word"] == 0 else 3
 
 
 def run_reference(a, ws, rank):

@@ -17,6 +17,8 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
                         reduction to index_select + cat, golden example
   oracle_staging        pinned: golden example, round trip through the gather
   oracle_gather         pinned: per-slot brute force, -1 sentinel, golden
+  oracle_fill_index_copy pinned: equals oracle_staging on plan-built indices;
+                        a hand-worked permuted case
   oracle_ragged_plan    pinned: cumsum / repeat closed forms, tiling of every
                         request across ranks, cp=1 special case, golden
 """
@@ -80,9 +82,10 @@ def _declare(lib):
     lib.oracle_compose_dense.argtypes = [_I, _I, _I, _L, _L, _P, _P, _P, _P, _P, _L, _P]
     lib.oracle_staging.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L]
     lib.oracle_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P]
+    lib.oracle_fill_index_copy.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P]
     lib.oracle_ragged_plan.argtypes = [_I, _I, _I, _P, _P, _P, _L] + [_P] * 11
     for f in ("oracle_sizes", "oracle_compose_plan", "oracle_compose_dense",
-              "oracle_staging", "oracle_gather", "oracle_ragged_plan"):
+              "oracle_staging", "oracle_gather", "oracle_ragged_plan", "oracle_fill_index_copy"):
         getattr(lib, f).restype = _I
     return lib
 
@@ -191,6 +194,29 @@ def staging(cur_lens, writer, cur_rows, staging_bufs, *, page_size, cp_size, lib
     _check(rc, "oracle_staging")
 
 
+def fill_index_copy(cur_lens, staging_rows, token_writer_row, writer, cur_rows_per_writer, staging_bufs, *,
+                    page_size, cp_size, row_bytes, lib=None) -> int:
+    """The fill as an index copy for arbitrary row indices (in place on
+    ``staging_bufs``).  Returns the status bits."""
+    lib = lib or load()
+    cl, wr = _i32(cur_lens), _i32(writer)
+    sr = np.ascontiguousarray(np.asarray(staging_rows, dtype=np.int64))
+    tw = _i32(token_writer_row)
+    rows = [np.ascontiguousarray(r, dtype=np.uint8) for r in cur_rows_per_writer]
+    caps = np.array([r.shape[0] if r.ndim == 2 else 0 for r in rows], np.int64)
+    for st in staging_bufs:
+        assert st.flags.c_contiguous and st.dtype == np.uint8
+    cap_pages = staging_bufs[0].shape[0] // page_size
+    rt = (ctypes.c_void_p * cp_size)(*[r.ctypes.data if r.size else None for r in rows])
+    stt = (ctypes.c_void_p * cp_size)(*[st.ctypes.data for st in staging_bufs])
+    status = np.zeros(1, np.int32)
+    rc = lib.oracle_fill_index_copy(len(cl), page_size, cp_size, row_bytes, _ptr(cl), _ptr(sr), _ptr(tw), _ptr(wr),
+                                    len(wr), ctypes.cast(rt, ctypes.c_void_p), _ptr(caps),
+                                    ctypes.cast(stt, ctypes.c_void_p), cap_pages, _ptr(status))
+    _check(rc, "oracle_fill_index_copy")
+    return int(status[0])
+
+
 def gather(table_bufs, cap_pages, owner, src, *, page_size, row_bytes, dense_cap, lib=None):
     """Slot-dense page gather, descriptor by descriptor.  Returns (dense, status)."""
     lib = lib or load()
@@ -231,6 +257,6 @@ def ragged_plan(prefix_lens, q_lens, cp_index, *, chunk, k_align=1, lib=None) ->
 
 
 __all__ = [
-    "build", "load", "compile_oracle", "sizes", "compose_plan", "compose_dense", "staging",
+    "build", "load", "compile_oracle", "sizes", "compose_plan", "compose_dense", "staging", "fill_index_copy",
     "gather", "ragged_plan", "OracleError",
 ]

@@ -266,6 +266,48 @@ int oracle_staging(int B, int ps, int cp, int64_t R, const int32_t *cur_lens,
 }
 
 /*
+ * The fill as the index copy of [A], for any row indices: for every token t,
+ * with w = writer[staging_rows[t] / ps - 1],
+ *     staging[w] row staging_rows[t] <- cur_rows[w] row token_writer_row[t]
+ * in token order, then for every request whose current length is not a
+ * multiple of ps, the rows after its last token's staging row up to the end
+ * of that staging page are set to zero.  A row index outside its buffer or a
+ * writer outside [0, cp) skips that token and raises ORC_ROW_OOB /
+ * ORC_WRITER_OOB.  cur_rows[w] is [cur_cap[w]][R]; staging[w] is
+ * [staging_cap_pages * ps][R].
+ */
+int oracle_fill_index_copy(int B, int ps, int cp, int64_t R, const int32_t *cur_lens,
+                           const int64_t *staging_rows, const int32_t *token_writer_row,
+                           const int32_t *writer, int64_t C, const uint8_t *const *cur_rows,
+                           const int64_t *cur_cap, uint8_t *const *staging, int64_t staging_cap_pages,
+                           int32_t *status) {
+  int64_t T = 0;
+  for (int b = 0; b < B; ++b) T += cur_lens[b];
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t sr = staging_rows[t];
+    int64_t slot = sr / ps;
+    if (sr < ps || sr >= staging_cap_pages * ps || slot > C) { *status |= ORC_ROW_OOB; continue; }
+    int32_t w = writer[slot - 1];
+    if (w < 0 || w >= cp) { *status |= ORC_WRITER_OOB; continue; }
+    int32_t r = token_writer_row[t];
+    if (r < 0 || r >= cur_cap[w]) { *status |= ORC_ROW_OOB; continue; }
+    memcpy(staging[w] + sr * R, cur_rows[w] + (int64_t)r * R, (size_t)R);
+  }
+  int64_t last = -1;
+  for (int b = 0; b < B; ++b) {
+    last += cur_lens[b];
+    if (cur_lens[b] % ps == 0) continue;
+    int64_t sr = staging_rows[last];
+    int64_t slot = sr / ps;
+    if (sr < ps || sr >= staging_cap_pages * ps || slot > C) { *status |= ORC_ROW_OOB; continue; }
+    int32_t w = writer[slot - 1];
+    if (w < 0 || w >= cp) { *status |= ORC_WRITER_OOB; continue; }
+    for (int64_t row = sr + 1; row < (slot + 1) * ps; ++row) memset(staging[w] + row * R, 0, (size_t)R);
+  }
+  return ORC_OK;
+}
+
+/*
  * Slot-dense page gather [A][E], descriptor by descriptor: dense page d is a
  * copy of page src[d] of table[owner[d]], or zeros when owner[d] == -1.  A
  * descriptor outside the table or the source's capacity is a violation: the

@@ -1,12 +1,13 @@
 // A single-warp ring of bulk async copies (TMA, non-tensor form) through
 // shared memory: global -> shared with mbarrier completion, shared -> global
-// as bulk groups.  Shared by the page gather and the fused compose.
+// as bulk groups.  Shared by the page gather, the fill and the fused compose.
 //
 // kStages shared-memory stages of `piece_bytes` each; at most kLoads loads in
 // flight, so kStages - kLoads stages hold stores that are still draining and
 // loads overlap stores.  Lane 0 issues every copy; the other lanes only take
-// part in the warp-uniform bookkeeping.  Every copy carries an L2
-// evict_first policy (each byte is moved once).  Waits on the mbarriers are
+// part in the warp-uniform bookkeeping.  Loads carry an L2 evict_first policy
+// (each byte is read once); stores too, unless the caller keeps them in L2
+// for the next kernel.  Waits on the mbarriers are
 // bounded by a time limit: on a timeout the ring raises
 // CPKV_STATUS_TIMEOUT, stops issuing and still waits (bounded) for every load
 // it issued before the CTA may exit.
@@ -30,15 +31,18 @@ struct BulkRing {
   int32_t piece_bytes;
   int64_t head, tail;     // consumed / issued (warp-uniform)
   bool dead;              // lane 0: a bounded wait gave up
-  uint64_t policy;
+  uint64_t load_policy, store_policy;
 
+  // keep_stores: stores get L2 evict_last (the next kernel reads them back)
+  // instead of evict_first.
   CPKV_DEV void init(uint8_t *smem_, uint64_t *full_, uint8_t **dst_, uint32_t *bytes_, int *live_,
-                     int32_t *status_, int32_t piece_bytes_) {
+                     int32_t *status_, int32_t piece_bytes_, bool keep_stores = false) {
     smem = smem_; full = full_; ring_dst = dst_; ring_bytes = bytes_; ring_live = live_;
     status = status_; piece_bytes = piece_bytes_;
     head = tail = 0;
     dead = false;
-    policy = l2_policy_evict_first();
+    load_policy = l2_policy_evict_first();
+    store_policy = keep_stores ? l2_policy_evict_last() : load_policy;
     if ((threadIdx.x & 31) == 0) {
       for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
       fence_barrier_init();
@@ -59,7 +63,7 @@ struct BulkRing {
           raise_status(status, CPKV_STATUS_TIMEOUT);
         }
       }
-      if (landed && !dead) bulk_store_s2g_hint(ring_dst[s], smem + (size_t)s * piece_bytes, ring_bytes[s], policy);
+      if (landed && !dead) bulk_store_s2g_hint(ring_dst[s], smem + (size_t)s * piece_bytes, ring_bytes[s], store_policy);
       bulk_commit();
     }
     ++head;
@@ -78,7 +82,7 @@ struct BulkRing {
         ring_bytes[s] = bytes;
         ring_live[s] = 1;
         mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_load_g2s_hint(smem + (size_t)s * piece_bytes, src, bytes, &full[s], policy);
+        bulk_load_g2s_hint(smem + (size_t)s * piece_bytes, src, bytes, &full[s], load_policy);
       }
     }
     ++tail;
@@ -97,6 +101,12 @@ struct BulkRing {
 CPKV_DEV void warp_zero(uint8_t *dst, uint32_t bytes) {
   const uint4 z = make_uint4(0, 0, 0, 0);
   for (uint32_t i = threadIdx.x & 31; i < bytes / 16; i += 32) st_stream16(dst + 16 * (size_t)i, z);
+}
+
+// The same with an L2 cache policy on the stores.
+CPKV_DEV void warp_zero_hint(uint8_t *dst, uint32_t bytes, uint64_t pol) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (uint32_t i = threadIdx.x & 31; i < bytes / 16; i += 32) st16_hint(dst + 16 * (size_t)i, z, pol);
 }
 
 }  // namespace cpkv

@@ -318,6 +318,46 @@ def pin_staging_gather_roundtrip(lib, batch, dense_extra=0):
         assert np.array_equal(stg[tw[t]][plan["staging_rows"][t]], rows[t])
 
 
+def pin_fill_index_copy(lib, batch):
+    """The general index copy agrees with the staging definition on
+    plan-built indices (pad rows zeroed, other pages untouched)."""
+    ps, cp, R = batch.page_size, batch.cp_size, batch.row_bytes
+    plan = oracle.compose_plan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                               page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages, lib=lib)
+    rows = wl.host_current_rows(batch)
+    per_writer = wl.split_rows_by_writer(batch, rows)
+    a = [np.full(((batch.C + 1) * ps, R), 0x3C, np.uint8) for _ in range(cp)]
+    b = [x.copy() for x in a]
+    st = oracle.fill_index_copy(batch.cur_lens, plan["staging_rows"], plan["token_writer_row"], batch.writer,
+                                per_writer, a, page_size=ps, cp_size=cp, row_bytes=R, lib=lib)
+    assert st == 0
+    oracle.staging(batch.cur_lens, batch.writer, rows, b, page_size=ps, cp_size=cp, lib=lib)
+    for w in range(cp):
+        assert np.array_equal(a[w], b[w]), w
+
+
+def pin_fill_index_copy_permuted(lib):
+    """Hand-worked: ps=2, cp=1, one request of 3 tokens on current pages 0, 1
+    (staging slots 1, 2).  Source rows of the first page swapped: token 0 <-
+    row 1, token 1 <- row 0, token 2 <- row 2; staging rows 2, 3, 4; row 5 is
+    the pad after the last token and becomes zero; rows 0, 1 (slot 0) keep
+    their guard bytes."""
+    R = 16
+    rows = np.stack([np.full(R, 10 + i, np.uint8) for i in range(3)])
+    stg = [np.full((3 * 2, R), 0xEE, np.uint8)]
+    st = oracle.fill_index_copy([3], [2, 3, 4], [1, 0, 2], [0, 0], [rows], stg, page_size=2, cp_size=1,
+                                row_bytes=R, lib=lib)
+    assert st == 0
+    want = np.stack([np.full(R, v, np.uint8) for v in (0xEE, 0xEE, 11, 10, 12, 0)])
+    assert np.array_equal(stg[0], want)
+    # an out-of-range source row is skipped and flagged
+    stg = [np.full((3 * 2, R), 0xEE, np.uint8)]
+    st = oracle.fill_index_copy([3], [2, 3, 4], [1, 7, 2], [0, 0], [rows], stg, page_size=2, cp_size=1,
+                                row_bytes=R, lib=lib)
+    assert st == oracle.ROW_OOB
+    assert np.all(stg[0][3] == 0xEE)
+
+
 def pin_gather_sentinel_and_oob(lib):
     rng = np.random.default_rng(3)
     ps, R = 4, 16
@@ -452,6 +492,11 @@ def edge_batches():
     # writers not round-robin: all current pages on one rank, others idle
     out.append(mk("one_writer", 19, page_size=4, cp_size=4, num_pool_pages=64, row_bytes=R,
                   prefix_lens=[4, 8], cur_lens=[7, 6], writer=[2, 2, 2, 2], row_kind="bytes"))
+    # contiguous in-seq split of each request's current pages over the writers
+    cur = [37, 9, 64, 20]
+    out.append(mk("contiguous_writers", 20, page_size=8, cp_size=3, num_pool_pages=128, row_bytes=R,
+                  prefix_lens=[16, 0, 8, 24], cur_lens=cur, writer=wl.contiguous_writers(cur, 8, 3),
+                  row_kind="bytes"))
     return out
 
 
@@ -462,6 +507,12 @@ def ragged_edge_batches():
         q = rng.integers(0, 5 * chunk, size=B).astype(np.int32)
         pfx = rng.integers(0, 100, size=B).astype(np.int32)
         out.append(wl.RaggedBatch(f"ragged_cp{cp}", 21, cp, chunk, k_align, pfx, q))
+    # the other CP splits: contiguous in-seq blocks and zigzag (2*cp slots per request)
+    for split in ("contiguous", "zigzag"):
+        for cp, chunk, B in ((2, 4, 6), (4, 8, 9), (8, 64, 12)):
+            q = rng.integers(0, 20 * chunk, size=B).astype(np.int32)
+            pfx = rng.integers(0, 300, size=B).astype(np.int32)
+            out.append(wl.RaggedBatch(f"ragged_{split}_cp{cp}", 22, cp, chunk, 1, pfx, q, split=split))
     return out
 
 
@@ -470,6 +521,8 @@ ALL_PINS = [
     ("golden_ragged", lambda lib: pin_golden_ragged(lib)),
     ("cp1_index_select_cat", lambda lib: pin_cp1_index_select_cat(lib)),
     ("gather_sentinel", lambda lib: pin_gather_sentinel_and_oob(lib)),
+    ("fill_index_copy_permuted", lambda lib: pin_fill_index_copy_permuted(lib)),
+    ("fill_index_copy", lambda lib: [pin_fill_index_copy(lib, b) for b in edge_batches()]),
     ("errors", lambda lib: pin_errors(lib)),
     ("plan_brute_force", lambda lib: [pin_plan_brute_force(lib, b, 2) for b in edge_batches()]),
     ("dense_token_level", lambda lib: [pin_dense_token_level(lib, b, 1) for b in edge_batches()]),

@@ -320,3 +320,69 @@ def test_fused_bad_descriptor_is_zeroed_and_flagged():
     assert int(status.item()) == cpkv.STATUS_DESC_OOB
     page = batch.page_size
     assert torch.all(dense[:page] == 0) and torch.all(dense[page:2 * page] == 0)
+
+
+# ---------------------------------------------------------------------------
+# fill with row indices that do not form page runs (row-by-row path)
+# ---------------------------------------------------------------------------
+
+def _fill_case(batch, mutate):
+    plan, _ = _plan_pair(batch)
+    ps, cp, R = batch.page_size, batch.cp_size, batch.row_bytes
+    sr = plan["staging_rows"].cpu().numpy().copy()
+    tw = plan["token_writer_row"].cpu().numpy().copy()
+    mutate(batch, sr, tw)
+    rows = wl.host_current_rows(batch)
+    per_writer = wl.split_rows_by_writer(batch, rows)
+    want = [np.full(((batch.C + 1) * ps, R), 0x77, np.uint8) for _ in range(cp)]
+    st = oracle.fill_index_copy(batch.cur_lens, sr, tw, batch.writer, per_writer, want, page_size=ps, cp_size=cp,
+                                row_bytes=R)
+    assert st == 0
+    staging = [torch.full(((batch.C + 1) * ps, R), 0x77, dtype=torch.uint8, device="cuda") for _ in range(cp)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_fill_current(batch.cur_lens, [torch.from_numpy(r).cuda() for r in per_writer], staging, page_size=ps,
+                           cp_size=cp, row_bytes=R, staging_cap_pages=batch.C + 1,
+                           d_staging_rows=torch.from_numpy(sr).cuda(), d_token_writer_row=torch.from_numpy(tw).cuda(),
+                           d_writer=plan.d_writer, num_cur_pages=batch.C, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for w in range(cp):
+        assert np.array_equal(staging[w].cpu().numpy(), want[w]), w
+
+
+def _pages(batch):
+    """(first token, rows, is last page of its request) of every current page."""
+    out, t = [], 0
+    for n in batch.cur_lens.tolist():
+        for k in range(0, n, batch.page_size):
+            m = min(batch.page_size, n - k)
+            out.append((t + k, m, k + m == n))
+        t += n
+    return out
+
+
+@pytest.mark.parametrize("batch", [b for b in pins.edge_batches() if b.T > 0], ids=lambda b: b.name)
+def test_fill_reversed_source_rows(batch):
+    """Source rows reversed inside every page: no page is a run."""
+    def mutate(b, sr, tw):
+        for t0, n, _ in _pages(b):
+            tw[t0:t0 + n] = tw[t0:t0 + n][::-1]
+    _fill_case(batch, mutate)
+
+
+@pytest.mark.parametrize("batch", [b for b in pins.edge_batches() if b.T > 0], ids=lambda b: b.name)
+def test_fill_mixed_runs_and_shuffled_pages(batch):
+    """Staging rows shuffled inside every other full page that is not a
+    request's last page; all other pages stay runs."""
+    rng = np.random.default_rng(3)
+
+    def mutate(b, sr, tw):
+        for j, (t0, n, last) in enumerate(_pages(b)):
+            if j % 2 == 0 and n == b.page_size and not last:
+                sr[t0:t0 + n] = sr[t0:t0 + n][rng.permutation(n)]
+    _fill_case(batch, mutate)
+
+
+def test_fill_traced_full_size_runs():
+    """The traced batch (every page a run) against the index-copy oracle."""
+    _fill_case(wl.traced_batch(), lambda b, sr, tw: None)

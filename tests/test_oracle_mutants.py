@@ -40,6 +40,10 @@ MUTANTS = [
     ("staging_pad_not_zeroed", "else memset(page + r * R, 0, (size_t)R);", "else (void)0;"),
     ("gather_sentinel_wrong", "if (o == -1) { memset(dst, 0, (size_t)page_bytes); continue; }",
      "if (o == -2) { memset(dst, 0, (size_t)page_bytes); continue; }"),
+    ("fill_pad_overwrites_last_row", "for (int64_t row = sr + 1; row < (slot + 1) * ps; ++row)",
+     "for (int64_t row = sr; row < (slot + 1) * ps; ++row)"),
+    ("fill_writer_of_wrong_slot", "    int32_t w = writer[slot - 1];\n    if (w < 0 || w >= cp) { *status |= ORC_WRITER_OOB; continue; }\n    int32_t r",
+     "    int32_t w = writer[slot % C];\n    if (w < 0 || w >= cp) { *status |= ORC_WRITER_OOB; continue; }\n    int32_t r"),
     ("ragged_kbase_unaligned", "kbase[b + 1] = kbase[b] + ceil_div64(kv, k_align) * k_align;",
      "kbase[b + 1] = kbase[b] + kv;"),
     ("ragged_kv_dropped_prefix", "int64_t kv = (int64_t)prefix_lens[b] + q_lens[b];", "int64_t kv = q_lens[b];"),

@@ -118,6 +118,16 @@ def round_robin_writers(C: int, cp_size: int) -> np.ndarray:
     return (np.arange(C, dtype=np.int64) % cp_size).astype(np.int32)
 
 
+def contiguous_writers(cur_lens, page_size: int, cp_size: int) -> np.ndarray:
+    """In-seq contiguous split: each request's current pages are cut into
+    cp_size contiguous blocks and block r is written by rank r."""
+    out = []
+    for n in pages_per_len(cur_lens, page_size).tolist():
+        local = np.arange(n, dtype=np.int64)
+        out.append((local * cp_size) // max(n, 1))
+    return (np.concatenate(out) if out else np.zeros(0, np.int64)).astype(np.int32)
+
+
 def make_compose_batch(
     name: str,
     seed: int,
@@ -301,11 +311,36 @@ class RaggedBatch:
     def num_chunks(self) -> int:
         return int(pages_per_len(self.q_lens, self.chunk).sum())
 
+    split: str = "interleaved"
+
     def cp_index(self, rank: int) -> np.ndarray:
-        """Chunk ids owned by ``rank`` under the interleaved assignment
-        (global chunk id modulo cp_size), ascending."""
-        ids = np.arange(self.num_chunks, dtype=np.int64)
-        return ids[ids % self.cp_size == rank].astype(np.int32)
+        """Chunk ids owned by ``rank``, ascending, under the batch's split:
+
+        interleaved  global chunk id modulo cp_size (the default);
+        contiguous   each request's chunks cut into cp_size contiguous blocks
+                     (in-seq split), rank r takes block r of every request;
+        zigzag       each request's chunks dealt to 2*cp_size slots, rank r
+                     owning slots r and 2*cp_size-1-r (load-balanced causal
+                     split).
+        """
+        if self.split == "interleaved":
+            ids = np.arange(self.num_chunks, dtype=np.int64)
+            return ids[ids % self.cp_size == rank].astype(np.int32)
+        out = []
+        first = 0
+        for n in pages_per_len(self.q_lens, self.chunk).tolist():
+            local = np.arange(n, dtype=np.int64)
+            if self.split == "contiguous":
+                owner = (local * self.cp_size) // max(n, 1)
+                mine = owner == rank
+            elif self.split == "zigzag":
+                slot = (local * 2 * self.cp_size) // max(n, 1)
+                mine = (slot == rank) | (slot == 2 * self.cp_size - 1 - rank)
+            else:
+                raise ValueError(self.split)
+            out.append(first + local[mine])
+            first += n
+        return (np.concatenate(out) if out else np.zeros(0, np.int64)).astype(np.int32)
 
 
 def ragged_batch(seed: int = 1005) -> RaggedBatch:
@@ -355,7 +390,7 @@ def ceil_div(a: int, b: int) -> int:
 
 
 __all__ = [
-    "ComposeBatch", "RaggedBatch", "MLA_ROW_BYTES", "NSA_FP8_ROW_BYTES", "CONFIGS",
+    "ComposeBatch", "RaggedBatch", "MLA_ROW_BYTES", "NSA_FP8_ROW_BYTES", "CONFIGS", "contiguous_writers",
     "tiny_batch", "traced_batch", "traced_78_layer_batch", "fp8_nsa_batch", "ragged_batch",
     "ragged_from_compose", "make_compose_batch", "lognormal_split", "round_robin_writers",
     "random_rows", "host_pool", "host_current_rows", "token_writer", "split_rows_by_writer",
