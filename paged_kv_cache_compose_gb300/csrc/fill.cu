@@ -3,31 +3,29 @@
 // a single index copy of layer-invariant row indices; "fp8 -> uint8"
 // message of commits 0d87bc5: rows are opaque bytes).
 //
-// The work is cut by current page: the tokens of page i are consecutive in
-// batch order, so with the plan's row indices they form one run of
-// consecutive source rows (in their writer's current-row buffer) and one run
-// of consecutive staging rows starting on a page boundary.  For each page the
-// warp first checks that the page's indices really form such a run; if so it
-// moves the page with the bulk-copy ring (bulk_ring.cuh) in pieces of at most
-// 24 KB, and zeroes the pad rows after a request's last token up to the end
-// of its staging page.  Any page whose indices do not form a run is copied row
-// by row, exactly as an index copy (16-byte vectors), with its pad rows zeroed
-// after the request's last token.  Either way the result is the index copy
-// the contract describes.
+// One launch.  Blocks [0, nRow) copy rows: one warp per token row, each lane
+// moving 16-byte vectors, RIF rows in flight per warp (all loads issued
+// before the stores); the grid is one resident wave.  RIF follows the row
+// width so that a warp keeps about 2-3 KB in flight: 2 rows of up to 96
+// vectors (the 1152-byte MLA row), 4 rows of up to 64 vectors (the 656-byte
+// fp8 NSA row).  Blocks [nRow, nRow + B) zero the pad rows after each
+// request's last token, up to the end of its staging page.  Current rows are
+// read once (L2 evict_first); staging rows are written with evict_last
+// because the gather that follows reads them back.
 //
-// Current rows are read once (L2 evict_first); staging rows are stored with
-// evict_last because the gather that follows reads them back from L2.
+// (A variant that moves whole pages with bulk copies when a page's indices
+// form a run was slower here: each page first needs a round trip of index
+// loads, and a layer has only a few pages per CTA to overlap them with.)
 #include <stdint.h>
 
-#include "bulk_ring.cuh"
+#include "common.cuh"
 
 namespace cpkv {
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kLoadsInFlight = 2;
-constexpr int kCtasPerSm = 2;
-constexpr int kMaxPieceBytes = 24 * 1024;
+constexpr int kFillThreads = 256;
+constexpr int kWarpsPerBlock = kFillThreads / 32;
+constexpr int kBlocksPerSm = 4;    // one resident wave (<= 64 registers x 256 threads x 4 = 64K)
 
 template <int MAXB>
 struct FillParams {
@@ -37,146 +35,138 @@ struct FillParams {
   const int64_t *staging_rows;
   const int32_t *token_writer_row, *writer;
   int32_t *status;
-  int64_t C, staging_cap_rows, R, page_bytes, units;
-  int32_t ps, cp, B, pieces, piece_bytes;
+  int64_t T, C, staging_cap_rows, R;
+  int ps, cp, B, nRow, vpr;  // vpr = R / 16
   int32_t cur_lens[MAXB];
 };
 
-// Copy one token row (index-copy semantics), validating every index.
+struct RowJob {
+  const uint8_t *src;
+  uint8_t *dst;
+};
+
+// Resolve token t to (source row, staging row); nullptr src when skipped.
 template <int MAXB>
-__device__ void copy_row(const FillParams<MAXB> &p, int64_t t, uint64_t read_once, uint64_t keep) {
-  const int lane = threadIdx.x & 31;
+__device__ RowJob resolve_row(const FillParams<MAXB> &p, int64_t t) {
+  RowJob j{nullptr, nullptr};
   const int64_t sr = p.staging_rows[t];
   const int64_t slot = sr / p.ps;
   if (sr < p.ps || sr >= p.staging_cap_rows || slot > p.C) {
-    if (lane == 0) raise_status(p.status, CPKV_STATUS_ROW_OOB);
-    return;
+    raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    return j;
   }
   const int32_t w = p.writer[slot - 1];
   if (w < 0 || w >= p.cp) {
-    if (lane == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
-    return;
+    raise_status(p.status, CPKV_STATUS_WRITER_OOB);
+    return j;
   }
   const int32_t r = p.token_writer_row[t];
   if (r < 0 || r >= p.cur_cap[w]) {
-    if (lane == 0) raise_status(p.status, CPKV_STATUS_ROW_OOB);
-    return;
+    raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    return j;
   }
-  const uint8_t *src = p.cur_rows[w] + (int64_t)r * p.R;
-  uint8_t *dst = p.staging[w] + sr * p.R;
-  for (int64_t c = lane; c < p.R / 16; c += 32)
-    st16_hint(dst + 16 * c, ld_stream16_hint(src + 16 * c, read_once), keep);
+  j.src = p.cur_rows[w] + (int64_t)r * p.R;
+  j.dst = p.staging[w] + sr * p.R;
+  return j;
 }
 
-// Zero the rows after staging row `sr_last` up to the end of its page.
+// RIF rows per warp per iteration, VPL vectors per lane per row (vpr <= 32 * VPL).
+template <int MAXB, int RIF, int VPL>
+__device__ void copy_rows_unrolled(const FillParams<MAXB> &p, uint64_t read_once, uint64_t keep) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)p.nRow * kWarpsPerBlock;
+  const int vpr = p.vpr;
+  for (int64_t t0 = warp_id * RIF; t0 < p.T; t0 += nwarps * RIF) {
+    RowJob job[RIF];
+    uint4 v[RIF][VPL];
+#pragma unroll
+    for (int r = 0; r < RIF; ++r) job[r] = (t0 + r < p.T) ? resolve_row(p, t0 + r) : RowJob{nullptr, nullptr};
+#pragma unroll
+    for (int r = 0; r < RIF; ++r) {
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) {
+        const int c = lane + 32 * k;
+        if (job[r].src != nullptr && c < vpr) v[r][k] = ld_stream16_hint(job[r].src + 16 * (int64_t)c, read_once);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RIF; ++r) {
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) {
+        const int c = lane + 32 * k;
+        if (job[r].src != nullptr && c < vpr) st16_hint(job[r].dst + 16 * (int64_t)c, v[r][k], keep);
+      }
+    }
+  }
+}
+
+// Rows wider than 128 vectors (2 KB): one row per warp, a plain loop.
 template <int MAXB>
-__device__ void zero_after(const FillParams<MAXB> &p, int64_t sr_last, uint64_t keep) {
-  const int64_t slot = sr_last / p.ps;
-  if (sr_last < p.ps || sr_last >= p.staging_cap_rows || slot > p.C) {
-    if ((threadIdx.x & 31) == 0) raise_status(p.status, CPKV_STATUS_ROW_OOB);
+__device__ void copy_rows_wide(const FillParams<MAXB> &p, uint64_t read_once, uint64_t keep) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)p.nRow * kWarpsPerBlock;
+  for (int64_t t = warp_id; t < p.T; t += nwarps) {
+    const RowJob job = resolve_row(p, t);
+    if (job.src == nullptr) continue;
+    for (int c = lane; c < p.vpr; c += 32)
+      st16_hint(job.dst + 16 * (int64_t)c, ld_stream16_hint(job.src + 16 * (int64_t)c, read_once), keep);
+  }
+}
+
+// Zero the rows after request b's last token up to the end of its staging page.
+template <int MAXB>
+__device__ void zero_pad_rows(const FillParams<MAXB> &p, int b) {
+  __shared__ int64_t last_tok;
+  if (b >= p.B) return;
+  const int32_t rem = p.cur_lens[b] % p.ps;
+  if (rem == 0) return;
+  if (threadIdx.x == 0) {
+    int64_t s = 0;
+    for (int k = 0; k <= b; ++k) s += p.cur_lens[k];
+    last_tok = s - 1;
+  }
+  __syncthreads();
+  const int64_t sr = p.staging_rows[last_tok];
+  const int64_t slot = sr / p.ps;
+  if (sr < p.ps || sr >= p.staging_cap_rows || slot > p.C) {
+    if (threadIdx.x == 0) raise_status(p.status, CPKV_STATUS_ROW_OOB);
     return;
   }
   const int32_t w = p.writer[slot - 1];
   if (w < 0 || w >= p.cp) {
-    if ((threadIdx.x & 31) == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
+    if (threadIdx.x == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
     return;
   }
-  const int64_t first = sr_last + 1, end = (slot + 1) * p.ps;
-  if (first < end) warp_zero_hint(p.staging[w] + first * p.R, (uint32_t)((end - first) * p.R), keep);
-}
-
-template <int MAXB>
-__global__ void __launch_bounds__(32) fill_pages_kernel(const __grid_constant__ FillParams<MAXB> p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[kStages];
-  __shared__ uint8_t *ring_dst[kStages];
-  __shared__ uint32_t ring_bytes[kStages];
-  __shared__ int ring_live[kStages];
-  __shared__ int32_t cur_page_start[MAXB + 1];  // first batch current page of request b
-  __shared__ int64_t token_start[MAXB + 1];     // first batch token of request b
-  const int lane = threadIdx.x;
-  const uint64_t read_once = l2_policy_evict_first();
+  const int64_t first = sr + 1, end = (slot + 1) * p.ps;  // [first, end) rows to zero
+  uint8_t *base = p.staging[w] + first * p.R;
+  const int64_t nvec = (end - first) * p.vpr;
+  const uint4 z = make_uint4(0, 0, 0, 0);
   const uint64_t keep = l2_policy_evict_last();
+  for (int64_t i = threadIdx.x; i < nvec; i += kFillThreads) st16_hint(base + 16 * i, z, keep);
+}
 
-  {  // request-level exclusive scans, 32 requests per step
-    int32_t carry_pages = 0;
-    int64_t carry_tok = 0;
-    for (int base = 0; base < p.B; base += 32) {
-      const int b = base + lane;
-      const int32_t n = b < p.B ? p.cur_lens[b] : 0;
-      const int32_t np = (n + p.ps - 1) / p.ps;
-      const int32_t inc_p = warp_inclusive_scan<int32_t>(np);
-      const int64_t inc_t = warp_inclusive_scan<int64_t>((int64_t)n);
-      if (b < p.B) {
-        cur_page_start[b] = carry_pages + inc_p - np;
-        token_start[b] = carry_tok + inc_t - n;
-      }
-      carry_pages += __shfl_sync(0xffffffffu, inc_p, 31);
-      carry_tok += __shfl_sync(0xffffffffu, inc_t, 31);
-    }
-    if (lane == 0) {
-      cur_page_start[p.B] = carry_pages;
-      token_start[p.B] = carry_tok;
-    }
-    __syncwarp();
+// RIF = 0 selects the wide-row loop.
+template <int MAXB, int RIF, int VPL>
+__global__ void __launch_bounds__(kFillThreads, kBlocksPerSm) fill_current_kernel(const __grid_constant__ FillParams<MAXB> p) {
+  if ((int)blockIdx.x < p.nRow) {
+    const uint64_t read_once = l2_policy_evict_first();
+    const uint64_t keep = l2_policy_evict_last();
+    if constexpr (RIF == 0) copy_rows_wide(p, read_once, keep);
+    else copy_rows_unrolled<MAXB, RIF, VPL>(p, read_once, keep);
+  } else {
+    zero_pad_rows(p, blockIdx.x - p.nRow);
   }
-
-  BulkRing<kStages, kLoadsInFlight> ring;
-  ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes, /*keep_stores=*/true);
-  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-    const int64_t i = u / p.pieces;  // batch current page
-    const int32_t k = (int32_t)(u - i * p.pieces);
-    const int b = upper_index<int32_t>(cur_page_start, p.B, (int32_t)i);
-    const int32_t kp = (int32_t)i - cur_page_start[b];
-    const int64_t tok0 = token_start[b] + (int64_t)kp * p.ps;
-    const int64_t n = min64(p.ps, (int64_t)p.cur_lens[b] - (int64_t)kp * p.ps);  // rows of this page
-    const bool last_of_request = (int64_t)kp * p.ps + n == p.cur_lens[b];
-
-    // does the page form one run: page-aligned staging rows, consecutive source rows?
-    const int64_t sr0 = p.staging_rows[tok0];
-    const int32_t r0 = p.token_writer_row[tok0];
-    const int64_t slot = sr0 / p.ps;
-    bool run = sr0 % p.ps == 0 && sr0 >= p.ps && slot <= p.C && sr0 + p.ps <= p.staging_cap_rows;
-    int32_t w = -1;
-    if (run) {
-      w = p.writer[slot - 1];
-      run = w >= 0 && w < p.cp && r0 >= 0 && (int64_t)r0 + n <= p.cur_cap[w];
-    }
-    bool mine = true;
-    for (int64_t j = lane; j < n; j += 32)
-      mine &= p.staging_rows[tok0 + j] == sr0 + j && p.token_writer_row[tok0 + j] == r0 + j;
-    run = __all_sync(0xffffffffu, mine) && run;
-
-    if (run) {
-      const int64_t off = (int64_t)k * p.piece_bytes;
-      const uint32_t bytes = (uint32_t)min64(p.piece_bytes, p.page_bytes - off);
-      uint8_t *dst = p.staging[w] + sr0 * p.R + off;
-      const int64_t rows_bytes = n * p.R;
-      const int64_t copy = off < rows_bytes ? min64(bytes, rows_bytes - off) : 0;
-      if (copy > 0) ring.push(p.cur_rows[w] + (int64_t)r0 * p.R + off, dst, (uint32_t)copy);
-      // rows past n exist only on a request's last (partial) page: zero them
-      if (copy < bytes && last_of_request) warp_zero_hint(dst + copy, bytes - (uint32_t)copy, keep);
-    } else if (k == 0) {
-      for (int64_t j = 0; j < n; ++j) copy_row(p, tok0 + j, read_once, keep);
-      __syncwarp();  // the row copies are ordered before the pad zeroing
-      if (last_of_request && p.cur_lens[b] % p.ps != 0) zero_after(p, p.staging_rows[tok0 + n - 1], keep);
-    }
-  }
-  ring.drain();
 }
 
 template <int MAXB>
-int launch_fill(const FillParams<MAXB> &prm, int grid, size_t smem, cudaStream_t s, int slot) {
-  static int configured[256][2] = {{0}};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 256 && !configured[dev][slot]) {
-    if (cudaFuncSetAttribute(fill_pages_kernel<MAXB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStages * kMaxPieceBytes) != cudaSuccess)
-      return CPKV_ERR_CUDA;
-    configured[dev][slot] = 1;
-  }
-  fill_pages_kernel<MAXB><<<grid, 32, smem, s>>>(prm);
+int launch_fill(const FillParams<MAXB> &prm, int grid, cudaStream_t s) {
+  if (prm.vpr <= 32) fill_current_kernel<MAXB, 4, 1><<<grid, kFillThreads, 0, s>>>(prm);
+  else if (prm.vpr <= 64) fill_current_kernel<MAXB, 4, 2><<<grid, kFillThreads, 0, s>>>(prm);
+  else if (prm.vpr <= 96) fill_current_kernel<MAXB, 2, 3><<<grid, kFillThreads, 0, s>>>(prm);
+  else if (prm.vpr <= 128) fill_current_kernel<MAXB, 2, 4><<<grid, kFillThreads, 0, s>>>(prm);
+  else fill_current_kernel<MAXB, 0, 0><<<grid, kFillThreads, 0, s>>>(prm);
   return launch_status();
 }
 
@@ -203,7 +193,6 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
     C += ceil_div(h_cur_lens[b], page_size);
   }
   if (num_cur_pages != C) return CPKV_ERR_ARG;
-  if (T > INT32_MAX - 1 || C > INT32_MAX - 2) return CPKV_ERR_LIMIT;
   if (staging_cap_pages < C + 1) return CPKV_ERR_CAPACITY;
   if (T > 0 && (d_staging_rows == nullptr || d_token_writer_row == nullptr || d_writer == nullptr))
     return CPKV_ERR_ARG;
@@ -212,17 +201,13 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
     if (h_cur_rows_cap[w] < 0) return CPKV_ERR_ARG;
     if (h_cur_rows_cap[w] > 0 && (h_cur_rows[w] == nullptr || !aligned16(h_cur_rows[w]))) return CPKV_ERR_ARG;
   }
-  if (C == 0) return CPKV_OK;
+  if (T == 0 && C == 0) return CPKV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  const int64_t page_bytes = (int64_t)page_size * row_bytes;
-  const int64_t pieces = ceil_div(page_bytes, kMaxPieceBytes);
-  const int64_t piece_bytes = ceil_div(ceil_div(page_bytes, pieces), 16) * 16;
-  if (pieces > INT32_MAX || C > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
-  const int64_t units = C * pieces;
-  const int64_t cap = (int64_t)device_sm_count() * kCtasPerSm;
-  const int grid = (int)(units < cap ? units : cap);
-  const size_t smem = (size_t)kStages * piece_bytes;
+  const int64_t row_warps = ceil_div(T, 2);
+  const int64_t row_blocks_needed = ceil_div(row_warps, kWarpsPerBlock);
+  const int64_t row_blocks_cap = (int64_t)device_sm_count() * kBlocksPerSm;
+  const int nRow = (int)(row_blocks_needed < row_blocks_cap ? row_blocks_needed : row_blocks_cap);
 
 #define CPKV_FILL_FILL(prm)                                                                  \
   for (int w = 0; w < CPKV_MAX_CP; ++w) {                                                    \
@@ -231,19 +216,19 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
     prm.staging[w] = w < cp_size ? static_cast<uint8_t *>(h_staging[w]) : nullptr;           \
   }                                                                                          \
   prm.staging_rows = d_staging_rows; prm.token_writer_row = d_token_writer_row;              \
-  prm.writer = d_writer; prm.status = d_status; prm.C = C;                                   \
+  prm.writer = d_writer; prm.status = d_status; prm.T = T; prm.C = C;                        \
   prm.staging_cap_rows = staging_cap_pages * page_size; prm.R = row_bytes;                   \
-  prm.page_bytes = page_bytes; prm.units = units; prm.ps = page_size; prm.cp = cp_size;      \
-  prm.B = B; prm.pieces = (int32_t)pieces; prm.piece_bytes = (int32_t)piece_bytes;          \
+  prm.ps = page_size; prm.cp = cp_size; prm.B = B; prm.nRow = nRow;                          \
+  prm.vpr = (int)(row_bytes / 16);                                                           \
   for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
 
   if (B <= 64) {
     FillParams<64> prm;
     CPKV_FILL_FILL(prm)
-    return launch_fill(prm, grid, smem, s, 0);
+    return launch_fill(prm, nRow + B, s);
   }
   FillParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_FILL(prm)
 #undef CPKV_FILL_FILL
-  return launch_fill(prm, grid, smem, s, 1);
+  return launch_fill(prm, nRow + B, s);
 }

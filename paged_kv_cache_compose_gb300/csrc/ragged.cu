@@ -7,8 +7,10 @@
 // One launch of G CTAs of 1024 threads.  Every CTA rebuilds the request-level
 // scans (chunk ids, k bases) in shared memory, then walks cp_index in tiles of
 // 1024 owned chunks with two block scans per tile (segment starts, token
-// counts) and carries across tiles.  CTA 0 writes the segment arrays; tile j's
-// topk offsets are written by CTA j % G with coalesced stores.
+// counts) and carries across tiles.  CTA 0 writes the segment arrays.  The
+// rank's q tokens are cut into G equal ranges; CTA g writes the topk offsets
+// of range g with coalesced stores (a token finds its chunk by binary search
+// over the tile's token offsets in shared memory).
 #include <stdint.h>
 
 #include "common.cuh"
@@ -29,6 +31,7 @@ struct RaggedParams {
   int64_t seg_cap;
   int64_t *counts;
   int32_t *status;
+  int64_t q_span;  // q tokens per CTA for the topk offsets
   int32_t prefix_lens[MAXB];
   int32_t q_lens_in[MAXB];
 };
@@ -109,12 +112,14 @@ __global__ void __launch_bounds__(kRaggedThreads) ragged_plan_kernel(const __gri
       }
     }
 
-    if (tile % gridDim.x == blockIdx.x) {
+    // this CTA's slice of the tile's q tokens
+    const int64_t lo_q = (int64_t)blockIdx.x * p.q_span, hi_q = lo_q + p.q_span;
+    if (q_carry < hi_q && q_carry + ntok > lo_q) {
       tile_qpos[tid] = qpos;
       tile_kb[tid] = (int32_t)kbase[b];
       if (tid == 0) {
-        tile_q0 = q_carry;
-        tile_q1 = q_carry + ntok;
+        tile_q0 = q_carry > lo_q ? q_carry : lo_q;
+        tile_q1 = q_carry + ntok < hi_q ? q_carry + ntok : hi_q;
       }
       __syncthreads();
       const int nk = (int)min64(kRaggedThreads, p.n - tile * kRaggedThreads);
@@ -170,16 +175,21 @@ extern "C" int cpkv_ragged_plan_build(int B, int chunk, int k_align, const int32
   if (total_chunks > INT32_MAX || total_kv > INT32_MAX) return CPKV_ERR_LIMIT;
   if (n_owned > INT32_MAX) return CPKV_ERR_LIMIT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t ntiles = ceil_div(n_owned, kRaggedThreads);
+  // one CTA per kTokensPerCta q tokens (upper bound n_owned * chunk), at most one per SM
+  constexpr int64_t kTokensPerCta = 2048;
+  const int64_t q_max = n_owned * chunk;
   const int64_t sms = device_sm_count();
-  const int grid = (int)(ntiles < 1 ? 1 : (ntiles < sms ? ntiles : sms));
+  int64_t g = ceil_div(q_max, kTokensPerCta);
+  g = g < 1 ? 1 : (g < sms ? g : sms);
+  const int grid = (int)g;
+  const int64_t q_span = q_max > 0 ? ceil_div(q_max, g) : 1;
 
 #define CPKV_FILL_RAGGED(prm)                                                                   \
   prm.B = B; prm.chunk = chunk; prm.k_align = k_align; prm.n = n_owned; prm.cp_index = d_cp_index; \
   prm.topk = d_topk_offsets; prm.topk_cap = topk_cap; prm.seg_req = d_seg_req; prm.kv_lens = d_kv_lens; \
   prm.q_starts = d_q_starts; prm.q_lens = d_q_lens; prm.k_bases = d_k_bases; prm.q_bases = d_q_bases; \
   prm.current_bases = d_current_bases; prm.seg_cap = seg_cap; prm.counts = d_counts;            \
-  prm.status = d_status;                                                                        \
+  prm.status = d_status; prm.q_span = q_span;                                                   \
   for (int b = 0; b < B; ++b) { prm.prefix_lens[b] = h_prefix_lens[b]; prm.q_lens_in[b] = h_q_lens[b]; }
 
   if (B <= 64) {
