@@ -222,6 +222,15 @@ class ComposeWorkload:
             self.launches_per_step = 3 + self.num_layers  # plan (2) + ragged (1) + one fused compose per layer
             self.layer_bytes = self.bytes["fused"]
             self.kernels = {"fused": self.bytes["fused"]}
+        elif variant == "prefetch":
+            # layer-ahead: prefix pages of layer l+1 gathered on a side stream while layer l is consumed
+            self.launches_per_step = 3 + 3 * self.num_layers  # plan + ragged + (prefetch, fill, current gather)
+            self.layer_bytes = self.bytes["total"]
+            self.kernels = {"gather": self.bytes["gather"], "fill": self.bytes["fill"]}
+            self.side = torch.cuda.Stream(device=self.device)
+            self.prefetched = [torch.cuda.Event() for _ in range(self.num_layers)]
+            self.consumed = [torch.cuda.Event() for _ in range(self.num_layers)]
+            self.plan_ready = torch.cuda.Event()
         else:
             raise ValueError(variant)
 
@@ -234,8 +243,37 @@ class ComposeWorkload:
         self.cpkv.cpkv_ragged_plan_build(self.rb.prefix_lens, self.rb.q_lens, self.d_cp_index, len(self.cp_index),
                                          chunk=self.rb.chunk, k_align=self.rb.k_align, out=self.ragged_out,
                                          d_counts=self.ragged_counts, d_status=self.plan.d_status, stream=stream)
+        if self.variant == "prefetch":
+            return self._prefetch_layers()
         for layer in range(self.num_layers):
             self.run_kernel("all", layer, stream)
+
+    def _prefetch_layers(self):
+        """Layer l's prefix pages are gathered on the side stream one layer
+        ahead; the main stream consumes layer l (fill + current pages) once
+        its prefix is in.  The side stream reuses a dense buffer only after
+        the layer that used it two layers earlier has been consumed."""
+        torch = self.torch
+        main = torch.cuda.current_stream()
+        self.plan_ready.record(main)
+        side = self.side
+        side.wait_event(self.plan_ready)
+
+        def prefetch(layer):
+            with torch.cuda.stream(side):
+                if layer >= 2:
+                    side.wait_event(self.consumed[layer - 2])
+                self.layers.prefetch(self.pools_of(layer), self.layers.dense[layer % 2])
+                self.prefetched[layer].record(side)
+
+        prefetch(0)
+        for layer in range(self.num_layers):
+            if layer + 1 < self.num_layers:
+                prefetch(layer + 1)
+            main.wait_event(self.prefetched[layer])
+            self.layers.consume(self.rows[layer], self.layers.dense[layer % 2])
+            self.consumed[layer].record(main)
+        main.wait_stream(side)
 
     def run_kernel(self, kind, layer, stream=None):
         """Launch one layer's work: ``all`` of it, or one kernel of it."""
@@ -436,9 +474,11 @@ def main(argv=None):
                     help="plans: latency of the per-batch plan builders (ragged plan config, all CP ranks and "
                          "splits; compose plan of the traced and fp8 batches)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--variant", default="staging", choices=["staging", "fused"],
+    ap.add_argument("--variant", default="staging", choices=["staging", "fused", "prefetch"],
                     help="staging: fill + slot-dense gather per layer (the pages' method); "
-                         "fused: one-pass single-GPU compose without the staging round trip")
+                         "fused: one-pass single-GPU compose without the staging round trip; "
+                         "prefetch: staging method with each layer's prefix pages gathered one layer ahead "
+                         "on a side stream")
     ap.add_argument("--no-graph", action="store_true", help="launch layer by layer instead of replaying a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

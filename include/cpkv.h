@@ -194,6 +194,29 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
                         const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
                         void *d_dense, int32_t *d_status, cpkv_stream_t stream);
 
+/* Slot kinds of a gather descriptor (for cpkv_compose_gather_kinds). */
+#define CPKV_GATHER_POOL 1     /* owner in [0, cp): a prefix page from a pool            */
+#define CPKV_GATHER_STAGING 2  /* owner in [cp, 2cp): a current page from a staging      */
+#define CPKV_GATHER_ZERO 4     /* owner -1 (and any invalid descriptor): a zero page      */
+#define CPKV_GATHER_ALL 7
+
+/*
+ * cpkv_compose_gather_kinds — the gather restricted to some slot kinds;
+ * slots of other kinds are left untouched.  This splits a layer's compose
+ * the way the layer-ahead prefetcher of the pages does ("prefetch staging"
+ * message of commits 0d87bc5): the prefix pages (and zero slots) of layer
+ * l + 1 do not depend on layer l and can be gathered early, e.g. on a side
+ * stream (kinds = CPKV_GATHER_POOL | CPKV_GATHER_ZERO); consuming the layer
+ * is then the fill followed by the current pages only
+ * (kinds = CPKV_GATHER_STAGING).  The two calls together write exactly what
+ * one cpkv_compose_gather writes.  kinds outside [0, CPKV_GATHER_ALL] returns
+ * CPKV_ERR_ARG; other arguments as cpkv_compose_gather.
+ */
+int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
+                              const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                              const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages, int kinds,
+                              void *d_dense, int32_t *d_status, cpkv_stream_t stream);
+
 /*
  * cpkv_compose_fused — per layer: the single-GPU compose in one pass, without
  * the staging round trip.  The staging exchange ("staging-direct compose")

@@ -10,6 +10,7 @@ from .cpkv import (  # noqa: F401
     CpkvError,
     cpkv_compose_fused,
     cpkv_compose_gather,
+    cpkv_compose_gather_kinds,
     cpkv_fill_current,
     cpkv_plan_build,
     cpkv_plan_sizes,
@@ -22,7 +23,7 @@ from .cpkv import (  # noqa: F401
 )
 
 __all__ = [
-    "cpkv", "CpkvError", "cpkv_compose_fused", "cpkv_compose_gather", "cpkv_fill_current", "cpkv_plan_build", "cpkv_plan_sizes",
+    "cpkv", "CpkvError", "cpkv_compose_fused", "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_fill_current", "cpkv_plan_build", "cpkv_plan_sizes",
     "cpkv_ragged_plan_build", "cpkv_ragged_plan_sizes", "cpkv_version", "cpkv_writer_token_counts",
     "plan_buffers", "ragged_buffers",
 ]

@@ -34,12 +34,17 @@ STATUS_CHUNK_OOB = 64
 STATUS_OUT_CAPACITY = 128
 STATUS_TIMEOUT = 256
 
+GATHER_POOL = 1
+GATHER_STAGING = 2
+GATHER_ZERO = 4
+GATHER_ALL = 7
+
 MAX_CP = 64
 MAX_BATCH = 1024
 
 EXPORTED = (
     "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_fill_current",
-    "cpkv_compose_gather", "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
+    "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
     "cpkv_version",
 )
 
@@ -66,6 +71,7 @@ def _declare(lib):
     lib.cpkv_plan_build.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _L] + [_P] * 11
     lib.cpkv_fill_current.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
     lib.cpkv_compose_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_compose_gather_kinds.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _I, _P, _P, _P]
     lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
     lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
@@ -207,6 +213,17 @@ def cpkv_compose_gather(src_table: Sequence, src_cap_pages, d_owner, d_src, d_de
                                     _dp(d_owner), _dp(d_src), dense_cap_pages, _dp(d_dense), _dp(d_status),
                                     _stream(stream))
     _check("cpkv_compose_gather", rc)
+
+
+def cpkv_compose_gather_kinds(src_table: Sequence, src_cap_pages, d_owner, d_src, d_dense, *, page_size, cp_size,
+                              row_bytes, dense_cap_pages, kinds, d_status, stream=None):
+    """The gather restricted to slot kinds (GATHER_POOL | GATHER_STAGING | GATHER_ZERO)."""
+    caps = _host_i64(src_cap_pages)
+    tbl = _ptr_array(src_table)
+    rc = load().cpkv_compose_gather_kinds(page_size, cp_size, row_bytes, ctypes.cast(tbl, _P), _hp(caps),
+                                          _dp(d_owner), _dp(d_src), dense_cap_pages, kinds, _dp(d_dense),
+                                          _dp(d_status), _stream(stream))
+    _check("cpkv_compose_gather_kinds", rc)
 
 
 def cpkv_compose_fused(cur_lens, pools: Sequence, cur_rows: Sequence, d_owner, d_src, d_token_writer_row, d_dense,

@@ -36,7 +36,7 @@ struct GatherParams {
   uint8_t *dense;
   int32_t *status;
   int64_t dense_cap, page_bytes, units;
-  int32_t n_table, pieces, piece_bytes;
+  int32_t n_table, n_pool, pieces, piece_bytes, kinds;
 };
 
 struct Unit {
@@ -45,7 +45,15 @@ struct Unit {
   uint32_t bytes;
 };
 
-__device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, bool report) {
+// Kind of a descriptor: pool page, staging page, or zero slot (owner -1 and
+// invalid descriptors, which are zero-filled).
+__device__ __forceinline__ int slot_kind(const GatherParams &p, int32_t o) {
+  if (o >= 0 && o < p.n_pool) return CPKV_GATHER_POOL;
+  if (o >= p.n_pool && o < p.n_table) return CPKV_GATHER_STAGING;
+  return CPKV_GATHER_ZERO;
+}
+
+__device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, bool report, bool *skip) {
   const int64_t d = u / p.pieces;
   const int32_t k = (int32_t)(u - d * p.pieces);
   const int64_t off = (int64_t)k * p.piece_bytes;
@@ -54,7 +62,8 @@ __device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, b
   x.dst = p.dense + d * p.page_bytes + off;
   x.src = nullptr;
   const int32_t o = p.owner[d];
-  if (o == -1) return x;
+  *skip = (slot_kind(p, o) & p.kinds) == 0;
+  if (*skip || o == -1) return x;
   const int32_t s = p.src[d];
   if (o < -1 || o >= p.n_table || s < 0 || s >= p.cap_pages[o]) {
     if (report && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
@@ -73,7 +82,9 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
   BulkRing<kStages, kLoadsInFlight> ring;
   ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
   for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-    const Unit x = resolve_unit(p, u, threadIdx.x == 0);
+    bool skip;
+    const Unit x = resolve_unit(p, u, threadIdx.x == 0, &skip);
+    if (skip) continue;
     if (x.src == nullptr) warp_zero(x.dst, x.bytes);
     else ring.push(x.src, x.dst, x.bytes);
   }
@@ -83,11 +94,12 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
 }  // namespace
 }  // namespace cpkv
 
-extern "C" int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
-                                   const void *const *h_src_table, const int64_t *h_src_cap_pages,
-                                   const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
-                                   void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
+extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
+                                         const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                                         const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
+                                         int kinds, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
   using namespace cpkv;
+  if (kinds < 0 || kinds > CPKV_GATHER_ALL) return CPKV_ERR_ARG;
   if (page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
   if (row_bytes <= 0 || row_bytes % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
   if (h_src_table == nullptr || h_src_cap_pages == nullptr || d_status == nullptr) return CPKV_ERR_ARG;
@@ -116,6 +128,8 @@ extern "C" int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes
   prm.page_bytes = page_bytes;
   prm.units = dense_cap_pages * pieces;
   prm.n_table = n_table;
+  prm.n_pool = cp_size;
+  prm.kinds = kinds;
   prm.pieces = (int32_t)pieces;
   prm.piece_bytes = (int32_t)piece_bytes;
 
@@ -135,4 +149,12 @@ extern "C" int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   gather_pages_kernel<<<grid, 32, smem, s>>>(prm);
   return launch_status();
+}
+
+extern "C" int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
+                                   const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                                   const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
+                                   void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
+  return cpkv_compose_gather_kinds(page_size, cp_size, row_bytes, h_src_table, h_src_cap_pages, d_owner, d_src,
+                                   dense_cap_pages, CPKV_GATHER_ALL, d_dense, d_status, stream);
 }

@@ -82,6 +82,26 @@ class ComposeLayers:
                                  cp_size=p.cp_size, row_bytes=self.row_bytes, dense_cap_pages=p.dense_cap_pages,
                                  d_status=p.d_status, stream=stream)
 
+    def gather_kinds(self, pools, dense, kinds, stream=None):
+        """The gather restricted to slot kinds (cpkv.GATHER_*)."""
+        p = self.plan
+        table = list(pools) + list(self.staging)
+        caps = [t.shape[0] if t is not None else 0 for t in pools] + [p.staging_cap_pages] * p.cp_size
+        cpkv.cpkv_compose_gather_kinds(table, caps, p["owner"], p["src"], dense, page_size=p.page_size,
+                                       cp_size=p.cp_size, row_bytes=self.row_bytes,
+                                       dense_cap_pages=p.dense_cap_pages, kinds=kinds, d_status=p.d_status,
+                                       stream=stream)
+
+    def prefetch(self, pools, dense, stream=None):
+        """Layer-ahead part of a compose: prefix pages and zero slots only."""
+        self.gather_kinds(pools, dense, cpkv.GATHER_POOL | cpkv.GATHER_ZERO, stream)
+
+    def consume(self, cur_rows_per_writer, dense, stream=None):
+        """The rest of the layer once its current rows exist: fill, then the
+        current pages only."""
+        self.fill(cur_rows_per_writer, stream)
+        self.gather_kinds([None] * self.plan.cp_size, dense, cpkv.GATHER_STAGING, stream)
+
     def compose_fused(self, pools, cur_rows_per_writer, dense, stream=None):
         """One-pass single-GPU compose of a layer (no staging round trip)."""
         p = self.plan

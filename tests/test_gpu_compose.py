@@ -386,3 +386,44 @@ def test_fill_mixed_runs_and_shuffled_pages(batch):
 def test_fill_traced_full_size_runs():
     """The traced batch (every page a run) against the index-copy oracle."""
     _fill_case(wl.traced_batch(), lambda b, sr, tw: None)
+
+
+# ---------------------------------------------------------------------------
+# layer-ahead split: prefix/zero slots early, current slots at consume
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_prefetch_then_consume_equals_compose(batch):
+    plan, _ = _plan_pair(batch, dense_extra=2)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs = wl.host_pool(batch)
+    rows = wl.host_current_rows(batch)
+    d_slabs = [torch.from_numpy(s).cuda() for s in slabs]
+    d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+    ps = batch.page_size
+    dense = torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows, page_size=ps,
+                                cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    layers.prefetch(d_slabs, dense)
+    torch.cuda.synchronize()
+    # after the prefetch: prefix and zero slots final, current slots untouched
+    got = dense.cpu().numpy().reshape(plan.dense_cap_pages, ps, batch.row_bytes)
+    owner = plan["owner"].cpu().numpy()
+    w3 = want.reshape(plan.dense_cap_pages, ps, batch.row_bytes)
+    for d in range(plan.dense_cap_pages):
+        if owner[d] >= batch.cp_size:
+            assert np.all(got[d] == 0xCD), d
+        else:
+            assert np.array_equal(got[d], w3[d]), d
+    layers.consume(d_rows, dense)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    assert np.array_equal(dense.cpu().numpy(), want)
+
+
+def test_gather_kinds_rejects_bad_mask():
+    batch = wl.tiny_batch()
+    plan, _ = _plan_pair(batch)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    with pytest.raises(cpkv.CpkvError):
+        layers.gather_kinds([torch.from_numpy(s).cuda() for s in wl.host_pool(batch)], layers.dense[0], 8)

@@ -64,7 +64,8 @@ def _check_plan(work):
 
 
 @pytest.mark.parametrize("config,variant", [("traced_78", "staging"), ("fp8_nsa", "staging"),
-                                            ("traced_78", "fused"), ("fp8_nsa", "fused")])
+                                            ("traced_78", "fused"), ("fp8_nsa", "fused"),
+                                            ("traced_78", "prefetch")])
 def test_benchmark_workload_matches_oracle(config, variant):
     work = bench.ComposeWorkload(config, variant=variant)
     try:
@@ -79,7 +80,7 @@ def test_benchmark_workload_matches_oracle(config, variant):
         _check_plan(work)
         _check_layer(work, work.num_layers - 2)
         g = _check_layer(work, work.num_layers - 1)
-        if variant == "staging":
+        if variant in ("staging", "prefetch"):
             _check_staging(work, g)
     finally:
         del work
