@@ -6,8 +6,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <utility>
-
 #include "cpkv.h"
 
 #define CPKV_DEV __device__ __forceinline__
@@ -180,18 +178,6 @@ CPKV_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "
 CPKV_DEV int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 // ---------------------------------------------------------------------------
-// programmatic dependent launch (a kernel launched with the programmatic
-// stream-serialization attribute may start before the previous kernel in the
-// stream has finished)
-// ---------------------------------------------------------------------------
-// Wait until the previous kernel in the stream has completed and its writes
-// are visible.  Returns at once when the launch had no such dependency.
-CPKV_DEV void pdl_wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Allow the next kernel in the stream to start launching now.
-CPKV_DEV void pdl_allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-// ---------------------------------------------------------------------------
 // scans
 // ---------------------------------------------------------------------------
 template <typename T>
@@ -255,24 +241,5 @@ inline int launch_status() {
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// Launch `kernel` with the programmatic stream-serialization attribute: it may
-// begin while the previous kernel in the stream is still running, and must
-// call pdl_wait_prior_grid() before it touches anything that kernel writes.
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args &&...args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
 
 }  // namespace cpkv

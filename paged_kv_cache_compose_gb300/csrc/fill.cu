@@ -150,11 +150,6 @@ __device__ void zero_pad_rows(const FillParams<MAXB> &p, int b) {
 // RIF = 0 selects the wide-row loop.
 template <int MAXB, int RIF, int VPL>
 __global__ void __launch_bounds__(kFillThreads, kBlocksPerSm) fill_current_kernel(const __grid_constant__ FillParams<MAXB> p) {
-  // The previous kernel in the stream (typically the gather of the previous
-  // layer, which reads the stagings) must be complete before any staging row
-  // is written; once it is, the next kernel (the gather) may start launching.
-  pdl_wait_prior_grid();
-  pdl_allow_next_grid();
   if ((int)blockIdx.x < p.nRow) {
     const uint64_t read_once = l2_policy_evict_first();
     const uint64_t keep = l2_policy_evict_last();
@@ -167,14 +162,11 @@ __global__ void __launch_bounds__(kFillThreads, kBlocksPerSm) fill_current_kerne
 
 template <int MAXB>
 int launch_fill(const FillParams<MAXB> &prm, int grid, cudaStream_t s) {
-  cudaError_t e;
-  const dim3 g(grid), b(kFillThreads);
-  if (prm.vpr <= 32) e = launch_pdl(fill_current_kernel<MAXB, 4, 1>, g, b, 0, s, prm);
-  else if (prm.vpr <= 64) e = launch_pdl(fill_current_kernel<MAXB, 4, 2>, g, b, 0, s, prm);
-  else if (prm.vpr <= 96) e = launch_pdl(fill_current_kernel<MAXB, 2, 3>, g, b, 0, s, prm);
-  else if (prm.vpr <= 128) e = launch_pdl(fill_current_kernel<MAXB, 2, 4>, g, b, 0, s, prm);
-  else e = launch_pdl(fill_current_kernel<MAXB, 0, 0>, g, b, 0, s, prm);
-  if (e != cudaSuccess) return CPKV_ERR_CUDA;
+  if (prm.vpr <= 32) fill_current_kernel<MAXB, 4, 1><<<grid, kFillThreads, 0, s>>>(prm);
+  else if (prm.vpr <= 64) fill_current_kernel<MAXB, 4, 2><<<grid, kFillThreads, 0, s>>>(prm);
+  else if (prm.vpr <= 96) fill_current_kernel<MAXB, 2, 3><<<grid, kFillThreads, 0, s>>>(prm);
+  else if (prm.vpr <= 128) fill_current_kernel<MAXB, 2, 4><<<grid, kFillThreads, 0, s>>>(prm);
+  else fill_current_kernel<MAXB, 0, 0><<<grid, kFillThreads, 0, s>>>(prm);
   return launch_status();
 }
 

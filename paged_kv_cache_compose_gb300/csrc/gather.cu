@@ -17,12 +17,6 @@
 // written for this gather.  Zero units (owner -1 or an invalid descriptor)
 // are written with plain 16-byte stores by the whole warp.  Every mbarrier
 // wait is bounded (see bulk_ring.cuh).
-//
-// The kernel is launched as a programmatic dependent of the previous kernel
-// in the stream: it first moves pool pages and zero slots (which depend on no
-// earlier kernel of the compose), then waits for the previous kernel, then
-// moves the current pages from the stagings.  Run right after the fill, the
-// first part overlaps the fill.
 #include <stdint.h>
 
 #include "bulk_ring.cuh"
@@ -87,21 +81,12 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
   __shared__ int ring_live[kStages];
   BulkRing<kStages, kLoadsInFlight> ring;
   ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
-  // Pool pages and zero slots depend on nothing the previous kernel in the
-  // stream writes (when launched right after cpkv_fill_current they overlap
-  // it); current pages come from the stagings that kernel fills, so they wait.
-  for (int pass = 0; pass < 2; ++pass) {
-    if (pass == 1) {
-      pdl_wait_prior_grid();
-      pdl_allow_next_grid();
-    }
-    for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-      bool skip;
-      const Unit x = resolve_unit(p, u, pass == 0 && threadIdx.x == 0, &skip);
-      if (skip || (slot_kind(p, p.owner[u / p.pieces]) == CPKV_GATHER_STAGING) != (pass == 1)) continue;
-      if (x.src == nullptr) warp_zero(x.dst, x.bytes);
-      else ring.push(x.src, x.dst, x.bytes);
-    }
+  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
+    bool skip;
+    const Unit x = resolve_unit(p, u, threadIdx.x == 0, &skip);
+    if (skip) continue;
+    if (x.src == nullptr) warp_zero(x.dst, x.bytes);
+    else ring.push(x.src, x.dst, x.bytes);
   }
   ring.drain();
 }
@@ -162,7 +147,7 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
   const int64_t cap = (int64_t)device_sm_count() * kCtasPerSm;
   const int grid = (int)(prm.units < cap ? prm.units : cap);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_pdl(gather_pages_kernel, dim3(grid), dim3(32), smem, s, prm) != cudaSuccess) return CPKV_ERR_CUDA;
+  gather_pages_kernel<<<grid, 32, smem, s>>>(prm);
   return launch_status();
 }
 
