@@ -186,23 +186,32 @@ class ComposeWorkload:
                                 device=self.device)
         self.layers = ComposeLayers(self.plan, b.row_bytes, num_dense=2)
         # pools: one per layer (own slab) unless the config shares one pool over its layers
-        self.shared_pool = config.startswith("fp8")
+        self.shared_pool = config in ("fp8_nsa", "index_k")
         n_pools = 1 if self.shared_pool else self.num_layers
         self.pools = [wl.device_pool(b, layer, self.device) for layer in range(n_pools)]
-        # all layers' current rows in one allocation, writer-major inside a layer,
-        # so the end-to-end leg can upload them with one copy
+        # all layers' current rows in one allocation (so the end-to-end leg can
+        # upload them with one copy): per layer, writer-major rows, or for planar
+        # pages plane-major then writer-major, each block 16-byte aligned
         counts = [int(x) for x in self.plan.tokens_per_writer]
-        self.rows_all = torch.empty((self.num_layers, b.T, b.row_bytes), dtype=torch.uint8, device=self.device)
+        planes = b.planes or (b.row_bytes,)
+        blocks = [(p, w, -(-counts[w] * wp // 16) * 16) for p, wp in enumerate(planes) for w in range(b.cp_size)]
+        per_layer = sum(n for _, _, n in blocks)
+        self.rows_all = torch.empty((self.num_layers, per_layer), dtype=torch.uint8, device=self.device)
         self.rows = []
         for layer in range(self.num_layers):
             g = wl.device_current_rows(b, layer, self.device)
-            views, off = [], 0
-            for w, part in enumerate(wl.device_split_rows_by_writer(b, g)):
-                dst = self.rows_all[layer, off:off + counts[w]]
-                dst.copy_(part)
-                views.append(dst)
-                off += counts[w]
-            self.rows.append(views)
+            parts = wl.device_split_rows_by_writer(b, g)
+            views = [[None] * b.cp_size for _ in planes]
+            off, col = 0, [0]
+            for wp in planes:
+                col.append(col[-1] + wp)
+            for p, w, n in blocks:
+                wp = planes[p]
+                dst = self.rows_all[layer, off:off + counts[w] * wp].view(counts[w], wp)
+                dst.copy_(parts[w][:, col[p]:col[p + 1]])
+                views[p][w] = dst
+                off += n
+            self.rows.append(views if b.planes else views[0])
             del g
         # ragged index plan of CP rank 0 over the batch's q tokens
         self.rb = wl.ragged_from_compose(b)
@@ -282,7 +291,10 @@ class ComposeWorkload:
             self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream)
             return
         if kind in ("all", "fill"):
-            self.layers.fill(self.rows[layer], stream)
+            if self.batch.planes:
+                self.layers.fill_planes(self.rows[layer], list(self.batch.planes), stream)
+            else:
+                self.layers.fill(self.rows[layer], stream)
         if kind in ("all", "gather"):
             self.layers.gather(self.pools_of(layer), dense, stream)
 
@@ -470,7 +482,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="traced_78", choices=["traced_78", "fp8_nsa", "plans"],
+    ap.add_argument("--config", default="traced_78", choices=["traced_78", "fp8_nsa", "index_k", "plans"],
                     help="plans: latency of the per-batch plan builders (ragged plan config, all CP ranks and "
                          "splits; compose plan of the traced and fp8 batches)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -596,7 +608,9 @@ def main(argv=None):
                          "U[0,16K] page-floored, page_size=64, cp=8 writer regions on one GPU, MLA 576xbf16 rows, "
                          "4096-page pool slab per layer" if a.config == "traced_78" else
                          "fp8 NSA compose, 78 layers: bs=32, 131072 current tokens, prefix U[0,64K], page_size=64, "
-                         "cp=8, 656-byte rows, one 2^20-page pool shared by the layers"),
+                         "cp=8, 656-byte rows, one 2^20-page pool shared by the layers" if a.config == "fp8_nsa" else
+                         "NSA indexer-key compose, 78 layers: the fp8 NSA batch with planar pages of 64 x (128-byte "
+                         "fp8 key + 4-byte scale) = 8448 bytes, one 2^20-page pool shared by the layers"),
             "B": b.B, "T": b.T, "C": work.plan.C, "D": work.plan.D, "layers": work.num_layers,
             "page_size": b.page_size, "cp_size": b.cp_size, "row_bytes": b.row_bytes,
             "variant": work.variant,

@@ -176,6 +176,41 @@ int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_bytes, cons
                       cpkv_stream_t stream);
 
 /*
+ * cpkv_fill_current_planes — per layer: the fill for planar pages (the
+ * NSA indexer's "index" kind, whose fill the pages keep separate from the
+ * token-KV index copy and point at the staging page inverse; "prefetch
+ * staging" message of commits 0d87bc5).  A planar page of ps tokens stores
+ * n_planes planes one after the other; plane p holds the ps tokens'
+ * h_plane_bytes[p]-byte slices in token order (reading: the indexer keys are
+ * a 128-byte fp8 key plane followed by a 4-byte fp32 scale plane, a page of
+ * 64 * 132 = 8448 bytes).  One plane of width R is the row layout.
+ *
+ * For every token t, with sr = d_staging_rows[t], slot = sr / ps,
+ * off = sr % ps, w = d_writer[slot - 1]:
+ *   plane p of staging[w] page slot, token off  <-  row d_token_writer_row[t]
+ *   of h_cur_planes[p * cp + w]
+ * then, for every request whose current length is not a multiple of ps, the
+ * slices after its last token up to the end of that page are zeroed in every
+ * plane.  Other staging bytes are not written.
+ *   n_planes          1..4; h_plane_bytes[p] a positive multiple of 4 and
+ *                     ps * sum(h_plane_bytes) a multiple of 16
+ *   h_cur_planes      host array [n_planes * cp] of device pointers: writer
+ *                     w's rows of plane p, [h_cur_rows_cap[w]][plane_bytes[p]],
+ *                     16-byte aligned
+ *   h_staging         host array [cp] of device pointers, each
+ *                     [staging_cap_pages][ps * sum(plane_bytes)] bytes
+ * The gather of planar pages is cpkv_compose_gather with
+ * row_bytes = sum(plane_bytes) (pages are copied as opaque bytes).
+ * Status bits: ROW_OOB / WRITER_OOB (that token is skipped).
+ */
+int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n_planes, const int32_t *h_plane_bytes,
+                             const int32_t *h_cur_lens, const void *const *h_cur_planes,
+                             const int64_t *h_cur_rows_cap, void *const *h_staging, int64_t staging_cap_pages,
+                             const int64_t *d_staging_rows, const int32_t *d_token_writer_row,
+                             const int32_t *d_writer, int64_t num_cur_pages, int32_t *d_status,
+                             cpkv_stream_t stream);
+
+/*
  * cpkv_compose_gather — per layer: the slot-dense page gather.  ONE call
  * fills every dense page: prefix pages from the owners' pools, all current
  * pages from the writers' stagings.
@@ -185,6 +220,8 @@ int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_bytes, cons
  *                    each a page array [h_src_cap_pages[k]][ps][R], 16-byte aligned
  *   d_owner, d_src   device int32 [dense_cap_pages] (from cpkv_plan_build)
  *   d_dense          device [dense_cap_pages * ps][R], 16-byte aligned
+ *   row_bytes        R; pages are opaque ps*R bytes, which must be a
+ *                    multiple of 16 (R itself need not be)
  * dense page d <- page d_src[d] of table[d_owner[d]] (ps*R contiguous bytes);
  * owner -1 -> zeros.  A descriptor outside the table or the source's capacity
  * raises DESC_OOB and its page is zero-filled.

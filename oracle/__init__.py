@@ -19,6 +19,10 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
   oracle_gather         pinned: per-slot brute force, -1 sentinel, golden
   oracle_fill_index_copy pinned: equals oracle_staging on plan-built indices;
                         a hand-worked permuted case
+  oracle_fill_planes, oracle_compose_dense_planes
+                        pinned: one plane equals the row functions; a
+                        hand-worked two-plane page; plane-by-plane reduction
+                        to the row definition
   oracle_ragged_plan    pinned: cumsum / repeat closed forms, tiling of every
                         request across ranks, cp=1 special case, golden
 """
@@ -84,8 +88,11 @@ def _declare(lib):
     lib.oracle_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P]
     lib.oracle_fill_index_copy.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P]
     lib.oracle_ragged_plan.argtypes = [_I, _I, _I, _P, _P, _P, _L] + [_P] * 11
+    lib.oracle_fill_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P]
+    lib.oracle_compose_dense_planes.argtypes = [_I, _I, _I, _I, _P, _L, _P, _P, _P, _P, _P, _L, _P]
     for f in ("oracle_sizes", "oracle_compose_plan", "oracle_compose_dense",
-              "oracle_staging", "oracle_gather", "oracle_ragged_plan", "oracle_fill_index_copy"):
+              "oracle_staging", "oracle_gather", "oracle_ragged_plan", "oracle_fill_index_copy",
+              "oracle_fill_planes", "oracle_compose_dense_planes"):
         getattr(lib, f).restype = _I
     return lib
 
@@ -217,6 +224,50 @@ def fill_index_copy(cur_lens, staging_rows, token_writer_row, writer, cur_rows_p
     return int(status[0])
 
 
+def fill_planes(cur_lens, staging_rows, token_writer_row, writer, cur_planes, staging_bufs, *, page_size, cp_size,
+                plane_bytes, lib=None) -> int:
+    """Planar fill as an index copy (in place on ``staging_bufs``, each
+    [staging_cap_pages, page_bytes] uint8).  ``cur_planes[p][w]`` is writer
+    w's plane-p rows [rows_w, plane_bytes[p]].  Returns the status bits."""
+    lib = lib or load()
+    cl, wr, pb = _i32(cur_lens), _i32(writer), _i32(plane_bytes)
+    sr = np.ascontiguousarray(np.asarray(staging_rows, dtype=np.int64))
+    tw = _i32(token_writer_row)
+    n_planes = len(pb)
+    flat = [np.ascontiguousarray(cur_planes[p][w], dtype=np.uint8) for p in range(n_planes) for w in range(cp_size)]
+    caps = np.array([flat[w].shape[0] for w in range(cp_size)], np.int64)
+    pt = (ctypes.c_void_p * len(flat))(*[a.ctypes.data if a.size else None for a in flat])
+    stt = (ctypes.c_void_p * cp_size)(*[s.ctypes.data for s in staging_bufs])
+    cap_pages = staging_bufs[0].shape[0]
+    status = np.zeros(1, np.int32)
+    rc = lib.oracle_fill_planes(len(cl), page_size, cp_size, n_planes, _ptr(pb), _ptr(cl), _ptr(sr), _ptr(tw),
+                                _ptr(wr), len(wr), ctypes.cast(pt, ctypes.c_void_p), _ptr(caps),
+                                ctypes.cast(stt, ctypes.c_void_p), cap_pages, _ptr(status))
+    _check(rc, "oracle_fill_planes")
+    return int(status[0])
+
+
+def compose_dense_planes(prefix_lens, cur_lens, prefix_pages, pool_slabs, cur_planes, *, page_size, cp_size,
+                         plane_bytes, dense_cap=None, lib=None) -> np.ndarray:
+    """Dense planar KV [dense_cap, page_bytes] by the plain definition.
+    ``pool_slabs[r]``: [slab_pages, page_bytes]; ``cur_planes[p]``: [T, plane_bytes[p]] batch order."""
+    lib = lib or load()
+    pl, cl, pp, pb = _i32(prefix_lens), _i32(cur_lens), _i32(prefix_pages), _i32(plane_bytes)
+    slabs = [np.ascontiguousarray(s, dtype=np.uint8) for s in pool_slabs]
+    planes = [np.ascontiguousarray(c, dtype=np.uint8) for c in cur_planes]
+    page_bytes = int(page_size * pb.sum())
+    T, C, D = sizes(pl, cl, page_size, lib)
+    cap = D if dense_cap is None else int(dense_cap)
+    st = (ctypes.c_void_p * cp_size)(*[s.ctypes.data for s in slabs])
+    ct = (ctypes.c_void_p * len(planes))(*[c.ctypes.data if c.size else None for c in planes])
+    dense = np.empty((cap, page_bytes), np.uint8)
+    rc = lib.oracle_compose_dense_planes(len(pl), page_size, cp_size, len(pb), _ptr(pb), slabs[0].shape[0], _ptr(pl),
+                                         _ptr(cl), _ptr(pp), ctypes.cast(st, ctypes.c_void_p),
+                                         ctypes.cast(ct, ctypes.c_void_p), cap, _ptr(dense))
+    _check(rc, "oracle_compose_dense_planes")
+    return dense
+
+
 def gather(table_bufs, cap_pages, owner, src, *, page_size, row_bytes, dense_cap, lib=None):
     """Slot-dense page gather, descriptor by descriptor.  Returns (dense, status)."""
     lib = lib or load()
@@ -258,5 +309,6 @@ def ragged_plan(prefix_lens, q_lens, cp_index, *, chunk, k_align=1, lib=None) ->
 
 __all__ = [
     "build", "load", "compile_oracle", "sizes", "compose_plan", "compose_dense", "staging", "fill_index_copy",
+    "fill_planes", "compose_dense_planes",
     "gather", "ragged_plan", "OracleError",
 ]

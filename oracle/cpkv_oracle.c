@@ -308,6 +308,115 @@ int oracle_fill_index_copy(int B, int ps, int cp, int64_t R, const int32_t *cur_
 }
 
 /*
+ * Planar pages (the index kind of [P]: its own fill kernel, pointed at the
+ * staging page inverse).  Reading taken here: a page of ps tokens stores
+ * n_planes planes one after the other; plane p holds the ps tokens' w_p-byte
+ * slices in token order, so token `off` of the page has its plane-p slice at
+ * byte  ps * (w_0 + ... + w_{p-1}) + off * w_p  of the page, and a page is
+ * ps * (w_0 + ... + w_{n-1}) bytes.  One plane of width R is the row layout.
+ *
+ * The fill as an index copy over planes: for every token t, with
+ * sr = staging_rows[t], slot = sr / ps, off = sr % ps and
+ * w = writer[slot - 1], plane p of staging[w] page `slot` row `off` <-
+ * cur_planes[p * cp + w] row token_writer_row[t] (w_p bytes); then for every
+ * request whose current length is not a multiple of ps, the slices of the
+ * rows after its last token up to the end of that page are zero in every
+ * plane.  Violations skip the token and raise ORC_ROW_OOB / ORC_WRITER_OOB.
+ */
+int oracle_fill_planes(int B, int ps, int cp, int n_planes, const int32_t *plane_bytes,
+                       const int32_t *cur_lens, const int64_t *staging_rows,
+                       const int32_t *token_writer_row, const int32_t *writer, int64_t C,
+                       const uint8_t *const *cur_planes, const int64_t *cur_cap,
+                       uint8_t *const *staging, int64_t staging_cap_pages, int32_t *status) {
+  int64_t page_bytes = 0;
+  for (int p = 0; p < n_planes; ++p) page_bytes += (int64_t)ps * plane_bytes[p];
+  int64_t T = 0;
+  for (int b = 0; b < B; ++b) T += cur_lens[b];
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t sr = staging_rows[t];
+    int64_t slot = sr / ps, off = sr % ps;
+    if (sr < ps || sr >= staging_cap_pages * ps || slot > C) { *status |= ORC_ROW_OOB; continue; }
+    int32_t w = writer[slot - 1];
+    if (w < 0 || w >= cp) { *status |= ORC_WRITER_OOB; continue; }
+    int32_t r = token_writer_row[t];
+    if (r < 0 || r >= cur_cap[w]) { *status |= ORC_ROW_OOB; continue; }
+    int64_t plane_start = 0;
+    for (int p = 0; p < n_planes; ++p) {
+      int64_t wp = plane_bytes[p];
+      memcpy(staging[w] + slot * page_bytes + plane_start + off * wp, cur_planes[p * cp + w] + r * wp,
+             (size_t)wp);
+      plane_start += ps * wp;
+    }
+  }
+  int64_t last = -1;
+  for (int b = 0; b < B; ++b) {
+    last += cur_lens[b];
+    if (cur_lens[b] % ps == 0) continue;
+    int64_t sr = staging_rows[last];
+    int64_t slot = sr / ps;
+    if (sr < ps || sr >= staging_cap_pages * ps || slot > C) { *status |= ORC_ROW_OOB; continue; }
+    int32_t w = writer[slot - 1];
+    if (w < 0 || w >= cp) { *status |= ORC_WRITER_OOB; continue; }
+    int64_t plane_start = 0;
+    for (int p = 0; p < n_planes; ++p) {
+      int64_t wp = plane_bytes[p];
+      for (int64_t off = sr % ps + 1; off < ps; ++off)
+        memset(staging[w] + slot * page_bytes + plane_start + off * wp, 0, (size_t)wp);
+      plane_start += ps * wp;
+    }
+  }
+  return ORC_OK;
+}
+
+/*
+ * The plain definition of the composed dense KV for planar pages: request by
+ * request, its prefix tokens' slices copied from their pool pages, then its
+ * current tokens' slices from the batch-ordered current planes
+ * (cur_planes[p] is [T][w_p]), then zero slices up to the page boundary;
+ * pages past the batch are zero.  Pool slab r is [slab_pages][page_bytes].
+ */
+int oracle_compose_dense_planes(int B, int ps, int cp, int n_planes, const int32_t *plane_bytes,
+                                int64_t slab_pages, const int32_t *prefix_lens, const int32_t *cur_lens,
+                                const int32_t *prefix_pages, const uint8_t *const *pool_slabs,
+                                const uint8_t *const *cur_planes, int64_t dense_cap, uint8_t *dense_out) {
+  int64_t T, C, D;
+  int rc = oracle_sizes(B, ps, prefix_lens, cur_lens, &T, &C, &D);
+  if (rc) return rc;
+  if (dense_cap < D) return ORC_CAPACITY;
+  int64_t page_bytes = 0;
+  for (int p = 0; p < n_planes; ++p) page_bytes += (int64_t)ps * plane_bytes[p];
+  int64_t row = 0, pfx_cur = 0, tok = 0;  /* row = dense token position */
+  for (int b = 0; b < B; ++b) {
+    int64_t n_tok = prefix_lens[b] + cur_lens[b];
+    int64_t padded = ((n_tok + ps - 1) / ps) * ps;
+    for (int64_t k = 0; k < padded; ++k) {
+      int64_t page = (row + k) / ps, off = (row + k) % ps;
+      int64_t plane_start = 0;
+      for (int p = 0; p < n_planes; ++p) {
+        int64_t wp = plane_bytes[p];
+        uint8_t *dst = dense_out + page * page_bytes + plane_start + off * wp;
+        if (k < prefix_lens[b]) {
+          int64_t lp = prefix_pages[pfx_cur + k / ps];
+          int64_t owner = lp % cp, local = lp / cp;
+          if (lp < 1 || local >= slab_pages) return ORC_BAD_ARG;
+          memcpy(dst, pool_slabs[owner] + local * page_bytes + plane_start + (k % ps) * wp, (size_t)wp);
+        } else if (k < n_tok) {
+          memcpy(dst, cur_planes[p] + (tok + k - prefix_lens[b]) * wp, (size_t)wp);
+        } else {
+          memset(dst, 0, (size_t)wp);
+        }
+        plane_start += ps * wp;
+      }
+    }
+    row += padded;
+    pfx_cur += prefix_lens[b] / ps;
+    tok += cur_lens[b];
+  }
+  if (row < dense_cap * ps) memset(dense_out + (row / ps) * page_bytes, 0, (size_t)((dense_cap - row / ps) * page_bytes));
+  return ORC_OK;
+}
+
+/*
  * Slot-dense page gather [A][E], descriptor by descriptor: dense page d is a
  * copy of page src[d] of table[owner[d]], or zeros when owner[d] == -1.  A
  * descriptor outside the table or the source's capacity is a violation: the

@@ -44,6 +44,7 @@ MAX_BATCH = 1024
 
 EXPORTED = (
     "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_fill_current",
+    "cpkv_fill_current_planes",
     "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
     "cpkv_version",
 )
@@ -71,6 +72,7 @@ def _declare(lib):
     lib.cpkv_plan_build.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _L] + [_P] * 11
     lib.cpkv_fill_current.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
     lib.cpkv_compose_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_fill_current_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
     lib.cpkv_compose_gather_kinds.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _I, _P, _P, _P]
     lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
@@ -202,6 +204,24 @@ def cpkv_fill_current(cur_lens, cur_rows: Sequence, staging: Sequence, *, page_s
         ctypes.cast(stg_arr, _P), staging_cap_pages, _dp(d_staging_rows), _dp(d_token_writer_row),
         _dp(d_writer), num_cur_pages, _dp(d_status), _stream(stream))
     _check("cpkv_fill_current", rc)
+
+
+def cpkv_fill_current_planes(cur_lens, cur_planes: Sequence, staging: Sequence, *, page_size, cp_size, plane_bytes,
+                             staging_cap_pages, d_staging_rows, d_token_writer_row, d_writer, num_cur_pages,
+                             d_status, cur_rows_cap=None, stream=None):
+    """Planar-page fill.  ``cur_planes[p][w]``: writer w's rows of plane p (uint8 CUDA tensors)."""
+    cl, pb = _host_i32(cur_lens), _host_i32(plane_bytes)
+    n_planes = len(pb)
+    if cur_rows_cap is None:
+        cur_rows_cap = [cur_planes[0][w].numel() // int(pb[0]) for w in range(cp_size)]
+    caps = _host_i64(cur_rows_cap)
+    flat = _ptr_array([cur_planes[p][w] for p in range(n_planes) for w in range(cp_size)])
+    stg = _ptr_array(staging)
+    rc = load().cpkv_fill_current_planes(len(cl), page_size, cp_size, n_planes, _hp(pb), _hp(cl),
+                                         ctypes.cast(flat, _P), _hp(caps), ctypes.cast(stg, _P), staging_cap_pages,
+                                         _dp(d_staging_rows), _dp(d_token_writer_row), _dp(d_writer), num_cur_pages,
+                                         _dp(d_status), _stream(stream))
+    _check("cpkv_fill_current_planes", rc)
 
 
 def cpkv_compose_gather(src_table: Sequence, src_cap_pages, d_owner, d_src, d_dense, *, page_size, cp_size,

@@ -1,0 +1,227 @@
+// cpkv_fill_current_planes: the per-layer fill for planar pages — the
+// "index" kind of the pages, whose fill kernel is its own and is only pointed
+// at the staging page inverse ("prefetch staging" message of commits
+// 0d87bc5).  A planar page of ps tokens stores its planes one after the
+// other; plane p holds the ps tokens' w_p-byte slices in token order (the NSA
+// indexer keys: a 128-byte fp8 key plane, then a 4-byte fp32 scale plane).
+// A token row therefore is not contiguous in the page, which is why an index
+// copy of whole rows cannot fill it.
+//
+// For every token t (an index copy over planes, any row indices):
+//   sr = staging_rows[t], slot = sr / ps, off = sr % ps, w = writer[slot - 1]
+//   plane p of staging[w] page slot, token off  <-  cur_planes[p][w] row
+//   token_writer_row[t]
+// and for every request whose current length is not a multiple of ps, the
+// slices after its last token up to the end of that page are zero in every
+// plane.
+//
+// Blocks [0, nTile) take tiles of 256 tokens: the tile's indices are resolved
+// once into shared memory, then each plane is copied as a flat loop over
+// (token, unit) with consecutive threads on consecutive units, so a warp
+// reads and writes contiguous bytes (a unit is 16 bytes when the plane allows
+// it, else 4).  Blocks [nTile, nTile + B) zero the pad slices.
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace cpkv {
+namespace {
+
+constexpr int kThreads = 256;  // also the tokens per tile
+constexpr int kMaxPlanes = 4;
+
+template <int MAXB>
+struct PlaneParams {
+  const uint8_t *planes[kMaxPlanes][CPKV_MAX_CP];  // writer w's rows of plane p
+  int64_t cur_cap[CPKV_MAX_CP];
+  uint8_t *staging[CPKV_MAX_CP];
+  const int64_t *staging_rows;
+  const int32_t *token_writer_row, *writer;
+  int32_t *status;
+  int64_t T, C, staging_cap_rows, page_bytes;
+  int32_t plane_bytes[kMaxPlanes], plane_start[kMaxPlanes], plane_unit[kMaxPlanes];
+  int32_t n_planes, ps, cp, B, nTile;
+  int32_t cur_lens[MAXB];
+};
+
+template <int MAXB>
+__device__ void copy_tile(const PlaneParams<MAXB> &p, int64_t t0) {
+  __shared__ uint8_t *dst_page[kThreads];  // staging page base of each token (nullptr: skip)
+  __shared__ int32_t dst_off[kThreads];    // token slot inside the page
+  __shared__ int32_t src_row[kThreads];
+  __shared__ int32_t src_w[kThreads];
+  const int j = threadIdx.x;
+  const int64_t t = t0 + j;
+  uint8_t *page = nullptr;
+  int32_t off = 0, row = 0, w = 0;
+  if (t < p.T) {
+    const int64_t sr = p.staging_rows[t];
+    const int64_t slot = sr / p.ps;
+    if (sr < p.ps || sr >= p.staging_cap_rows || slot > p.C) {
+      raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    } else {
+      w = p.writer[slot - 1];
+      row = p.token_writer_row[t];
+      if (w < 0 || w >= p.cp) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
+      else if (row < 0 || row >= p.cur_cap[w]) raise_status(p.status, CPKV_STATUS_ROW_OOB);
+      else {
+        page = p.staging[w] + slot * p.page_bytes;
+        off = (int32_t)(sr - slot * p.ps);
+      }
+    }
+  }
+  dst_page[j] = page;
+  dst_off[j] = off;
+  src_row[j] = row;
+  src_w[j] = w;
+  __syncthreads();
+  const int ntok = (int)min64(kThreads, p.T - t0);
+  for (int pl = 0; pl < p.n_planes; ++pl) {
+    const int32_t wp = p.plane_bytes[pl], unit = p.plane_unit[pl], start = p.plane_start[pl];
+    const int32_t upt = wp / unit;  // units per token
+    const int total = ntok * upt;
+    for (int i = j; i < total; i += kThreads) {
+      const int k = i / upt, u = i - k * upt;
+      uint8_t *dp = dst_page[k];
+      if (dp == nullptr) continue;
+      uint8_t *d = dp + start + (int64_t)dst_off[k] * wp + (int64_t)u * unit;
+      const uint8_t *s = p.planes[pl][src_w[k]] + (int64_t)src_row[k] * wp + (int64_t)u * unit;
+      if (unit == 16) {
+        *reinterpret_cast<uint4 *>(d) = ld_stream16(s);
+      } else {
+        *reinterpret_cast<uint32_t *>(d) = __ldg(reinterpret_cast<const uint32_t *>(s));
+      }
+    }
+  }
+}
+
+// Zero the slices after request b's last token up to the end of its page.
+template <int MAXB>
+__device__ void zero_pad(const PlaneParams<MAXB> &p, int b) {
+  __shared__ int64_t last_tok;
+  if (b >= p.B) return;
+  const int32_t rem = p.cur_lens[b] % p.ps;
+  if (rem == 0) return;
+  if (threadIdx.x == 0) {
+    int64_t s = 0;
+    for (int k = 0; k <= b; ++k) s += p.cur_lens[k];
+    last_tok = s - 1;
+  }
+  __syncthreads();
+  const int64_t sr = p.staging_rows[last_tok];
+  const int64_t slot = sr / p.ps;
+  if (sr < p.ps || sr >= p.staging_cap_rows || slot > p.C) {
+    if (threadIdx.x == 0) raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    return;
+  }
+  const int32_t w = p.writer[slot - 1];
+  if (w < 0 || w >= p.cp) {
+    if (threadIdx.x == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
+    return;
+  }
+  uint8_t *page = p.staging[w] + slot * p.page_bytes;
+  const int64_t first = sr - slot * p.ps + 1;  // first pad token slot
+  for (int pl = 0; pl < p.n_planes; ++pl) {
+    uint32_t *z = reinterpret_cast<uint32_t *>(page + p.plane_start[pl] + first * p.plane_bytes[pl]);
+    const int64_t words = (p.ps - first) * p.plane_bytes[pl] / 4;
+    for (int64_t i = threadIdx.x; i < words; i += kThreads) z[i] = 0u;
+  }
+}
+
+template <int MAXB>
+__global__ void __launch_bounds__(kThreads) fill_planes_kernel(const __grid_constant__ PlaneParams<MAXB> p) {
+  if ((int)blockIdx.x < p.nTile) {
+    for (int64_t t0 = (int64_t)blockIdx.x * kThreads; t0 < p.T; t0 += (int64_t)p.nTile * kThreads) {
+      copy_tile(p, t0);
+      __syncthreads();  // the tile's shared indices are reused by the next tile
+    }
+  } else {
+    zero_pad(p, blockIdx.x - p.nTile);
+  }
+}
+
+}  // namespace
+}  // namespace cpkv
+
+extern "C" int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n_planes, const int32_t *h_plane_bytes,
+                                        const int32_t *h_cur_lens, const void *const *h_cur_planes,
+                                        const int64_t *h_cur_rows_cap, void *const *h_staging,
+                                        int64_t staging_cap_pages, const int64_t *d_staging_rows,
+                                        const int32_t *d_token_writer_row, const int32_t *d_writer,
+                                        int64_t num_cur_pages, int32_t *d_status, cpkv_stream_t stream) {
+  using namespace cpkv;
+  if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
+  if (n_planes < 1 || n_planes > kMaxPlanes || h_plane_bytes == nullptr) return CPKV_ERR_ARG;
+  if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
+  if (h_cur_planes == nullptr || h_cur_rows_cap == nullptr || h_staging == nullptr || d_status == nullptr)
+    return CPKV_ERR_ARG;
+  if (B > 0 && h_cur_lens == nullptr) return CPKV_ERR_ARG;
+  int64_t row_bytes = 0;
+  for (int p = 0; p < n_planes; ++p) {
+    if (h_plane_bytes[p] <= 0 || h_plane_bytes[p] % 4 != 0) return CPKV_ERR_ARG;
+    row_bytes += h_plane_bytes[p];
+  }
+  const int64_t page_bytes = (int64_t)page_size * row_bytes;
+  if (page_bytes % 16 != 0 || page_bytes > INT32_MAX) return CPKV_ERR_ARG;
+  int64_t T = 0, C = 0;
+  for (int b = 0; b < B; ++b) {
+    if (h_cur_lens[b] < 0) return CPKV_ERR_ARG;
+    T += h_cur_lens[b];
+    C += ceil_div(h_cur_lens[b], page_size);
+  }
+  if (num_cur_pages != C) return CPKV_ERR_ARG;
+  if (T > INT32_MAX - 1 || C > INT32_MAX - 2) return CPKV_ERR_LIMIT;
+  if (staging_cap_pages < C + 1) return CPKV_ERR_CAPACITY;
+  if (T > 0 && (d_staging_rows == nullptr || d_token_writer_row == nullptr || d_writer == nullptr))
+    return CPKV_ERR_ARG;
+  for (int w = 0; w < cp_size; ++w) {
+    if (h_staging[w] == nullptr || !aligned16(h_staging[w])) return CPKV_ERR_ARG;
+    if (h_cur_rows_cap[w] < 0) return CPKV_ERR_ARG;
+    for (int p = 0; p < n_planes; ++p) {
+      const void *ptr = h_cur_planes[p * cp_size + w];
+      if (h_cur_rows_cap[w] > 0 && (ptr == nullptr || !aligned16(ptr))) return CPKV_ERR_ARG;
+    }
+  }
+  if (T == 0) return CPKV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t tiles = ceil_div(T, kThreads);
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  const int nTile = (int)(tiles < cap ? tiles : cap);
+
+#define CPKV_FILL_PLANES(prm)                                                                          \
+  for (int p = 0; p < kMaxPlanes; ++p)                                                                 \
+    for (int w = 0; w < CPKV_MAX_CP; ++w)                                                              \
+      prm.planes[p][w] = (p < n_planes && w < cp_size)                                                 \
+                             ? static_cast<const uint8_t *>(h_cur_planes[p * cp_size + w]) : nullptr;  \
+  for (int w = 0; w < CPKV_MAX_CP; ++w) {                                                              \
+    prm.cur_cap[w] = w < cp_size ? h_cur_rows_cap[w] : 0;                                              \
+    prm.staging[w] = w < cp_size ? static_cast<uint8_t *>(h_staging[w]) : nullptr;                     \
+  }                                                                                                    \
+  {                                                                                                    \
+    int32_t start = 0;                                                                                 \
+    for (int p = 0; p < kMaxPlanes; ++p) {                                                             \
+      const int32_t wp = p < n_planes ? h_plane_bytes[p] : 0;                                          \
+      prm.plane_bytes[p] = wp;                                                                         \
+      prm.plane_start[p] = start;                                                                      \
+      prm.plane_unit[p] = (wp % 16 == 0 && start % 16 == 0) ? 16 : 4;                                 \
+      start += page_size * wp;                                                                         \
+    }                                                                                                  \
+  }                                                                                                    \
+  prm.staging_rows = d_staging_rows; prm.token_writer_row = d_token_writer_row; prm.writer = d_writer; \
+  prm.status = d_status; prm.T = T; prm.C = C; prm.staging_cap_rows = staging_cap_pages * page_size;  \
+  prm.page_bytes = page_bytes; prm.n_planes = n_planes; prm.ps = page_size; prm.cp = cp_size;         \
+  prm.B = B; prm.nTile = nTile;                                                                        \
+  for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
+
+  if (B <= 64) {
+    PlaneParams<64> prm;
+    CPKV_FILL_PLANES(prm)
+    fill_planes_kernel<64><<<nTile + B, kThreads, 0, s>>>(prm);
+    return launch_status();
+  }
+  PlaneParams<CPKV_MAX_BATCH> prm;
+  CPKV_FILL_PLANES(prm)
+#undef CPKV_FILL_PLANES
+  fill_planes_kernel<CPKV_MAX_BATCH><<<nTile + B, kThreads, 0, s>>>(prm);
+  return launch_status();
+}

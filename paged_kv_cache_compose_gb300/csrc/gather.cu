@@ -101,7 +101,7 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
   using namespace cpkv;
   if (kinds < 0 || kinds > CPKV_GATHER_ALL) return CPKV_ERR_ARG;
   if (page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
-  if (row_bytes <= 0 || row_bytes % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
+  if (row_bytes <= 0 || ((int64_t)page_size * row_bytes) % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
   if (h_src_table == nullptr || h_src_cap_pages == nullptr || d_status == nullptr) return CPKV_ERR_ARG;
   if (dense_cap_pages == 0) return CPKV_OK;
   if (d_owner == nullptr || d_src == nullptr || d_dense == nullptr || !aligned16(d_dense)) return CPKV_ERR_ARG;

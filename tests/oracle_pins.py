@@ -358,6 +358,79 @@ def pin_fill_index_copy_permuted(lib):
     assert np.all(stg[0][3] == 0xEE)
 
 
+def pin_planes_golden(lib):
+    """Hand-worked two-plane page: ps=2, planes of 8 and 4 bytes, cp=1, one
+    request with a 2-token prefix on logical page 3 and 1 current token on
+    page 5 (writer 0).  Pool page 3 = [0x11 x8][0x12 x8][0x21 x4][0x22 x4]
+    (plane 0 rows 0,1 then plane 1 rows 0,1); the current token is 0x31 x8 /
+    0x41 x4.  Dense page 0 is the pool page; dense page 1 is
+    [0x31 x8][0 x8][0x41 x4][0 x4]; staging slot 1 holds the same bytes and
+    slot 0 keeps its guard bytes."""
+    ps, pb = 2, [8, 4]
+    page = bytes([0x11] * 8 + [0x12] * 8 + [0x21] * 4 + [0x22] * 4)
+    slab = np.zeros((6, 24), np.uint8)
+    slab[3] = np.frombuffer(page, np.uint8)
+    cur = [np.full((1, 8), 0x31, np.uint8), np.full((1, 4), 0x41, np.uint8)]
+    dense = oracle.compose_dense_planes([2], [1], [3], [slab], cur, page_size=ps, cp_size=1, plane_bytes=pb, lib=lib)
+    want1 = np.frombuffer(bytes([0x31] * 8 + [0] * 8 + [0x41] * 4 + [0] * 4), np.uint8)
+    assert np.array_equal(dense[0], slab[3]) and np.array_equal(dense[1], want1)
+    stg = [np.full((2, 24), 0xEE, np.uint8)]
+    st = oracle.fill_planes([1], [2], [0], [0], [[cur[0]], [cur[1]]], stg, page_size=ps, cp_size=1, plane_bytes=pb,
+                            lib=lib)
+    assert st == 0
+    assert np.all(stg[0][0] == 0xEE) and np.array_equal(stg[0][1], want1)
+
+
+def _split_planes(pages, ps, pb):
+    """[n, ps*sum(pb)] planar pages -> list over planes of [n, ps, w_p] row pages."""
+    out, start = [], 0
+    for w in pb:
+        out.append(pages[:, start:start + ps * w].reshape(pages.shape[0], ps, w))
+        start += ps * w
+    return out
+
+
+def pin_planes_reduce_to_rows(lib, batch, pb=(128, 4)):
+    """Plane p of the planar compose equals the row compose (width w_p) of
+    plane p of every input; one plane of width R equals the row layout."""
+    ps, cp = batch.page_size, batch.cp_size
+    rng = np.random.default_rng(batch.seed + 77)
+    pbytes = ps * sum(pb)
+    slabs = [np.frombuffer(rng.bytes(batch.slab_pages * pbytes), np.uint8).reshape(batch.slab_pages, pbytes).copy()
+             for _ in range(cp)]
+    planes = [np.frombuffer(rng.bytes(batch.T * w), np.uint8).reshape(batch.T, w).copy() for w in pb]
+    dense = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, planes,
+                                        page_size=ps, cp_size=cp, plane_bytes=list(pb), lib=lib)
+    dense_planes = _split_planes(dense, ps, pb)
+    slab_planes = [_split_planes(s, ps, pb) for s in slabs]
+    for p, w in enumerate(pb):
+        want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages,
+                                    [np.ascontiguousarray(sp[p]) for sp in slab_planes], planes[p], page_size=ps,
+                                    cp_size=cp, lib=lib)
+        assert np.array_equal(dense_planes[p].reshape(-1, w), want), p
+    # fill: plane by plane equals the row index copy
+    plan = oracle.compose_plan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                               page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages, lib=lib)
+    tw = wl.token_writer(batch)
+    per_writer = [[np.ascontiguousarray(pl[tw == w]) for w in range(cp)] for pl in planes]
+    stg = [np.full((batch.C + 1, pbytes), 0x5D, np.uint8) for _ in range(cp)]
+    st = oracle.fill_planes(batch.cur_lens, plan["staging_rows"], plan["token_writer_row"], batch.writer, per_writer,
+                            stg, page_size=ps, cp_size=cp, plane_bytes=list(pb), lib=lib)
+    assert st == 0
+    for p, w in enumerate(pb):
+        rows_stg = [np.ascontiguousarray(_split_planes(x, ps, pb)[p]).reshape(-1, w) for x in stg]
+        ref = [np.full(((batch.C + 1) * ps, w), 0x5D, np.uint8) for _ in range(cp)]
+        oracle.fill_index_copy(batch.cur_lens, plan["staging_rows"], plan["token_writer_row"], batch.writer,
+                               per_writer[p], ref, page_size=ps, cp_size=cp, row_bytes=w, lib=lib)
+        for x in range(cp):
+            assert np.array_equal(rows_stg[x], ref[x]), (p, x)
+    # one plane of width R: the row layout itself
+    one = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages,
+                                      [s.reshape(batch.slab_pages, -1)[:, :ps * pb[0]].copy() for s in slabs],
+                                      [planes[0]], page_size=ps, cp_size=cp, plane_bytes=[pb[0]], lib=lib)
+    assert np.array_equal(one.reshape(-1, pb[0]), dense_planes[0].reshape(-1, pb[0]))
+
+
 def pin_gather_sentinel_and_oob(lib):
     rng = np.random.default_rng(3)
     ps, R = 4, 16
@@ -522,6 +595,8 @@ ALL_PINS = [
     ("cp1_index_select_cat", lambda lib: pin_cp1_index_select_cat(lib)),
     ("gather_sentinel", lambda lib: pin_gather_sentinel_and_oob(lib)),
     ("fill_index_copy_permuted", lambda lib: pin_fill_index_copy_permuted(lib)),
+    ("planes_golden", lambda lib: pin_planes_golden(lib)),
+    ("planes_reduce_to_rows", lambda lib: [pin_planes_reduce_to_rows(lib, b) for b in edge_batches() if b.B > 0]),
     ("fill_index_copy", lambda lib: [pin_fill_index_copy(lib, b) for b in edge_batches()]),
     ("errors", lambda lib: pin_errors(lib)),
     ("plan_brute_force", lambda lib: [pin_plan_brute_force(lib, b, 2) for b in edge_batches()]),

@@ -1,0 +1,110 @@
+"""GPU parity of the planar-page (NSA indexer key) fill and compose against
+the oracle's planar definitions, byte-exact."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins as pins
+import workloads as wl
+from paged_kv_cache_compose_gb300 import cpkv
+from paged_kv_cache_compose_gb300.runtime import ComposeLayers, ComposePlan
+
+pytestmark = pytest.mark.gpu
+
+
+def _planar(batch, planes=wl.INDEX_K_PLANES):
+    return dataclasses.replace(batch, row_bytes=sum(planes), planes=tuple(planes), row_kind="bytes")
+
+
+def _inputs(batch, seed=0):
+    rng = np.random.default_rng(batch.seed + 1000 + seed)
+    pbytes = batch.page_size * batch.row_bytes
+    slabs = [np.frombuffer(rng.bytes(batch.slab_pages * pbytes), np.uint8).reshape(batch.slab_pages, pbytes).copy()
+             for _ in range(batch.cp_size)]
+    rows = np.frombuffer(rng.bytes(batch.T * batch.row_bytes), np.uint8).reshape(batch.T, batch.row_bytes).copy()
+    planes = wl.split_planes(rows, batch.planes)
+    tw = wl.token_writer(batch)
+    per_writer = [[np.ascontiguousarray(pl[tw == w]) for w in range(batch.cp_size)] for pl in planes]
+    return slabs, planes, per_writer
+
+
+def _edge_planar():
+    return [_planar(b) for b in pins.edge_batches() if (b.page_size * 132) % 16 == 0]
+
+
+def _compose(batch, per_writer_mut=None, reverse_rows=False):
+    ps, cp = batch.page_size, batch.cp_size
+    plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                       page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages,
+                       dense_cap_pages=None).build()
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs, planes, per_writer = _inputs(batch)
+    for st in layers.staging:
+        st.fill_(0x6B)
+    d_planes = [[torch.from_numpy(x).cuda() for x in pw] for pw in per_writer]
+    tw = plan["token_writer_row"]
+    if reverse_rows:  # source rows reversed inside every page: the index copy must still hold
+        h = tw.cpu().numpy().copy()
+        t = 0
+        for n in batch.cur_lens.tolist():
+            for k in range(0, n, ps):
+                m = min(ps, n - k)
+                h[t + k:t + k + m] = h[t + k:t + k + m][::-1]
+            t += n
+        tw = torch.from_numpy(h).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_fill_current_planes(batch.cur_lens, d_planes, layers.staging, page_size=ps, cp_size=cp,
+                                  plane_bytes=list(batch.planes), staging_cap_pages=plan.staging_cap_pages,
+                                  d_staging_rows=plan["staging_rows"], d_token_writer_row=tw, d_writer=plan.d_writer,
+                                  num_cur_pages=plan.C, d_status=status)
+    dense = torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
+    layers.gather([torch.from_numpy(s).cuda() for s in slabs], dense)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and int(plan.d_status.item()) == 0
+    # staging against the planar index copy
+    want_stg = [np.full((plan.staging_cap_pages, ps * batch.row_bytes), 0x6B, np.uint8) for _ in range(cp)]
+    st = oracle.fill_planes(batch.cur_lens, plan["staging_rows"].cpu().numpy(), tw.cpu().numpy(), batch.writer,
+                            per_writer, want_stg, page_size=ps, cp_size=cp, plane_bytes=list(batch.planes))
+    assert st == 0
+    for w in range(cp):
+        assert np.array_equal(layers.staging[w].cpu().numpy().reshape(plan.staging_cap_pages, -1), want_stg[w]), w
+    return dense, plan, slabs, planes
+
+
+@pytest.mark.parametrize("batch", _edge_planar(), ids=lambda b: b.name)
+def test_planar_compose_matches_oracle(batch):
+    dense, plan, slabs, planes = _compose(batch)
+    want = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, planes,
+                                       page_size=batch.page_size, cp_size=batch.cp_size,
+                                       plane_bytes=list(batch.planes))
+    assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, -1), want)
+
+
+@pytest.mark.parametrize("batch", _edge_planar()[:4], ids=lambda b: b.name)
+def test_planar_fill_reversed_rows(batch):
+    _compose(batch, reverse_rows=True)
+
+
+@pytest.mark.parametrize("planes", [(16,), (64, 4), (4, 4, 8), (128, 4), (32, 16, 4, 12)])
+def test_planar_plane_shapes(planes):
+    b = _planar(wl.tiny_batch(), planes)
+    dense, plan, slabs, cur = _compose(b)
+    want = oracle.compose_dense_planes(b.prefix_lens, b.cur_lens, b.prefix_pages, slabs, cur, page_size=b.page_size,
+                                       cp_size=b.cp_size, plane_bytes=list(planes))
+    assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, -1), want)
+
+
+def test_planar_rejects_bad_planes():
+    b = _planar(wl.tiny_batch())
+    plan = ComposePlan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer, page_size=b.page_size,
+                       cp_size=b.cp_size, num_pool_pages=b.num_pool_pages).build()
+    layers = ComposeLayers(plan, b.row_bytes)
+    with pytest.raises(cpkv.CpkvError):
+        cpkv.cpkv_fill_current_planes(b.cur_lens, [[None] * 2, [None] * 2], layers.staging, page_size=16, cp_size=2,
+                                      plane_bytes=[130, 2], staging_cap_pages=plan.staging_cap_pages,
+                                      d_staging_rows=plan["staging_rows"], d_token_writer_row=plan["token_writer_row"],
+                                      d_writer=plan.d_writer, num_cur_pages=plan.C, d_status=plan.d_status,
+                                      cur_rows_cap=[0, 0])

@@ -44,6 +44,14 @@ MUTANTS = [
      "for (int64_t row = sr; row < (slot + 1) * ps; ++row)"),
     ("fill_writer_of_wrong_slot", "    int32_t w = writer[slot - 1];\n    if (w < 0 || w >= cp) { *status |= ORC_WRITER_OOB; continue; }\n    int32_t r",
      "    int32_t w = writer[slot % C];\n    if (w < 0 || w >= cp) { *status |= ORC_WRITER_OOB; continue; }\n    int32_t r"),
+    ("planes_offset_ignores_plane_start",
+     "memcpy(staging[w] + slot * page_bytes + plane_start + off * wp, cur_planes[p * cp + w] + r * wp,",
+     "memcpy(staging[w] + slot * page_bytes + off * wp, cur_planes[p * cp + w] + r * wp,"),
+    ("planes_dense_pool_offset_dropped",
+     "memcpy(dst, pool_slabs[owner] + local * page_bytes + plane_start + (k % ps) * wp, (size_t)wp);",
+     "memcpy(dst, pool_slabs[owner] + local * page_bytes + (k % ps) * wp, (size_t)wp);"),
+    ("planes_pad_from_wrong_row", "for (int64_t off = sr % ps + 1; off < ps; ++off)",
+     "for (int64_t off = sr % ps + 2; off < ps; ++off)"),
     ("ragged_kbase_unaligned", "kbase[b + 1] = kbase[b] + ceil_div64(kv, k_align) * k_align;",
      "kbase[b + 1] = kbase[b] + kv;"),
     ("ragged_kv_dropped_prefix", "int64_t kv = (int64_t)prefix_lens[b] + q_lens[b];", "int64_t kv = q_lens[b];"),

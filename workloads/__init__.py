@@ -48,6 +48,7 @@ class ComposeBatch:
     cur_pages: np.ndarray  # CSR by request: ceil(cur_lens[b] / page_size) entries each
     writer: np.ndarray  # [C] writer rank of each current page, batch order
     row_kind: str  # "bf16" (N(0,1) values) or "bytes" (uniform random bytes)
+    planes: tuple | None = None  # planar pages: bytes per token of each plane (sum = row_bytes)
 
     @property
     def B(self) -> int:
@@ -362,11 +363,32 @@ def ragged_from_compose(batch: ComposeBatch, chunk: int | None = None) -> Ragged
     )
 
 
+INDEX_K_PLANES = (128, 4)  # NSA indexer key: 128 fp8 bytes, then a 4-byte fp32 scale plane
+
+
+def index_k_batch(seed: int = 1004, *, num_layers: int = 78, num_pool_pages: int = 1 << 20) -> ComposeBatch:
+    """The NSA indexer keys of the fp8 NSA batch (same lengths, pages and
+    writers): planar pages of 64 tokens x (128 + 4) bytes = 8448 bytes."""
+    b = fp8_nsa_batch(seed, num_layers=num_layers, num_pool_pages=num_pool_pages)
+    return dataclasses.replace(b, name="index_k", row_bytes=sum(INDEX_K_PLANES), planes=INDEX_K_PLANES,
+                               row_kind="bytes")
+
+
+def split_planes(rows: np.ndarray, planes) -> list:
+    """[n, sum(planes)] rows -> per-plane contiguous [n, w_p] arrays."""
+    out, start = [], 0
+    for w in planes:
+        out.append(np.ascontiguousarray(rows[:, start:start + w]))
+        start += w
+    return out
+
+
 CONFIGS = {
     "tiny": tiny_batch,
     "traced": traced_batch,
     "traced_78": traced_78_layer_batch,
     "fp8_nsa": fp8_nsa_batch,
+    "index_k": index_k_batch,
 }
 
 
@@ -394,7 +416,7 @@ __all__ = [
     "tiny_batch", "traced_batch", "traced_78_layer_batch", "fp8_nsa_batch", "ragged_batch",
     "ragged_from_compose", "make_compose_batch", "lognormal_split", "round_robin_writers",
     "random_rows", "host_pool", "host_current_rows", "token_writer", "split_rows_by_writer",
-    "bf16_bits", "pages_per_len", "describe", "ceil_div",
+    "bf16_bits", "pages_per_len", "describe", "ceil_div", "index_k_batch", "split_planes", "INDEX_K_PLANES",
 ]
 
 
