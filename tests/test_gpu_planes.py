@@ -70,7 +70,7 @@ def _compose(batch, per_writer_mut=None, reverse_rows=False):
                             per_writer, want_stg, page_size=ps, cp_size=cp, plane_bytes=list(batch.planes))
     assert st == 0
     for w in range(cp):
-        assert np.array_equal(layers.staging[w].cpu().numpy().reshape(plan.staging_cap_pages, -1), want_stg[w]), w
+        assert np.array_equal(layers.staging[w].cpu().numpy().reshape(plan.staging_cap_pages, ps * batch.row_bytes), want_stg[w]), w
     return dense, plan, slabs, planes
 
 
@@ -80,7 +80,7 @@ def test_planar_compose_matches_oracle(batch):
     want = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, planes,
                                        page_size=batch.page_size, cp_size=batch.cp_size,
                                        plane_bytes=list(batch.planes))
-    assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, -1), want)
+    assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, batch.page_size * batch.row_bytes), want)
 
 
 @pytest.mark.parametrize("batch", _edge_planar()[:4], ids=lambda b: b.name)
@@ -94,7 +94,7 @@ def test_planar_plane_shapes(planes):
     dense, plan, slabs, cur = _compose(b)
     want = oracle.compose_dense_planes(b.prefix_lens, b.cur_lens, b.prefix_pages, slabs, cur, page_size=b.page_size,
                                        cp_size=b.cp_size, plane_bytes=list(planes))
-    assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, -1), want)
+    assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, b.page_size * b.row_bytes), want)
 
 
 def test_planar_rejects_bad_planes():
