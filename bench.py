@@ -616,7 +616,7 @@ def main(argv=None):
             "variant": work.variant,
             "bytes_per_layer": work.layer_bytes, "single_pass_ideal_bytes_per_layer": work.bytes["single_pass_ideal"],
             "l2": "inputs larger than L2: every layer reads its own pool slab and rows (%.1f GB per step)" % (
-                (sum(s.numel() for p in work.pools for s in p) + sum(r.numel() for rr in work.rows for r in rr)) / 1e9),
+                (sum(s.numel() for p in work.pools for s in p) + work.rows_all.numel()) / 1e9),
             "cuda_graph": not a.no_graph,
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
