@@ -29,6 +29,7 @@ namespace {
 
 constexpr int kThreads = 256;  // also the tokens per tile
 constexpr int kMaxPlanes = 4;
+constexpr int kUnroll = 4;     // units per thread in flight
 
 template <int MAXB>
 struct PlaneParams {
@@ -80,16 +81,30 @@ __device__ void copy_tile(const PlaneParams<MAXB> &p, int64_t t0) {
     const int32_t wp = p.plane_bytes[pl], unit = p.plane_unit[pl], start = p.plane_start[pl];
     const int32_t upt = wp / unit;  // units per token
     const int total = ntok * upt;
-    for (int i = j; i < total; i += kThreads) {
-      const int k = i / upt, u = i - k * upt;
-      uint8_t *dp = dst_page[k];
-      if (dp == nullptr) continue;
-      uint8_t *d = dp + start + (int64_t)dst_off[k] * wp + (int64_t)u * unit;
-      const uint8_t *s = p.planes[pl][src_w[k]] + (int64_t)src_row[k] * wp + (int64_t)u * unit;
-      if (unit == 16) {
-        *reinterpret_cast<uint4 *>(d) = ld_stream16(s);
-      } else {
-        *reinterpret_cast<uint32_t *>(d) = __ldg(reinterpret_cast<const uint32_t *>(s));
+    // kUnroll units per thread in flight: all loads, then all stores
+    for (int base = 0; base < total; base += kThreads * kUnroll) {
+      uint4 v[kUnroll];
+      uint8_t *dst[kUnroll];
+#pragma unroll
+      for (int r = 0; r < kUnroll; ++r) {
+        const int i = base + j + r * kThreads;
+        dst[r] = nullptr;
+        if (i < total) {
+          const int k = i / upt, u = i - k * upt;
+          uint8_t *dp = dst_page[k];
+          if (dp != nullptr) {
+            dst[r] = dp + start + (int64_t)dst_off[k] * wp + (int64_t)u * unit;
+            const uint8_t *s = p.planes[pl][src_w[k]] + (int64_t)src_row[k] * wp + (int64_t)u * unit;
+            if (unit == 16) v[r] = ld_stream16(s);
+            else v[r].x = __ldg(reinterpret_cast<const uint32_t *>(s));
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kUnroll; ++r) {
+        if (dst[r] == nullptr) continue;
+        if (unit == 16) *reinterpret_cast<uint4 *>(dst[r]) = v[r];
+        else *reinterpret_cast<uint32_t *>(dst[r]) = v[r].x;
       }
     }
   }

@@ -83,14 +83,25 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
 
   BulkRing<kStages, kLoadsInFlight> ring;
   ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
-  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
+  // units u = blockIdx.x + i * gridDim.x; descriptors loaded 32 at a time
+  const int64_t step = gridDim.x;
+  for (int64_t base = blockIdx.x; base < p.units; base += 32 * step) {
+   const int64_t mine = base + lane * step;
+   int32_t my_o = -1, my_s = 0;
+   if (mine < p.units) {
+     my_o = p.owner[mine / p.pieces];
+     my_s = p.src[mine / p.pieces];
+   }
+   for (int jj = 0; jj < 32; ++jj) {
+    const int64_t u = base + jj * step;
+    if (u >= p.units) break;  // uniform across the warp
     const int64_t d = u / p.pieces;
     const int32_t k = (int32_t)(u - d * p.pieces);
     const int64_t off = (int64_t)k * p.piece_bytes;
     const uint32_t bytes = (uint32_t)min64(p.piece_bytes, p.page_bytes - off);
     uint8_t *dst = p.dense + d * p.page_bytes + off;
-    const int32_t o = p.owner[d];
-    const int32_t s = p.src[d];
+    const int32_t o = __shfl_sync(0xffffffffu, my_o, jj);
+    const int32_t s = __shfl_sync(0xffffffffu, my_s, jj);
     if (o >= 0 && o < p.cp && s >= 0 && s < p.pool_cap[o]) {
       ring.push(p.pool[o] + (int64_t)s * p.page_bytes + off, dst, bytes);
       continue;
@@ -124,6 +135,7 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
     }
     if (copy > 0) ring.push(from, dst, (uint32_t)copy);
     if (copy < bytes) warp_zero(dst + copy, bytes - (uint32_t)copy);
+   }
   }
   ring.drain();
 }

@@ -53,7 +53,9 @@ __device__ __forceinline__ int slot_kind(const GatherParams &p, int32_t o) {
   return CPKV_GATHER_ZERO;
 }
 
-__device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, bool report, bool *skip) {
+// Unit u of this launch, given its page's descriptor (o, s).
+__device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, int32_t o, int32_t s, bool report,
+                                             bool *skip) {
   const int64_t d = u / p.pieces;
   const int32_t k = (int32_t)(u - d * p.pieces);
   const int64_t off = (int64_t)k * p.piece_bytes;
@@ -61,10 +63,8 @@ __device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, b
   x.bytes = (uint32_t)min64(p.piece_bytes, p.page_bytes - off);
   x.dst = p.dense + d * p.page_bytes + off;
   x.src = nullptr;
-  const int32_t o = p.owner[d];
   *skip = (slot_kind(p, o) & p.kinds) == 0;
   if (*skip || o == -1) return x;
-  const int32_t s = p.src[d];
   if (o < -1 || o >= p.n_table || s < 0 || s >= p.cap_pages[o]) {
     if (report && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
     return x;
@@ -81,12 +81,29 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
   __shared__ int ring_live[kStages];
   BulkRing<kStages, kLoadsInFlight> ring;
   ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
-  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-    bool skip;
-    const Unit x = resolve_unit(p, u, threadIdx.x == 0, &skip);
-    if (skip) continue;
-    if (x.src == nullptr) warp_zero(x.dst, x.bytes);
-    else ring.push(x.src, x.dst, x.bytes);
+  // The CTA's units are u = blockIdx.x + i * gridDim.x.  Their descriptors
+  // are loaded 32 at a time (one per lane) and handed out with shuffles, so
+  // no copy waits on a descriptor load of its own.
+  const int lane = threadIdx.x;
+  const int64_t step = gridDim.x;
+  for (int64_t base = blockIdx.x; base < p.units; base += 32 * step) {
+    const int64_t mine = base + lane * step;
+    int32_t my_o = -1, my_s = 0;
+    if (mine < p.units) {
+      my_o = p.owner[mine / p.pieces];
+      my_s = p.src[mine / p.pieces];
+    }
+    for (int j = 0; j < 32; ++j) {
+      const int64_t u = base + j * step;
+      if (u >= p.units) break;  // uniform across the warp
+      const int32_t o = __shfl_sync(0xffffffffu, my_o, j);
+      const int32_t sr = __shfl_sync(0xffffffffu, my_s, j);
+      bool skip;
+      const Unit x = resolve_unit(p, u, o, sr, lane == 0, &skip);
+      if (skip) continue;
+      if (x.src == nullptr) warp_zero(x.dst, x.bytes);
+      else ring.push(x.src, x.dst, x.bytes);
+    }
   }
   ring.drain();
 }
