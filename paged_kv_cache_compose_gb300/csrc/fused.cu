@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kLoadsInFlight = 2;
-constexpr int kCtasPerSm = 2;
+constexpr int kMaxCtasPerSm = 3;  // one-warp CTAs per SM, as many as shared memory allows
 constexpr int kMaxPieceBytes = 24 * 1024;
 
 template <int MAXB>
@@ -140,6 +140,12 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
   ring.drain();
 }
 
+inline int64_t ctas_per_sm(size_t ring_smem) {
+  // 227 KB of shared memory per SM; allow for static shared memory and the 1 KB per-CTA reserve
+  const int64_t fit = (int64_t)(227 * 1024) / (int64_t)(ring_smem + 14 * 1024);
+  return fit < 1 ? 1 : (fit > kMaxCtasPerSm ? kMaxCtasPerSm : fit);
+}
+
 }  // namespace
 }  // namespace cpkv
 
@@ -177,7 +183,7 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
   if (pieces > INT32_MAX || dense_cap_pages > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
   const int64_t units = dense_cap_pages * pieces;
   const size_t smem = (size_t)kStages * piece_bytes;
-  const int64_t cap = (int64_t)device_sm_count() * kCtasPerSm;
+  const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(smem);
   const int grid = (int)(units < cap ? units : cap);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 

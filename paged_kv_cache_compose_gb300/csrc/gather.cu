@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kLoadsInFlight = 2;
-constexpr int kCtasPerSm = 2;
+constexpr int kMaxCtasPerSm = 3;  // one-warp CTAs per SM, as many as shared memory allows
 constexpr int kMaxPieceBytes = 24 * 1024;
 
 struct GatherParams {
@@ -108,6 +108,12 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
   ring.drain();
 }
 
+inline int64_t ctas_per_sm(size_t ring_smem) {
+  // 227 KB of shared memory per SM; allow for static shared memory and the 1 KB per-CTA reserve
+  const int64_t fit = (int64_t)(227 * 1024) / (int64_t)(ring_smem + 14 * 1024);
+  return fit < 1 ? 1 : (fit > kMaxCtasPerSm ? kMaxCtasPerSm : fit);
+}
+
 }  // namespace
 }  // namespace cpkv
 
@@ -160,8 +166,9 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
       return CPKV_ERR_CUDA;
     configured[dev] = 1;
   }
-  // One-warp CTAs, kCtasPerSm per SM (4 loads of <= 24 KB in flight per SM).
-  const int64_t cap = (int64_t)device_sm_count() * kCtasPerSm;
+  // One-warp CTAs: 3 per SM when their rings fit in shared memory (small
+  // pages), else 2 (24 KB pieces).
+  const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(smem);
   const int grid = (int)(prm.units < cap ? prm.units : cap);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   gather_pages_kernel<<<grid, 32, smem, s>>>(prm);
