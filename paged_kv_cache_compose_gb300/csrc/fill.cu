@@ -70,32 +70,51 @@ __device__ RowJob resolve_row(const FillParams<MAXB> &p, int64_t t) {
   return j;
 }
 
-// RIF rows per warp per iteration, VPL vectors per lane per row (vpr <= 32 * VPL).
+// Warp w handles rows w*RIF + i*stride + [0, RIF) in iteration i (stride =
+// RIF * warps).  The indices of 32/RIF iterations are resolved at once, one
+// row per lane (their dependent index loads overlap), and each iteration
+// takes its rows' pointers by shuffle.  RIF rows are copied per iteration,
+// each lane moving VPL 16-byte vectors per row (vpr <= 32 * VPL), all loads
+// issued before the stores.
 template <int MAXB, int RIF, int VPL>
 __device__ void copy_rows_unrolled(const FillParams<MAXB> &p, uint64_t read_once, uint64_t keep) {
+  static_assert(32 % RIF == 0, "RIF divides the warp");
+  constexpr int kIters = 32 / RIF;  // iterations resolved per batch
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  const int64_t nwarps = (int64_t)p.nRow * kWarpsPerBlock;
+  const int64_t stride = (int64_t)p.nRow * kWarpsPerBlock * RIF;
   const int vpr = p.vpr;
-  for (int64_t t0 = warp_id * RIF; t0 < p.T; t0 += nwarps * RIF) {
-    RowJob job[RIF];
-    uint4 v[RIF][VPL];
+  for (int64_t tb = warp_id * RIF; tb < p.T; tb += kIters * stride) {
+    const int64_t tl = tb + (int64_t)(lane / RIF) * stride + (lane % RIF);
+    const RowJob mine = tl < p.T ? resolve_row(p, tl) : RowJob{nullptr, nullptr};
+    for (int it = 0; it < kIters; ++it) {
+      const int64_t t0 = tb + (int64_t)it * stride;
+      if (t0 >= p.T) break;  // uniform across the warp
+      RowJob job[RIF];
+      uint4 v[RIF][VPL];
 #pragma unroll
-    for (int r = 0; r < RIF; ++r) job[r] = (t0 + r < p.T) ? resolve_row(p, t0 + r) : RowJob{nullptr, nullptr};
-#pragma unroll
-    for (int r = 0; r < RIF; ++r) {
-#pragma unroll
-      for (int k = 0; k < VPL; ++k) {
-        const int c = lane + 32 * k;
-        if (job[r].src != nullptr && c < vpr) v[r][k] = ld_stream16_hint(job[r].src + 16 * (int64_t)c, read_once);
+      for (int r = 0; r < RIF; ++r) {
+        const int from = it * RIF + r;
+        job[r].src = reinterpret_cast<const uint8_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine.src), from));
+        job[r].dst = reinterpret_cast<uint8_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine.dst), from));
       }
-    }
 #pragma unroll
-    for (int r = 0; r < RIF; ++r) {
+      for (int r = 0; r < RIF; ++r) {
 #pragma unroll
-      for (int k = 0; k < VPL; ++k) {
-        const int c = lane + 32 * k;
-        if (job[r].src != nullptr && c < vpr) st16_hint(job[r].dst + 16 * (int64_t)c, v[r][k], keep);
+        for (int k = 0; k < VPL; ++k) {
+          const int c = lane + 32 * k;
+          if (job[r].src != nullptr && c < vpr) v[r][k] = ld_stream16_hint(job[r].src + 16 * (int64_t)c, read_once);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RIF; ++r) {
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+          const int c = lane + 32 * k;
+          if (job[r].src != nullptr && c < vpr) st16_hint(job[r].dst + 16 * (int64_t)c, v[r][k], keep);
+        }
       }
     }
   }
