@@ -15,7 +15,7 @@
 // slices after its last token up to the end of that page are zero in every
 // plane.
 //
-// Blocks [0, nTile) take tiles of 256 tokens: the tile's indices are resolved
+// Blocks [0, nTile) take tiles of 128 tokens: the tile's indices are resolved
 // once into shared memory, then each plane is copied as a flat loop over
 // (token, unit) with consecutive threads on consecutive units, so a warp
 // reads and writes contiguous bytes (a unit is 16 bytes when the plane allows
@@ -27,7 +27,7 @@
 namespace cpkv {
 namespace {
 
-constexpr int kThreads = 256;  // also the tokens per tile
+constexpr int kThreads = 128;  // also the tokens per tile
 constexpr int kMaxPlanes = 4;
 constexpr int kUnroll = 4;     // units per thread in flight
 
@@ -200,7 +200,7 @@ extern "C" int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n
   if (T == 0) return CPKV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t tiles = ceil_div(T, kThreads);
-  const int64_t cap = (int64_t)device_sm_count() * 8;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
   const int nTile = (int)(tiles < cap ? tiles : cap);
 
 #define CPKV_FILL_PLANES(prm)                                                                          \
