@@ -92,6 +92,13 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
      my_o = p.owner[mine / p.pieces];
      my_s = p.src[mine / p.pieces];
    }
+   // for a current page, also its first token's row in the writer's buffer
+   int32_t my_row0 = -1;
+   if (my_o >= p.cp && my_o < 2 * p.cp && my_s >= 1 && my_s <= p.C && p.B > 0) {
+     const int b = upper_index<int32_t>(cur_page_start, p.B, my_s - 1);
+     const int64_t tok0 = token_start[b] + (int64_t)(my_s - 1 - cur_page_start[b]) * p.ps;
+     my_row0 = p.token_writer_row[tok0];
+   }
    for (int jj = 0; jj < 32; ++jj) {
     const int64_t u = base + jj * step;
     if (u >= p.units) break;  // uniform across the warp
@@ -102,6 +109,7 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
     uint8_t *dst = p.dense + d * p.page_bytes + off;
     const int32_t o = __shfl_sync(0xffffffffu, my_o, jj);
     const int32_t s = __shfl_sync(0xffffffffu, my_s, jj);
+    const int32_t row0 = __shfl_sync(0xffffffffu, my_row0, jj);
     if (o >= 0 && o < p.cp && s >= 0 && s < p.pool_cap[o]) {
       ring.push(p.pool[o] + (int64_t)s * p.page_bytes + off, dst, bytes);
       continue;
@@ -117,9 +125,7 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
       } else {
         const int b = upper_index<int32_t>(cur_page_start, p.B, i);
         const int32_t kp = i - cur_page_start[b];
-        const int64_t tok0 = token_start[b] + (int64_t)kp * p.ps;
         const int64_t n = min64(p.ps, (int64_t)p.cur_lens[b] - (int64_t)kp * p.ps);
-        const int32_t row0 = p.token_writer_row[tok0];
         if (n < 1 || row0 < 0 || row0 + n > p.cur_cap[w]) {
           bad = true;
         } else {
