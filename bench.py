@@ -36,7 +36,6 @@ import workloads as wl  # noqa: E402
 
 METRIC = "compose GB/s and % of HBM peak; ms per 78-layer compose at bs=12/44.6K tokens"
 FALLBACK_HBM_GBS = 6800.0
-L2_BYTES = 126 * 1024 * 1024
 
 
 # ---------------------------------------------------------------------------
