@@ -230,6 +230,12 @@ class ComposeWorkload:
             self.launches_per_step = 3 + self.num_layers  # plan (2) + ragged (1) + one fused compose per layer
             self.layer_bytes = self.bytes["fused"]
             self.kernels = {"fused": self.bytes["fused"]}
+        elif variant == "layer":
+            if b.planes:
+                raise ValueError("the one-launch layer compose takes row-major pages only")
+            self.launches_per_step = 3 + self.num_layers  # plan (2) + ragged (1) + one fill+gather launch per layer
+            self.layer_bytes = self.bytes["total"]
+            self.kernels = {"layer": self.bytes["total"]}
         elif variant == "prefetch":
             # layer-ahead: prefix pages of layer l+1 gathered on a side stream while layer l is consumed
             self.launches_per_step = 3 + 3 * self.num_layers  # plan + ragged + (prefetch, fill, current gather)
@@ -288,6 +294,9 @@ class ComposeWorkload:
         dense = self.layers.dense[layer % 2]
         if self.variant == "fused":
             self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream)
+            return
+        if self.variant == "layer":
+            self.layers.compose_one_launch(self.pools_of(layer), self.rows[layer], dense, stream)
             return
         if kind in ("all", "fill"):
             if self.batch.planes:
@@ -485,7 +494,7 @@ def main(argv=None):
                     help="plans: latency of the per-batch plan builders (ragged plan config, all CP ranks and "
                          "splits; compose plan of the traced and fp8 batches)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--variant", default="staging", choices=["staging", "fused", "prefetch"],
+    ap.add_argument("--variant", default="staging", choices=["staging", "fused", "prefetch", "layer"],
                     help="staging: fill + slot-dense gather per layer (the pages' method); "
                          "fused: one-pass single-GPU compose without the staging round trip; "
                          "prefetch: staging method with each layer's prefix pages gathered one layer ahead "
@@ -568,7 +577,7 @@ def main(argv=None):
         torch.cuda.synchronize()
         kern[kind] = k0.elapsed_time(k1) / (reps * work.num_layers)
     kgbs = {k: work.kernels[k] / (kern[k] / 1e3) / 1e9 for k in kern}
-    top = "fused" if work.variant == "fused" else "gather"
+    top = {"fused": "fused", "layer": "layer"}.get(work.variant, "gather")
     status = work.status()
 
     traffic = kernel_traffic(top, a.config)
@@ -621,8 +630,9 @@ def main(argv=None):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": ("gather_pages_kernel (cpkv_compose_gather)" if top == "gather"
-                       else "compose_fused_kernel (cpkv_compose_fused)"),
+            "kernel": {"gather": "gather_pages_kernel (cpkv_compose_gather)",
+                       "fused": "compose_fused_kernel (cpkv_compose_fused)",
+                       "layer": "compose_layer_kernel (cpkv_compose_layer)"}[top],
             "achieved": round(kgbs[top], 1),
             "peak": hbm_peak,
             "peak_source": peak_src,

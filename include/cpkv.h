@@ -255,6 +255,37 @@ int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
                               void *d_dense, int32_t *d_status, cpkv_stream_t stream);
 
 /*
+ * cpkv_compose_layer — per layer: cpkv_fill_current followed by
+ * cpkv_compose_gather in one launch, for the plan of cpkv_plan_build.  Each
+ * CTA first fills its share of current pages into the stagings, then gathers
+ * its pool pages (and zero slots) into the dense buffer, then gathers back
+ * from the stagings exactly the current pieces it wrote.  The stagings and
+ * the dense buffer end up byte-identical to the two-call form; every staging
+ * byte is still written and read back.
+ *   h_cur_lens       host int32 [B]
+ *   h_cur_rows       host array [cp] of device pointers, writer w's current
+ *                    rows [h_cur_rows_cap[w]][R], 16-byte aligned
+ *   h_src_table      host array [2*cp] of device pointers
+ *                    [pool_0 .. pool_{cp-1} | staging_0 .. staging_{cp-1}],
+ *                    page arrays of h_src_cap_pages[k] pages; each staging
+ *                    needs at least C + 1 pages
+ *   d_owner, d_src, d_token_writer_row: from cpkv_plan_build (current page
+ *                    i = src - 1 holds n_i rows that are consecutive in its
+ *                    writer's buffer from token_writer_row of its first token)
+ *   d_dense          device [dense_cap_pages * ps][R], 16-byte aligned
+ * A descriptor outside the table or its capacity raises DESC_OOB, current
+ * rows outside the writer's buffer raise ROW_OOB; either dense page is
+ * zero-filled and its staging slot is not written.  Errors: ARG for bad
+ * sizes, null or unaligned pointers, CAPACITY for a staging under C + 1
+ * pages, LIMIT for B > CPKV_MAX_BATCH, CUDA for a failed launch.
+ */
+int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
+                       const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
+                       const void *const *h_src_table, const int64_t *h_src_cap_pages, const int32_t *d_owner,
+                       const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
+                       void *d_dense, int32_t *d_status, cpkv_stream_t stream);
+
+/*
  * cpkv_compose_fused — per layer: the single-GPU compose in one pass, without
  * the staging round trip.  The staging exchange ("staging-direct compose")
  * carries current pages between GPUs; when every writer region is on this

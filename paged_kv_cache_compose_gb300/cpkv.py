@@ -45,7 +45,7 @@ MAX_BATCH = 1024
 EXPORTED = (
     "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_fill_current",
     "cpkv_fill_current_planes",
-    "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
+    "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
     "cpkv_version",
 )
 
@@ -74,6 +74,7 @@ def _declare(lib):
     lib.cpkv_compose_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_fill_current_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
     lib.cpkv_compose_gather_kinds.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _I, _P, _P, _P]
+    lib.cpkv_compose_layer.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
     lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
@@ -244,6 +245,22 @@ def cpkv_compose_gather_kinds(src_table: Sequence, src_cap_pages, d_owner, d_src
                                           _dp(d_owner), _dp(d_src), dense_cap_pages, kinds, _dp(d_dense),
                                           _dp(d_status), _stream(stream))
     _check("cpkv_compose_gather_kinds", rc)
+
+
+def cpkv_compose_layer(cur_lens, cur_rows: Sequence, src_table: Sequence, src_cap_pages, d_owner, d_src,
+                       d_token_writer_row, d_dense, *, page_size, cp_size, row_bytes, dense_cap_pages, d_status,
+                       cur_rows_cap=None, stream=None):
+    """Fill + slot-dense gather of one layer in a single launch."""
+    cl = _host_i32(cur_lens)
+    if cur_rows_cap is None:
+        cur_rows_cap = [t.numel() // row_bytes for t in cur_rows]
+    rcaps, tcaps = _host_i64(cur_rows_cap), _host_i64(src_cap_pages)
+    rarr, tarr = _ptr_array(cur_rows), _ptr_array(src_table)
+    rc = load().cpkv_compose_layer(len(cl), page_size, cp_size, row_bytes, _hp(cl), ctypes.cast(rarr, _P), _hp(rcaps),
+                                   ctypes.cast(tarr, _P), _hp(tcaps), _dp(d_owner), _dp(d_src),
+                                   _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense), _dp(d_status),
+                                   _stream(stream))
+    _check("cpkv_compose_layer", rc)
 
 
 def cpkv_compose_fused(cur_lens, pools: Sequence, cur_rows: Sequence, d_owner, d_src, d_token_writer_row, d_dense,

@@ -1,0 +1,295 @@
+// cpkv_compose_layer: one layer of the staging compose ("staging-direct
+// compose" message of commits d63fbd4) — the fill of the current pages into
+// the writers' stagings followed by the slot-dense gather over the 2*cp
+// pointer table — in a single launch.
+//
+// Every CTA walks its units (pieces of dense pages, u = blockIdx.x + i*grid)
+// twice.  The first pass does, unit by unit,
+//   A  for a current page: the page's rows, copied from its writer's
+//      current-row buffer, go to staging slot src of writer owner - cp,
+//      followed by zero pad rows (the fill);
+//   B  for a pool page or zero slot: the page goes to the dense buffer (the
+//      prefix part of the gather);
+// the second pass does
+//   C  for a current page: staging slot src of writer owner - cp is copied
+//      back into the dense buffer (the current part of the gather).
+// A CTA gathers in C exactly the staging pieces it wrote in A, after its own
+// writes have completed, so no CTA waits on another, and the fill's reads
+// share DRAM time with the prefix pages' reads and writes instead of running
+// alone.  Every byte the two-kernel form moves is moved: the stagings are
+// written in full and read back.
+//
+// The staging layout and the current pages' rows follow the plan of
+// cpkv_plan_build: current page i (src = i + 1) holds its n_i tokens, whose
+// rows are consecutive in their writer's buffer starting at
+// token_writer_row of the page's first token.  The outputs (stagings and
+// dense buffer) are byte-identical to cpkv_fill_current followed by
+// cpkv_compose_gather on those plan arrays.
+#include <stdint.h>
+
+#include "bulk_ring.cuh"
+
+namespace cpkv {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kLoadsInFlight = 2;
+constexpr int kMaxCtasPerSm = 3;
+constexpr int kMaxPieceBytes = 24 * 1024;
+
+template <int MAXB>
+struct LayerParams {
+  const uint8_t *table[2 * CPKV_MAX_CP];  // pools, then stagings
+  int64_t cap_pages[2 * CPKV_MAX_CP];
+  const uint8_t *cur_rows[CPKV_MAX_CP];
+  int64_t cur_cap[CPKV_MAX_CP];
+  const int32_t *owner, *src, *token_writer_row;
+  uint8_t *dense;
+  int32_t *status;
+  int64_t dense_cap, page_bytes, units, R, C;
+  int32_t cp, ps, B, pieces, piece_bytes;
+  int32_t cur_lens[MAXB];
+};
+
+// Where a current page's rows come from: n rows starting at row0 of its
+// writer's buffer.  Returns 0, or the status bit to raise when the descriptor
+// (CPKV_STATUS_DESC_OOB) or the rows (CPKV_STATUS_ROW_OOB) are out of range;
+// such a page is zero-filled in the dense buffer and its staging slot is left
+// untouched.
+template <int MAXB>
+__device__ __forceinline__ int32_t current_rows(const LayerParams<MAXB> &p, const int32_t *cur_page_start,
+                                                int32_t o, int32_t s, int32_t row0, int64_t *n) {
+  const int32_t w = o - p.cp, i = s - 1;
+  if (i < 0 || i >= p.C || p.B == 0 || s >= p.cap_pages[o]) return CPKV_STATUS_DESC_OOB;
+  const int b = upper_index<int32_t>(cur_page_start, p.B, i);
+  const int32_t kp = i - cur_page_start[b];
+  *n = min64(p.ps, (int64_t)p.cur_lens[b] - (int64_t)kp * p.ps);
+  if (*n < 1) return CPKV_STATUS_DESC_OOB;
+  return row0 >= 0 && row0 + *n <= p.cur_cap[w] ? 0 : CPKV_STATUS_ROW_OOB;
+}
+
+// The bulk ring with a per-piece choice of L2 policy for the store: staging
+// pieces are kept in L2 for their read-back, dense pieces stream through.
+struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
+  uint32_t keep_mask;  // bit s: the piece in stage s is stored with keep_policy (warp-uniform)
+  uint64_t keep_policy, stream_policy;
+
+  CPKV_DEV void consume_one() {
+    store_policy = ((keep_mask >> (int)(head % kStages)) & 1u) ? keep_policy : stream_policy;
+    consume();
+  }
+  CPKV_DEV void push_with(const void *src, void *dst, uint32_t bytes, bool keep_in_l2) {
+    if (tail - head == kLoadsInFlight) consume_one();  // push() then finds a free load slot
+    const uint32_t bit = 1u << (int)(tail % kStages);
+    keep_mask = keep_in_l2 ? (keep_mask | bit) : (keep_mask & ~bit);
+    push(src, dst, bytes);
+  }
+  CPKV_DEV void drain_all() {
+    while (head < tail) consume_one();
+    if ((threadIdx.x & 31) == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+
+template <int MAXB>
+__global__ void __launch_bounds__(32) compose_layer_kernel(const __grid_constant__ LayerParams<MAXB> p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ uint8_t *ring_dst[kStages];
+  __shared__ uint32_t ring_bytes[kStages];
+  __shared__ int ring_live[kStages];
+  __shared__ int32_t cur_page_start[MAXB + 1];
+  __shared__ int64_t token_start[MAXB + 1];
+  const int lane = threadIdx.x;
+  const uint64_t keep = l2_policy_evict_last();
+
+  {  // request-level exclusive scans, 32 requests per step
+    int32_t carry_pages = 0;
+    int64_t carry_tok = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      const int32_t n = b < p.B ? p.cur_lens[b] : 0;
+      const int32_t np = (n + p.ps - 1) / p.ps;
+      const int32_t inc_p = warp_inclusive_scan<int32_t>(np);
+      const int64_t inc_t = warp_inclusive_scan<int64_t>((int64_t)n);
+      if (b < p.B) {
+        cur_page_start[b] = carry_pages + inc_p - np;
+        token_start[b] = carry_tok + inc_t - n;
+      }
+      carry_pages += __shfl_sync(0xffffffffu, inc_p, 31);
+      carry_tok += __shfl_sync(0xffffffffu, inc_t, 31);
+    }
+    if (lane == 0) {
+      cur_page_start[p.B] = carry_pages;
+      token_start[p.B] = carry_tok;
+    }
+    __syncwarp();
+  }
+
+  // Pass 1 runs phases A and B together in unit order: staging stores carry
+  // evict_last (pass 2 reads them back), dense stores evict_first.  Pass 2 is
+  // phase C.
+  LayerRing ring;
+  ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
+  ring.keep_mask = 0;
+  ring.keep_policy = keep;
+  ring.stream_policy = ring.load_policy;
+  const int64_t step = gridDim.x;
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {
+      // Every staging piece this CTA wrote in pass 1 is complete (bulk stores
+      // drained, the lanes' zero stores fenced) before pass 2 reads those
+      // pieces back with bulk copies.
+      ring.drain_all();
+      __threadfence();
+      fence_proxy_async_global();
+      __syncwarp();
+    }
+    for (int64_t base = blockIdx.x; base < p.units; base += 32 * step) {
+      const int64_t mine = base + lane * step;
+      int32_t my_o = -1, my_s = 0, my_row0 = -1;
+      if (mine < p.units) {
+        my_o = p.owner[mine / p.pieces];
+        my_s = p.src[mine / p.pieces];
+      }
+      if (my_o >= p.cp && my_o < 2 * p.cp && my_s >= 1 && my_s <= p.C && p.B > 0) {
+        const int b = upper_index<int32_t>(cur_page_start, p.B, my_s - 1);
+        my_row0 = p.token_writer_row[token_start[b] + (int64_t)(my_s - 1 - cur_page_start[b]) * p.ps];
+      }
+      for (int j = 0; j < 32; ++j) {
+        const int64_t u = base + j * step;
+        if (u >= p.units) break;  // uniform across the warp
+        const int32_t o = __shfl_sync(0xffffffffu, my_o, j);
+        const int32_t s = __shfl_sync(0xffffffffu, my_s, j);
+        const int32_t row0 = __shfl_sync(0xffffffffu, my_row0, j);
+        const int64_t d = u / p.pieces;
+        const int32_t k = (int32_t)(u - d * p.pieces);
+        const int64_t off = (int64_t)k * p.piece_bytes;
+        const uint32_t bytes = (uint32_t)min64(p.piece_bytes, p.page_bytes - off);
+        uint8_t *dst = p.dense + d * p.page_bytes + off;
+        const bool is_current = o >= p.cp && o < 2 * p.cp;
+        if (!is_current) {  // phase B: pool pages, zero slots, invalid descriptors
+          if (pass == 1) continue;
+          if (o >= 0 && o < p.cp && s >= 0 && s < p.cap_pages[o]) {
+            ring.push_with(p.table[o] + (int64_t)s * p.page_bytes + off, dst, bytes, false);
+          } else {
+            if (o != -1 && lane == 0 && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
+            warp_zero(dst, bytes);
+          }
+          continue;
+        }
+        int64_t n = 0;
+        const int32_t bad = current_rows(p, cur_page_start, o, s, row0, &n);
+        if (pass == 0) {  // phase A, the fill: rows, then zero pad rows, into staging slot s
+          if (bad) continue;
+          uint8_t *stg = const_cast<uint8_t *>(p.table[o]) + (int64_t)s * p.page_bytes + off;
+          const int64_t rows_bytes = n * p.R;
+          const int64_t copy = off < rows_bytes ? min64(bytes, rows_bytes - off) : 0;
+          if (copy > 0)
+            ring.push_with(p.cur_rows[o - p.cp] + (int64_t)row0 * p.R + off, stg, (uint32_t)copy, true);
+          if (copy < bytes) warp_zero_hint(stg + copy, bytes - (uint32_t)copy, keep);
+        } else if (!bad) {  // phase C: the staging piece written in pass 1, into the dense page
+          ring.push_with(p.table[o] + (int64_t)s * p.page_bytes + off, dst, bytes, false);
+        } else {
+          if (lane == 0 && k == 0) raise_status(p.status, bad);
+          warp_zero(dst, bytes);
+        }
+      }
+    }
+  }
+  ring.drain_all();
+}
+
+inline int64_t ctas_per_sm(size_t ring_smem) {
+  // 227 KB of shared memory per SM; allow for static shared memory and the 1 KB per-CTA reserve
+  const int64_t fit = (int64_t)(227 * 1024) / (int64_t)(ring_smem + 14 * 1024);
+  return fit < 1 ? 1 : (fit > kMaxCtasPerSm ? kMaxCtasPerSm : fit);
+}
+
+}  // namespace
+}  // namespace cpkv
+
+extern "C" int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
+                                  const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
+                                  const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                                  const int32_t *d_owner, const int32_t *d_src, const int32_t *d_token_writer_row,
+                                  int64_t dense_cap_pages, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
+  using namespace cpkv;
+  if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
+  if (row_bytes <= 0 || row_bytes % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
+  if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
+  if (h_cur_rows == nullptr || h_cur_rows_cap == nullptr || h_src_table == nullptr || h_src_cap_pages == nullptr ||
+      d_status == nullptr)
+    return CPKV_ERR_ARG;
+  if (B > 0 && h_cur_lens == nullptr) return CPKV_ERR_ARG;
+  int64_t T = 0, C = 0;
+  for (int b = 0; b < B; ++b) {
+    if (h_cur_lens[b] < 0) return CPKV_ERR_ARG;
+    T += h_cur_lens[b];
+    C += ceil_div(h_cur_lens[b], page_size);
+  }
+  if (T > INT32_MAX - 1 || C > INT32_MAX - 2) return CPKV_ERR_LIMIT;
+  for (int k = 0; k < 2 * cp_size; ++k) {
+    if (h_src_cap_pages[k] < 0) return CPKV_ERR_ARG;
+    if (h_src_cap_pages[k] > 0 && (h_src_table[k] == nullptr || !aligned16(h_src_table[k]))) return CPKV_ERR_ARG;
+  }
+  for (int w = 0; w < cp_size; ++w) {
+    if (C > 0 && h_src_cap_pages[cp_size + w] < C + 1) return CPKV_ERR_CAPACITY;  // staging slots 1..C
+    if (h_cur_rows_cap[w] < 0) return CPKV_ERR_ARG;
+    if (h_cur_rows_cap[w] > 0 && (h_cur_rows[w] == nullptr || !aligned16(h_cur_rows[w]))) return CPKV_ERR_ARG;
+  }
+  if (dense_cap_pages == 0) return CPKV_OK;
+  if (d_owner == nullptr || d_src == nullptr || d_dense == nullptr || !aligned16(d_dense)) return CPKV_ERR_ARG;
+  if (T > 0 && d_token_writer_row == nullptr) return CPKV_ERR_ARG;
+  const int64_t page_bytes = (int64_t)page_size * row_bytes;
+  const int64_t pieces = ceil_div(page_bytes, kMaxPieceBytes);
+  const int64_t piece_bytes = ceil_div(ceil_div(page_bytes, pieces), 16) * 16;
+  if (pieces > INT32_MAX || dense_cap_pages > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
+  const int64_t units = dense_cap_pages * pieces;
+  const size_t smem = (size_t)kStages * piece_bytes;
+  const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(smem);
+  const int grid = (int)(units < cap ? units : cap);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+#define CPKV_FILL_LAYER(prm)                                                                         \
+  for (int k = 0; k < 2 * CPKV_MAX_CP; ++k) {                                                        \
+    prm.table[k] = k < 2 * cp_size ? static_cast<const uint8_t *>(h_src_table[k]) : nullptr;         \
+    prm.cap_pages[k] = k < 2 * cp_size ? h_src_cap_pages[k] : 0;                                     \
+  }                                                                                                  \
+  for (int w = 0; w < CPKV_MAX_CP; ++w) {                                                            \
+    prm.cur_rows[w] = w < cp_size ? static_cast<const uint8_t *>(h_cur_rows[w]) : nullptr;          \
+    prm.cur_cap[w] = w < cp_size ? h_cur_rows_cap[w] : 0;                                            \
+  }                                                                                                  \
+  prm.owner = d_owner; prm.src = d_src; prm.token_writer_row = d_token_writer_row;                   \
+  prm.dense = static_cast<uint8_t *>(d_dense); prm.status = d_status; prm.dense_cap = dense_cap_pages; \
+  prm.page_bytes = page_bytes; prm.units = units; prm.R = row_bytes; prm.C = C; prm.cp = cp_size;   \
+  prm.ps = page_size; prm.B = B; prm.pieces = (int32_t)pieces; prm.piece_bytes = (int32_t)piece_bytes; \
+  for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
+
+  static int configured[256][2] = {{0}};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (B <= 64) {
+    if (dev >= 0 && dev < 256 && !configured[dev][0]) {
+      if (cudaFuncSetAttribute(compose_layer_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kStages * kMaxPieceBytes) != cudaSuccess)
+        return CPKV_ERR_CUDA;
+      configured[dev][0] = 1;
+    }
+    LayerParams<64> prm;
+    CPKV_FILL_LAYER(prm)
+    compose_layer_kernel<64><<<grid, 32, smem, s>>>(prm);
+    return launch_status();
+  }
+  if (dev >= 0 && dev < 256 && !configured[dev][1]) {
+    if (cudaFuncSetAttribute(compose_layer_kernel<CPKV_MAX_BATCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStages * kMaxPieceBytes) != cudaSuccess)
+      return CPKV_ERR_CUDA;
+    configured[dev][1] = 1;
+  }
+  LayerParams<CPKV_MAX_BATCH> prm;
+  CPKV_FILL_LAYER(prm)
+#undef CPKV_FILL_LAYER
+  compose_layer_kernel<CPKV_MAX_BATCH><<<grid, 32, smem, s>>>(prm);
+  return launch_status();
+}

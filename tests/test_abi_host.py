@@ -93,6 +93,17 @@ def test_host_errors_before_any_launch(lib):
     caps = np.array([1, 1], np.int64)
     rc = lib.cpkv_compose_gather(2, 1, 64, ctypes.cast(tbl, ctypes.c_void_p), caps.ctypes.data, 64, 64, 1, 8, 64, null)
     assert rc == cpkv.CPKV_ERR_ARG
+    # one-launch layer compose: a staging without room for slots 1..C, then a row width not a multiple of 16
+    rows = (ctypes.c_void_p * 1)(16)
+    rcap = np.array([4], np.int64)
+    tcaps = np.array([8, 1], np.int64)
+    rc = lib.cpkv_compose_layer(1, 2, 1, 64, cl.ctypes.data, ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data,
+                                ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 64, null)
+    assert rc == cpkv.CPKV_ERR_CAPACITY
+    tcaps = np.array([8, 3], np.int64)
+    rc = lib.cpkv_compose_layer(1, 2, 1, 40, cl.ctypes.data, ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data,
+                                ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 64, null)
+    assert rc == cpkv.CPKV_ERR_ARG
     # ragged: bad chunk / k_align
     rc = lib.cpkv_ragged_plan_build(1, 0, 1, pl.ctypes.data, cl.ctypes.data, null, 0, null, 0, *([null] * 7), 0,
                                     null, null, null)

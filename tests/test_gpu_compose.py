@@ -323,6 +323,91 @@ def test_fused_bad_descriptor_is_zeroed_and_flagged():
 
 
 # ---------------------------------------------------------------------------
+# one-launch layer compose: fill + gather in one kernel, same stagings and dense
+# ---------------------------------------------------------------------------
+
+def _run_one_launch(batch, dense_extra=2, layer=0, guard=0x5A):
+    plan, want_plan = _plan_pair(batch, dense_extra)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs = wl.host_pool(batch, layer)
+    rows = wl.host_current_rows(batch, layer)
+    d_slabs = [torch.from_numpy(s).cuda() for s in slabs]
+    d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+    for s in layers.staging:
+        s.fill_(guard)
+    dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
+                       device="cuda")
+    layers.compose_one_launch(d_slabs, d_rows, dense)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense.cpu().numpy(), want)
+    want_stg = [np.full(tuple(s.shape), guard, np.uint8) for s in layers.staging]
+    oracle.staging(batch.cur_lens, batch.writer, rows, want_stg, page_size=batch.page_size, cp_size=batch.cp_size)
+    for w, s in enumerate(layers.staging):
+        assert np.array_equal(s.cpu().numpy(), want_stg[w]), w
+
+
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_one_launch_matches_oracle_edge_cases(batch):
+    _run_one_launch(batch)
+
+
+@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (3, 48), (128, 1152), (64, 4096), (7, 16), (1, 16)])
+def test_one_launch_page_geometries(ps, R):
+    """Pieces that straddle the end of a partial page's rows, several pieces per page."""
+    rng = np.random.default_rng(ps * 11 + R)
+    B = 7
+    pfx = (rng.integers(0, 6 * ps, B) // ps) * ps
+    cur = rng.integers(0, 5 * ps, B)
+    batch = wl.make_compose_batch("geo1", 37, page_size=ps, cp_size=3, num_pool_pages=400, row_bytes=R,
+                                  prefix_lens=pfx, cur_lens=cur, row_kind="bytes")
+    _run_one_launch(batch, dense_extra=1)
+
+
+def test_one_launch_large_batch_template():
+    rng = np.random.default_rng(9)
+    B, ps = 200, 16
+    batch = wl.make_compose_batch("b200", 9, page_size=ps, cp_size=5, num_pool_pages=20000, row_bytes=96,
+                                  prefix_lens=(rng.integers(0, 90, B) // ps) * ps, cur_lens=rng.integers(0, 50, B),
+                                  row_kind="bytes")
+    _run_one_launch(batch, dense_extra=0)
+
+
+def test_one_launch_bad_descriptor_and_rows_are_zeroed_and_flagged():
+    batch = wl.tiny_batch()
+    plan, _ = _plan_pair(batch, dense_extra=0)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs = [torch.from_numpy(s).cuda() for s in wl.host_pool(batch)]
+    rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, wl.host_current_rows(batch))]
+    owner = plan["owner"].clone()
+    src = plan["src"].clone()
+    owner[0] = 2 * batch.cp_size  # outside the table
+    src[1] = 10_000               # beyond the slab / current page range
+    table = list(slabs) + list(layers.staging)
+    caps = [t.shape[0] for t in slabs] + [plan.staging_cap_pages] * batch.cp_size
+    dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
+                       device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_compose_layer(batch.cur_lens, rows, table, caps, owner, src, plan["token_writer_row"], dense,
+                            page_size=batch.page_size, cp_size=batch.cp_size, row_bytes=batch.row_bytes,
+                            dense_cap_pages=plan.dense_cap_pages, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == cpkv.STATUS_DESC_OOB
+    page = batch.page_size
+    assert torch.all(dense[:page] == 0) and torch.all(dense[page:2 * page] == 0)
+    # a writer buffer one row short: that writer's last current page is zeroed, ROW_OOB
+    caps_rows = [rows[0].shape[0] - 1] + [r.shape[0] for r in rows[1:]]
+    status.zero_()
+    cpkv.cpkv_compose_layer(batch.cur_lens, rows, table, caps, plan["owner"], plan["src"], plan["token_writer_row"],
+                            dense, page_size=batch.page_size, cp_size=batch.cp_size, row_bytes=batch.row_bytes,
+                            dense_cap_pages=plan.dense_cap_pages, d_status=status, cur_rows_cap=caps_rows)
+    torch.cuda.synchronize()
+    assert int(status.item()) == cpkv.STATUS_ROW_OOB
+
+
+# ---------------------------------------------------------------------------
 # fill with row indices that do not form page runs (row-by-row path)
 # ---------------------------------------------------------------------------
 

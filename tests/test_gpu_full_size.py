@@ -80,7 +80,8 @@ def _check_plan(work):
 
 @pytest.mark.parametrize("config,variant", [("traced_78", "staging"), ("fp8_nsa", "staging"),
                                             ("traced_78", "fused"), ("fp8_nsa", "fused"),
-                                            ("traced_78", "prefetch"), ("index_k", "staging")])
+                                            ("traced_78", "prefetch"), ("index_k", "staging"),
+                                            ("traced_78", "layer"), ("fp8_nsa", "layer")])
 def test_benchmark_workload_matches_oracle(config, variant):
     work = bench.ComposeWorkload(config, variant=variant)
     try:
@@ -95,7 +96,7 @@ def test_benchmark_workload_matches_oracle(config, variant):
         _check_plan(work)
         _check_layer(work, work.num_layers - 2)
         g = _check_layer(work, work.num_layers - 1)
-        if variant in ("staging", "prefetch") and g is not None:
+        if variant in ("staging", "prefetch", "layer") and g is not None:
             _check_staging(work, g)
     finally:
         del work

@@ -2,8 +2,8 @@
 
 Each case draws a batch (requests, page size, cp, row width, prefix/current
 lengths, writer assignment, shared prefix pages, capacity padding) from a
-fixed seed, runs the plan, the fill + gather, the fused compose and the
-prefix/current split on the GPU, and the ragged plan for every rank, and
+fixed seed, runs the plan, the fill + gather, the one-launch layer compose, the fused
+compose and the prefix/current split on the GPU, and the ragged plan for every rank, and
 compares everything with the CPU oracle.
 """
 import numpy as np
@@ -93,6 +93,16 @@ def test_fuzz_compose(seed):
     oracle.staging(batch.cur_lens, batch.writer, rows, want_stg, page_size=ps, cp_size=cp)
     for w in range(cp):
         assert np.array_equal(stg[w], want_stg[w]), w
+    # the one-launch layer compose: same dense buffer, same stagings
+    for s in layers.staging:
+        s.fill_(0x42)
+    one = torch.full((cap * ps, R), 0xD1, dtype=torch.uint8, device="cuda")
+    layers.compose_one_launch(d_slabs, d_rows, one)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    assert np.array_equal(one.cpu().numpy(), want)
+    for w in range(cp):
+        assert np.array_equal(layers.staging[w].cpu().numpy(), want_stg[w]), w
 
 
 @pytest.mark.parametrize("seed", range(30))
