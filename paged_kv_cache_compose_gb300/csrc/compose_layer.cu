@@ -32,6 +32,12 @@
 namespace cpkv {
 namespace {
 
+// Order this thread's earlier global accesses (generic proxy) before its later
+// bulk copies (async proxy) of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 constexpr int kStages = 4;
 constexpr int kLoadsInFlight = 2;
 constexpr int kMaxCtasPerSm = 3;
