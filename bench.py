@@ -62,6 +62,8 @@ def layer_bytes(prefix_lens, cur_lens, page_size, row_bytes, dense_cap_pages):
         "gather_write": gather_write, "fill": fill_read + fill_write, "gather": gather_read + gather_write,
         "total": fill_read + fill_write + gather_read + gather_write,
         "single_pass_ideal": T * R + int((pl // ps).sum()) * ps * R + D * ps * R, "T": T, "D": D, "pad_rows": pad,
+        # one-launch staging compose: the pad rows are written to the dense page, not read back
+        "layer": fill_read + fill_write + gather_read - pad * R + gather_write,
         # one-pass compose: current rows and prefix pages read once, every dense slot written once
         "fused": T * R + int((pl // ps).sum()) * ps * R + dense_cap_pages * ps * R,
     }
@@ -234,8 +236,8 @@ class ComposeWorkload:
             if b.planes:
                 raise ValueError("the one-launch layer compose takes row-major pages only")
             self.launches_per_step = 3 + self.num_layers  # plan (2) + ragged (1) + one fill+gather launch per layer
-            self.layer_bytes = self.bytes["total"]
-            self.kernels = {"layer": self.bytes["total"]}
+            self.layer_bytes = self.bytes["layer"]
+            self.kernels = {"layer": self.bytes["layer"]}
         elif variant == "prefetch":
             # layer-ahead: prefix pages of layer l+1 gathered on a side stream while layer l is consumed
             self.launches_per_step = 3 + 3 * self.num_layers  # plan + ragged + (prefetch, fill, current gather)

@@ -3,21 +3,23 @@
 // the writers' stagings followed by the slot-dense gather over the 2*cp
 // pointer table — in a single launch.
 //
-// Every CTA walks its units (pieces of dense pages, u = blockIdx.x + i*grid)
-// twice.  The first pass does, unit by unit,
-//   A  for a current page: the page's rows, copied from its writer's
-//      current-row buffer, go to staging slot src of writer owner - cp,
-//      followed by zero pad rows (the fill);
-//   B  for a pool page or zero slot: the page goes to the dense buffer (the
-//      prefix part of the gather);
-// the second pass does
-//   C  for a current page: staging slot src of writer owner - cp is copied
-//      back into the dense buffer (the current part of the gather).
-// A CTA gathers in C exactly the staging pieces it wrote in A, after its own
-// writes have completed, so no CTA waits on another, and the fill's reads
-// share DRAM time with the prefix pages' reads and writes instead of running
-// alone.  Every byte the two-kernel form moves is moved: the stagings are
-// written in full and read back.
+// Every one-warp CTA walks its units (pieces of dense pages,
+// u = blockIdx.x + i*grid) once, through one ring of bulk copies:
+//   - a pool page or zero slot goes to the dense buffer (the prefix part of
+//     the gather);
+//   - a current page's rows, copied from its writer's current-row buffer, go
+//     to staging slot src of writer owner - cp (the fill), and zero pad rows
+//     go to both the staging slot and the dense page;
+//   - a few bulk groups later, once `cp.async.bulk.wait_group` shows that the
+//     staging store has completed, the same rows are copied back from the
+//     staging slot into the dense page (the current part of the gather).
+// A CTA reads back only staging pieces it wrote itself, so no CTA waits on
+// another, and the fill's reads share DRAM time with the prefix pages'
+// streams instead of running alone.  Every staging row is written and read
+// back; the pad rows, zero in both places, are written to the dense page
+// directly instead of being read back.  Staging stores carry an L2
+// evict_last policy (their read-back follows within microseconds), all other
+// copies evict_first.
 //
 // The staging layout and the current pages' rows follow the plan of
 // cpkv_plan_build: current page i (src = i + 1) holds its n_i tokens, whose
@@ -32,16 +34,35 @@
 namespace cpkv {
 namespace {
 
-// Order this thread's earlier global accesses (generic proxy) before its later
-// bulk copies (async proxy) of global memory.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 constexpr int kStages = 4;
 constexpr int kLoadsInFlight = 2;
 constexpr int kMaxCtasPerSm = 3;
 constexpr int kMaxPieceBytes = 24 * 1024;
+constexpr int kReadbackQueue = 8;  // staging pieces waiting for their read-back, per CTA
+constexpr int kReadbackLag = 4;    // bulk groups committed after a staging store before its read-back
+
+// Wait until at most n (0..7; more counts as 7) of this thread's most recent
+// bulk groups are still pending, and every older one has completed: its
+// writes are done, not only its shared-memory reads.
+__device__ __forceinline__ void bulk_wait_complete_dyn(int64_t n) {
+  switch (n <= 0 ? 0 : (n >= 7 ? 7 : (int)n)) {
+    case 0: asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.bulk.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.bulk.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.bulk.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.bulk.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group 7;" ::: "memory"); break;
+  }
+}
+
+struct Readback {
+  const uint8_t *src;  // staging piece
+  uint8_t *dst;        // dense piece
+  uint32_t bytes;
+  int64_t q;           // ring index of the copy that stored the staging piece
+};
 
 template <int MAXB>
 struct LayerParams {
@@ -74,11 +95,15 @@ __device__ __forceinline__ int32_t current_rows(const LayerParams<MAXB> &p, cons
   return row0 >= 0 && row0 + *n <= p.cur_cap[w] ? 0 : CPKV_STATUS_ROW_OOB;
 }
 
-// The bulk ring with a per-piece choice of L2 policy for the store: staging
-// pieces are kept in L2 for their read-back, dense pieces stream through.
+// The bulk ring with a per-piece choice of L2 policy for the store, and a
+// queue of staging read-backs.  Every consume() commits exactly one bulk
+// group, so the store of the copy with ring index q is group q, and group q
+// has completed once wait_group(head - q - 1) returns.
 struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
   uint32_t keep_mask;  // bit s: the piece in stage s is stored with keep_policy (warp-uniform)
   uint64_t keep_policy, stream_policy;
+  Readback *rq;        // kReadbackQueue entries (shared; lane 0 writes, the warp reads)
+  int64_t rq_head, rq_tail;
 
   CPKV_DEV void consume_one() {
     store_policy = ((keep_mask >> (int)(head % kStages)) & 1u) ? keep_policy : stream_policy;
@@ -90,7 +115,36 @@ struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
     keep_mask = keep_in_l2 ? (keep_mask | bit) : (keep_mask & ~bit);
     push(src, dst, bytes);
   }
+  // Issue the oldest read-back once its staging store has completed.
+  CPKV_DEV void readback_front() {
+    const Readback r = rq[rq_head % kReadbackQueue];
+    while (head <= r.q) consume_one();  // the staging store has been issued
+    if ((threadIdx.x & 31) == 0) bulk_wait_complete_dyn(head - r.q - 1);
+    __syncwarp();
+    ++rq_head;
+    push_with(r.src, r.dst, r.bytes, false);
+  }
+  // Issue the read-backs whose stores are kReadbackLag groups old (all of
+  // them when `all`).
+  CPKV_DEV void service(bool all) {
+    while (rq_head < rq_tail) {
+      const int64_t q = rq[rq_head % kReadbackQueue].q;
+      if (!all && rq_tail - rq_head < kReadbackQueue && head - q - 1 < kReadbackLag) break;
+      readback_front();
+    }
+  }
+  // Store `bytes` of rows into a staging piece now; copy them back from there
+  // into the dense piece later.
+  CPKV_DEV void stage(const uint8_t *rows, uint8_t *stg, uint8_t *dst, uint32_t bytes) {
+    if (rq_tail - rq_head == kReadbackQueue) readback_front();
+    const int64_t q = tail;
+    push_with(rows, stg, bytes, true);
+    if ((threadIdx.x & 31) == 0) rq[rq_tail % kReadbackQueue] = Readback{stg, dst, bytes, q};
+    __syncwarp();
+    ++rq_tail;
+  }
   CPKV_DEV void drain_all() {
+    service(true);
     while (head < tail) consume_one();
     if ((threadIdx.x & 31) == 0) bulk_wait_all();
     __syncwarp();
@@ -106,8 +160,9 @@ __global__ void __launch_bounds__(32) compose_layer_kernel(const __grid_constant
   __shared__ int ring_live[kStages];
   __shared__ int32_t cur_page_start[MAXB + 1];
   __shared__ int64_t token_start[MAXB + 1];
+  __shared__ Readback readbacks[kReadbackQueue];
   const int lane = threadIdx.x;
-  const uint64_t keep = l2_policy_evict_last();
+  const uint64_t keep = l2_policy_evict_last();  // staging stores
 
   {  // request-level exclusive scans, 32 requests per step
     int32_t carry_pages = 0;
@@ -132,75 +187,61 @@ __global__ void __launch_bounds__(32) compose_layer_kernel(const __grid_constant
     __syncwarp();
   }
 
-  // Pass 1 runs phases A and B together in unit order: staging stores carry
-  // evict_last (pass 2 reads them back), dense stores evict_first.  Pass 2 is
-  // phase C.
   LayerRing ring;
   ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
   ring.keep_mask = 0;
   ring.keep_policy = keep;
   ring.stream_policy = ring.load_policy;
+  ring.rq = readbacks;
+  ring.rq_head = ring.rq_tail = 0;
   const int64_t step = gridDim.x;
-  for (int pass = 0; pass < 2; ++pass) {
-    if (pass == 1) {
-      // Every staging piece this CTA wrote in pass 1 is complete (bulk stores
-      // drained, the lanes' zero stores fenced) before pass 2 reads those
-      // pieces back with bulk copies.
-      ring.drain_all();
-      __threadfence();
-      fence_proxy_async_global();
-      __syncwarp();
+  for (int64_t base = blockIdx.x; base < p.units; base += 32 * step) {
+    const int64_t mine = base + lane * step;
+    int32_t my_o = -1, my_s = 0, my_row0 = -1;
+    if (mine < p.units) {
+      my_o = p.owner[mine / p.pieces];
+      my_s = p.src[mine / p.pieces];
     }
-    for (int64_t base = blockIdx.x; base < p.units; base += 32 * step) {
-      const int64_t mine = base + lane * step;
-      int32_t my_o = -1, my_s = 0, my_row0 = -1;
-      if (mine < p.units) {
-        my_o = p.owner[mine / p.pieces];
-        my_s = p.src[mine / p.pieces];
-      }
-      if (my_o >= p.cp && my_o < 2 * p.cp && my_s >= 1 && my_s <= p.C && p.B > 0) {
-        const int b = upper_index<int32_t>(cur_page_start, p.B, my_s - 1);
-        my_row0 = p.token_writer_row[token_start[b] + (int64_t)(my_s - 1 - cur_page_start[b]) * p.ps];
-      }
-      for (int j = 0; j < 32; ++j) {
-        const int64_t u = base + j * step;
-        if (u >= p.units) break;  // uniform across the warp
-        const int32_t o = __shfl_sync(0xffffffffu, my_o, j);
-        const int32_t s = __shfl_sync(0xffffffffu, my_s, j);
-        const int32_t row0 = __shfl_sync(0xffffffffu, my_row0, j);
-        const int64_t d = u / p.pieces;
-        const int32_t k = (int32_t)(u - d * p.pieces);
-        const int64_t off = (int64_t)k * p.piece_bytes;
-        const uint32_t bytes = (uint32_t)min64(p.piece_bytes, p.page_bytes - off);
-        uint8_t *dst = p.dense + d * p.page_bytes + off;
-        const bool is_current = o >= p.cp && o < 2 * p.cp;
-        if (!is_current) {  // phase B: pool pages, zero slots, invalid descriptors
-          if (pass == 1) continue;
-          if (o >= 0 && o < p.cp && s >= 0 && s < p.cap_pages[o]) {
-            ring.push_with(p.table[o] + (int64_t)s * p.page_bytes + off, dst, bytes, false);
-          } else {
-            if (o != -1 && lane == 0 && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
-            warp_zero(dst, bytes);
-          }
-          continue;
+    if (my_o >= p.cp && my_o < 2 * p.cp && my_s >= 1 && my_s <= p.C && p.B > 0) {
+      const int b = upper_index<int32_t>(cur_page_start, p.B, my_s - 1);
+      my_row0 = p.token_writer_row[token_start[b] + (int64_t)(my_s - 1 - cur_page_start[b]) * p.ps];
+    }
+    for (int j = 0; j < 32; ++j) {
+      const int64_t u = base + j * step;
+      if (u >= p.units) break;  // uniform across the warp
+      const int32_t o = __shfl_sync(0xffffffffu, my_o, j);
+      const int32_t s = __shfl_sync(0xffffffffu, my_s, j);
+      const int32_t row0 = __shfl_sync(0xffffffffu, my_row0, j);
+      const int64_t d = u / p.pieces;
+      const int32_t k = (int32_t)(u - d * p.pieces);
+      const int64_t off = (int64_t)k * p.piece_bytes;
+      const uint32_t bytes = (uint32_t)min64(p.piece_bytes, p.page_bytes - off);
+      uint8_t *dst = p.dense + d * p.page_bytes + off;
+      if (!(o >= p.cp && o < 2 * p.cp)) {  // pool pages, zero slots, invalid descriptors
+        if (o >= 0 && o < p.cp && s >= 0 && s < p.cap_pages[o]) {
+          ring.push_with(p.table[o] + (int64_t)s * p.page_bytes + off, dst, bytes, false);
+        } else {
+          if (o != -1 && lane == 0 && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
+          warp_zero(dst, bytes);
         }
+      } else {
         int64_t n = 0;
         const int32_t bad = current_rows(p, cur_page_start, o, s, row0, &n);
-        if (pass == 0) {  // phase A, the fill: rows, then zero pad rows, into staging slot s
-          if (bad) continue;
+        if (bad) {
+          if (lane == 0 && k == 0) raise_status(p.status, bad);
+          warp_zero(dst, bytes);
+        } else {
           uint8_t *stg = const_cast<uint8_t *>(p.table[o]) + (int64_t)s * p.page_bytes + off;
           const int64_t rows_bytes = n * p.R;
           const int64_t copy = off < rows_bytes ? min64(bytes, rows_bytes - off) : 0;
-          if (copy > 0)
-            ring.push_with(p.cur_rows[o - p.cp] + (int64_t)row0 * p.R + off, stg, (uint32_t)copy, true);
-          if (copy < bytes) warp_zero_hint(stg + copy, bytes - (uint32_t)copy, keep);
-        } else if (!bad) {  // phase C: the staging piece written in pass 1, into the dense page
-          ring.push_with(p.table[o] + (int64_t)s * p.page_bytes + off, dst, bytes, false);
-        } else {
-          if (lane == 0 && k == 0) raise_status(p.status, bad);
-          warp_zero(dst, bytes);
+          if (copy > 0) ring.stage(p.cur_rows[o - p.cp] + (int64_t)row0 * p.R + off, stg, dst, (uint32_t)copy);
+          if (copy < bytes) {
+            warp_zero_hint(stg + copy, bytes - (uint32_t)copy, keep);
+            warp_zero(dst + copy, bytes - (uint32_t)copy);
+          }
         }
       }
+      ring.service(false);
     }
   }
   ring.drain_all();

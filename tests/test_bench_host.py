@@ -40,3 +40,15 @@ def test_read_peaks_fallback(tmp_path, monkeypatch):
     assert bench.read_peaks()[:2] == (bench.FALLBACK_HBM_GBS, "fallback")
     (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 7100.5, "bf16_tflops": 1900}')
     assert bench.read_peaks()[:2] == (7100.5, "measured")
+
+
+def test_layer_bytes_hand_counted():
+    """ps=4, R=16, prefix [4, 0], current [3, 5], dense_cap 5: T=8 rows, 4 pad
+    rows (1 + 3), D=4 pages (1 prefix + 1 + 2 current)."""
+    lb = bench.layer_bytes([4, 0], [3, 5], 4, 16, 5)
+    assert (lb["T"], lb["D"], lb["pad_rows"]) == (8, 4, 4)
+    assert lb["fill"] == 8 * 16 + 12 * 16
+    assert lb["gather"] == 4 * 4 * 16 + 5 * 4 * 16
+    assert lb["total"] == 896
+    assert lb["layer"] == 896 - 4 * 16      # pad rows zeroed in the dense page, not read back
+    assert lb["fused"] == 8 * 16 + 4 * 16 + 5 * 4 * 16
