@@ -42,12 +42,16 @@ FALLBACK_HBM_GBS = 6800.0
 # accounting
 # ---------------------------------------------------------------------------
 
-def layer_bytes(prefix_lens, cur_lens, page_size, row_bytes, dense_cap_pages):
+def layer_bytes(prefix_lens, cur_lens, page_size, row_bytes, dense_cap_pages, planes=None):
     """Algorithmic bytes of one layer's fill + gather.
 
     fill:   read T rows, write T rows + the pad rows of each request's last page
     gather: read every described page (prefix and current, D pages), write
             every dense slot (dense_cap pages; slots past D are zero-filled)
+    layer:  the one-launch form reads back only the staged slices: not the pad
+            rows, nor the slices of planes whose width or page offset is not a
+            16-byte multiple (those go to the staging and the dense page from
+            the same registers)
     """
     pl = np.asarray(prefix_lens, np.int64)
     cl = np.asarray(cur_lens, np.int64)
@@ -57,13 +61,18 @@ def layer_bytes(prefix_lens, cur_lens, page_size, row_bytes, dense_cap_pages):
     D = int((pl // ps).sum() + ((cl + ps - 1) // ps).sum())
     fill_read, fill_write = T * R, (T + pad) * R
     gather_read, gather_write = D * ps * R, dense_cap_pages * ps * R
+    unstaged, at = 0, 0
+    for w in (planes or (R,)):
+        if w % 16 or at % 16:
+            unstaged += w
+        at += ps * w
     return {
         "fill_read": fill_read, "fill_write": fill_write, "gather_read": gather_read,
         "gather_write": gather_write, "fill": fill_read + fill_write, "gather": gather_read + gather_write,
         "total": fill_read + fill_write + gather_read + gather_write,
         "single_pass_ideal": T * R + int((pl // ps).sum()) * ps * R + D * ps * R, "T": T, "D": D, "pad_rows": pad,
         # one-launch staging compose: the pad rows are written to the dense page, not read back
-        "layer": fill_read + fill_write + gather_read - pad * R + gather_write,
+        "layer": fill_read + fill_write + gather_read - pad * R - T * unstaged + gather_write,
         # one-pass compose: current rows and prefix pages read once, every dense slot written once
         "fused": T * R + int((pl // ps).sum()) * ps * R + dense_cap_pages * ps * R,
     }
@@ -221,7 +230,8 @@ class ComposeWorkload:
         self.ragged_out = cpkv.ragged_buffers(max(S, 1), max(Q, 1), self.device)
         self.d_cp_index = torch.from_numpy(self.cp_index).to(self.device)
         self.ragged_counts = torch.zeros(2, dtype=torch.int64, device=self.device)
-        self.bytes = layer_bytes(b.prefix_lens, b.cur_lens, b.page_size, b.row_bytes, self.plan.dense_cap_pages)
+        self.bytes = layer_bytes(b.prefix_lens, b.cur_lens, b.page_size, b.row_bytes, self.plan.dense_cap_pages,
+                                 b.planes)
         self.graph = None
         self.variant = variant
         if variant == "staging":
@@ -233,8 +243,6 @@ class ComposeWorkload:
             self.layer_bytes = self.bytes["fused"]
             self.kernels = {"fused": self.bytes["fused"]}
         elif variant == "layer":
-            if b.planes:
-                raise ValueError("the one-launch layer compose takes row-major pages only")
             self.launches_per_step = 3 + self.num_layers  # plan (2) + ragged (1) + one fill+gather launch per layer
             self.layer_bytes = self.bytes["layer"]
             self.kernels = {"layer": self.bytes["layer"]}
@@ -298,7 +306,8 @@ class ComposeWorkload:
             self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream)
             return
         if self.variant == "layer":
-            self.layers.compose_one_launch(self.pools_of(layer), self.rows[layer], dense, stream)
+            self.layers.compose_one_launch(self.pools_of(layer), self.rows[layer], dense, stream,
+                                           plane_bytes=list(self.batch.planes) if self.batch.planes else None)
             return
         if kind in ("all", "fill"):
             if self.batch.planes:

@@ -257,11 +257,12 @@ int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
 /*
  * cpkv_compose_layer — per layer: cpkv_fill_current followed by
  * cpkv_compose_gather in one launch, for the plan of cpkv_plan_build.  Each
- * CTA first fills its share of current pages into the stagings, then gathers
- * its pool pages (and zero slots) into the dense buffer, then gathers back
- * from the stagings exactly the current pieces it wrote.  The stagings and
- * the dense buffer end up byte-identical to the two-call form; every staging
- * byte is still written and read back.
+ * CTA copies its pool pages (and zeroes its zero slots) into the dense
+ * buffer, stores the rows of its current pages into their staging slots,
+ * and reads each staged piece back into the dense page once that store has
+ * completed.  The stagings and the dense buffer end up byte-identical to the
+ * two-call form; every staged row is written and read back (pad rows, zero
+ * in both, are written to the dense page directly).
  *   h_cur_lens       host int32 [B]
  *   h_cur_rows       host array [cp] of device pointers, writer w's current
  *                    rows [h_cur_rows_cap[w]][R], 16-byte aligned
@@ -284,6 +285,28 @@ int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row_bytes, con
                        const void *const *h_src_table, const int64_t *h_src_cap_pages, const int32_t *d_owner,
                        const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
                        void *d_dense, int32_t *d_status, cpkv_stream_t stream);
+
+/*
+ * cpkv_compose_layer_planes — cpkv_compose_layer for planar pages (the
+ * layout of cpkv_fill_current_planes): per layer, cpkv_fill_current_planes
+ * followed by cpkv_compose_gather with row_bytes = sum(plane_bytes), in one
+ * launch, with the same stagings and dense buffer as those two calls.  A
+ * plane whose slices are 16-byte multiples at a 16-byte-aligned offset in
+ * the page is staged and read back with bulk copies; the slices of any other
+ * plane are written by the lanes to the staging and the dense page alike.
+ *   n_planes          1..4; h_plane_bytes[p] a positive multiple of 4 and
+ *                     ps * sum(h_plane_bytes) a multiple of 16
+ *   h_cur_planes      host array [n_planes * cp] of device pointers: writer
+ *                     w's rows of plane p, [h_cur_rows_cap[w]][plane_bytes[p]],
+ *                     16-byte aligned
+ *   other arguments, status bits and errors: as cpkv_compose_layer.
+ */
+int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int n_planes, const int32_t *h_plane_bytes,
+                              const int32_t *h_cur_lens, const void *const *h_cur_planes,
+                              const int64_t *h_cur_rows_cap, const void *const *h_src_table,
+                              const int64_t *h_src_cap_pages, const int32_t *d_owner, const int32_t *d_src,
+                              const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
+                              int32_t *d_status, cpkv_stream_t stream);
 
 /*
  * cpkv_compose_fused — per layer: the single-GPU compose in one pass, without

@@ -45,7 +45,8 @@ MAX_BATCH = 1024
 EXPORTED = (
     "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_fill_current",
     "cpkv_fill_current_planes",
-    "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
+    "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_layer_planes",
+    "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
     "cpkv_version",
 )
 
@@ -75,6 +76,7 @@ def _declare(lib):
     lib.cpkv_fill_current_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
     lib.cpkv_compose_gather_kinds.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _I, _P, _P, _P]
     lib.cpkv_compose_layer.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_compose_layer_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
     lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
@@ -261,6 +263,25 @@ def cpkv_compose_layer(cur_lens, cur_rows: Sequence, src_table: Sequence, src_ca
                                    _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense), _dp(d_status),
                                    _stream(stream))
     _check("cpkv_compose_layer", rc)
+
+
+def cpkv_compose_layer_planes(cur_lens, cur_planes: Sequence, src_table: Sequence, src_cap_pages, d_owner, d_src,
+                              d_token_writer_row, d_dense, *, page_size, cp_size, plane_bytes, dense_cap_pages,
+                              d_status, cur_rows_cap=None, stream=None):
+    """Fill + gather of one layer of planar pages in a single launch
+    (``cur_planes[p][w]``: writer w's rows of plane p)."""
+    cl, pb = _host_i32(cur_lens), _host_i32(plane_bytes)
+    n_planes = len(pb)
+    if cur_rows_cap is None:
+        cur_rows_cap = [cur_planes[0][w].numel() // int(pb[0]) for w in range(cp_size)]
+    rcaps, tcaps = _host_i64(cur_rows_cap), _host_i64(src_cap_pages)
+    flat = _ptr_array([cur_planes[p][w] for p in range(n_planes) for w in range(cp_size)])
+    tarr = _ptr_array(src_table)
+    rc = load().cpkv_compose_layer_planes(len(cl), page_size, cp_size, n_planes, _hp(pb), _hp(cl),
+                                          ctypes.cast(flat, _P), _hp(rcaps), ctypes.cast(tarr, _P), _hp(tcaps),
+                                          _dp(d_owner), _dp(d_src), _dp(d_token_writer_row), dense_cap_pages,
+                                          _dp(d_dense), _dp(d_status), _stream(stream))
+    _check("cpkv_compose_layer_planes", rc)
 
 
 def cpkv_compose_fused(cur_lens, pools: Sequence, cur_rows: Sequence, d_owner, d_src, d_token_writer_row, d_dense,

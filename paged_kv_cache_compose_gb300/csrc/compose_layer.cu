@@ -3,8 +3,9 @@
 // the writers' stagings followed by the slot-dense gather over the 2*cp
 // pointer table — in a single launch.
 //
-// Every one-warp CTA walks its units (pieces of dense pages,
-// u = blockIdx.x + i*grid) once, through one ring of bulk copies:
+// Every CTA walks its units (pieces of dense pages, u = blockIdx.x + i*grid)
+// once; one warp drives a ring of bulk copies (for planar pages a second warp
+// does the plain stores: zero slots, pad slices, lane-copied planes):
 //   - a pool page or zero slot goes to the dense buffer (the prefix part of
 //     the gather);
 //   - a current page's rows, copied from its writer's current-row buffer, go
@@ -21,12 +22,21 @@
 // evict_last policy (their read-back follows within microseconds), all other
 // copies evict_first.
 //
+// Pages may be planar (cpkv_compose_layer_planes): plane q of a page holds
+// the ps tokens' plane_bytes[q]-byte slices, the planes one after the other.
+// A plane whose slices are 16-byte multiples starting 16-byte aligned in the
+// page is staged and read back as above; the slices of any other plane (the
+// 4-byte scales of the NSA indexer keys) are copied by the warp's lanes,
+// 4 bytes at a time, into both the staging slot and the dense page.  The row
+// layout is the one-plane case.
+//
 // The staging layout and the current pages' rows follow the plan of
 // cpkv_plan_build: current page i (src = i + 1) holds its n_i tokens, whose
 // rows are consecutive in their writer's buffer starting at
 // token_writer_row of the page's first token.  The outputs (stagings and
 // dense buffer) are byte-identical to cpkv_fill_current followed by
-// cpkv_compose_gather on those plan arrays.
+// cpkv_compose_gather on those plan arrays (cpkv_fill_current_planes for
+// planar pages).
 #include <stdint.h>
 
 #include "bulk_ring.cuh"
@@ -40,6 +50,8 @@ constexpr int kMaxCtasPerSm = 3;
 constexpr int kMaxPieceBytes = 24 * 1024;
 constexpr int kReadbackQueue = 8;  // staging pieces waiting for their read-back, per CTA
 constexpr int kReadbackLag = 4;    // bulk groups committed after a staging store before its read-back
+constexpr int kMaxPlanes = 4;
+constexpr int kWordsPerLane = 8;   // 4-byte words a lane keeps in flight when lanes copy a plane slice
 
 // Wait until at most n (0..7; more counts as 7) of this thread's most recent
 // bulk groups are still pending, and every older one has completed: its
@@ -64,27 +76,83 @@ struct Readback {
   int64_t q;           // ring index of the copy that stored the staging piece
 };
 
-template <int MAXB>
+// NP: plane slots (1 for the row layout, which keeps the launch's parameter
+// block small).
+template <int MAXB, int NP>
 struct LayerParams {
   const uint8_t *table[2 * CPKV_MAX_CP];  // pools, then stagings
   int64_t cap_pages[2 * CPKV_MAX_CP];
-  const uint8_t *cur_rows[CPKV_MAX_CP];
-  int64_t cur_cap[CPKV_MAX_CP];
+  const uint8_t *cur_rows[NP][CPKV_MAX_CP];  // plane q of writer w's current rows
+  int64_t cur_cap[CPKV_MAX_CP];              // rows of writer w (every plane)
+  int64_t plane_off[NP];                     // byte offset of plane q in a page
+  int32_t plane_bytes[NP];
+  int32_t plane_bulk[NP];                    // plane q is staged with bulk copies
   const int32_t *owner, *src, *token_writer_row;
   uint8_t *dense;
   int32_t *status;
-  int64_t dense_cap, page_bytes, units, R, C;
-  int32_t cp, ps, B, pieces, piece_bytes;
+  int64_t dense_cap, page_bytes, units, C;
+  int32_t cp, ps, B, pieces, piece_bytes, n_planes;
   int32_t cur_lens[MAXB];
 };
+
+__device__ __forceinline__ uint32_t ld_stream4(const void *p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st4(void *p, uint32_t v) {
+  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st4_hint(void *p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+
+// Copy `bytes` (a multiple of 4) from src to both stg (L2 policy `pol`) and
+// dst with the warp's lanes, kWordsPerLane loads in flight per lane.
+__device__ __forceinline__ void warp_copy_words(const uint8_t *src, uint8_t *stg, uint8_t *dst, uint32_t bytes,
+                                                uint64_t pol) {
+  const uint32_t words = bytes / 4, lane = threadIdx.x & 31;
+  for (uint32_t base = 0; base < words; base += 32 * kWordsPerLane) {
+    uint32_t v[kWordsPerLane];
+#pragma unroll
+    for (int k = 0; k < kWordsPerLane; ++k) {
+      const uint32_t i = base + k * 32 + lane;
+      if (i < words) v[k] = ld_stream4(src + 4 * (size_t)i);
+    }
+#pragma unroll
+    for (int k = 0; k < kWordsPerLane; ++k) {
+      const uint32_t i = base + k * 32 + lane;
+      if (i < words) {
+        st4_hint(stg + 4 * (size_t)i, v[k], pol);
+        st4(dst + 4 * (size_t)i, v[k]);
+      }
+    }
+  }
+}
+
+// Zero `bytes` (a multiple of 4) at dst with the warp's lanes: 16-byte stores
+// when dst and bytes allow, else 4-byte stores; with an L2 policy when `hint`.
+__device__ __forceinline__ void warp_zero_span(uint8_t *dst, uint32_t bytes, bool hint, uint64_t pol) {
+  if (((reinterpret_cast<uintptr_t>(dst) | bytes) & 15u) == 0) {
+    if (hint) warp_zero_hint(dst, bytes, pol);
+    else warp_zero(dst, bytes);
+    return;
+  }
+  for (uint32_t i = threadIdx.x & 31; i < bytes / 4; i += 32) {
+    if (hint) st4_hint(dst + 4 * (size_t)i, 0u, pol);
+    else st4(dst + 4 * (size_t)i, 0u);
+  }
+}
 
 // Where a current page's rows come from: n rows starting at row0 of its
 // writer's buffer.  Returns 0, or the status bit to raise when the descriptor
 // (CPKV_STATUS_DESC_OOB) or the rows (CPKV_STATUS_ROW_OOB) are out of range;
 // such a page is zero-filled in the dense buffer and its staging slot is left
 // untouched.
-template <int MAXB>
-__device__ __forceinline__ int32_t current_rows(const LayerParams<MAXB> &p, const int32_t *cur_page_start,
+template <typename Params>
+__device__ __forceinline__ int32_t current_rows(const Params &p, const int32_t *cur_page_start,
                                                 int32_t o, int32_t s, int32_t row0, int64_t *n) {
   const int32_t w = o - p.cp, i = s - 1;
   if (i < 0 || i >= p.C || p.B == 0 || s >= p.cap_pages[o]) return CPKV_STATUS_DESC_OOB;
@@ -151,8 +219,10 @@ struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
   }
 };
 
-template <int MAXB>
-__global__ void __launch_bounds__(32) compose_layer_kernel(const __grid_constant__ LayerParams<MAXB> p) {
+// PLANAR false: one plane, staged with bulk copies (the row layout).
+template <int MAXB, bool PLANAR>
+__global__ void __launch_bounds__(64, 1)
+    compose_layer_kernel(const __grid_constant__ LayerParams<MAXB, PLANAR ? kMaxPlanes : 1> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ uint8_t *ring_dst[kStages];
@@ -161,10 +231,16 @@ __global__ void __launch_bounds__(32) compose_layer_kernel(const __grid_constant
   __shared__ int32_t cur_page_start[MAXB + 1];
   __shared__ int64_t token_start[MAXB + 1];
   __shared__ Readback readbacks[kReadbackQueue];
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const bool copy_warp = threadIdx.x < 32;
+  // Planar pages: warp 0 issues every bulk copy, warp 1 does every plain
+  // store (zero slots, pad slices, lane-copied plane slices), so that a load
+  // it waits on never holds up the ring; the two warps write disjoint bytes.
+  // Row layout (one warp): the same warp does both.
+  const bool copy_role = copy_warp, store_role = PLANAR ? !copy_warp : true;
   const uint64_t keep = l2_policy_evict_last();  // staging stores
 
-  {  // request-level exclusive scans, 32 requests per step
+  if (copy_warp) {  // request-level exclusive scans, 32 requests per step
     int32_t carry_pages = 0;
     int64_t carry_tok = 0;
     for (int base = 0; base < p.B; base += 32) {
@@ -184,16 +260,18 @@ __global__ void __launch_bounds__(32) compose_layer_kernel(const __grid_constant
       cur_page_start[p.B] = carry_pages;
       token_start[p.B] = carry_tok;
     }
-    __syncwarp();
   }
+  __syncthreads();
 
   LayerRing ring;
-  ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
-  ring.keep_mask = 0;
-  ring.keep_policy = keep;
-  ring.stream_policy = ring.load_policy;
-  ring.rq = readbacks;
-  ring.rq_head = ring.rq_tail = 0;
+  if (copy_warp) {
+    ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
+    ring.keep_mask = 0;
+    ring.keep_policy = keep;
+    ring.stream_policy = ring.load_policy;
+    ring.rq = readbacks;
+    ring.rq_head = ring.rq_tail = 0;
+  }
   const int64_t step = gridDim.x;
   for (int64_t base = blockIdx.x; base < p.units; base += 32 * step) {
     const int64_t mine = base + lane * step;
@@ -219,8 +297,8 @@ __global__ void __launch_bounds__(32) compose_layer_kernel(const __grid_constant
       uint8_t *dst = p.dense + d * p.page_bytes + off;
       if (!(o >= p.cp && o < 2 * p.cp)) {  // pool pages, zero slots, invalid descriptors
         if (o >= 0 && o < p.cp && s >= 0 && s < p.cap_pages[o]) {
-          ring.push_with(p.table[o] + (int64_t)s * p.page_bytes + off, dst, bytes, false);
-        } else {
+          if (copy_role) ring.push_with(p.table[o] + (int64_t)s * p.page_bytes + off, dst, bytes, false);
+        } else if (store_role) {
           if (o != -1 && lane == 0 && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
           warp_zero(dst, bytes);
         }
@@ -228,23 +306,38 @@ __global__ void __launch_bounds__(32) compose_layer_kernel(const __grid_constant
         int64_t n = 0;
         const int32_t bad = current_rows(p, cur_page_start, o, s, row0, &n);
         if (bad) {
-          if (lane == 0 && k == 0) raise_status(p.status, bad);
-          warp_zero(dst, bytes);
+          if (store_role) {
+            if (lane == 0 && k == 0) raise_status(p.status, bad);
+            warp_zero(dst, bytes);
+          }
         } else {
-          uint8_t *stg = const_cast<uint8_t *>(p.table[o]) + (int64_t)s * p.page_bytes + off;
-          const int64_t rows_bytes = n * p.R;
-          const int64_t copy = off < rows_bytes ? min64(bytes, rows_bytes - off) : 0;
-          if (copy > 0) ring.stage(p.cur_rows[o - p.cp] + (int64_t)row0 * p.R + off, stg, dst, (uint32_t)copy);
-          if (copy < bytes) {
-            warp_zero_hint(stg + copy, bytes - (uint32_t)copy, keep);
-            warp_zero(dst + copy, bytes - (uint32_t)copy);
+          // per plane: the rows' slices inside this piece, then the pad slices
+          uint8_t *stg_page = const_cast<uint8_t *>(p.table[o]) + (int64_t)s * p.page_bytes;
+          uint8_t *dense_page = p.dense + d * p.page_bytes;
+          const int64_t end = off + bytes;
+          const int n_planes = PLANAR ? p.n_planes : 1;
+          for (int q = 0; q < n_planes; ++q) {
+            const int64_t P = PLANAR ? p.plane_off[q] : 0, w = p.plane_bytes[q];
+            const bool bulk = PLANAR ? p.plane_bulk[q] != 0 : true;
+            const int64_t rows_end = P + n * w, plane_end = P + (int64_t)p.ps * w;
+            const int64_t lo = off > P ? off : P, hi = min64(end, rows_end);
+            if (lo < hi && (bulk ? copy_role : store_role)) {
+              const uint8_t *from = p.cur_rows[q][o - p.cp] + (int64_t)row0 * w + (lo - P);
+              if (bulk) ring.stage(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo));
+              else warp_copy_words(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo), keep);
+            }
+            const int64_t zlo = off > rows_end ? off : rows_end, zhi = min64(end, plane_end);
+            if (zlo < zhi && store_role) {
+              warp_zero_span(stg_page + zlo, (uint32_t)(zhi - zlo), true, keep);
+              warp_zero_span(dense_page + zlo, (uint32_t)(zhi - zlo), false, 0);
+            }
           }
         }
       }
-      ring.service(false);
+      if (copy_warp) ring.service(false);
     }
   }
-  ring.drain_all();
+  if (copy_warp) ring.drain_all();
 }
 
 inline int64_t ctas_per_sm(size_t ring_smem) {
@@ -256,16 +349,43 @@ inline int64_t ctas_per_sm(size_t ring_smem) {
 }  // namespace
 }  // namespace cpkv
 
-extern "C" int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
-                                  const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
-                                  const void *const *h_src_table, const int64_t *h_src_cap_pages,
-                                  const int32_t *d_owner, const int32_t *d_src, const int32_t *d_token_writer_row,
-                                  int64_t dense_cap_pages, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
+namespace {
+
+// Launch one instantiation of the kernel, raising its shared-memory limit on
+// the first launch on each device.
+template <typename Params>
+int launch_layer(void (*kernel)(Params), int which, int threads, int grid, size_t smem, cudaStream_t s,
+                 const Params &prm) {
+  using namespace cpkv;
+  static int configured[256][4] = {{0}};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CPKV_ERR_CUDA;
+  if (dev >= 0 && dev < 256 && !configured[dev][which]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStages * kMaxPieceBytes) !=
+        cudaSuccess)
+      return CPKV_ERR_CUDA;
+    configured[dev][which] = 1;
+  }
+  kernel<<<grid, threads, smem, s>>>(prm);
+  return launch_status();
+}
+
+int compose_layer_impl(int B, int page_size, int cp_size, int n_planes, const int32_t *h_plane_bytes,
+                       const int32_t *h_cur_lens, const void *const *h_cur_planes, const int64_t *h_cur_rows_cap,
+                       const void *const *h_src_table, const int64_t *h_src_cap_pages, const int32_t *d_owner,
+                       const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
+                       void *d_dense, int32_t *d_status, cudaStream_t s) {
   using namespace cpkv;
   if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
-  if (row_bytes <= 0 || row_bytes % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
+  if (n_planes < 1 || n_planes > kMaxPlanes || h_plane_bytes == nullptr || dense_cap_pages < 0) return CPKV_ERR_ARG;
+  int64_t row_bytes = 0;
+  for (int q = 0; q < n_planes; ++q) {
+    if (h_plane_bytes[q] <= 0 || h_plane_bytes[q] % 4 != 0) return CPKV_ERR_ARG;
+    row_bytes += h_plane_bytes[q];
+  }
+  if (((int64_t)page_size * row_bytes) % 16 != 0) return CPKV_ERR_ARG;
   if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
-  if (h_cur_rows == nullptr || h_cur_rows_cap == nullptr || h_src_table == nullptr || h_src_cap_pages == nullptr ||
+  if (h_cur_planes == nullptr || h_cur_rows_cap == nullptr || h_src_table == nullptr || h_src_cap_pages == nullptr ||
       d_status == nullptr)
     return CPKV_ERR_ARG;
   if (B > 0 && h_cur_lens == nullptr) return CPKV_ERR_ARG;
@@ -283,7 +403,10 @@ extern "C" int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row
   for (int w = 0; w < cp_size; ++w) {
     if (C > 0 && h_src_cap_pages[cp_size + w] < C + 1) return CPKV_ERR_CAPACITY;  // staging slots 1..C
     if (h_cur_rows_cap[w] < 0) return CPKV_ERR_ARG;
-    if (h_cur_rows_cap[w] > 0 && (h_cur_rows[w] == nullptr || !aligned16(h_cur_rows[w]))) return CPKV_ERR_ARG;
+    for (int q = 0; q < n_planes; ++q) {
+      const void *rows = h_cur_planes[q * cp_size + w];
+      if (h_cur_rows_cap[w] > 0 && (rows == nullptr || !aligned16(rows))) return CPKV_ERR_ARG;
+    }
   }
   if (dense_cap_pages == 0) return CPKV_OK;
   if (d_owner == nullptr || d_src == nullptr || d_dense == nullptr || !aligned16(d_dense)) return CPKV_ERR_ARG;
@@ -296,47 +419,77 @@ extern "C" int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row
   const size_t smem = (size_t)kStages * piece_bytes;
   const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(smem);
   const int grid = (int)(units < cap ? units : cap);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-#define CPKV_FILL_LAYER(prm)                                                                         \
-  for (int k = 0; k < 2 * CPKV_MAX_CP; ++k) {                                                        \
-    prm.table[k] = k < 2 * cp_size ? static_cast<const uint8_t *>(h_src_table[k]) : nullptr;         \
-    prm.cap_pages[k] = k < 2 * cp_size ? h_src_cap_pages[k] : 0;                                     \
-  }                                                                                                  \
-  for (int w = 0; w < CPKV_MAX_CP; ++w) {                                                            \
-    prm.cur_rows[w] = w < cp_size ? static_cast<const uint8_t *>(h_cur_rows[w]) : nullptr;          \
-    prm.cur_cap[w] = w < cp_size ? h_cur_rows_cap[w] : 0;                                            \
-  }                                                                                                  \
-  prm.owner = d_owner; prm.src = d_src; prm.token_writer_row = d_token_writer_row;                   \
-  prm.dense = static_cast<uint8_t *>(d_dense); prm.status = d_status; prm.dense_cap = dense_cap_pages; \
-  prm.page_bytes = page_bytes; prm.units = units; prm.R = row_bytes; prm.C = C; prm.cp = cp_size;   \
-  prm.ps = page_size; prm.B = B; prm.pieces = (int32_t)pieces; prm.piece_bytes = (int32_t)piece_bytes; \
+#define CPKV_FILL_LAYER(prm)                                                                           \
+  for (int k = 0; k < 2 * CPKV_MAX_CP; ++k) {                                                          \
+    prm.table[k] = k < 2 * cp_size ? static_cast<const uint8_t *>(h_src_table[k]) : nullptr;           \
+    prm.cap_pages[k] = k < 2 * cp_size ? h_src_cap_pages[k] : 0;                                       \
+  }                                                                                                    \
+  for (int q = 0; q < (int)(sizeof(prm.plane_bytes) / sizeof(int32_t)); ++q)                           \
+    for (int w = 0; w < CPKV_MAX_CP; ++w)                                                              \
+      prm.cur_rows[q][w] =                                                                             \
+          q < n_planes && w < cp_size ? static_cast<const uint8_t *>(h_cur_planes[q * cp_size + w]) : nullptr; \
+  for (int w = 0; w < CPKV_MAX_CP; ++w) prm.cur_cap[w] = w < cp_size ? h_cur_rows_cap[w] : 0;         \
+  {                                                                                                    \
+    int64_t at = 0;                                                                                    \
+    for (int q = 0; q < (int)(sizeof(prm.plane_bytes) / sizeof(int32_t)); ++q) {                     \
+      const int32_t wq = q < n_planes ? h_plane_bytes[q] : 0;                                          \
+      prm.plane_off[q] = at;                                                                           \
+      prm.plane_bytes[q] = wq;                                                                         \
+      prm.plane_bulk[q] = (wq % 16 == 0 && at % 16 == 0) ? 1 : 0;                                      \
+      at += (int64_t)page_size * wq;                                                                   \
+    }                                                                                                  \
+  }                                                                                                    \
+  prm.owner = d_owner; prm.src = d_src; prm.token_writer_row = d_token_writer_row;                     \
+  prm.dense = static_cast<uint8_t *>(d_dense); prm.status = d_status; prm.dense_cap = dense_cap_pages;   \
+  prm.page_bytes = page_bytes; prm.units = units; prm.C = C; prm.cp = cp_size; prm.ps = page_size;     \
+  prm.B = B; prm.pieces = (int32_t)pieces; prm.piece_bytes = (int32_t)piece_bytes; prm.n_planes = n_planes; \
   for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
 
-  static int configured[256][2] = {{0}};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (B <= 64) {
-    if (dev >= 0 && dev < 256 && !configured[dev][0]) {
-      if (cudaFuncSetAttribute(compose_layer_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kStages * kMaxPieceBytes) != cudaSuccess)
-        return CPKV_ERR_CUDA;
-      configured[dev][0] = 1;
-    }
-    LayerParams<64> prm;
+  const bool planar = !(n_planes == 1 && h_plane_bytes[0] % 16 == 0);
+  if (B <= 64 && planar) {
+    LayerParams<64, kMaxPlanes> prm;
     CPKV_FILL_LAYER(prm)
-    compose_layer_kernel<64><<<grid, 32, smem, s>>>(prm);
-    return launch_status();
+    return launch_layer(compose_layer_kernel<64, true>, 0, 64, grid, smem, s, prm);
   }
-  if (dev >= 0 && dev < 256 && !configured[dev][1]) {
-    if (cudaFuncSetAttribute(compose_layer_kernel<CPKV_MAX_BATCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStages * kMaxPieceBytes) != cudaSuccess)
-      return CPKV_ERR_CUDA;
-    configured[dev][1] = 1;
+  if (B <= 64) {
+    LayerParams<64, 1> prm;
+    CPKV_FILL_LAYER(prm)
+    return launch_layer(compose_layer_kernel<64, false>, 1, 32, grid, smem, s, prm);
   }
-  LayerParams<CPKV_MAX_BATCH> prm;
+  if (planar) {
+    LayerParams<CPKV_MAX_BATCH, kMaxPlanes> prm;
+    CPKV_FILL_LAYER(prm)
+    return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true>, 2, 64, grid, smem, s, prm);
+  }
+  LayerParams<CPKV_MAX_BATCH, 1> prm;
   CPKV_FILL_LAYER(prm)
 #undef CPKV_FILL_LAYER
-  compose_layer_kernel<CPKV_MAX_BATCH><<<grid, 32, smem, s>>>(prm);
-  return launch_status();
+  return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, false>, 3, 32, grid, smem, s, prm);
+}
+
+}  // namespace
+
+extern "C" int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
+                                  const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
+                                  const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                                  const int32_t *d_owner, const int32_t *d_src, const int32_t *d_token_writer_row,
+                                  int64_t dense_cap_pages, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
+  if (row_bytes <= 0 || row_bytes % 16 != 0 || row_bytes > INT32_MAX) return CPKV_ERR_ARG;
+  const int32_t plane = (int32_t)row_bytes;
+  return compose_layer_impl(B, page_size, cp_size, 1, &plane, h_cur_lens, h_cur_rows, h_cur_rows_cap, h_src_table,
+                            h_src_cap_pages, d_owner, d_src, d_token_writer_row, dense_cap_pages, d_dense, d_status,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int n_planes,
+                                         const int32_t *h_plane_bytes, const int32_t *h_cur_lens,
+                                         const void *const *h_cur_planes, const int64_t *h_cur_rows_cap,
+                                         const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                                         const int32_t *d_owner, const int32_t *d_src,
+                                         const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
+                                         int32_t *d_status, cpkv_stream_t stream) {
+  return compose_layer_impl(B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens, h_cur_planes, h_cur_rows_cap,
+                            h_src_table, h_src_cap_pages, d_owner, d_src, d_token_writer_row, dense_cap_pages,
+                            d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
 }

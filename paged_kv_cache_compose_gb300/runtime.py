@@ -119,11 +119,19 @@ class ComposeLayers:
                                 dense, page_size=p.page_size, cp_size=p.cp_size, row_bytes=self.row_bytes,
                                 dense_cap_pages=p.dense_cap_pages, d_status=p.d_status, stream=stream)
 
-    def compose_one_launch(self, pools, cur_rows_per_writer, dense, stream=None):
-        """Fill + gather of a layer in a single launch (cpkv_compose_layer)."""
+    def compose_one_launch(self, pools, cur_rows_per_writer, dense, stream=None, plane_bytes=None):
+        """Fill + gather of a layer in a single launch (cpkv_compose_layer; for
+        planar pages, ``plane_bytes`` and ``cur_rows_per_writer[p][w]``,
+        cpkv_compose_layer_planes)."""
         p = self.plan
         table = list(pools) + list(self.staging)
         caps = [t.shape[0] for t in pools] + [p.staging_cap_pages] * p.cp_size
+        if plane_bytes is not None:
+            cpkv.cpkv_compose_layer_planes(p.cur_lens, cur_rows_per_writer, table, caps, p["owner"], p["src"],
+                                           p["token_writer_row"], dense, page_size=p.page_size, cp_size=p.cp_size,
+                                           plane_bytes=plane_bytes, dense_cap_pages=p.dense_cap_pages,
+                                           d_status=p.d_status, stream=stream)
+            return
         cpkv.cpkv_compose_layer(p.cur_lens, cur_rows_per_writer, table, caps, p["owner"], p["src"],
                                 p["token_writer_row"], dense, page_size=p.page_size, cp_size=p.cp_size,
                                 row_bytes=self.row_bytes, dense_cap_pages=p.dense_cap_pages, d_status=p.d_status,

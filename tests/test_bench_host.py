@@ -52,3 +52,13 @@ def test_layer_bytes_hand_counted():
     assert lb["total"] == 896
     assert lb["layer"] == 896 - 4 * 16      # pad rows zeroed in the dense page, not read back
     assert lb["fused"] == 8 * 16 + 4 * 16 + 5 * 4 * 16
+
+
+def test_layer_bytes_planar_unstaged_planes():
+    """Planes (128, 4) at ps=4: the 4-byte scale plane is not staged; planes
+    (16, 4, 16) at ps=3: the third plane starts at byte 60, not staged."""
+    lb = bench.layer_bytes([4, 0], [3, 5], 4, 132, 5, planes=(128, 4))
+    assert lb["layer"] == lb["total"] - 4 * 132 - 8 * 4
+    lb = bench.layer_bytes([3], [4], 3, 36, 3, planes=(16, 4, 16))
+    # T=4, pad=2; plane offsets 0, 48, 60: planes 2 (width 4) and 3 (offset 60) unstaged
+    assert lb["layer"] == lb["total"] - 2 * 36 - 4 * (4 + 16)

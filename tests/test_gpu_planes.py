@@ -108,3 +108,78 @@ def test_planar_rejects_bad_planes():
                                       d_staging_rows=plan["staging_rows"], d_token_writer_row=plan["token_writer_row"],
                                       d_writer=plan.d_writer, num_cur_pages=plan.C, d_status=plan.d_status,
                                       cur_rows_cap=[0, 0])
+
+
+# ---------------------------------------------------------------------------
+# one-launch layer compose of planar pages: same stagings and dense buffer
+# ---------------------------------------------------------------------------
+
+def _one_launch(batch, dense_extra=1, guard=0x3C):
+    ps, cp = batch.page_size, batch.cp_size
+    T, C, D = oracle.sizes(batch.prefix_lens, batch.cur_lens, ps)
+    plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                       page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages,
+                       dense_cap_pages=D + dense_extra).build()
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs, planes, per_writer = _inputs(batch)
+    for st in layers.staging:
+        st.fill_(guard)
+    d_planes = [[torch.from_numpy(x).cuda() for x in pw] for pw in per_writer]
+    dense = torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
+    layers.compose_one_launch([torch.from_numpy(s).cuda() for s in slabs], d_planes, dense,
+                              plane_bytes=list(batch.planes))
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    want = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, planes,
+                                       page_size=ps, cp_size=cp, plane_bytes=list(batch.planes),
+                                       dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, ps * batch.row_bytes), want)
+    want_stg = [np.full((plan.staging_cap_pages, ps * batch.row_bytes), guard, np.uint8) for _ in range(cp)]
+    st = oracle.fill_planes(batch.cur_lens, plan["staging_rows"].cpu().numpy(),
+                            plan["token_writer_row"].cpu().numpy(), batch.writer, per_writer, want_stg,
+                            page_size=ps, cp_size=cp, plane_bytes=list(batch.planes))
+    assert st == 0
+    for w in range(cp):
+        got = layers.staging[w].cpu().numpy().reshape(plan.staging_cap_pages, ps * batch.row_bytes)
+        assert np.array_equal(got, want_stg[w]), w
+
+
+@pytest.mark.parametrize("batch", _edge_planar(), ids=lambda b: b.name)
+def test_planar_one_launch_matches_oracle(batch):
+    _one_launch(batch)
+
+
+@pytest.mark.parametrize("ps,planes", [(16, (16,)), (16, (64, 4)), (16, (4, 4, 8)), (16, (128, 4)),
+                                       (16, (32, 16, 4, 12)), (3, (4, 16, 12)), (64, (512, 16)), (64, (384, 4, 12)),
+                                       (1, (4, 12)), (64, (128, 4))])
+def test_planar_one_launch_plane_shapes(ps, planes):
+    """Staged and lane-copied planes, a 16-byte plane at an unaligned offset
+    (ps=3), and pages of several pieces whose boundaries cut a plane."""
+    rng = np.random.default_rng(ps * 100 + sum(planes))
+    B = 6
+    pfx = (rng.integers(0, 5 * ps, B) // ps) * ps
+    cur = rng.integers(0, 4 * ps, B)
+    b = wl.make_compose_batch("pl", 77, page_size=ps, cp_size=3, num_pool_pages=300, row_bytes=sum(planes),
+                              prefix_lens=pfx, cur_lens=cur, row_kind="bytes")
+    _one_launch(_planar(b, planes))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_planar_one_launch_fuzz(seed):
+    rng = np.random.default_rng(50_000 + seed)
+    ps = int(rng.choice([1, 2, 3, 4, 8, 16, 64]))
+    while True:
+        planes = tuple(int(4 * rng.integers(1, 40)) for _ in range(int(rng.integers(1, 5))))
+        if (ps * sum(planes)) % 16 == 0:
+            break
+    cp = int(rng.integers(1, 9))
+    B = int(rng.integers(0, 20))
+    pfx = rng.integers(0, 5, size=B) * ps
+    cur = rng.integers(0, 4 * ps + 1, size=B)
+    mode = int(rng.integers(0, 3))
+    C = int(((cur + ps - 1) // ps).sum())
+    writer = (wl.round_robin_writers(C, cp) if mode == 0 else wl.contiguous_writers(cur, ps, cp) if mode == 1
+              else rng.integers(0, cp, size=C).astype(np.int32))
+    b = wl.make_compose_batch(f"plf{seed}", seed, page_size=ps, cp_size=cp, num_pool_pages=int(pfx.sum() // ps) + C + 9,
+                              row_bytes=sum(planes), prefix_lens=pfx, cur_lens=cur, writer=writer, row_kind="bytes")
+    _one_launch(_planar(b, planes), dense_extra=int(rng.integers(0, 3)))
