@@ -1,6 +1,7 @@
 // cpkv_plan_build: the per-batch compose plan on the device.
 //
-// Two launches on the caller's stream:
+// Two launches on the caller's stream, the second a programmatic dependent
+// of the first (it starts early and waits only before the inverse scatters):
 //   1. plan_init_inverses  — page_inverse[:] = -1, staging_page_inverse[:] = 0
 //                            (P entries each; the only P-sized work).
 //   2. plan_main           — blocks [0, nA): one thread per dense slot:
@@ -40,6 +41,9 @@ struct PlanParams {
 
 __global__ void plan_init_inverses(int32_t *__restrict__ pi, int32_t *__restrict__ spi, int64_t P,
                                    bool vec) {
+  // plan_main may start now: it waits for this grid only before its first
+  // access to the inverses.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if (vec) {
@@ -73,6 +77,35 @@ struct RequestScan {
 
 template <int MAXB>
 __device__ void build_request_scan(const PlanParams<MAXB> &p, RequestScan &rs) {
+  if (p.B <= 32) {  // one warp: shuffle scans and a single barrier
+    if (threadIdx.x < 32) {
+      const int b = threadIdx.x;
+      int64_t npp = 0, ncp = 0, cur = 0;
+      if (b < p.B) {
+        npp = p.prefix_lens[b] / p.ps;
+        cur = p.cur_lens[b];
+        ncp = (cur + p.ps - 1) / p.ps;
+      }
+      const int64_t ds = warp_inclusive_scan<int64_t>(npp + ncp);
+      const int64_t cs = warp_inclusive_scan<int64_t>(ncp);
+      const int64_t pp = warp_inclusive_scan<int64_t>(npp);
+      const int64_t ts = warp_inclusive_scan<int64_t>(cur);
+      if (b < p.B) {
+        rs.dense_start[b] = (int32_t)(ds - npp - ncp);
+        rs.cur_page_start[b] = (int32_t)(cs - ncp);
+        rs.prefix_page_start[b] = (int32_t)(pp - npp);
+        rs.token_start[b] = ts - cur;
+      }
+      if (b == 31) {  // lanes past B add nothing, so lane 31 holds the totals
+        rs.dense_start[p.B] = (int32_t)ds;
+        rs.cur_page_start[p.B] = (int32_t)cs;
+        rs.prefix_page_start[p.B] = (int32_t)pp;
+        rs.token_start[p.B] = ts;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   const int b = threadIdx.x;
   const int ps = p.ps;
   int64_t npp = 0, ncp = 0, cur = 0;
@@ -123,8 +156,13 @@ __device__ void plan_dense_slots(const PlanParams<MAXB> &p, const RequestScan &r
     const int32_t k = (int32_t)d - rs.dense_start[b];
     const int32_t npp = p.prefix_lens[b] / p.ps;
     const unsigned int slot = (unsigned int)d;
-    if (k < npp) {
-      const int32_t lp = p.prefix_pages[rs.prefix_page_start[b] + k];
+    // the page tables are loaded before waiting for plan_init_inverses
+    const bool is_prefix = k < npp;
+    const int32_t i = is_prefix ? 0 : rs.cur_page_start[b] + (k - npp);
+    const int32_t lp = is_prefix ? p.prefix_pages[rs.prefix_page_start[b] + k] : p.cur_pages[i];
+    const int32_t w = is_prefix ? 0 : p.writer[i];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (is_prefix) {
       if (lp < 1 || lp >= p.P) {
         raise_status(p.status, CPKV_STATUS_PAGE_OOB);
       } else {
@@ -136,9 +174,6 @@ __device__ void plan_dense_slots(const PlanParams<MAXB> &p, const RequestScan &r
           raise_status(p.status, CPKV_STATUS_CURRENT_IN_PREFIX);
       }
     } else {
-      const int32_t i = rs.cur_page_start[b] + (k - npp);
-      const int32_t lp = p.cur_pages[i];
-      const int32_t w = p.writer[i];
       if (lp < 1 || lp >= p.P) {
         raise_status(p.status, CPKV_STATUS_PAGE_OOB);
       } else if (w < 0 || w >= p.cp) {
@@ -251,10 +286,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_main(const __grid_constant_
   }
 }
 
+// plan_main is a programmatic dependent of plan_init_inverses: its request
+// scans, page-table loads, descriptors and token arrays overlap the init;
+// only the inverse scatters wait for it (griddepcontrol.wait).
 template <int MAXB>
 int launch_plan(const PlanParams<MAXB> &prm, int nB, cudaStream_t s) {
   const int grid = prm.nA + nB;
-  if (grid > 0) plan_main<MAXB><<<grid, kPlanThreads, 0, s>>>(prm);
+  if (grid == 0) return CPKV_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, plan_main<MAXB>, prm) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CPKV_ERR_CUDA;
+  }
   return launch_status();
 }
 
