@@ -180,7 +180,7 @@ class ComposeWorkload:
     per-layer current rows, stagings, dense double buffer, ragged plan."""
 
     def __init__(self, config: str = "traced_78", device="cuda", num_layers: int | None = None,
-                 variant: str = "staging"):
+                 variant: str = "staging", pool_pages: int | None = None):
         import torch
 
         from paged_kv_cache_compose_gb300 import cpkv
@@ -188,7 +188,10 @@ class ComposeWorkload:
 
         self.torch, self.cpkv = torch, cpkv
         self.config = config
-        self.batch = b = wl.CONFIGS[config]()
+        if pool_pages is not None and config not in ("fp8_nsa", "index_k"):
+            raise ValueError("--pool-pages applies to the shared-pool workloads only")
+        self.batch = b = (wl.CONFIGS[config]() if pool_pages is None
+                          else wl.CONFIGS[config](num_pool_pages=pool_pages))
         self.num_layers = b.num_layers if num_layers is None else min(num_layers, b.num_layers)
         self.device = torch.device(device)
         self.plan = ComposePlan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer,
@@ -516,6 +519,9 @@ def main(argv=None):
     ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's bounded sample")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small cases for profiling; the headline uses all 78)")
+    ap.add_argument("--pool-pages", type=int, default=None,
+                    help="pool size of the shared-pool workloads (fp8_nsa, index_k): small device footprints for "
+                         "profiling; every launch still moves the same pages")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
 
@@ -538,7 +544,7 @@ def main(argv=None):
     from paged_kv_cache_compose_gb300 import build as cpkv_build
 
     cpkv_build.build()
-    work = ComposeWorkload(a.config, device=device, num_layers=a.layers, variant=a.variant)
+    work = ComposeWorkload(a.config, device=device, num_layers=a.layers, variant=a.variant, pool_pages=a.pool_pages)
     hbm_peak, peak_src, _ = read_peaks()
 
     # warm-up (also the first use of every kernel), then capture

@@ -7,8 +7,8 @@
 // source page, so the kernel moves pages with bulk async copies (TMA,
 // non-tensor form): global -> shared with mbarrier completion, then
 // shared -> global tracked by bulk groups.  Each page is cut into `pieces`
-// equal 16-byte-multiple units (<= 24 KB); units are dealt round-robin to a
-// persistent grid of one-warp CTAs, two per SM.  Each CTA runs a BulkRing of
+// equal 16-byte-multiple units (<= 16 KB); units are dealt round-robin to a
+// persistent grid of one-warp CTAs, 3 or 4 per SM.  Each CTA runs a BulkRing of
 // 4 shared-memory stages with at most 2 loads outstanding, so the other
 // stages hold stores still draining: loads and stores overlap instead of a
 // stage waiting for its own store.  Every copy carries an L2 evict_first
@@ -19,6 +19,8 @@
 // wait is bounded (see bulk_ring.cuh).
 #include <stdint.h>
 
+#include <mutex>
+
 #include "bulk_ring.cuh"
 
 namespace cpkv {
@@ -26,8 +28,12 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kLoadsInFlight = 2;
-constexpr int kMaxCtasPerSm = 3;  // one-warp CTAs per SM, as many as shared memory allows
-constexpr int kMaxPieceBytes = 24 * 1024;
+constexpr int kMaxPieceBytes = 16 * 1024;
+// One-warp CTAs per SM, as many as shared memory allows up to: 4 when pages
+// are cut into several pieces, 3 for pages of one piece (more CTAs measured
+// slower there).
+constexpr int kMaxCtasPerSmPieces = 4;
+constexpr int kMaxCtasPerSmOnePiece = 3;
 
 struct GatherParams {
   const uint8_t *table[2 * CPKV_MAX_CP];
@@ -108,10 +114,35 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
   ring.drain();
 }
 
-inline int64_t ctas_per_sm(size_t ring_smem) {
-  // 227 KB of shared memory per SM; allow for static shared memory and the 1 KB per-CTA reserve
-  const int64_t fit = (int64_t)(227 * 1024) / (int64_t)(ring_smem + 14 * 1024);
-  return fit < 1 ? 1 : (fit > kMaxCtasPerSm ? kMaxCtasPerSm : fit);
+// Resident CTAs per SM for `ring_smem` bytes of dynamic shared memory (the
+// occupancy calculator, cached per device and size), at most `cap`.
+inline int64_t ctas_per_sm(size_t ring_smem, int cap) {
+  struct Entry {
+    int dev;
+    size_t smem;
+    int ctas;
+  };
+  static Entry cache[16];
+  static int n_cached = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 1;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  int ctas = 0;
+  for (int i = 0; i < n_cached; ++i)
+    if (cache[i].dev == dev && cache[i].smem == ring_smem) ctas = cache[i].ctas;
+  if (ctas == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, gather_pages_kernel, 32, ring_smem) != cudaSuccess ||
+        ctas < 1) {
+      (void)cudaGetLastError();
+      ctas = 1;
+    }
+    if (n_cached < 16) cache[n_cached++] = Entry{dev, ring_smem, ctas};
+  }
+  return ctas > cap ? cap : ctas;
 }
 
 }  // namespace
@@ -166,9 +197,8 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
       return CPKV_ERR_CUDA;
     configured[dev] = 1;
   }
-  // One-warp CTAs: 3 per SM when their rings fit in shared memory (small
-  // pages), else 2 (24 KB pieces).
-  const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(smem);
+  const int64_t cap =
+      (int64_t)device_sm_count() * ctas_per_sm(smem, pieces > 1 ? kMaxCtasPerSmPieces : kMaxCtasPerSmOnePiece);
   const int grid = (int)(prm.units < cap ? prm.units : cap);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   gather_pages_kernel<<<grid, 32, smem, s>>>(prm);
