@@ -306,7 +306,8 @@ class ComposeWorkload:
         """Launch one layer's work: ``all`` of it, or one kernel of it."""
         dense = self.layers.dense[layer % 2]
         if self.variant == "fused":
-            self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream)
+            self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream,
+                                      plane_bytes=list(self.batch.planes) if self.batch.planes else None)
             return
         if self.variant == "layer":
             self.layers.compose_one_launch(self.pools_of(layer), self.rows[layer], dense, stream,
@@ -648,8 +649,10 @@ def main(argv=None):
         "roofline": {
             "bound": "hbm",
             "kernel": {"gather": "gather_pages_kernel (cpkv_compose_gather)",
-                       "fused": "compose_fused_kernel (cpkv_compose_fused)",
-                       "layer": "compose_layer_kernel (cpkv_compose_layer)"}[top],
+                       "fused": ("compose_layer_kernel (cpkv_compose_fused_planes)" if work.batch.planes
+                                 else "compose_fused_kernel (cpkv_compose_fused)"),
+                       "layer": ("compose_layer_kernel (cpkv_compose_layer_planes)" if work.batch.planes
+                                 else "compose_layer_kernel (cpkv_compose_layer)")}[top],
             "achieved": round(kgbs[top], 1),
             "peak": hbm_peak,
             "peak_source": peak_src,

@@ -336,6 +336,25 @@ int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row_bytes, con
                        void *d_dense, int32_t *d_status, cpkv_stream_t stream);
 
 /*
+ * cpkv_compose_fused_planes — cpkv_compose_fused for planar pages (the layout
+ * of cpkv_fill_current_planes): output byte-identical to
+ * cpkv_fill_current_planes followed by cpkv_compose_gather, in one pass
+ * without stagings.  Plane slices that are 16-byte multiples at a
+ * 16-byte-aligned page offset move with bulk copies, other slices with the
+ * lanes.  One plane of a 16-byte-multiple width is cpkv_compose_fused.
+ *   n_planes, h_plane_bytes, h_cur_planes: as cpkv_compose_layer_planes
+ *   h_pools, h_pool_cap_pages: as cpkv_compose_fused
+ * A descriptor outside the table raises DESC_OOB, rows outside a writer's
+ * buffer ROW_OOB; either page is zero-filled.  Errors: as cpkv_compose_layer.
+ */
+int cpkv_compose_fused_planes(int B, int page_size, int cp_size, int n_planes, const int32_t *h_plane_bytes,
+                              const int32_t *h_cur_lens, const void *const *h_pools,
+                              const int64_t *h_pool_cap_pages, const void *const *h_cur_planes,
+                              const int64_t *h_cur_rows_cap, const int32_t *d_owner, const int32_t *d_src,
+                              const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
+                              int32_t *d_status, cpkv_stream_t stream);
+
+/*
  * cpkv_ragged_plan_sizes — exact segment count S and q-token count Q_r of a
  * rank's ragged plan, from a host copy of its cp_index (host only).
  */

@@ -9,6 +9,7 @@ from . import cpkv  # noqa: F401
 from .cpkv import (  # noqa: F401
     CpkvError,
     cpkv_compose_fused,
+    cpkv_compose_fused_planes,
     cpkv_compose_gather,
     cpkv_compose_gather_kinds,
     cpkv_compose_layer,
@@ -26,7 +27,7 @@ from .cpkv import (  # noqa: F401
 )
 
 __all__ = [
-    "cpkv", "CpkvError", "cpkv_compose_fused", "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_layer_planes", "cpkv_fill_current", "cpkv_fill_current_planes", "cpkv_plan_build", "cpkv_plan_sizes",
+    "cpkv", "CpkvError", "cpkv_compose_fused", "cpkv_compose_fused_planes", "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_layer_planes", "cpkv_fill_current", "cpkv_fill_current_planes", "cpkv_plan_build", "cpkv_plan_sizes",
     "cpkv_ragged_plan_build", "cpkv_ragged_plan_sizes", "cpkv_version", "cpkv_writer_token_counts",
     "plan_buffers", "ragged_buffers",
 ]

@@ -46,7 +46,7 @@ EXPORTED = (
     "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_fill_current",
     "cpkv_fill_current_planes",
     "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_layer_planes",
-    "cpkv_compose_fused", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
+    "cpkv_compose_fused", "cpkv_compose_fused_planes", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
     "cpkv_version",
 )
 
@@ -78,6 +78,7 @@ def _declare(lib):
     lib.cpkv_compose_layer.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_compose_layer_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_compose_fused_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
     lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
     for name in EXPORTED:
@@ -300,6 +301,27 @@ def cpkv_compose_fused(cur_lens, pools: Sequence, cur_rows: Sequence, d_owner, d
                                    _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense), _dp(d_status),
                                    _stream(stream))
     _check("cpkv_compose_fused", rc)
+
+
+def cpkv_compose_fused_planes(cur_lens, pools: Sequence, cur_planes: Sequence, d_owner, d_src, d_token_writer_row,
+                              d_dense, *, page_size, cp_size, plane_bytes, dense_cap_pages, d_status,
+                              pool_cap_pages=None, cur_rows_cap=None, stream=None):
+    """Single-GPU compose of one layer of planar pages without staging
+    (``cur_planes[p][w]``: writer w's rows of plane p)."""
+    cl, pb = _host_i32(cur_lens), _host_i32(plane_bytes)
+    n_planes = len(pb)
+    if pool_cap_pages is None:
+        pool_cap_pages = [t.shape[0] for t in pools]
+    if cur_rows_cap is None:
+        cur_rows_cap = [cur_planes[0][w].numel() // int(pb[0]) for w in range(cp_size)]
+    pcaps, rcaps = _host_i64(pool_cap_pages), _host_i64(cur_rows_cap)
+    parr = _ptr_array(pools)
+    flat = _ptr_array([cur_planes[p][w] for p in range(n_planes) for w in range(cp_size)])
+    rc = load().cpkv_compose_fused_planes(len(cl), page_size, cp_size, n_planes, _hp(pb), _hp(cl),
+                                          ctypes.cast(parr, _P), _hp(pcaps), ctypes.cast(flat, _P), _hp(rcaps),
+                                          _dp(d_owner), _dp(d_src), _dp(d_token_writer_row), dense_cap_pages,
+                                          _dp(d_dense), _dp(d_status), _stream(stream))
+    _check("cpkv_compose_fused_planes", rc)
 
 
 def cpkv_ragged_plan_build(prefix_lens, q_lens, d_cp_index, n_owned: int, *, chunk, k_align, out, d_counts,

@@ -109,8 +109,10 @@ __device__ __forceinline__ void st4_hint(void *p, uint32_t v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
 }
 
-// Copy `bytes` (a multiple of 4) from src to both stg (L2 policy `pol`) and
-// dst with the warp's lanes, kWordsPerLane loads in flight per lane.
+// Copy `bytes` (a multiple of 4) from src to dst, and to stg (L2 policy
+// `pol`) when STAGE, with the warp's lanes, kWordsPerLane loads in flight per
+// lane.
+template <bool STAGE>
 __device__ __forceinline__ void warp_copy_words(const uint8_t *src, uint8_t *stg, uint8_t *dst, uint32_t bytes,
                                                 uint64_t pol) {
   const uint32_t words = bytes / 4, lane = threadIdx.x & 31;
@@ -125,7 +127,7 @@ __device__ __forceinline__ void warp_copy_words(const uint8_t *src, uint8_t *stg
     for (int k = 0; k < kWordsPerLane; ++k) {
       const uint32_t i = base + k * 32 + lane;
       if (i < words) {
-        st4_hint(stg + 4 * (size_t)i, v[k], pol);
+        if (STAGE) st4_hint(stg + 4 * (size_t)i, v[k], pol);
         st4(dst + 4 * (size_t)i, v[k]);
       }
     }
@@ -148,14 +150,14 @@ __device__ __forceinline__ void warp_zero_span(uint8_t *dst, uint32_t bytes, boo
 
 // Where a current page's rows come from: n rows starting at row0 of its
 // writer's buffer.  Returns 0, or the status bit to raise when the descriptor
-// (CPKV_STATUS_DESC_OOB) or the rows (CPKV_STATUS_ROW_OOB) are out of range;
-// such a page is zero-filled in the dense buffer and its staging slot is left
-// untouched.
+// (CPKV_STATUS_DESC_OOB: also a staging slot past the staging's capacity when
+// `staged`) or the rows (CPKV_STATUS_ROW_OOB) are out of range; such a page is
+// zero-filled in the dense buffer and its staging slot is left untouched.
 template <typename Params>
-__device__ __forceinline__ int32_t current_rows(const Params &p, const int32_t *cur_page_start,
+__device__ __forceinline__ int32_t current_rows(const Params &p, const int32_t *cur_page_start, bool staged,
                                                 int32_t o, int32_t s, int32_t row0, int64_t *n) {
   const int32_t w = o - p.cp, i = s - 1;
-  if (i < 0 || i >= p.C || p.B == 0 || s >= p.cap_pages[o]) return CPKV_STATUS_DESC_OOB;
+  if (i < 0 || i >= p.C || p.B == 0 || (staged && s >= p.cap_pages[o])) return CPKV_STATUS_DESC_OOB;
   const int b = upper_index<int32_t>(cur_page_start, p.B, i);
   const int32_t kp = i - cur_page_start[b];
   *n = min64(p.ps, (int64_t)p.cur_lens[b] - (int64_t)kp * p.ps);
@@ -220,7 +222,9 @@ struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
 };
 
 // PLANAR false: one plane, staged with bulk copies (the row layout).
-template <int MAXB, bool PLANAR>
+// STAGED false: the single-GPU compose without stagings (owner cp + w names
+// writer w's current page src - 1, read straight from its rows).
+template <int MAXB, bool PLANAR, bool STAGED>
 __global__ void __launch_bounds__(64, 1)
     compose_layer_kernel(const __grid_constant__ LayerParams<MAXB, PLANAR ? kMaxPlanes : 1> p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(64, 1)
         }
       } else {
         int64_t n = 0;
-        const int32_t bad = current_rows(p, cur_page_start, o, s, row0, &n);
+        const int32_t bad = current_rows(p, cur_page_start, STAGED, o, s, row0, &n);
         if (bad) {
           if (store_role) {
             if (lane == 0 && k == 0) raise_status(p.status, bad);
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(64, 1)
           }
         } else {
           // per plane: the rows' slices inside this piece, then the pad slices
-          uint8_t *stg_page = const_cast<uint8_t *>(p.table[o]) + (int64_t)s * p.page_bytes;
+          uint8_t *stg_page = STAGED ? const_cast<uint8_t *>(p.table[o]) + (int64_t)s * p.page_bytes : nullptr;
           uint8_t *dense_page = p.dense + d * p.page_bytes;
           const int64_t end = off + bytes;
           const int n_planes = PLANAR ? p.n_planes : 1;
@@ -323,12 +327,13 @@ __global__ void __launch_bounds__(64, 1)
             const int64_t lo = off > P ? off : P, hi = min64(end, rows_end);
             if (lo < hi && (bulk ? copy_role : store_role)) {
               const uint8_t *from = p.cur_rows[q][o - p.cp] + (int64_t)row0 * w + (lo - P);
-              if (bulk) ring.stage(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo));
-              else warp_copy_words(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo), keep);
+              if (bulk && STAGED) ring.stage(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo));
+              else if (bulk) ring.push_with(from, dense_page + lo, (uint32_t)(hi - lo), false);
+              else warp_copy_words<STAGED>(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo), keep);
             }
             const int64_t zlo = off > rows_end ? off : rows_end, zhi = min64(end, plane_end);
             if (zlo < zhi && store_role) {
-              warp_zero_span(stg_page + zlo, (uint32_t)(zhi - zlo), true, keep);
+              if (STAGED) warp_zero_span(stg_page + zlo, (uint32_t)(zhi - zlo), true, keep);
               warp_zero_span(dense_page + zlo, (uint32_t)(zhi - zlo), false, 0);
             }
           }
@@ -357,7 +362,7 @@ template <typename Params>
 int launch_layer(void (*kernel)(Params), int which, int threads, int grid, size_t smem, cudaStream_t s,
                  const Params &prm) {
   using namespace cpkv;
-  static int configured[256][4] = {{0}};
+  static int configured[256][6] = {{0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CPKV_ERR_CUDA;
   if (dev >= 0 && dev < 256 && !configured[dev][which]) {
@@ -370,7 +375,9 @@ int launch_layer(void (*kernel)(Params), int which, int threads, int grid, size_
   return launch_status();
 }
 
-int compose_layer_impl(int B, int page_size, int cp_size, int n_planes, const int32_t *h_plane_bytes,
+// staged: h_src_table / h_src_cap_pages hold 2*cp entries (pools, then
+// stagings); else cp entries (pools only) and no staging is written.
+int compose_layer_impl(bool staged, int B, int page_size, int cp_size, int n_planes, const int32_t *h_plane_bytes,
                        const int32_t *h_cur_lens, const void *const *h_cur_planes, const int64_t *h_cur_rows_cap,
                        const void *const *h_src_table, const int64_t *h_src_cap_pages, const int32_t *d_owner,
                        const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
@@ -396,12 +403,13 @@ int compose_layer_impl(int B, int page_size, int cp_size, int n_planes, const in
     C += ceil_div(h_cur_lens[b], page_size);
   }
   if (T > INT32_MAX - 1 || C > INT32_MAX - 2) return CPKV_ERR_LIMIT;
-  for (int k = 0; k < 2 * cp_size; ++k) {
+  const int n_table = staged ? 2 * cp_size : cp_size;
+  for (int k = 0; k < n_table; ++k) {
     if (h_src_cap_pages[k] < 0) return CPKV_ERR_ARG;
     if (h_src_cap_pages[k] > 0 && (h_src_table[k] == nullptr || !aligned16(h_src_table[k]))) return CPKV_ERR_ARG;
   }
   for (int w = 0; w < cp_size; ++w) {
-    if (C > 0 && h_src_cap_pages[cp_size + w] < C + 1) return CPKV_ERR_CAPACITY;  // staging slots 1..C
+    if (staged && C > 0 && h_src_cap_pages[cp_size + w] < C + 1) return CPKV_ERR_CAPACITY;  // staging slots 1..C
     if (h_cur_rows_cap[w] < 0) return CPKV_ERR_ARG;
     for (int q = 0; q < n_planes; ++q) {
       const void *rows = h_cur_planes[q * cp_size + w];
@@ -422,8 +430,8 @@ int compose_layer_impl(int B, int page_size, int cp_size, int n_planes, const in
 
 #define CPKV_FILL_LAYER(prm)                                                                           \
   for (int k = 0; k < 2 * CPKV_MAX_CP; ++k) {                                                          \
-    prm.table[k] = k < 2 * cp_size ? static_cast<const uint8_t *>(h_src_table[k]) : nullptr;           \
-    prm.cap_pages[k] = k < 2 * cp_size ? h_src_cap_pages[k] : 0;                                       \
+    prm.table[k] = k < n_table ? static_cast<const uint8_t *>(h_src_table[k]) : nullptr;               \
+    prm.cap_pages[k] = k < n_table ? h_src_cap_pages[k] : 0;                                           \
   }                                                                                                    \
   for (int q = 0; q < (int)(sizeof(prm.plane_bytes) / sizeof(int32_t)); ++q)                           \
     for (int w = 0; w < CPKV_MAX_CP; ++w)                                                              \
@@ -446,26 +454,31 @@ int compose_layer_impl(int B, int page_size, int cp_size, int n_planes, const in
   prm.B = B; prm.pieces = (int32_t)pieces; prm.piece_bytes = (int32_t)piece_bytes; prm.n_planes = n_planes; \
   for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
 
+  // Row layout without stagings is cpkv_compose_fused (fused.cu); the
+  // callers route it there.
   const bool planar = !(n_planes == 1 && h_plane_bytes[0] % 16 == 0);
-  if (B <= 64 && planar) {
-    LayerParams<64, kMaxPlanes> prm;
-    CPKV_FILL_LAYER(prm)
-    return launch_layer(compose_layer_kernel<64, true>, 0, 64, grid, smem, s, prm);
-  }
+  if (!planar && !staged) return CPKV_ERR_ARG;
   if (B <= 64) {
+    if (planar) {
+      LayerParams<64, kMaxPlanes> prm;
+      CPKV_FILL_LAYER(prm)
+      if (staged) return launch_layer(compose_layer_kernel<64, true, true>, 0, 64, grid, smem, s, prm);
+      return launch_layer(compose_layer_kernel<64, true, false>, 1, 64, grid, smem, s, prm);
+    }
     LayerParams<64, 1> prm;
     CPKV_FILL_LAYER(prm)
-    return launch_layer(compose_layer_kernel<64, false>, 1, 32, grid, smem, s, prm);
+    return launch_layer(compose_layer_kernel<64, false, true>, 2, 32, grid, smem, s, prm);
   }
   if (planar) {
     LayerParams<CPKV_MAX_BATCH, kMaxPlanes> prm;
     CPKV_FILL_LAYER(prm)
-    return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true>, 2, 64, grid, smem, s, prm);
+    if (staged) return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true, true>, 3, 64, grid, smem, s, prm);
+    return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true, false>, 4, 64, grid, smem, s, prm);
   }
   LayerParams<CPKV_MAX_BATCH, 1> prm;
   CPKV_FILL_LAYER(prm)
 #undef CPKV_FILL_LAYER
-  return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, false>, 3, 32, grid, smem, s, prm);
+  return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, false, true>, 5, 32, grid, smem, s, prm);
 }
 
 }  // namespace
@@ -477,7 +490,7 @@ extern "C" int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row
                                   int64_t dense_cap_pages, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
   if (row_bytes <= 0 || row_bytes % 16 != 0 || row_bytes > INT32_MAX) return CPKV_ERR_ARG;
   const int32_t plane = (int32_t)row_bytes;
-  return compose_layer_impl(B, page_size, cp_size, 1, &plane, h_cur_lens, h_cur_rows, h_cur_rows_cap, h_src_table,
+  return compose_layer_impl(true, B, page_size, cp_size, 1, &plane, h_cur_lens, h_cur_rows, h_cur_rows_cap, h_src_table,
                             h_src_cap_pages, d_owner, d_src, d_token_writer_row, dense_cap_pages, d_dense, d_status,
                             reinterpret_cast<cudaStream_t>(stream));
 }
@@ -489,7 +502,23 @@ extern "C" int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int 
                                          const int32_t *d_owner, const int32_t *d_src,
                                          const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
                                          int32_t *d_status, cpkv_stream_t stream) {
-  return compose_layer_impl(B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens, h_cur_planes, h_cur_rows_cap,
-                            h_src_table, h_src_cap_pages, d_owner, d_src, d_token_writer_row, dense_cap_pages,
-                            d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
+  return compose_layer_impl(true, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens, h_cur_planes,
+                            h_cur_rows_cap, h_src_table, h_src_cap_pages, d_owner, d_src, d_token_writer_row,
+                            dense_cap_pages, d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int cpkv_compose_fused_planes(int B, int page_size, int cp_size, int n_planes,
+                                         const int32_t *h_plane_bytes, const int32_t *h_cur_lens,
+                                         const void *const *h_pools, const int64_t *h_pool_cap_pages,
+                                         const void *const *h_cur_planes, const int64_t *h_cur_rows_cap,
+                                         const int32_t *d_owner, const int32_t *d_src,
+                                         const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
+                                         int32_t *d_status, cpkv_stream_t stream) {
+  if (n_planes == 1 && h_plane_bytes != nullptr && h_plane_bytes[0] > 0 && h_plane_bytes[0] % 16 == 0)
+    return cpkv_compose_fused(B, page_size, cp_size, h_plane_bytes[0], h_cur_lens, h_pools, h_pool_cap_pages,
+                              h_cur_planes, h_cur_rows_cap, d_owner, d_src, d_token_writer_row, dense_cap_pages,
+                              d_dense, d_status, stream);
+  return compose_layer_impl(false, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens, h_cur_planes,
+                            h_cur_rows_cap, h_pools, h_pool_cap_pages, d_owner, d_src, d_token_writer_row,
+                            dense_cap_pages, d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -112,9 +112,16 @@ class ComposeLayers:
         self.fill(cur_rows_per_writer, stream)
         self.gather_kinds([None] * self.plan.cp_size, dense, cpkv.GATHER_STAGING, stream)
 
-    def compose_fused(self, pools, cur_rows_per_writer, dense, stream=None):
-        """One-pass single-GPU compose of a layer (no staging round trip)."""
+    def compose_fused(self, pools, cur_rows_per_writer, dense, stream=None, plane_bytes=None):
+        """One-pass single-GPU compose of a layer (no staging round trip); for
+        planar pages, ``plane_bytes`` and ``cur_rows_per_writer[p][w]``."""
         p = self.plan
+        if plane_bytes is not None:
+            cpkv.cpkv_compose_fused_planes(p.cur_lens, pools, cur_rows_per_writer, p["owner"], p["src"],
+                                           p["token_writer_row"], dense, page_size=p.page_size, cp_size=p.cp_size,
+                                           plane_bytes=plane_bytes, dense_cap_pages=p.dense_cap_pages,
+                                           d_status=p.d_status, stream=stream)
+            return
         cpkv.cpkv_compose_fused(p.cur_lens, pools, cur_rows_per_writer, p["owner"], p["src"], p["token_writer_row"],
                                 dense, page_size=p.page_size, cp_size=p.cp_size, row_bytes=self.row_bytes,
                                 dense_cap_pages=p.dense_cap_pages, d_status=p.d_status, stream=stream)

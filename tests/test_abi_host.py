@@ -112,6 +112,14 @@ def test_host_errors_before_any_launch(lib):
                                            ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 64,
                                            null)
         assert rc == cpkv.CPKV_ERR_ARG, (n_planes, pb, ps)
+    # planar fused compose: the same plane checks
+    for n_planes, pb, ps in ((0, [16], 2), (5, [16] * 5, 2), (2, [128, 2], 2), (2, [128, 4], 3)):
+        pba = np.array(pb, np.int32)
+        rc = lib.cpkv_compose_fused_planes(1, ps, 1, n_planes, pba.ctypes.data, cl.ctypes.data,
+                                           ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data,
+                                           ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data, 64, 64, 64, 4, 64, 64,
+                                           null)
+        assert rc == cpkv.CPKV_ERR_ARG, (n_planes, pb, ps)
     # ragged: bad chunk / k_align
     rc = lib.cpkv_ragged_plan_build(1, 0, 1, pl.ctypes.data, cl.ctypes.data, null, 0, null, 0, *([null] * 7), 0,
                                     null, null, null)

@@ -81,7 +81,8 @@ def _check_plan(work):
 @pytest.mark.parametrize("config,variant", [("traced_78", "staging"), ("fp8_nsa", "staging"),
                                             ("traced_78", "fused"), ("fp8_nsa", "fused"),
                                             ("traced_78", "prefetch"), ("index_k", "staging"),
-                                            ("traced_78", "layer"), ("fp8_nsa", "layer"), ("index_k", "layer")])
+                                            ("traced_78", "layer"), ("fp8_nsa", "layer"), ("index_k", "layer"),
+                                            ("index_k", "fused")])
 def test_benchmark_workload_matches_oracle(config, variant):
     work = bench.ComposeWorkload(config, variant=variant)
     try:

@@ -114,7 +114,10 @@ def test_planar_rejects_bad_planes():
 # one-launch layer compose of planar pages: same stagings and dense buffer
 # ---------------------------------------------------------------------------
 
-def _one_launch(batch, dense_extra=1, guard=0x3C):
+def _one_launch(batch, dense_extra=1, guard=0x3C, fused=False):
+    """The one-launch layer compose (fused=False: the stagings are checked
+    too) or the planar fused compose (fused=True: the stagings must keep
+    their guard bytes)."""
     ps, cp = batch.page_size, batch.cp_size
     T, C, D = oracle.sizes(batch.prefix_lens, batch.cur_lens, ps)
     plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
@@ -126,8 +129,11 @@ def _one_launch(batch, dense_extra=1, guard=0x3C):
         st.fill_(guard)
     d_planes = [[torch.from_numpy(x).cuda() for x in pw] for pw in per_writer]
     dense = torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
-    layers.compose_one_launch([torch.from_numpy(s).cuda() for s in slabs], d_planes, dense,
-                              plane_bytes=list(batch.planes))
+    pools = [torch.from_numpy(s).cuda() for s in slabs]
+    if fused:
+        layers.compose_fused(pools, d_planes, dense, plane_bytes=list(batch.planes))
+    else:
+        layers.compose_one_launch(pools, d_planes, dense, plane_bytes=list(batch.planes))
     torch.cuda.synchronize()
     assert int(plan.d_status.item()) == 0
     want = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, planes,
@@ -135,10 +141,11 @@ def _one_launch(batch, dense_extra=1, guard=0x3C):
                                        dense_cap=plan.dense_cap_pages)
     assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, ps * batch.row_bytes), want)
     want_stg = [np.full((plan.staging_cap_pages, ps * batch.row_bytes), guard, np.uint8) for _ in range(cp)]
-    st = oracle.fill_planes(batch.cur_lens, plan["staging_rows"].cpu().numpy(),
-                            plan["token_writer_row"].cpu().numpy(), batch.writer, per_writer, want_stg,
-                            page_size=ps, cp_size=cp, plane_bytes=list(batch.planes))
-    assert st == 0
+    if not fused:
+        st = oracle.fill_planes(batch.cur_lens, plan["staging_rows"].cpu().numpy(),
+                                plan["token_writer_row"].cpu().numpy(), batch.writer, per_writer, want_stg,
+                                page_size=ps, cp_size=cp, plane_bytes=list(batch.planes))
+        assert st == 0
     for w in range(cp):
         got = layers.staging[w].cpu().numpy().reshape(plan.staging_cap_pages, ps * batch.row_bytes)
         assert np.array_equal(got, want_stg[w]), w
@@ -182,4 +189,57 @@ def test_planar_one_launch_fuzz(seed):
               else rng.integers(0, cp, size=C).astype(np.int32))
     b = wl.make_compose_batch(f"plf{seed}", seed, page_size=ps, cp_size=cp, num_pool_pages=int(pfx.sum() // ps) + C + 9,
                               row_bytes=sum(planes), prefix_lens=pfx, cur_lens=cur, writer=writer, row_kind="bytes")
-    _one_launch(_planar(b, planes), dense_extra=int(rng.integers(0, 3)))
+    extra = int(rng.integers(0, 3))
+    _one_launch(_planar(b, planes), dense_extra=extra)
+    _one_launch(_planar(b, planes), dense_extra=extra, fused=True)
+
+
+# ---------------------------------------------------------------------------
+# planar fused compose (no stagings): same dense buffer, stagings untouched
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("batch", _edge_planar(), ids=lambda b: b.name)
+def test_planar_fused_matches_oracle(batch):
+    _one_launch(batch, fused=True)
+
+
+@pytest.mark.parametrize("ps,planes", [(16, (64, 4)), (16, (4, 4, 8)), (16, (128, 4)), (16, (32, 16, 4, 12)),
+                                       (3, (4, 16, 12)), (64, (512, 16)), (64, (384, 4, 12)), (1, (4, 12)),
+                                       (64, (128, 4)), (16, (16,))])
+def test_planar_fused_plane_shapes(ps, planes):
+    rng = np.random.default_rng(ps * 101 + sum(planes))
+    B = 6
+    pfx = (rng.integers(0, 5 * ps, B) // ps) * ps
+    cur = rng.integers(0, 4 * ps, B)
+    b = wl.make_compose_batch("plF", 78, page_size=ps, cp_size=3, num_pool_pages=300, row_bytes=sum(planes),
+                              prefix_lens=pfx, cur_lens=cur, row_kind="bytes")
+    _one_launch(_planar(b, planes), fused=True)
+
+
+def test_planar_fused_bad_descriptor_and_rows_are_zeroed_and_flagged():
+    b = _planar(wl.tiny_batch())
+    ps, cp = b.page_size, b.cp_size
+    plan = ComposePlan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer, page_size=ps, cp_size=cp,
+                       num_pool_pages=b.num_pool_pages).build()
+    slabs, planes, per_writer = _inputs(b)
+    pools = [torch.from_numpy(s).cuda() for s in slabs]
+    d_planes = [[torch.from_numpy(x).cuda() for x in pw] for pw in per_writer]
+    owner, src = plan["owner"].clone(), plan["src"].clone()
+    owner[0] = 2 * cp           # outside the table
+    src[1] = 10_000             # beyond the slab / current page range
+    dense = torch.full((plan.dense_cap_pages * ps, b.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_compose_fused_planes(b.cur_lens, pools, d_planes, owner, src, plan["token_writer_row"], dense,
+                                   page_size=ps, cp_size=cp, plane_bytes=list(b.planes),
+                                   dense_cap_pages=plan.dense_cap_pages, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == cpkv.STATUS_DESC_OOB
+    assert torch.all(dense[:2 * ps] == 0)
+    # writer 0's buffers one row short: its last current page is zeroed, ROW_OOB
+    caps = [per_writer[0][0].shape[0] - 1] + [per_writer[0][w].shape[0] for w in range(1, cp)]
+    status.zero_()
+    cpkv.cpkv_compose_fused_planes(b.cur_lens, pools, d_planes, plan["owner"], plan["src"], plan["token_writer_row"],
+                                   dense, page_size=ps, cp_size=cp, plane_bytes=list(b.planes),
+                                   dense_cap_pages=plan.dense_cap_pages, d_status=status, cur_rows_cap=caps)
+    torch.cuda.synchronize()
+    assert int(status.item()) == cpkv.STATUS_ROW_OOB
