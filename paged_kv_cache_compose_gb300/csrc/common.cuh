@@ -229,8 +229,18 @@ CPKV_DEV int upper_index(const T *a, int n, T x) {
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// Number of SMs of the current device (cached per device ordinal).
+// Number of SMs of the current device (cached per device; thread-safe).
 int device_sm_count();
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device and kernel (thread-safe).  CPKV_OK or CPKV_ERR_CUDA.
+int ensure_dynamic_smem(const void *kernel, int bytes);
+
+// One-dimensional grid for a persistent kernel of `threads`-thread CTAs with
+// `smem` bytes of dynamic shared memory: the SM count times the CTAs that stay
+// resident on one SM (occupancy calculator, cached per device, kernel and
+// size), at most `cap_per_sm` CTAs per SM, at most `units` CTAs, at least 1.
+int persistent_grid(const void *kernel, int threads, size_t smem, int cap_per_sm, int64_t units);
 
 // Map the last launch error to CPKV_ERR_CUDA.
 inline int launch_status() {

@@ -345,32 +345,20 @@ __global__ void __launch_bounds__(64, 1)
   if (copy_warp) ring.drain_all();
 }
 
-inline int64_t ctas_per_sm(size_t ring_smem) {
-  // 227 KB of shared memory per SM; allow for static shared memory and the 1 KB per-CTA reserve
-  const int64_t fit = (int64_t)(227 * 1024) / (int64_t)(ring_smem + 14 * 1024);
-  return fit < 1 ? 1 : (fit > kMaxCtasPerSm ? kMaxCtasPerSm : fit);
-}
-
 }  // namespace
 }  // namespace cpkv
 
 namespace {
 
-// Launch one instantiation of the kernel, raising its shared-memory limit on
-// the first launch on each device.
+// Launch one instantiation of the kernel on a persistent grid sized by the
+// occupancy calculator.
 template <typename Params>
-int launch_layer(void (*kernel)(Params), int which, int threads, int grid, size_t smem, cudaStream_t s,
+int launch_layer(void (*kernel)(Params), int threads, int64_t units, size_t smem, cudaStream_t s,
                  const Params &prm) {
   using namespace cpkv;
-  static int configured[256][6] = {{0}};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CPKV_ERR_CUDA;
-  if (dev >= 0 && dev < 256 && !configured[dev][which]) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStages * kMaxPieceBytes) !=
-        cudaSuccess)
-      return CPKV_ERR_CUDA;
-    configured[dev][which] = 1;
-  }
+  const void *fn = reinterpret_cast<const void *>(kernel);
+  if (ensure_dynamic_smem(fn, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
+  const int grid = persistent_grid(fn, threads, smem, kMaxCtasPerSm, units);
   kernel<<<grid, threads, smem, s>>>(prm);
   return launch_status();
 }
@@ -425,8 +413,6 @@ int compose_layer_impl(bool staged, int B, int page_size, int cp_size, int n_pla
   if (pieces > INT32_MAX || dense_cap_pages > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
   const int64_t units = dense_cap_pages * pieces;
   const size_t smem = (size_t)kStages * piece_bytes;
-  const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(smem);
-  const int grid = (int)(units < cap ? units : cap);
 
 #define CPKV_FILL_LAYER(prm)                                                                           \
   for (int k = 0; k < 2 * CPKV_MAX_CP; ++k) {                                                          \
@@ -462,23 +448,23 @@ int compose_layer_impl(bool staged, int B, int page_size, int cp_size, int n_pla
     if (planar) {
       LayerParams<64, kMaxPlanes> prm;
       CPKV_FILL_LAYER(prm)
-      if (staged) return launch_layer(compose_layer_kernel<64, true, true>, 0, 64, grid, smem, s, prm);
-      return launch_layer(compose_layer_kernel<64, true, false>, 1, 64, grid, smem, s, prm);
+      if (staged) return launch_layer(compose_layer_kernel<64, true, true>, 64, units, smem, s, prm);
+      return launch_layer(compose_layer_kernel<64, true, false>, 64, units, smem, s, prm);
     }
     LayerParams<64, 1> prm;
     CPKV_FILL_LAYER(prm)
-    return launch_layer(compose_layer_kernel<64, false, true>, 2, 32, grid, smem, s, prm);
+    return launch_layer(compose_layer_kernel<64, false, true>, 32, units, smem, s, prm);
   }
   if (planar) {
     LayerParams<CPKV_MAX_BATCH, kMaxPlanes> prm;
     CPKV_FILL_LAYER(prm)
-    if (staged) return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true, true>, 3, 64, grid, smem, s, prm);
-    return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true, false>, 4, 64, grid, smem, s, prm);
+    if (staged) return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true, true>, 64, units, smem, s, prm);
+    return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true, false>, 64, units, smem, s, prm);
   }
   LayerParams<CPKV_MAX_BATCH, 1> prm;
   CPKV_FILL_LAYER(prm)
 #undef CPKV_FILL_LAYER
-  return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, false, true>, 5, 32, grid, smem, s, prm);
+  return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, false, true>, 32, units, smem, s, prm);
 }
 
 }  // namespace

@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kLoadsInFlight = 2;
-constexpr int kMaxCtasPerSm = 3;  // one-warp CTAs per SM, as many as shared memory allows
+constexpr int kMaxCtasPerSm = 3;  // one-warp CTAs per SM, at most; fewer when their rings do not fit
 constexpr int kMaxPieceBytes = 24 * 1024;
 
 template <int MAXB>
@@ -146,12 +146,6 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
   ring.drain();
 }
 
-inline int64_t ctas_per_sm(size_t ring_smem) {
-  // 227 KB of shared memory per SM; allow for static shared memory and the 1 KB per-CTA reserve
-  const int64_t fit = (int64_t)(227 * 1024) / (int64_t)(ring_smem + 14 * 1024);
-  return fit < 1 ? 1 : (fit > kMaxCtasPerSm ? kMaxCtasPerSm : fit);
-}
-
 }  // namespace
 }  // namespace cpkv
 
@@ -189,8 +183,6 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
   if (pieces > INT32_MAX || dense_cap_pages > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
   const int64_t units = dense_cap_pages * pieces;
   const size_t smem = (size_t)kStages * piece_bytes;
-  const int64_t cap = (int64_t)device_sm_count() * ctas_per_sm(smem);
-  const int grid = (int)(units < cap ? units : cap);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
 #define CPKV_FILL_FUSED(prm)                                                                        \
@@ -206,27 +198,18 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
   prm.ps = page_size; prm.B = B; prm.pieces = (int32_t)pieces; prm.piece_bytes = (int32_t)piece_bytes; \
   for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
 
-  static int configured[256][2] = {{0}};
-  int dev = 0;
-  cudaGetDevice(&dev);
   if (B <= 64) {
-    if (dev >= 0 && dev < 256 && !configured[dev][0]) {
-      if (cudaFuncSetAttribute(compose_fused_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kStages * kMaxPieceBytes) != cudaSuccess)
-        return CPKV_ERR_CUDA;
-      configured[dev][0] = 1;
-    }
+    const void *kernel = reinterpret_cast<const void *>(compose_fused_kernel<64>);
+    if (ensure_dynamic_smem(kernel, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
+    const int grid = persistent_grid(kernel, 32, smem, kMaxCtasPerSm, units);
     FusedParams<64> prm;
     CPKV_FILL_FUSED(prm)
     compose_fused_kernel<64><<<grid, 32, smem, s>>>(prm);
     return launch_status();
   }
-  if (dev >= 0 && dev < 256 && !configured[dev][1]) {
-    if (cudaFuncSetAttribute(compose_fused_kernel<CPKV_MAX_BATCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStages * kMaxPieceBytes) != cudaSuccess)
-      return CPKV_ERR_CUDA;
-    configured[dev][1] = 1;
-  }
+  const void *kernel = reinterpret_cast<const void *>(compose_fused_kernel<CPKV_MAX_BATCH>);
+  if (ensure_dynamic_smem(kernel, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
+  const int grid = persistent_grid(kernel, 32, smem, kMaxCtasPerSm, units);
   FusedParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_FUSED(prm)
 #undef CPKV_FILL_FUSED

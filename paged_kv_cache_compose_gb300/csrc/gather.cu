@@ -19,8 +19,6 @@
 // wait is bounded (see bulk_ring.cuh).
 #include <stdint.h>
 
-#include <mutex>
-
 #include "bulk_ring.cuh"
 
 namespace cpkv {
@@ -114,37 +112,6 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
   ring.drain();
 }
 
-// Resident CTAs per SM for `ring_smem` bytes of dynamic shared memory (the
-// occupancy calculator, cached per device and size), at most `cap`.
-inline int64_t ctas_per_sm(size_t ring_smem, int cap) {
-  struct Entry {
-    int dev;
-    size_t smem;
-    int ctas;
-  };
-  static Entry cache[16];
-  static int n_cached = 0;
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return 1;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  int ctas = 0;
-  for (int i = 0; i < n_cached; ++i)
-    if (cache[i].dev == dev && cache[i].smem == ring_smem) ctas = cache[i].ctas;
-  if (ctas == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, gather_pages_kernel, 32, ring_smem) != cudaSuccess ||
-        ctas < 1) {
-      (void)cudaGetLastError();
-      ctas = 1;
-    }
-    if (n_cached < 16) cache[n_cached++] = Entry{dev, ring_smem, ctas};
-  }
-  return ctas > cap ? cap : ctas;
-}
-
 }  // namespace
 }  // namespace cpkv
 
@@ -188,18 +155,10 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
   prm.piece_bytes = (int32_t)piece_bytes;
 
   const size_t smem = (size_t)kStages * piece_bytes;
-  static int configured[256] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 256 && !configured[dev]) {
-    if (cudaFuncSetAttribute(gather_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStages * kMaxPieceBytes) != cudaSuccess)
-      return CPKV_ERR_CUDA;
-    configured[dev] = 1;
-  }
-  const int64_t cap =
-      (int64_t)device_sm_count() * ctas_per_sm(smem, pieces > 1 ? kMaxCtasPerSmPieces : kMaxCtasPerSmOnePiece);
-  const int grid = (int)(prm.units < cap ? prm.units : cap);
+  const void *kernel = reinterpret_cast<const void *>(gather_pages_kernel);
+  if (ensure_dynamic_smem(kernel, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
+  const int grid =
+      persistent_grid(kernel, 32, smem, pieces > 1 ? kMaxCtasPerSmPieces : kMaxCtasPerSmOnePiece, prm.units);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   gather_pages_kernel<<<grid, 32, smem, s>>>(prm);
   return launch_status();

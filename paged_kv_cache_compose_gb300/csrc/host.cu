@@ -2,20 +2,87 @@
 // counts, ragged-plan sizing, error strings, device queries.  No GPU work.
 #include <stdint.h>
 
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 
 namespace cpkv {
+namespace {
+
+std::mutex g_query_mu;  // guards the device-query caches below
+
+struct KernelQuery {
+  int dev;
+  const void *kernel;
+  size_t smem;
+  int threads;
+  int value;
+};
+std::vector<KernelQuery> g_smem_limits;  // value: the limit set
+std::vector<KernelQuery> g_resident;     // value: resident CTAs per SM
+int g_sm_count[256] = {0};
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return dev;
+}
+
+}  // namespace
 
 int device_sm_count() {
-  static int cache[256] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 148;
-  if (cache[dev] == 0) {
+  const int dev = current_device();
+  if (dev < 0 || dev >= 256) return 1;
+  std::lock_guard<std::mutex> lock(g_query_mu);
+  if (g_sm_count[dev] == 0) {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev] = n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      return 1;
+    }
+    g_sm_count[dev] = n;
   }
-  return cache[dev];
+  return g_sm_count[dev];
+}
+
+int ensure_dynamic_smem(const void *kernel, int bytes) {
+  const int dev = current_device();
+  if (dev < 0) return CPKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_query_mu);
+  for (const KernelQuery &q : g_smem_limits)
+    if (q.dev == dev && q.kernel == kernel && q.value >= bytes) return CPKV_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CPKV_ERR_CUDA;
+  }
+  g_smem_limits.push_back(KernelQuery{dev, kernel, 0, 0, bytes});
+  return CPKV_OK;
+}
+
+int persistent_grid(const void *kernel, int threads, size_t smem, int cap_per_sm, int64_t units) {
+  const int sms = device_sm_count();
+  const int dev = current_device();
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_query_mu);
+    for (const KernelQuery &q : g_resident)
+      if (q.dev == dev && q.kernel == kernel && q.smem == smem && q.threads == threads) per_sm = q.value;
+    if (per_sm == 0) {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
+          per_sm < 1) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+      }
+      g_resident.push_back(KernelQuery{dev, kernel, smem, threads, per_sm});
+    }
+  }
+  if (per_sm > cap_per_sm) per_sm = cap_per_sm;
+  const int64_t grid = (int64_t)sms * per_sm;
+  return (int)(units < grid ? (units > 0 ? units : 1) : grid);
 }
 
 }  // namespace cpkv
