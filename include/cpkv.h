@@ -236,6 +236,12 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
 #define CPKV_GATHER_STAGING 2  /* owner in [cp, 2cp): a current page from a staging      */
 #define CPKV_GATHER_ZERO 4     /* owner -1 (and any invalid descriptor): a zero page      */
 #define CPKV_GATHER_ALL 7
+/* Flag for cpkv_compose_gather_kinds: the staging pages this call reads are
+ * consumed.  After a staging piece has been loaded, its L2 lines are dropped
+ * without being written back to DRAM, so the staging bytes are undefined
+ * after the call (the dense buffer is unaffected).  For stagings that are
+ * refilled before they are read again, as in the per-layer loop. */
+#define CPKV_GATHER_CONSUME_STAGING 8
 
 /*
  * cpkv_compose_gather_kinds — the gather restricted to some slot kinds;
@@ -246,8 +252,9 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
  * stream (kinds = CPKV_GATHER_POOL | CPKV_GATHER_ZERO); consuming the layer
  * is then the fill followed by the current pages only
  * (kinds = CPKV_GATHER_STAGING).  The two calls together write exactly what
- * one cpkv_compose_gather writes.  kinds outside [0, CPKV_GATHER_ALL] returns
- * CPKV_ERR_ARG; other arguments as cpkv_compose_gather.
+ * one cpkv_compose_gather writes.  kinds may also carry
+ * CPKV_GATHER_CONSUME_STAGING; any other value returns CPKV_ERR_ARG.  Other
+ * arguments as cpkv_compose_gather.
  */
 int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
                               const void *const *h_src_table, const int64_t *h_src_cap_pages,

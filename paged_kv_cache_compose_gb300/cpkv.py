@@ -38,6 +38,7 @@ GATHER_POOL = 1
 GATHER_STAGING = 2
 GATHER_ZERO = 4
 GATHER_ALL = 7
+GATHER_CONSUME_STAGING = 8  # flag: staging bytes are undefined after the gather (L2 lines dropped)
 
 MAX_CP = 64
 MAX_BATCH = 1024

@@ -77,14 +77,18 @@ __device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, i
   return x;
 }
 
+// kConsume: the staging pages are consumed; once a staging piece has been
+// loaded its L2 lines are dropped without write-back.
+template <bool kConsume>
 __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant__ GatherParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ uint8_t *ring_dst[kStages];
   __shared__ uint32_t ring_bytes[kStages];
   __shared__ int ring_live[kStages];
-  BulkRing<kStages, kLoadsInFlight> ring;
-  ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
+  __shared__ const uint8_t *ring_src[kStages];
+  BulkRing<kStages, kLoadsInFlight, kConsume> ring;
+  ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes, false, ring_src);
   // The CTA's units are u = blockIdx.x + i * gridDim.x.  Their descriptors
   // are loaded 32 at a time (one per lane) and handed out with shuffles, so
   // no copy waits on a descriptor load of its own.
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
       const Unit x = resolve_unit(p, u, o, sr, lane == 0, &skip);
       if (skip) continue;
       if (x.src == nullptr) warp_zero(x.dst, x.bytes);
-      else ring.push(x.src, x.dst, x.bytes);
+      else ring.push(x.src, x.dst, x.bytes, kConsume && o >= p.n_pool);
     }
   }
   ring.drain();
@@ -120,7 +124,9 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
                                          const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
                                          int kinds, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
   using namespace cpkv;
-  if (kinds < 0 || kinds > CPKV_GATHER_ALL) return CPKV_ERR_ARG;
+  if (kinds < 0 || kinds > (CPKV_GATHER_ALL | CPKV_GATHER_CONSUME_STAGING)) return CPKV_ERR_ARG;
+  const bool consume = (kinds & CPKV_GATHER_CONSUME_STAGING) != 0;
+  kinds &= CPKV_GATHER_ALL;
   if (page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
   if (row_bytes <= 0 || ((int64_t)page_size * row_bytes) % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
   if (h_src_table == nullptr || h_src_cap_pages == nullptr || d_status == nullptr) return CPKV_ERR_ARG;
@@ -155,12 +161,14 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
   prm.piece_bytes = (int32_t)piece_bytes;
 
   const size_t smem = (size_t)kStages * piece_bytes;
-  const void *kernel = reinterpret_cast<const void *>(gather_pages_kernel);
+  const void *kernel = consume ? reinterpret_cast<const void *>(gather_pages_kernel<true>)
+                               : reinterpret_cast<const void *>(gather_pages_kernel<false>);
   if (ensure_dynamic_smem(kernel, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
   const int grid =
       persistent_grid(kernel, 32, smem, pieces > 1 ? kMaxCtasPerSmPieces : kMaxCtasPerSmOnePiece, prm.units);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  gather_pages_kernel<<<grid, 32, smem, s>>>(prm);
+  if (consume) gather_pages_kernel<true><<<grid, 32, smem, s>>>(prm);
+  else gather_pages_kernel<false><<<grid, 32, smem, s>>>(prm);
   return launch_status();
 }
 

@@ -83,8 +83,14 @@ class ComposeLayers:
                                       d_token_writer_row=p["token_writer_row"], d_writer=p.d_writer,
                                       num_cur_pages=p.C, d_status=p.d_status, stream=stream)
 
-    def gather(self, pools, dense, stream=None):
-        """``pools``: the cp owner slabs [slab_pages, ps, R] of this layer."""
+    def gather(self, pools, dense, stream=None, consume_staging=False):
+        """``pools``: the cp owner slabs [slab_pages, ps, R] of this layer.
+        ``consume_staging``: the stagings are refilled before their next read,
+        so their L2 lines are dropped after the gather reads them (their bytes
+        are undefined afterwards)."""
+        if consume_staging:
+            self.gather_kinds(pools, dense, cpkv.GATHER_ALL | cpkv.GATHER_CONSUME_STAGING, stream)
+            return
         p = self.plan
         table = list(pools) + list(self.staging)
         caps = [t.shape[0] for t in pools] + [p.staging_cap_pages] * p.cp_size

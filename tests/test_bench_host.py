@@ -62,3 +62,8 @@ def test_layer_bytes_planar_unstaged_planes():
     lb = bench.layer_bytes([3], [4], 3, 36, 3, planes=(16, 4, 16))
     # T=4, pad=2; plane offsets 0, 48, 60: planes 2 (width 4) and 3 (offset 60) unstaged
     assert lb["layer"] == lb["total"] - 2 * 36 - 4 * (4 + 16)
+
+
+def test_pool_pages_only_for_shared_pool_workloads():
+    with pytest.raises(ValueError):
+        bench.ComposeWorkload("traced_78", device="cpu", pool_pages=4096)

@@ -510,5 +510,30 @@ def test_gather_kinds_rejects_bad_mask():
     batch = wl.tiny_batch()
     plan, _ = _plan_pair(batch)
     layers = ComposeLayers(plan, batch.row_bytes)
-    with pytest.raises(cpkv.CpkvError):
-        layers.gather_kinds([torch.from_numpy(s).cuda() for s in wl.host_pool(batch)], layers.dense[0], 8)
+    for bad in (-1, 16, 31):
+        with pytest.raises(cpkv.CpkvError):
+            layers.gather_kinds([torch.from_numpy(s).cuda() for s in wl.host_pool(batch)], layers.dense[0], bad)
+
+
+# ---------------------------------------------------------------------------
+# gather that consumes the stagings: same dense buffer (staging bytes undefined)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_gather_consuming_staging_matches_oracle(batch):
+    plan, _ = _plan_pair(batch, dense_extra=2)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs = wl.host_pool(batch)
+    rows = wl.host_current_rows(batch)
+    d_slabs = [torch.from_numpy(s).cuda() for s in slabs]
+    d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+    dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
+                       device="cuda")
+    for _ in range(2):  # the second layer refills the consumed stagings
+        layers.fill(d_rows)
+        layers.gather(d_slabs, dense, consume_staging=True)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense.cpu().numpy(), want)

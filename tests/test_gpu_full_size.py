@@ -82,9 +82,12 @@ def _check_plan(work):
                                             ("traced_78", "fused"), ("fp8_nsa", "fused"),
                                             ("traced_78", "prefetch"), ("index_k", "staging"),
                                             ("traced_78", "layer"), ("fp8_nsa", "layer"), ("index_k", "layer"),
-                                            ("index_k", "fused")])
+                                            ("index_k", "fused"), ("traced_78", "staging-consume"),
+                                            ("fp8_nsa", "staging-consume")])
 def test_benchmark_workload_matches_oracle(config, variant):
-    work = bench.ComposeWorkload(config, variant=variant)
+    consume = variant.endswith("-consume")  # plain variants keep their stagings, which are checked
+    variant = variant.removesuffix("-consume")
+    work = bench.ComposeWorkload(config, variant=variant, consume_staging=consume)
     try:
         for d in work.layers.dense:
             d.fill_(0xCD)
@@ -97,7 +100,7 @@ def test_benchmark_workload_matches_oracle(config, variant):
         _check_plan(work)
         _check_layer(work, work.num_layers - 2)
         g = _check_layer(work, work.num_layers - 1)
-        if variant in ("staging", "prefetch", "layer") and g is not None:
+        if variant in ("staging", "prefetch", "layer") and g is not None and not consume:
             _check_staging(work, g)
     finally:
         del work
