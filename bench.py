@@ -241,8 +241,8 @@ class ComposeWorkload:
         # them): by default for row-major pages, where it measured faster
         # (traced -6%, fp8 -1%); the planar index-key pages measured 1.5% slower
         if consume_staging is None:
-            consume_staging = variant == "staging" and not b.planes
-        self.consume_staging = bool(consume_staging) and variant == "staging"
+            consume_staging = variant in ("staging", "layer") and not b.planes
+        self.consume_staging = bool(consume_staging) and variant in ("staging", "layer")
         if variant == "staging":
             self.launches_per_step = 3 + 2 * self.num_layers  # plan (2) + ragged (1) + (fill + gather) per layer
             self.layer_bytes = self.bytes["total"]
@@ -317,7 +317,8 @@ class ComposeWorkload:
             return
         if self.variant == "layer":
             self.layers.compose_one_launch(self.pools_of(layer), self.rows[layer], dense, stream,
-                                           plane_bytes=list(self.batch.planes) if self.batch.planes else None)
+                                           plane_bytes=list(self.batch.planes) if self.batch.planes else None,
+                                           consume_staging=self.consume_staging)
             return
         if kind in ("all", "fill"):
             if self.batch.planes:
@@ -604,7 +605,7 @@ def main(argv=None):
         torch.cuda.synchronize()
         kern[kind] = k0.elapsed_time(k1) / (reps * work.num_layers)
     kernel_timing = "alone: a CUDA graph of the step's launches of that kernel only, replayed"
-    if work.consume_staging:
+    if work.consume_staging and work.variant == "staging":
         kernel_timing += (" (the gather consumes the stagings, so when replayed alone it reads them from DRAM: "
                           "all its algorithmic bytes cross DRAM; inside the step they are read from L2)")
     kgbs = {k: work.kernels[k] / (kern[k] / 1e3) / 1e9 for k in kern}

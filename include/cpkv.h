@@ -281,6 +281,10 @@ int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
  *                    i = src - 1 holds n_i rows that are consecutive in its
  *                    writer's buffer from token_writer_row of its first token)
  *   d_dense          device [dense_cap_pages * ps][R], 16-byte aligned
+ *   consume_staging  non-zero: the stagings are consumed, as with
+ *                    CPKV_GATHER_CONSUME_STAGING (each staged piece's L2
+ *                    lines are dropped once it has been read back; the
+ *                    staging bytes are undefined after the call)
  * A descriptor outside the table or its capacity raises DESC_OOB, current
  * rows outside the writer's buffer raise ROW_OOB; either dense page is
  * zero-filled and its staging slot is not written.  Errors: ARG for bad
@@ -291,7 +295,7 @@ int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row_bytes, con
                        const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
                        const void *const *h_src_table, const int64_t *h_src_cap_pages, const int32_t *d_owner,
                        const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
-                       void *d_dense, int32_t *d_status, cpkv_stream_t stream);
+                       void *d_dense, int consume_staging, int32_t *d_status, cpkv_stream_t stream);
 
 /*
  * cpkv_compose_layer_planes — cpkv_compose_layer for planar pages (the
@@ -313,7 +317,7 @@ int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int n_planes, c
                               const int64_t *h_cur_rows_cap, const void *const *h_src_table,
                               const int64_t *h_src_cap_pages, const int32_t *d_owner, const int32_t *d_src,
                               const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
-                              int32_t *d_status, cpkv_stream_t stream);
+                              int consume_staging, int32_t *d_status, cpkv_stream_t stream);
 
 /*
  * cpkv_compose_fused — per layer: the single-GPU compose in one pass, without

@@ -76,8 +76,9 @@ def _declare(lib):
     lib.cpkv_compose_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_fill_current_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
     lib.cpkv_compose_gather_kinds.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _I, _P, _P, _P]
-    lib.cpkv_compose_layer.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
-    lib.cpkv_compose_layer_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_compose_layer.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P, _P]
+    lib.cpkv_compose_layer_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P,
+                                              _P]
     lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_compose_fused_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
@@ -253,8 +254,9 @@ def cpkv_compose_gather_kinds(src_table: Sequence, src_cap_pages, d_owner, d_src
 
 def cpkv_compose_layer(cur_lens, cur_rows: Sequence, src_table: Sequence, src_cap_pages, d_owner, d_src,
                        d_token_writer_row, d_dense, *, page_size, cp_size, row_bytes, dense_cap_pages, d_status,
-                       cur_rows_cap=None, stream=None):
-    """Fill + slot-dense gather of one layer in a single launch."""
+                       cur_rows_cap=None, consume_staging=False, stream=None):
+    """Fill + slot-dense gather of one layer in a single launch (``consume_staging``:
+    the staging bytes are undefined afterwards)."""
     cl = _host_i32(cur_lens)
     if cur_rows_cap is None:
         cur_rows_cap = [t.numel() // row_bytes for t in cur_rows]
@@ -262,14 +264,14 @@ def cpkv_compose_layer(cur_lens, cur_rows: Sequence, src_table: Sequence, src_ca
     rarr, tarr = _ptr_array(cur_rows), _ptr_array(src_table)
     rc = load().cpkv_compose_layer(len(cl), page_size, cp_size, row_bytes, _hp(cl), ctypes.cast(rarr, _P), _hp(rcaps),
                                    ctypes.cast(tarr, _P), _hp(tcaps), _dp(d_owner), _dp(d_src),
-                                   _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense), _dp(d_status),
-                                   _stream(stream))
+                                   _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense), int(bool(consume_staging)),
+                                   _dp(d_status), _stream(stream))
     _check("cpkv_compose_layer", rc)
 
 
 def cpkv_compose_layer_planes(cur_lens, cur_planes: Sequence, src_table: Sequence, src_cap_pages, d_owner, d_src,
                               d_token_writer_row, d_dense, *, page_size, cp_size, plane_bytes, dense_cap_pages,
-                              d_status, cur_rows_cap=None, stream=None):
+                              d_status, cur_rows_cap=None, consume_staging=False, stream=None):
     """Fill + gather of one layer of planar pages in a single launch
     (``cur_planes[p][w]``: writer w's rows of plane p)."""
     cl, pb = _host_i32(cur_lens), _host_i32(plane_bytes)
@@ -282,7 +284,7 @@ def cpkv_compose_layer_planes(cur_lens, cur_planes: Sequence, src_table: Sequenc
     rc = load().cpkv_compose_layer_planes(len(cl), page_size, cp_size, n_planes, _hp(pb), _hp(cl),
                                           ctypes.cast(flat, _P), _hp(rcaps), ctypes.cast(tarr, _P), _hp(tcaps),
                                           _dp(d_owner), _dp(d_src), _dp(d_token_writer_row), dense_cap_pages,
-                                          _dp(d_dense), _dp(d_status), _stream(stream))
+                                          _dp(d_dense), int(bool(consume_staging)), _dp(d_status), _stream(stream))
     _check("cpkv_compose_layer_planes", rc)
 
 

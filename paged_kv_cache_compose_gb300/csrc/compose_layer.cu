@@ -168,8 +168,16 @@ __device__ __forceinline__ int32_t current_rows(const Params &p, const int32_t *
 // The bulk ring with a per-piece choice of L2 policy for the store, and a
 // queue of staging read-backs.  Every consume() commits exactly one bulk
 // group, so the store of the copy with ring index q is group q, and group q
-// has completed once wait_group(head - q - 1) returns.
-struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
+// has completed once wait_group(head - q - 1) returns.  kConsume: a
+// read-back's staging lines are dropped from L2 once it has landed.
+template <bool kConsume>
+struct LayerRing : BulkRing<kStages, kLoadsInFlight, kConsume> {
+  using Base = BulkRing<kStages, kLoadsInFlight, kConsume>;
+  using Base::consume;
+  using Base::head;
+  using Base::push;
+  using Base::store_policy;
+  using Base::tail;
   uint32_t keep_mask;  // bit s: the piece in stage s is stored with keep_policy (warp-uniform)
   uint64_t keep_policy, stream_policy;
   Readback *rq;        // kReadbackQueue entries (shared; lane 0 writes, the warp reads)
@@ -179,11 +187,11 @@ struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
     store_policy = ((keep_mask >> (int)(head % kStages)) & 1u) ? keep_policy : stream_policy;
     consume();
   }
-  CPKV_DEV void push_with(const void *src, void *dst, uint32_t bytes, bool keep_in_l2) {
+  CPKV_DEV void push_with(const void *src, void *dst, uint32_t bytes, bool keep_in_l2, bool discard_src = false) {
     if (tail - head == kLoadsInFlight) consume_one();  // push() then finds a free load slot
     const uint32_t bit = 1u << (int)(tail % kStages);
     keep_mask = keep_in_l2 ? (keep_mask | bit) : (keep_mask & ~bit);
-    push(src, dst, bytes);
+    push(src, dst, bytes, discard_src);
   }
   // Issue the oldest read-back once its staging store has completed.
   CPKV_DEV void readback_front() {
@@ -192,7 +200,7 @@ struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
     if ((threadIdx.x & 31) == 0) bulk_wait_complete_dyn(head - r.q - 1);
     __syncwarp();
     ++rq_head;
-    push_with(r.src, r.dst, r.bytes, false);
+    push_with(r.src, r.dst, r.bytes, false, kConsume);
   }
   // Issue the read-backs whose stores are kReadbackLag groups old (all of
   // them when `all`).
@@ -224,7 +232,9 @@ struct LayerRing : BulkRing<kStages, kLoadsInFlight> {
 // PLANAR false: one plane, staged with bulk copies (the row layout).
 // STAGED false: the single-GPU compose without stagings (owner cp + w names
 // writer w's current page src - 1, read straight from its rows).
-template <int MAXB, bool PLANAR, bool STAGED>
+// CONSUME (with STAGED): the stagings are consumed (their read-back lines are
+// dropped from L2).
+template <int MAXB, bool PLANAR, bool STAGED, bool CONSUME>
 __global__ void __launch_bounds__(64, 1)
     compose_layer_kernel(const __grid_constant__ LayerParams<MAXB, PLANAR ? kMaxPlanes : 1> p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -235,6 +245,7 @@ __global__ void __launch_bounds__(64, 1)
   __shared__ int32_t cur_page_start[MAXB + 1];
   __shared__ int64_t token_start[MAXB + 1];
   __shared__ Readback readbacks[kReadbackQueue];
+  __shared__ const uint8_t *ring_src[kStages];
   const int lane = threadIdx.x & 31;
   const bool copy_warp = threadIdx.x < 32;
   // Planar pages: warp 0 issues every bulk copy, warp 1 does every plain
@@ -267,9 +278,9 @@ __global__ void __launch_bounds__(64, 1)
   }
   __syncthreads();
 
-  LayerRing ring;
+  LayerRing<CONSUME> ring;
   if (copy_warp) {
-    ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes);
+    ring.init(smem, full, ring_dst, ring_bytes, ring_live, p.status, p.piece_bytes, false, ring_src);
     ring.keep_mask = 0;
     ring.keep_policy = keep;
     ring.stream_policy = ring.load_policy;
@@ -365,11 +376,11 @@ int launch_layer(void (*kernel)(Params), int threads, int64_t units, size_t smem
 
 // staged: h_src_table / h_src_cap_pages hold 2*cp entries (pools, then
 // stagings); else cp entries (pools only) and no staging is written.
-int compose_layer_impl(bool staged, int B, int page_size, int cp_size, int n_planes, const int32_t *h_plane_bytes,
-                       const int32_t *h_cur_lens, const void *const *h_cur_planes, const int64_t *h_cur_rows_cap,
-                       const void *const *h_src_table, const int64_t *h_src_cap_pages, const int32_t *d_owner,
-                       const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
-                       void *d_dense, int32_t *d_status, cudaStream_t s) {
+int compose_layer_impl(bool staged, bool consume_staging, int B, int page_size, int cp_size, int n_planes,
+                       const int32_t *h_plane_bytes, const int32_t *h_cur_lens, const void *const *h_cur_planes,
+                       const int64_t *h_cur_rows_cap, const void *const *h_src_table, const int64_t *h_src_cap_pages,
+                       const int32_t *d_owner, const int32_t *d_src, const int32_t *d_token_writer_row,
+                       int64_t dense_cap_pages, void *d_dense, int32_t *d_status, cudaStream_t s) {
   using namespace cpkv;
   if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
   if (n_planes < 1 || n_planes > kMaxPlanes || h_plane_bytes == nullptr || dense_cap_pages < 0) return CPKV_ERR_ARG;
@@ -444,27 +455,27 @@ int compose_layer_impl(bool staged, int B, int page_size, int cp_size, int n_pla
   // callers route it there.
   const bool planar = !(n_planes == 1 && h_plane_bytes[0] % 16 == 0);
   if (!planar && !staged) return CPKV_ERR_ARG;
+  // one instantiation per (batch template, planar, staged, consumed)
+#define CPKV_LAUNCH_LAYER(MAXB, NP, PL, ST, CO, THREADS)                                   \
+  {                                                                                        \
+    LayerParams<MAXB, NP> prm;                                                             \
+    CPKV_FILL_LAYER(prm)                                                                   \
+    return launch_layer(compose_layer_kernel<MAXB, PL, ST, CO>, THREADS, units, smem, s, prm); \
+  }
   if (B <= 64) {
-    if (planar) {
-      LayerParams<64, kMaxPlanes> prm;
-      CPKV_FILL_LAYER(prm)
-      if (staged) return launch_layer(compose_layer_kernel<64, true, true>, 64, units, smem, s, prm);
-      return launch_layer(compose_layer_kernel<64, true, false>, 64, units, smem, s, prm);
-    }
-    LayerParams<64, 1> prm;
-    CPKV_FILL_LAYER(prm)
-    return launch_layer(compose_layer_kernel<64, false, true>, 32, units, smem, s, prm);
+    if (planar && !staged) CPKV_LAUNCH_LAYER(64, kMaxPlanes, true, false, false, 64)
+    if (planar && consume_staging) CPKV_LAUNCH_LAYER(64, kMaxPlanes, true, true, true, 64)
+    if (planar) CPKV_LAUNCH_LAYER(64, kMaxPlanes, true, true, false, 64)
+    if (consume_staging) CPKV_LAUNCH_LAYER(64, 1, false, true, true, 32)
+    CPKV_LAUNCH_LAYER(64, 1, false, true, false, 32)
   }
-  if (planar) {
-    LayerParams<CPKV_MAX_BATCH, kMaxPlanes> prm;
-    CPKV_FILL_LAYER(prm)
-    if (staged) return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true, true>, 64, units, smem, s, prm);
-    return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, true, false>, 64, units, smem, s, prm);
-  }
-  LayerParams<CPKV_MAX_BATCH, 1> prm;
-  CPKV_FILL_LAYER(prm)
+  if (planar && !staged) CPKV_LAUNCH_LAYER(CPKV_MAX_BATCH, kMaxPlanes, true, false, false, 64)
+  if (planar && consume_staging) CPKV_LAUNCH_LAYER(CPKV_MAX_BATCH, kMaxPlanes, true, true, true, 64)
+  if (planar) CPKV_LAUNCH_LAYER(CPKV_MAX_BATCH, kMaxPlanes, true, true, false, 64)
+  if (consume_staging) CPKV_LAUNCH_LAYER(CPKV_MAX_BATCH, 1, false, true, true, 32)
+  CPKV_LAUNCH_LAYER(CPKV_MAX_BATCH, 1, false, true, false, 32)
+#undef CPKV_LAUNCH_LAYER
 #undef CPKV_FILL_LAYER
-  return launch_layer(compose_layer_kernel<CPKV_MAX_BATCH, false, true>, 32, units, smem, s, prm);
 }
 
 }  // namespace
@@ -473,12 +484,13 @@ extern "C" int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row
                                   const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
                                   const void *const *h_src_table, const int64_t *h_src_cap_pages,
                                   const int32_t *d_owner, const int32_t *d_src, const int32_t *d_token_writer_row,
-                                  int64_t dense_cap_pages, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
+                                  int64_t dense_cap_pages, void *d_dense, int consume_staging, int32_t *d_status,
+                                  cpkv_stream_t stream) {
   if (row_bytes <= 0 || row_bytes % 16 != 0 || row_bytes > INT32_MAX) return CPKV_ERR_ARG;
   const int32_t plane = (int32_t)row_bytes;
-  return compose_layer_impl(true, B, page_size, cp_size, 1, &plane, h_cur_lens, h_cur_rows, h_cur_rows_cap, h_src_table,
-                            h_src_cap_pages, d_owner, d_src, d_token_writer_row, dense_cap_pages, d_dense, d_status,
-                            reinterpret_cast<cudaStream_t>(stream));
+  return compose_layer_impl(true, consume_staging != 0, B, page_size, cp_size, 1, &plane, h_cur_lens, h_cur_rows,
+                            h_cur_rows_cap, h_src_table, h_src_cap_pages, d_owner, d_src, d_token_writer_row,
+                            dense_cap_pages, d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int n_planes,
@@ -487,9 +499,10 @@ extern "C" int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int 
                                          const void *const *h_src_table, const int64_t *h_src_cap_pages,
                                          const int32_t *d_owner, const int32_t *d_src,
                                          const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
-                                         int32_t *d_status, cpkv_stream_t stream) {
-  return compose_layer_impl(true, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens, h_cur_planes,
-                            h_cur_rows_cap, h_src_table, h_src_cap_pages, d_owner, d_src, d_token_writer_row,
+                                         int consume_staging, int32_t *d_status, cpkv_stream_t stream) {
+  return compose_layer_impl(true, consume_staging != 0, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens,
+                            h_cur_planes, h_cur_rows_cap, h_src_table, h_src_cap_pages, d_owner, d_src,
+                            d_token_writer_row,
                             dense_cap_pages, d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -504,7 +517,8 @@ extern "C" int cpkv_compose_fused_planes(int B, int page_size, int cp_size, int 
     return cpkv_compose_fused(B, page_size, cp_size, h_plane_bytes[0], h_cur_lens, h_pools, h_pool_cap_pages,
                               h_cur_planes, h_cur_rows_cap, d_owner, d_src, d_token_writer_row, dense_cap_pages,
                               d_dense, d_status, stream);
-  return compose_layer_impl(false, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens, h_cur_planes,
-                            h_cur_rows_cap, h_pools, h_pool_cap_pages, d_owner, d_src, d_token_writer_row,
+  return compose_layer_impl(false, false, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens,
+                            h_cur_planes, h_cur_rows_cap, h_pools, h_pool_cap_pages, d_owner, d_src,
+                            d_token_writer_row,
                             dense_cap_pages, d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -132,7 +132,8 @@ class ComposeLayers:
                                 dense, page_size=p.page_size, cp_size=p.cp_size, row_bytes=self.row_bytes,
                                 dense_cap_pages=p.dense_cap_pages, d_status=p.d_status, stream=stream)
 
-    def compose_one_launch(self, pools, cur_rows_per_writer, dense, stream=None, plane_bytes=None):
+    def compose_one_launch(self, pools, cur_rows_per_writer, dense, stream=None, plane_bytes=None,
+                           consume_staging=False):
         """Fill + gather of a layer in a single launch (cpkv_compose_layer; for
         planar pages, ``plane_bytes`` and ``cur_rows_per_writer[p][w]``,
         cpkv_compose_layer_planes)."""
@@ -143,12 +144,12 @@ class ComposeLayers:
             cpkv.cpkv_compose_layer_planes(p.cur_lens, cur_rows_per_writer, table, caps, p["owner"], p["src"],
                                            p["token_writer_row"], dense, page_size=p.page_size, cp_size=p.cp_size,
                                            plane_bytes=plane_bytes, dense_cap_pages=p.dense_cap_pages,
-                                           d_status=p.d_status, stream=stream)
+                                           d_status=p.d_status, consume_staging=consume_staging, stream=stream)
             return
         cpkv.cpkv_compose_layer(p.cur_lens, cur_rows_per_writer, table, caps, p["owner"], p["src"],
                                 p["token_writer_row"], dense, page_size=p.page_size, cp_size=p.cp_size,
                                 row_bytes=self.row_bytes, dense_cap_pages=p.dense_cap_pages, d_status=p.d_status,
-                                stream=stream)
+                                consume_staging=consume_staging, stream=stream)
 
     def compose_layer(self, layer: int, pools, cur_rows_per_writer, stream=None):
         """Fill + gather of one layer into the dense buffer of its parity."""

@@ -98,19 +98,19 @@ def test_host_errors_before_any_launch(lib):
     rcap = np.array([4], np.int64)
     tcaps = np.array([8, 1], np.int64)
     rc = lib.cpkv_compose_layer(1, 2, 1, 64, cl.ctypes.data, ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data,
-                                ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 64, null)
+                                ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 0, 64, null)
     assert rc == cpkv.CPKV_ERR_CAPACITY
     tcaps = np.array([8, 3], np.int64)
     rc = lib.cpkv_compose_layer(1, 2, 1, 40, cl.ctypes.data, ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data,
-                                ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 64, null)
+                                ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 0, 64, null)
     assert rc == cpkv.CPKV_ERR_ARG
     # planar layer compose: plane counts, widths and page sizes outside the contract
     for n_planes, pb, ps in ((0, [16], 2), (5, [16] * 5, 2), (2, [128, 2], 2), (2, [128, 4], 3)):
         pba = np.array(pb, np.int32)
         rc = lib.cpkv_compose_layer_planes(1, ps, 1, n_planes, pba.ctypes.data, cl.ctypes.data,
                                            ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data,
-                                           ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 64,
-                                           null)
+                                           ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, 0,
+                                           64, null)
         assert rc == cpkv.CPKV_ERR_ARG, (n_planes, pb, ps)
     # planar fused compose: the same plane checks
     for n_planes, pb, ps in ((0, [16], 2), (5, [16] * 5, 2), (2, [128, 2], 2), (2, [128, 4], 3)):

@@ -537,3 +537,22 @@ def test_gather_consuming_staging_matches_oracle(batch):
     want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
                                 page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
     assert np.array_equal(dense.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_one_launch_consuming_staging_matches_oracle(batch):
+    plan, _ = _plan_pair(batch, dense_extra=1)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    slabs = wl.host_pool(batch)
+    rows = wl.host_current_rows(batch)
+    d_slabs = [torch.from_numpy(s).cuda() for s in slabs]
+    d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+    dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
+                       device="cuda")
+    for _ in range(2):  # the second layer restages what the first consumed
+        layers.compose_one_launch(d_slabs, d_rows, dense, consume_staging=True)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense.cpu().numpy(), want)
