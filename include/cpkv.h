@@ -240,7 +240,10 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
  * consumed.  After a staging piece has been loaded, its L2 lines are dropped
  * without being written back to DRAM, so the staging bytes are undefined
  * after the call (the dense buffer is unaffected).  For stagings that are
- * refilled before they are read again, as in the per-layer loop. */
+ * refilled before they are read again, as in the per-layer loop.  Each
+ * staging page may be named by at most one descriptor of the call (plans of
+ * cpkv_plan_build name each staging slot once); a second read of a consumed
+ * page would see undefined bytes. */
 #define CPKV_GATHER_CONSUME_STAGING 8
 
 /*
