@@ -440,9 +440,29 @@ def compact_pool(batch, slabs):
     return nb, out
 
 
-def oracle_sample(work_or_batch, n_layers: int):
+class HostPages:
+    """One owner's pool slab on the host, generated page by page on demand
+    (seeded by batch, layer and owner): indexing it with page ids yields
+    [len(ids), ps, R] rows, so a compacted sample of a large pool never
+    materialises the pages it does not reference."""
+
+    def __init__(self, batch, layer: int, owner: int):
+        self.batch, self.layer, self.owner = batch, layer, owner
+
+    def __getitem__(self, ids):
+        b = self.batch
+        ids = np.asarray(ids, np.int64)
+        out = np.empty((len(ids), b.page_size, b.row_bytes), np.uint8)
+        for k, i in enumerate(ids.tolist()):
+            rng = np.random.default_rng([b.seed, 7, self.layer, self.owner, i])
+            out[k] = wl.random_rows(rng, b.page_size, b.row_bytes, b.row_kind)
+        return out
+
+
+def oracle_sample(work_or_batch, n_layers: int, shared_pool: bool = False):
     """Host inputs for ``n_layers`` layers of the workload: copied from the
-    device replica when there is one, else generated on the host; pools are
+    device replica when there is one, else generated on the host (only the
+    referenced pages; ``shared_pool``: one pool for all layers); pools are
     compacted to the pages the batch references."""
     b = work_or_batch.batch if hasattr(work_or_batch, "batch") else work_or_batch
     pools, rows = [], []
@@ -453,8 +473,10 @@ def oracle_sample(work_or_batch, n_layers: int):
             nb, slabs = compact_pool(b, w.pools_of(layer))
             rows.append([r.cpu().numpy() for r in w.rows[layer]])
         else:
-            nb, slabs = compact_pool(b, wl.host_pool(b, layer)) if not pools or not b.name.startswith("fp8") \
-                else (nb, pools[0])
+            if pools and shared_pool:
+                slabs = pools[0]
+            else:
+                nb, slabs = compact_pool(b, [HostPages(b, layer, o) for o in range(b.cp_size)])
             rows.append(wl.split_rows_by_writer(b, wl.host_current_rows(b, layer)))
         pools.append(slabs)
     return nb, pools, rows
@@ -487,6 +509,24 @@ def oracle_step(b, pools, rows_per_writer, lib=None):
     return moved
 
 
+def host_cpu() -> dict:
+    """The host the oracle runs on: logical CPUs and the CPU model."""
+    import platform
+
+    model = None
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                fields.setdefault(k.strip(), v.strip())
+        model = fields.get("model name") or (
+            f"implementer {fields['CPU implementer']} part {fields['CPU part']}" if "CPU part" in fields else None)
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "machine": platform.machine(), "model": model}
+
+
 def time_oracle(b, pools, rows, min_seconds=10.0, max_seconds=30.0):
     """Run oracle steps until at least ``min_seconds`` of work; GB/s of the work."""
     import oracle
@@ -512,7 +552,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="traced_78", choices=["traced_78", "fp8_nsa", "index_k", "plans"],
+    ap.add_argument("--config", default="traced_78", choices=["traced_78", "traced", "fp8_nsa", "index_k", "plans"],
                     help="plans: latency of the per-batch plan builders (ragged plan config, all CP ranks and "
                          "splits; compose plan of the traced and fp8 batches)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -576,16 +616,28 @@ def main(argv=None):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # Each step is bracketed by its own events as well (median / min / max).
+    # A one-layer workload re-reads the same pages every step, so L2 is
+    # flushed between its steps by a write larger than L2, outside the
+    # per-step events, and its time is the sum of the steps; the 78-layer
+    # workloads read 27+ GB of distinct inputs per step and run back to back.
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device) if work.num_layers == 1 else None
+    per_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(a.steps):
+    for s0, s1 in per_step:
+        if flush is not None:
+            flush.fill_(1)
+        s0.record()
         work.run()
+        s1.record()
     e1.record()
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms_total = e0.elapsed_time(e1)
+    step_ms = sorted(s0.elapsed_time(s1) for s0, s1 in per_step)
+    ms_total = sum(step_ms) if flush is not None else e0.elapsed_time(e1)
     ms_max, units_all = aggregate(ms_total, work.layer_bytes * work.num_layers * a.steps, ws)
     ms_step = ms_max / a.steps
     value_gbs = units_all / (ms_max / 1e3) / 1e9
@@ -625,7 +677,8 @@ def main(argv=None):
         gbs, secs, steps = time_oracle(b, pools, rows)
         cpu = {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"plan + ragged plan + {len(pools)} of {work.num_layers} layers (staging + gather) of "
-                         f"the same batch and inputs, repeated {steps}x over {secs:.1f}s, single-threaded C"}
+                         f"the same batch and inputs, repeated {steps}x over {secs:.1f}s, single-threaded C",
+               "host": host_cpu()}
 
     b = work.batch
     line = {
@@ -636,6 +689,8 @@ def main(argv=None):
         "steps": a.steps,
         "warmup": a.warmup,
         "ms_per_step": round(ms_step, 4),
+        "ms_per_step_stats": {"median": round(step_ms[len(step_ms) // 2], 4), "min": round(step_ms[0], 4),
+                              "max": round(step_ms[-1], 4), "steps_timed": len(step_ms)},
         "ms_per_78_layer_compose": round(ms_step * 78 / work.num_layers, 4),
         "pct_of_hbm_peak": round(100 * value_gbs / ws / hbm_peak, 2),
         "higher_is_better": True,
@@ -647,6 +702,8 @@ def main(argv=None):
             "workload": ("traced prefill compose, 78 layers: bs=12, 44600 current tokens (lognormal split), prefix "
                          "U[0,16K] page-floored, page_size=64, cp=8 writer regions on one GPU, MLA 576xbf16 rows, "
                          "4096-page pool slab per layer" if a.config == "traced_78" else
+                         "traced prefill compose, 1 layer: the same batch over its 200000-page randomly permuted "
+                         "pool" if a.config == "traced" else
                          "fp8 NSA compose, 78 layers: bs=32, 131072 current tokens, prefix U[0,64K], page_size=64, "
                          "cp=8, 656-byte rows, one 2^20-page pool shared by the layers" if a.config == "fp8_nsa" else
                          "NSA indexer-key compose, 78 layers: the fp8 NSA batch with planar pages of 64 x (128-byte "
@@ -656,8 +713,9 @@ def main(argv=None):
             "variant": work.variant,
             "consume_staging": work.consume_staging,
             "bytes_per_layer": work.layer_bytes, "single_pass_ideal_bytes_per_layer": work.bytes["single_pass_ideal"],
-            "l2": "inputs larger than L2: every layer reads its own pool slab and rows (%.1f GB per step)" % (
-                (sum(s.numel() for p in work.pools for s in p) + work.rows_all.numel()) / 1e9),
+            "l2": ("L2 flushed between steps (a 512 MB write outside the per-step events)" if work.num_layers == 1
+                   else "inputs larger than L2: every layer reads its own pool slab and rows (%.1f GB per step)" % (
+                       (sum(s.numel() for p in work.pools for s in p) + work.rows_all.numel()) / 1e9)),
             "cuda_graph": not a.no_graph,
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
@@ -845,7 +903,7 @@ def run_reference(a, ws, rank):
     oracle.build()
     batch = wl.CONFIGS[a.config]()
     n = min(a.cpu_layers, batch.num_layers)
-    b, pools, rows = oracle_sample(batch, n)
+    b, pools, rows = oracle_sample(batch, n, shared_pool=a.config in ("fp8_nsa", "index_k"))
     lib = oracle.load()
     for _ in range(a.warmup):
         oracle_step(b, pools, rows, lib)
