@@ -77,6 +77,9 @@ __device__ void copy_tile(const PlaneParams<MAXB> &p, int64_t t0) {
   src_w[j] = w;
   __syncthreads();
   const int ntok = (int)min64(kThreads, p.T - t0);
+  // rows are read once (evict_first); the staging is read back by the gather
+  // right after this kernel (evict_last)
+  const uint64_t stream_pol = l2_policy_evict_first(), keep_pol = l2_policy_evict_last();
   for (int pl = 0; pl < p.n_planes; ++pl) {
     const int32_t wp = p.plane_bytes[pl], unit = p.plane_unit[pl], start = p.plane_start[pl];
     const int32_t upt = wp / unit;  // units per token
@@ -95,7 +98,7 @@ __device__ void copy_tile(const PlaneParams<MAXB> &p, int64_t t0) {
           if (dp != nullptr) {
             dst[r] = dp + start + (int64_t)dst_off[k] * wp + (int64_t)u * unit;
             const uint8_t *s = p.planes[pl][src_w[k]] + (int64_t)src_row[k] * wp + (int64_t)u * unit;
-            if (unit == 16) v[r] = ld_stream16(s);
+            if (unit == 16) v[r] = ld_stream16_hint(s, stream_pol);
             else v[r].x = __ldg(reinterpret_cast<const uint32_t *>(s));
           }
         }
@@ -103,7 +106,7 @@ __device__ void copy_tile(const PlaneParams<MAXB> &p, int64_t t0) {
 #pragma unroll
       for (int r = 0; r < kUnroll; ++r) {
         if (dst[r] == nullptr) continue;
-        if (unit == 16) *reinterpret_cast<uint4 *>(dst[r]) = v[r];
+        if (unit == 16) st16_hint(dst[r], v[r], keep_pol);
         else *reinterpret_cast<uint32_t *>(dst[r]) = v[r].x;
       }
     }
