@@ -369,6 +369,17 @@ int cpkv_compose_fused_planes(int B, int page_size, int cp_size, int n_planes, c
                               int32_t *d_status, cpkv_stream_t stream);
 
 /*
+ * cpkv_selftest_ring_timeout — diagnostics: runs the bounded wait of the
+ * kernels' bulk-copy ring on a load that never arrives.  One warp arms a
+ * ring stage for 16 bytes that no copy delivers, then drains the ring; the
+ * wait gives up after the ring's time limit (2 s), the kernel raises
+ * CPKV_STATUS_TIMEOUT in *d_status, writes nothing to d_dst16 (16 bytes,
+ * 16-byte aligned) and returns normally.  No fault, no hang: the failure
+ * path every gather, fused and layer kernel takes on a stalled copy.
+ */
+int cpkv_selftest_ring_timeout(void *d_dst16, int32_t *d_status, cpkv_stream_t stream);
+
+/*
  * cpkv_ragged_plan_sizes — exact segment count S and q-token count Q_r of a
  * rank's ragged plan, from a host copy of its cp_index (host only).
  */

@@ -47,8 +47,8 @@ EXPORTED = (
     "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_fill_current",
     "cpkv_fill_current_planes",
     "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_layer_planes",
-    "cpkv_compose_fused", "cpkv_compose_fused_planes", "cpkv_ragged_plan_sizes", "cpkv_ragged_plan_build", "cpkv_error_string",
-    "cpkv_version",
+    "cpkv_compose_fused", "cpkv_compose_fused_planes", "cpkv_selftest_ring_timeout", "cpkv_ragged_plan_sizes",
+    "cpkv_ragged_plan_build", "cpkv_error_string", "cpkv_version",
 )
 
 
@@ -80,6 +80,7 @@ def _declare(lib):
     lib.cpkv_compose_layer_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P,
                                               _P]
     lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_selftest_ring_timeout.argtypes = [_P, _P, _P]
     lib.cpkv_compose_fused_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
     lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
@@ -325,6 +326,13 @@ def cpkv_compose_fused_planes(cur_lens, pools: Sequence, cur_planes: Sequence, d
                                           _dp(d_owner), _dp(d_src), _dp(d_token_writer_row), dense_cap_pages,
                                           _dp(d_dense), _dp(d_status), _stream(stream))
     _check("cpkv_compose_fused_planes", rc)
+
+
+def cpkv_selftest_ring_timeout(d_dst16, d_status, stream=None):
+    """Diagnostics: the bulk ring's bounded wait on a load that never arrives
+    (raises STATUS_TIMEOUT on the device, writes nothing to ``d_dst16``)."""
+    _check("cpkv_selftest_ring_timeout",
+           load().cpkv_selftest_ring_timeout(_dp(d_dst16), _dp(d_status), _stream(stream)))
 
 
 def cpkv_ragged_plan_build(prefix_lens, q_lens, d_cp_index, n_owned: int, *, chunk, k_align, out, d_counts,

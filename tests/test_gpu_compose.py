@@ -556,3 +556,29 @@ def test_one_launch_consuming_staging_matches_oracle(batch):
     want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
                                 page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
     assert np.array_equal(dense.cpu().numpy(), want)
+
+
+# ---------------------------------------------------------------------------
+# failure detection on the GPU without a fault: a copy that never lands
+# ---------------------------------------------------------------------------
+
+def test_ring_wait_times_out_and_the_context_stays_usable():
+    """The bulk ring's bounded wait gives up on a load that never arrives
+    (an mbarrier phase that nothing completes): TIMEOUT is raised, nothing is
+    stored, and the next compose on the same context is still byte-exact."""
+    import time
+
+    dst = torch.full((16,), 0x77, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    cpkv.cpkv_selftest_ring_timeout(dst, status)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(status.item()) == cpkv.STATUS_TIMEOUT
+    assert torch.all(dst == 0x77)
+    assert 1.5 < waited < 30.0  # the ring's 2 s limit, not a hang
+    batch = wl.tiny_batch()        # the context is fine: a compose right after is byte-exact
+    dense, plan, slabs, rows = _run_fused(batch)
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense, want)
