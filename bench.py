@@ -552,7 +552,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="traced_78", choices=["traced_78", "traced", "fp8_nsa", "index_k", "plans"],
+    ap.add_argument("--config", default="traced_78",
+                    choices=["traced_78", "traced", "traced_78_ps1", "fp8_nsa", "index_k", "plans"],
                     help="plans: latency of the per-batch plan builders (ragged plan config, all CP ranks and "
                          "splits; compose plan of the traced and fp8 batches)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -704,6 +705,9 @@ def main(argv=None):
                          "4096-page pool slab per layer" if a.config == "traced_78" else
                          "traced prefill compose, 1 layer: the same batch over its 200000-page randomly permuted "
                          "pool" if a.config == "traced" else
+                         "traced prefill compose with one-token pages, 78 layers: the same lengths, page_size=1 "
+                         "(88832 prefix + 44600 current pages of 1152 bytes per layer), 2^18-page pool slab per "
+                         "layer" if a.config == "traced_78_ps1" else
                          "fp8 NSA compose, 78 layers: bs=32, 131072 current tokens, prefix U[0,64K], page_size=64, "
                          "cp=8, 656-byte rows, one 2^20-page pool shared by the layers" if a.config == "fp8_nsa" else
                          "NSA indexer-key compose, 78 layers: the fp8 NSA batch with planar pages of 64 x (128-byte "

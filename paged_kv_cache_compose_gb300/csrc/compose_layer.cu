@@ -364,12 +364,12 @@ namespace {
 // Launch one instantiation of the kernel on a persistent grid sized by the
 // occupancy calculator.
 template <typename Params>
-int launch_layer(void (*kernel)(Params), int threads, int64_t units, size_t smem, cudaStream_t s,
+int launch_layer(void (*kernel)(Params), int threads, int64_t units, size_t smem, int cap_per_sm, cudaStream_t s,
                  const Params &prm) {
   using namespace cpkv;
   const void *fn = reinterpret_cast<const void *>(kernel);
   if (ensure_dynamic_smem(fn, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
-  const int grid = persistent_grid(fn, threads, smem, kMaxCtasPerSm, units);
+  const int grid = persistent_grid(fn, threads, smem, cap_per_sm, units);
   kernel<<<grid, threads, smem, s>>>(prm);
   return launch_status();
 }
@@ -424,6 +424,7 @@ int compose_layer_impl(bool staged, bool consume_staging, int B, int page_size, 
   if (pieces > INT32_MAX || dense_cap_pages > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
   const int64_t units = dense_cap_pages * pieces;
   const size_t smem = (size_t)kStages * piece_bytes;
+  const int cap_per_sm = pieces > 1 ? kMaxCtasPerSm : ring_cap_one_piece(piece_bytes, kLoadsInFlight, kMaxCtasPerSm);
 
 #define CPKV_FILL_LAYER(prm)                                                                           \
   for (int k = 0; k < 2 * CPKV_MAX_CP; ++k) {                                                          \
@@ -460,7 +461,7 @@ int compose_layer_impl(bool staged, bool consume_staging, int B, int page_size, 
   {                                                                                        \
     LayerParams<MAXB, NP> prm;                                                             \
     CPKV_FILL_LAYER(prm)                                                                   \
-    return launch_layer(compose_layer_kernel<MAXB, PL, ST, CO>, THREADS, units, smem, s, prm); \
+    return launch_layer(compose_layer_kernel<MAXB, PL, ST, CO>, THREADS, units, smem, cap_per_sm, s, prm); \
   }
   if (B <= 64) {
     if (planar && !staged) CPKV_LAUNCH_LAYER(64, kMaxPlanes, true, false, false, 64)

@@ -183,6 +183,7 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
   if (pieces > INT32_MAX || dense_cap_pages > INT64_MAX / pieces) return CPKV_ERR_LIMIT;
   const int64_t units = dense_cap_pages * pieces;
   const size_t smem = (size_t)kStages * piece_bytes;
+  const int cap_per_sm = pieces > 1 ? kMaxCtasPerSm : ring_cap_one_piece(piece_bytes, kLoadsInFlight, kMaxCtasPerSm);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
 #define CPKV_FILL_FUSED(prm)                                                                        \
@@ -201,7 +202,7 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
   if (B <= 64) {
     const void *kernel = reinterpret_cast<const void *>(compose_fused_kernel<64>);
     if (ensure_dynamic_smem(kernel, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
-    const int grid = persistent_grid(kernel, 32, smem, kMaxCtasPerSm, units);
+    const int grid = persistent_grid(kernel, 32, smem, cap_per_sm, units);
     FusedParams<64> prm;
     CPKV_FILL_FUSED(prm)
     compose_fused_kernel<64><<<grid, 32, smem, s>>>(prm);
@@ -209,7 +210,7 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
   }
   const void *kernel = reinterpret_cast<const void *>(compose_fused_kernel<CPKV_MAX_BATCH>);
   if (ensure_dynamic_smem(kernel, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
-  const int grid = persistent_grid(kernel, 32, smem, kMaxCtasPerSm, units);
+  const int grid = persistent_grid(kernel, 32, smem, cap_per_sm, units);
   FusedParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_FUSED(prm)
 #undef CPKV_FILL_FUSED

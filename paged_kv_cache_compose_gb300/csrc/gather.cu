@@ -165,7 +165,10 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
                                : reinterpret_cast<const void *>(gather_pages_kernel<false>);
   if (ensure_dynamic_smem(kernel, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
   const int grid =
-      persistent_grid(kernel, 32, smem, pieces > 1 ? kMaxCtasPerSmPieces : kMaxCtasPerSmOnePiece, prm.units);
+      persistent_grid(kernel, 32, smem,
+                      pieces > 1 ? kMaxCtasPerSmPieces
+                                 : ring_cap_one_piece(piece_bytes, kLoadsInFlight, kMaxCtasPerSmOnePiece),
+                      prm.units);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (consume) gather_pages_kernel<true><<<grid, 32, smem, s>>>(prm);
   else gather_pages_kernel<false><<<grid, 32, smem, s>>>(prm);

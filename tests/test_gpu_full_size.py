@@ -84,7 +84,8 @@ def _check_plan(work):
                                             ("traced_78", "layer"), ("fp8_nsa", "layer"), ("index_k", "layer"),
                                             ("index_k", "fused"), ("traced_78", "staging-consume"),
                                             ("fp8_nsa", "staging-consume"), ("traced_78", "layer-consume"),
-                                            ("index_k", "layer-consume")])
+                                            ("index_k", "layer-consume"), ("traced_78_ps1", "staging"),
+                                            ("traced_78_ps1", "fused"), ("traced_78_ps1", "staging-consume")])
 def test_benchmark_workload_matches_oracle(config, variant):
     consume = variant.endswith("-consume")  # plain variants keep their stagings, which are checked
     variant = variant.removesuffix("-consume")

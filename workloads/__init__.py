@@ -17,8 +17,9 @@ computed here.  The only structure it knows is the scenario itself:
   message: the ragged plan is keyed on ``cp_index``).
 
 Workload shapes follow the five benchmark configurations of this project
-(tiny, traced prefill, 78-layer loop, fp8 NSA, ragged plan).  Seeds: config k
-uses ``1000 + k``.  Streams are drawn in a fixed order from one
+(tiny, traced prefill, 78-layer loop, fp8 NSA, ragged plan), plus the NSA
+index keys of the fp8 batch and the traced lengths on one-token pages.
+Seeds: config k uses ``1000 + k``.  Streams are drawn in a fixed order from one
 ``numpy.random.Generator``.
 """
 from __future__ import annotations
@@ -212,6 +213,20 @@ def traced_78_layer_batch(seed: int = 1002) -> ComposeBatch:
     return traced_batch(seed, num_layers=78, num_pool_pages=4096)
 
 
+def traced_78_token_pages_batch(seed: int = 1006) -> ComposeBatch:
+    """The traced batch's lengths over 78 layers with pages of one token
+    (page_size = 1, a 1152-byte page per token): 88 832 prefix and 44 600
+    current pages per layer.  Each layer has its own pool slab of 2^18 pages
+    (8 owners x 32 768); page ids are a seeded permutation inside it and the
+    writers go round-robin over pages."""
+    tb = traced_batch()
+    rng = np.random.default_rng(seed)
+    return make_compose_batch(
+        "traced_ps1", seed, page_size=1, cp_size=8, num_pool_pages=1 << 18, row_bytes=MLA_ROW_BYTES,
+        prefix_lens=tb.prefix_lens, cur_lens=tb.cur_lens, rng=rng, num_layers=78,
+    )
+
+
 def fp8_nsa_batch(seed: int = 1004, *, num_layers: int = 78, num_pool_pages: int = 1 << 20) -> ComposeBatch:
     """FP8 NSA layout: ps=64, cp=8, bs=32, 131 072 current tokens split
     lognormally, prefix U[0,65536] floored to a page, 656-byte rows of random
@@ -387,6 +402,7 @@ CONFIGS = {
     "tiny": tiny_batch,
     "traced": traced_batch,
     "traced_78": traced_78_layer_batch,
+    "traced_78_ps1": traced_78_token_pages_batch,
     "fp8_nsa": fp8_nsa_batch,
     "index_k": index_k_batch,
 }
