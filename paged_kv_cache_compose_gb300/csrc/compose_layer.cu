@@ -20,7 +20,8 @@
 // back; the pad rows, zero in both places, are written to the dense page
 // directly instead of being read back.  Staging stores carry an L2
 // evict_last policy (their read-back follows within microseconds), all other
-// copies evict_first.
+// copies evict_first.  With consume_staging the staged lines are dropped from
+// L2 once read back, so they are never written back to DRAM.
 //
 // Pages may be planar (cpkv_compose_layer_planes): plane q of a page holds
 // the ps tokens' plane_bytes[q]-byte slices, the planes one after the other.

@@ -19,7 +19,9 @@
 //                         page's first token, then ps - n_i zero rows
 // The descriptors are the ones cpkv_plan_build writes for the gather.  The
 // output is byte-identical to cpkv_fill_current followed by
-// cpkv_compose_gather.  Same bulk-copy ring as the gather (bulk_ring.cuh).
+// cpkv_compose_gather.  Same bulk-copy ring as the gather (bulk_ring.cuh),
+// with up to 3 one-warp CTAs per SM for pages of several pieces and the
+// gather's in-flight rule for pages of one piece.
 #include <stdint.h>
 
 #include "bulk_ring.cuh"

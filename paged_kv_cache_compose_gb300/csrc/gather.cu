@@ -8,7 +8,10 @@
 // non-tensor form): global -> shared with mbarrier completion, then
 // shared -> global tracked by bulk groups.  Each page is cut into `pieces`
 // equal 16-byte-multiple units (<= 16 KB); units are dealt round-robin to a
-// persistent grid of one-warp CTAs, 3 or 4 per SM.  Each CTA runs a BulkRing of
+// persistent grid of one-warp CTAs: up to 4 per SM for pages of several
+// pieces, and for pages of one piece enough to keep about 56 KB of loads in
+// flight per SM (3 for 8448-byte pages, 24 for 1152-byte ones; see
+// ring_cap_one_piece).  Each CTA runs a BulkRing of
 // 4 shared-memory stages with at most 2 loads outstanding, so the other
 // stages hold stores still draining: loads and stores overlap instead of a
 // stage waiting for its own store.  Every copy carries an L2 evict_first
@@ -16,7 +19,10 @@
 // layer, and streaming them must not evict the staging the fill has just
 // written for this gather.  Zero units (owner -1 or an invalid descriptor)
 // are written with plain 16-byte stores by the whole warp.  Every mbarrier
-// wait is bounded (see bulk_ring.cuh).
+// wait is bounded (see bulk_ring.cuh).  With CPKV_GATHER_CONSUME_STAGING the
+// stagings are consumed: once a staging piece has landed in shared memory
+// its L2 lines are dropped, so the fill's dirty staging lines are never
+// written back to DRAM.
 #include <stdint.h>
 
 #include "bulk_ring.cuh"
