@@ -311,14 +311,18 @@ class ComposeWorkload:
     def run_kernel(self, kind, layer, stream=None):
         """Launch one layer's work: ``all`` of it, or one kernel of it."""
         dense = self.layers.dense[layer % 2]
+        # Every input of a layer's compose (plan, pools, rows) is complete before
+        # the step's layer loop starts, and no kernel of the loop writes one, so
+        # the one-launch forms may read them early (cpkv.FLAG_EARLY_INPUTS).
         if self.variant == "fused":
             self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream,
-                                      plane_bytes=list(self.batch.planes) if self.batch.planes else None)
+                                      plane_bytes=list(self.batch.planes) if self.batch.planes else None,
+                                      early_inputs=True)
             return
         if self.variant == "layer":
             self.layers.compose_one_launch(self.pools_of(layer), self.rows[layer], dense, stream,
                                            plane_bytes=list(self.batch.planes) if self.batch.planes else None,
-                                           consume_staging=self.consume_staging)
+                                           consume_staging=self.consume_staging, early_inputs=True)
             return
         if kind in ("all", "fill"):
             if self.batch.planes:

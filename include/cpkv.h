@@ -264,6 +264,22 @@ int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
                               const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages, int kinds,
                               void *d_dense, int32_t *d_status, cpkv_stream_t stream);
 
+/* Flags of cpkv_compose_layer(_planes) and cpkv_compose_fused(_planes). */
+/* The stagings are consumed, as with CPKV_GATHER_CONSUME_STAGING (layer
+ * compose only): each staged piece's L2 lines are dropped once it has been
+ * read back, and the staging bytes are undefined after the call. */
+#define CPKV_FLAG_CONSUME_STAGING 1
+/* Early inputs: the caller promises that everything the call reads (the plan
+ * arrays, the pools and the current rows) was complete before the previous
+ * kernel on the stream started, and that nothing still running writes it.
+ * The kernel is then launched as a programmatic dependent of the previous
+ * kernel (for pages of several pieces): its CTAs may start in the SM slots
+ * that launch's tail frees and read inputs at once, and they wait for it
+ * only before their first store.  In a per-layer loop whose inputs were
+ * produced before the loop this holds; directly after the kernel that writes
+ * the current rows or the plan it does not. */
+#define CPKV_FLAG_EARLY_INPUTS 2
+
 /*
  * cpkv_compose_layer — per layer: cpkv_fill_current followed by
  * cpkv_compose_gather in one launch, for the plan of cpkv_plan_build.  Each
@@ -284,10 +300,8 @@ int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
  *                    i = src - 1 holds n_i rows that are consecutive in its
  *                    writer's buffer from token_writer_row of its first token)
  *   d_dense          device [dense_cap_pages * ps][R], 16-byte aligned
- *   consume_staging  non-zero: the stagings are consumed, as with
- *                    CPKV_GATHER_CONSUME_STAGING (each staged piece's L2
- *                    lines are dropped once it has been read back; the
- *                    staging bytes are undefined after the call)
+ *   flags            CPKV_FLAG_CONSUME_STAGING, CPKV_FLAG_EARLY_INPUTS (or 0);
+ *                    other bits return CPKV_ERR_ARG
  * A descriptor outside the table or its capacity raises DESC_OOB, current
  * rows outside the writer's buffer raise ROW_OOB; either dense page is
  * zero-filled and its staging slot is not written.  Errors: ARG for bad
@@ -298,7 +312,7 @@ int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row_bytes, con
                        const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
                        const void *const *h_src_table, const int64_t *h_src_cap_pages, const int32_t *d_owner,
                        const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
-                       void *d_dense, int consume_staging, int32_t *d_status, cpkv_stream_t stream);
+                       void *d_dense, int flags, int32_t *d_status, cpkv_stream_t stream);
 
 /*
  * cpkv_compose_layer_planes — cpkv_compose_layer for planar pages (the
@@ -320,7 +334,7 @@ int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int n_planes, c
                               const int64_t *h_cur_rows_cap, const void *const *h_src_table,
                               const int64_t *h_src_cap_pages, const int32_t *d_owner, const int32_t *d_src,
                               const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
-                              int consume_staging, int32_t *d_status, cpkv_stream_t stream);
+                              int flags, int32_t *d_status, cpkv_stream_t stream);
 
 /*
  * cpkv_compose_fused — per layer: the single-GPU compose in one pass, without
@@ -342,12 +356,14 @@ int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int n_planes, c
  *   h_cur_rows       host array [cp] of device pointers, [h_cur_rows_cap[w]][R]
  *   d_owner, d_src, d_token_writer_row: from cpkv_plan_build
  *   d_dense          device [dense_cap_pages * ps][R], 16-byte aligned
+ *   flags            CPKV_FLAG_EARLY_INPUTS or 0; other bits return
+ *                    CPKV_ERR_ARG
  */
 int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
                        const void *const *h_pools, const int64_t *h_pool_cap_pages,
                        const void *const *h_cur_rows, const int64_t *h_cur_rows_cap, const int32_t *d_owner,
                        const int32_t *d_src, const int32_t *d_token_writer_row, int64_t dense_cap_pages,
-                       void *d_dense, int32_t *d_status, cpkv_stream_t stream);
+                       void *d_dense, int flags, int32_t *d_status, cpkv_stream_t stream);
 
 /*
  * cpkv_compose_fused_planes — cpkv_compose_fused for planar pages (the layout
@@ -357,7 +373,7 @@ int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row_bytes, con
  * 16-byte-aligned page offset move with bulk copies, other slices with the
  * lanes.  One plane of a 16-byte-multiple width is cpkv_compose_fused.
  *   n_planes, h_plane_bytes, h_cur_planes: as cpkv_compose_layer_planes
- *   h_pools, h_pool_cap_pages: as cpkv_compose_fused
+ *   h_pools, h_pool_cap_pages, flags: as cpkv_compose_fused
  * A descriptor outside the table raises DESC_OOB, rows outside a writer's
  * buffer ROW_OOB; either page is zero-filled.  Errors: as cpkv_compose_layer.
  */
@@ -366,7 +382,7 @@ int cpkv_compose_fused_planes(int B, int page_size, int cp_size, int n_planes, c
                               const int64_t *h_pool_cap_pages, const void *const *h_cur_planes,
                               const int64_t *h_cur_rows_cap, const int32_t *d_owner, const int32_t *d_src,
                               const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
-                              int32_t *d_status, cpkv_stream_t stream);
+                              int flags, int32_t *d_status, cpkv_stream_t stream);
 
 /*
  * cpkv_selftest_ring_timeout — diagnostics: runs the bounded wait of the

@@ -39,6 +39,12 @@ GATHER_STAGING = 2
 GATHER_ZERO = 4
 GATHER_ALL = 7
 GATHER_CONSUME_STAGING = 8  # flag: staging bytes are undefined after the gather (L2 lines dropped)
+FLAG_CONSUME_STAGING = 1    # layer compose: the stagings are consumed
+FLAG_EARLY_INPUTS = 2       # layer / fused compose: inputs complete before the previous kernel started
+
+
+def compose_flags(consume_staging=False, early_inputs=False) -> int:
+    return (FLAG_CONSUME_STAGING if consume_staging else 0) | (FLAG_EARLY_INPUTS if early_inputs else 0)
 
 MAX_CP = 64
 MAX_BATCH = 1024
@@ -79,9 +85,10 @@ def _declare(lib):
     lib.cpkv_compose_layer.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P, _P]
     lib.cpkv_compose_layer_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P,
                                               _P]
-    lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_compose_fused.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P, _P]
     lib.cpkv_selftest_ring_timeout.argtypes = [_P, _P, _P]
-    lib.cpkv_compose_fused_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]
+    lib.cpkv_compose_fused_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P,
+                                              _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
     lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
     for name in EXPORTED:
@@ -255,9 +262,10 @@ def cpkv_compose_gather_kinds(src_table: Sequence, src_cap_pages, d_owner, d_src
 
 def cpkv_compose_layer(cur_lens, cur_rows: Sequence, src_table: Sequence, src_cap_pages, d_owner, d_src,
                        d_token_writer_row, d_dense, *, page_size, cp_size, row_bytes, dense_cap_pages, d_status,
-                       cur_rows_cap=None, consume_staging=False, stream=None):
+                       cur_rows_cap=None, consume_staging=False, early_inputs=False, stream=None):
     """Fill + slot-dense gather of one layer in a single launch (``consume_staging``:
-    the staging bytes are undefined afterwards)."""
+    the staging bytes are undefined afterwards; ``early_inputs``: see
+    CPKV_FLAG_EARLY_INPUTS)."""
     cl = _host_i32(cur_lens)
     if cur_rows_cap is None:
         cur_rows_cap = [t.numel() // row_bytes for t in cur_rows]
@@ -265,14 +273,14 @@ def cpkv_compose_layer(cur_lens, cur_rows: Sequence, src_table: Sequence, src_ca
     rarr, tarr = _ptr_array(cur_rows), _ptr_array(src_table)
     rc = load().cpkv_compose_layer(len(cl), page_size, cp_size, row_bytes, _hp(cl), ctypes.cast(rarr, _P), _hp(rcaps),
                                    ctypes.cast(tarr, _P), _hp(tcaps), _dp(d_owner), _dp(d_src),
-                                   _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense), int(bool(consume_staging)),
-                                   _dp(d_status), _stream(stream))
+                                   _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense),
+                                   compose_flags(consume_staging, early_inputs), _dp(d_status), _stream(stream))
     _check("cpkv_compose_layer", rc)
 
 
 def cpkv_compose_layer_planes(cur_lens, cur_planes: Sequence, src_table: Sequence, src_cap_pages, d_owner, d_src,
                               d_token_writer_row, d_dense, *, page_size, cp_size, plane_bytes, dense_cap_pages,
-                              d_status, cur_rows_cap=None, consume_staging=False, stream=None):
+                              d_status, cur_rows_cap=None, consume_staging=False, early_inputs=False, stream=None):
     """Fill + gather of one layer of planar pages in a single launch
     (``cur_planes[p][w]``: writer w's rows of plane p)."""
     cl, pb = _host_i32(cur_lens), _host_i32(plane_bytes)
@@ -285,13 +293,14 @@ def cpkv_compose_layer_planes(cur_lens, cur_planes: Sequence, src_table: Sequenc
     rc = load().cpkv_compose_layer_planes(len(cl), page_size, cp_size, n_planes, _hp(pb), _hp(cl),
                                           ctypes.cast(flat, _P), _hp(rcaps), ctypes.cast(tarr, _P), _hp(tcaps),
                                           _dp(d_owner), _dp(d_src), _dp(d_token_writer_row), dense_cap_pages,
-                                          _dp(d_dense), int(bool(consume_staging)), _dp(d_status), _stream(stream))
+                                          _dp(d_dense), compose_flags(consume_staging, early_inputs), _dp(d_status),
+                                          _stream(stream))
     _check("cpkv_compose_layer_planes", rc)
 
 
 def cpkv_compose_fused(cur_lens, pools: Sequence, cur_rows: Sequence, d_owner, d_src, d_token_writer_row, d_dense,
                        *, page_size, cp_size, row_bytes, dense_cap_pages, d_status, pool_cap_pages=None,
-                       cur_rows_cap=None, stream=None):
+                       cur_rows_cap=None, early_inputs=False, stream=None):
     """Single-GPU compose of one layer without staging (pools + writers' current rows -> dense)."""
     cl = _host_i32(cur_lens)
     if pool_cap_pages is None:
@@ -302,14 +311,15 @@ def cpkv_compose_fused(cur_lens, pools: Sequence, cur_rows: Sequence, d_owner, d
     parr, rarr = _ptr_array(pools), _ptr_array(cur_rows)
     rc = load().cpkv_compose_fused(len(cl), page_size, cp_size, row_bytes, _hp(cl), ctypes.cast(parr, _P), _hp(pcaps),
                                    ctypes.cast(rarr, _P), _hp(rcaps), _dp(d_owner), _dp(d_src),
-                                   _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense), _dp(d_status),
+                                   _dp(d_token_writer_row), dense_cap_pages, _dp(d_dense),
+                                   compose_flags(early_inputs=early_inputs), _dp(d_status),
                                    _stream(stream))
     _check("cpkv_compose_fused", rc)
 
 
 def cpkv_compose_fused_planes(cur_lens, pools: Sequence, cur_planes: Sequence, d_owner, d_src, d_token_writer_row,
                               d_dense, *, page_size, cp_size, plane_bytes, dense_cap_pages, d_status,
-                              pool_cap_pages=None, cur_rows_cap=None, stream=None):
+                              pool_cap_pages=None, cur_rows_cap=None, early_inputs=False, stream=None):
     """Single-GPU compose of one layer of planar pages without staging
     (``cur_planes[p][w]``: writer w's rows of plane p)."""
     cl, pb = _host_i32(cur_lens), _host_i32(plane_bytes)
@@ -324,7 +334,8 @@ def cpkv_compose_fused_planes(cur_lens, pools: Sequence, cur_planes: Sequence, d
     rc = load().cpkv_compose_fused_planes(len(cl), page_size, cp_size, n_planes, _hp(pb), _hp(cl),
                                           ctypes.cast(parr, _P), _hp(pcaps), ctypes.cast(flat, _P), _hp(rcaps),
                                           _dp(d_owner), _dp(d_src), _dp(d_token_writer_row), dense_cap_pages,
-                                          _dp(d_dense), _dp(d_status), _stream(stream))
+                                          _dp(d_dense), compose_flags(early_inputs=early_inputs), _dp(d_status),
+                                          _stream(stream))
     _check("cpkv_compose_fused_planes", rc)
 
 

@@ -70,6 +70,17 @@ __device__ __forceinline__ void bulk_wait_complete_dyn(int64_t n) {
   }
 }
 
+// Wait, once per thread, for the previous kernel on the stream before the
+// first global store.  A no-op unless the launch is a programmatic dependent
+// (pages of several pieces, as for the fused compose: the CTAs may start in
+// the slots the previous launch's tail frees and issue loads first).
+__device__ __forceinline__ void store_gate(bool *open) {
+  if (!*open) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    *open = true;
+  }
+}
+
 struct Readback {
   const uint8_t *src;  // staging piece
   uint8_t *dst;        // dense piece
@@ -183,8 +194,10 @@ struct LayerRing : BulkRing<kStages, kLoadsInFlight, kConsume> {
   uint64_t keep_policy, stream_policy;
   Readback *rq;        // kReadbackQueue entries (shared; lane 0 writes, the warp reads)
   int64_t rq_head, rq_tail;
+  bool stores_open;    // the previous launch has completed (store_gate)
 
   CPKV_DEV void consume_one() {
+    store_gate(&stores_open);
     store_policy = ((keep_mask >> (int)(head % kStages)) & 1u) ? keep_policy : stream_policy;
     consume();
   }
@@ -255,6 +268,8 @@ __global__ void __launch_bounds__(64, 1)
   // Row layout (one warp): the same warp does both.
   const bool copy_role = copy_warp, store_role = PLANAR ? !copy_warp : true;
   const uint64_t keep = l2_policy_evict_last();  // staging stores
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  bool stores_open = false;  // plain stores of this warp wait for the previous launch once
 
   if (copy_warp) {  // request-level exclusive scans, 32 requests per step
     int32_t carry_pages = 0;
@@ -287,6 +302,7 @@ __global__ void __launch_bounds__(64, 1)
     ring.stream_policy = ring.load_policy;
     ring.rq = readbacks;
     ring.rq_head = ring.rq_tail = 0;
+    ring.stores_open = false;
   }
   const int64_t step = gridDim.x;
   for (int64_t base = blockIdx.x; base < p.units; base += 32 * step) {
@@ -316,6 +332,7 @@ __global__ void __launch_bounds__(64, 1)
           if (copy_role) ring.push_with(p.table[o] + (int64_t)s * p.page_bytes + off, dst, bytes, false);
         } else if (store_role) {
           if (o != -1 && lane == 0 && k == 0) raise_status(p.status, CPKV_STATUS_DESC_OOB);
+          store_gate(&stores_open);
           warp_zero(dst, bytes);
         }
       } else {
@@ -324,6 +341,7 @@ __global__ void __launch_bounds__(64, 1)
         if (bad) {
           if (store_role) {
             if (lane == 0 && k == 0) raise_status(p.status, bad);
+            store_gate(&stores_open);
             warp_zero(dst, bytes);
           }
         } else {
@@ -341,10 +359,14 @@ __global__ void __launch_bounds__(64, 1)
               const uint8_t *from = p.cur_rows[q][o - p.cp] + (int64_t)row0 * w + (lo - P);
               if (bulk && STAGED) ring.stage(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo));
               else if (bulk) ring.push_with(from, dense_page + lo, (uint32_t)(hi - lo), false);
-              else warp_copy_words<STAGED>(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo), keep);
+              else {
+                store_gate(&stores_open);
+                warp_copy_words<STAGED>(from, stg_page + lo, dense_page + lo, (uint32_t)(hi - lo), keep);
+              }
             }
             const int64_t zlo = off > rows_end ? off : rows_end, zhi = min64(end, plane_end);
             if (zlo < zhi && store_role) {
+              store_gate(&stores_open);
               if (STAGED) warp_zero_span(stg_page + zlo, (uint32_t)(zhi - zlo), true, keep);
               warp_zero_span(dense_page + zlo, (uint32_t)(zhi - zlo), false, 0);
             }
@@ -363,21 +385,35 @@ __global__ void __launch_bounds__(64, 1)
 namespace {
 
 // Launch one instantiation of the kernel on a persistent grid sized by the
-// occupancy calculator.
+// occupancy calculator; as a programmatic dependent of the previous kernel
+// when `dependent` (pages of several pieces).
 template <typename Params>
-int launch_layer(void (*kernel)(Params), int threads, int64_t units, size_t smem, int cap_per_sm, cudaStream_t s,
-                 const Params &prm) {
+int launch_layer(void (*kernel)(Params), int threads, int64_t units, size_t smem, int cap_per_sm, bool dependent,
+                 cudaStream_t s, const Params &prm) {
   using namespace cpkv;
   const void *fn = reinterpret_cast<const void *>(kernel);
   if (ensure_dynamic_smem(fn, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
   const int grid = persistent_grid(fn, threads, smem, cap_per_sm, units);
-  kernel<<<grid, threads, smem, s>>>(prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, prm) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CPKV_ERR_CUDA;
+  }
   return launch_status();
 }
 
 // staged: h_src_table / h_src_cap_pages hold 2*cp entries (pools, then
 // stagings); else cp entries (pools only) and no staging is written.
-int compose_layer_impl(bool staged, bool consume_staging, int B, int page_size, int cp_size, int n_planes,
+int compose_layer_impl(bool staged, bool consume_staging, bool early, int B, int page_size, int cp_size, int n_planes,
                        const int32_t *h_plane_bytes, const int32_t *h_cur_lens, const void *const *h_cur_planes,
                        const int64_t *h_cur_rows_cap, const void *const *h_src_table, const int64_t *h_src_cap_pages,
                        const int32_t *d_owner, const int32_t *d_src, const int32_t *d_token_writer_row,
@@ -462,7 +498,9 @@ int compose_layer_impl(bool staged, bool consume_staging, int B, int page_size, 
   {                                                                                        \
     LayerParams<MAXB, NP> prm;                                                             \
     CPKV_FILL_LAYER(prm)                                                                   \
-    return launch_layer(compose_layer_kernel<MAXB, PL, ST, CO>, THREADS, units, smem, cap_per_sm, s, prm); \
+    return launch_layer(compose_layer_kernel<MAXB, PL, ST, CO>, THREADS, units, smem, cap_per_sm,             \
+                        early && pieces > 1, s,                                                 \
+                        prm);                                                                   \
   }
   if (B <= 64) {
     if (planar && !staged) CPKV_LAUNCH_LAYER(64, kMaxPlanes, true, false, false, 64)
@@ -486,11 +524,13 @@ extern "C" int cpkv_compose_layer(int B, int page_size, int cp_size, int64_t row
                                   const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
                                   const void *const *h_src_table, const int64_t *h_src_cap_pages,
                                   const int32_t *d_owner, const int32_t *d_src, const int32_t *d_token_writer_row,
-                                  int64_t dense_cap_pages, void *d_dense, int consume_staging, int32_t *d_status,
+                                  int64_t dense_cap_pages, void *d_dense, int flags, int32_t *d_status,
                                   cpkv_stream_t stream) {
   if (row_bytes <= 0 || row_bytes % 16 != 0 || row_bytes > INT32_MAX) return CPKV_ERR_ARG;
+  if ((flags & ~(CPKV_FLAG_CONSUME_STAGING | CPKV_FLAG_EARLY_INPUTS)) != 0) return CPKV_ERR_ARG;
   const int32_t plane = (int32_t)row_bytes;
-  return compose_layer_impl(true, consume_staging != 0, B, page_size, cp_size, 1, &plane, h_cur_lens, h_cur_rows,
+  const bool consume = (flags & CPKV_FLAG_CONSUME_STAGING) != 0, early = (flags & CPKV_FLAG_EARLY_INPUTS) != 0;
+  return compose_layer_impl(true, consume, early, B, page_size, cp_size, 1, &plane, h_cur_lens, h_cur_rows,
                             h_cur_rows_cap, h_src_table, h_src_cap_pages, d_owner, d_src, d_token_writer_row,
                             dense_cap_pages, d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -501,8 +541,10 @@ extern "C" int cpkv_compose_layer_planes(int B, int page_size, int cp_size, int 
                                          const void *const *h_src_table, const int64_t *h_src_cap_pages,
                                          const int32_t *d_owner, const int32_t *d_src,
                                          const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
-                                         int consume_staging, int32_t *d_status, cpkv_stream_t stream) {
-  return compose_layer_impl(true, consume_staging != 0, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens,
+                                         int flags, int32_t *d_status, cpkv_stream_t stream) {
+  if ((flags & ~(CPKV_FLAG_CONSUME_STAGING | CPKV_FLAG_EARLY_INPUTS)) != 0) return CPKV_ERR_ARG;
+  const bool consume = (flags & CPKV_FLAG_CONSUME_STAGING) != 0, early = (flags & CPKV_FLAG_EARLY_INPUTS) != 0;
+  return compose_layer_impl(true, consume, early, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens,
                             h_cur_planes, h_cur_rows_cap, h_src_table, h_src_cap_pages, d_owner, d_src,
                             d_token_writer_row,
                             dense_cap_pages, d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
@@ -514,13 +556,14 @@ extern "C" int cpkv_compose_fused_planes(int B, int page_size, int cp_size, int 
                                          const void *const *h_cur_planes, const int64_t *h_cur_rows_cap,
                                          const int32_t *d_owner, const int32_t *d_src,
                                          const int32_t *d_token_writer_row, int64_t dense_cap_pages, void *d_dense,
-                                         int32_t *d_status, cpkv_stream_t stream) {
+                                         int flags, int32_t *d_status, cpkv_stream_t stream) {
+  if ((flags & ~CPKV_FLAG_EARLY_INPUTS) != 0) return CPKV_ERR_ARG;
   if (n_planes == 1 && h_plane_bytes != nullptr && h_plane_bytes[0] > 0 && h_plane_bytes[0] % 16 == 0)
     return cpkv_compose_fused(B, page_size, cp_size, h_plane_bytes[0], h_cur_lens, h_pools, h_pool_cap_pages,
                               h_cur_planes, h_cur_rows_cap, d_owner, d_src, d_token_writer_row, dense_cap_pages,
-                              d_dense, d_status, stream);
-  return compose_layer_impl(false, false, B, page_size, cp_size, n_planes, h_plane_bytes, h_cur_lens,
-                            h_cur_planes, h_cur_rows_cap, h_pools, h_pool_cap_pages, d_owner, d_src,
-                            d_token_writer_row,
-                            dense_cap_pages, d_dense, d_status, reinterpret_cast<cudaStream_t>(stream));
+                              d_dense, flags, d_status, stream);
+  return compose_layer_impl(false, false, (flags & CPKV_FLAG_EARLY_INPUTS) != 0, B, page_size, cp_size, n_planes,
+                            h_plane_bytes, h_cur_lens, h_cur_planes, h_cur_rows_cap, h_pools, h_pool_cap_pages,
+                            d_owner, d_src, d_token_writer_row, dense_cap_pages, d_dense, d_status,
+                            reinterpret_cast<cudaStream_t>(stream));
 }

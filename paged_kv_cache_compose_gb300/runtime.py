@@ -118,22 +118,25 @@ class ComposeLayers:
         self.fill(cur_rows_per_writer, stream)
         self.gather_kinds([None] * self.plan.cp_size, dense, cpkv.GATHER_STAGING, stream)
 
-    def compose_fused(self, pools, cur_rows_per_writer, dense, stream=None, plane_bytes=None):
+    def compose_fused(self, pools, cur_rows_per_writer, dense, stream=None, plane_bytes=None, early_inputs=False):
         """One-pass single-GPU compose of a layer (no staging round trip); for
-        planar pages, ``plane_bytes`` and ``cur_rows_per_writer[p][w]``."""
+        planar pages, ``plane_bytes`` and ``cur_rows_per_writer[p][w]``.
+        ``early_inputs``: the plan, pools and rows were complete before the
+        previous kernel on the stream started (cpkv.FLAG_EARLY_INPUTS)."""
         p = self.plan
         if plane_bytes is not None:
             cpkv.cpkv_compose_fused_planes(p.cur_lens, pools, cur_rows_per_writer, p["owner"], p["src"],
                                            p["token_writer_row"], dense, page_size=p.page_size, cp_size=p.cp_size,
                                            plane_bytes=plane_bytes, dense_cap_pages=p.dense_cap_pages,
-                                           d_status=p.d_status, stream=stream)
+                                           d_status=p.d_status, early_inputs=early_inputs, stream=stream)
             return
         cpkv.cpkv_compose_fused(p.cur_lens, pools, cur_rows_per_writer, p["owner"], p["src"], p["token_writer_row"],
                                 dense, page_size=p.page_size, cp_size=p.cp_size, row_bytes=self.row_bytes,
-                                dense_cap_pages=p.dense_cap_pages, d_status=p.d_status, stream=stream)
+                                dense_cap_pages=p.dense_cap_pages, d_status=p.d_status, early_inputs=early_inputs,
+                                stream=stream)
 
     def compose_one_launch(self, pools, cur_rows_per_writer, dense, stream=None, plane_bytes=None,
-                           consume_staging=False):
+                           consume_staging=False, early_inputs=False):
         """Fill + gather of a layer in a single launch (cpkv_compose_layer; for
         planar pages, ``plane_bytes`` and ``cur_rows_per_writer[p][w]``,
         cpkv_compose_layer_planes)."""
@@ -144,12 +147,13 @@ class ComposeLayers:
             cpkv.cpkv_compose_layer_planes(p.cur_lens, cur_rows_per_writer, table, caps, p["owner"], p["src"],
                                            p["token_writer_row"], dense, page_size=p.page_size, cp_size=p.cp_size,
                                            plane_bytes=plane_bytes, dense_cap_pages=p.dense_cap_pages,
-                                           d_status=p.d_status, consume_staging=consume_staging, stream=stream)
+                                           d_status=p.d_status, consume_staging=consume_staging,
+                                           early_inputs=early_inputs, stream=stream)
             return
         cpkv.cpkv_compose_layer(p.cur_lens, cur_rows_per_writer, table, caps, p["owner"], p["src"],
                                 p["token_writer_row"], dense, page_size=p.page_size, cp_size=p.cp_size,
                                 row_bytes=self.row_bytes, dense_cap_pages=p.dense_cap_pages, d_status=p.d_status,
-                                consume_staging=consume_staging, stream=stream)
+                                consume_staging=consume_staging, early_inputs=early_inputs, stream=stream)
 
     def compose_layer(self, layer: int, pools, cur_rows_per_writer, stream=None):
         """Fill + gather of one layer into the dense buffer of its parity."""

@@ -117,9 +117,21 @@ def test_host_errors_before_any_launch(lib):
         pba = np.array(pb, np.int32)
         rc = lib.cpkv_compose_fused_planes(1, ps, 1, n_planes, pba.ctypes.data, cl.ctypes.data,
                                            ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data,
-                                           ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data, 64, 64, 64, 4, 64, 64,
-                                           null)
+                                           ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data, 64, 64, 64, 4, 64, 0,
+                                           64, null)
         assert rc == cpkv.CPKV_ERR_ARG, (n_planes, pb, ps)
+    # unknown flag bits (and consuming, for the fused forms) are argument errors
+    tcaps = np.array([8, 3], np.int64)
+    for flags in (4, 8, -1):
+        rc = lib.cpkv_compose_layer(1, 2, 1, 64, cl.ctypes.data, ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data,
+                                    ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data, 64, 64, 64, 4, 64, flags,
+                                    64, null)
+        assert rc == cpkv.CPKV_ERR_ARG, flags
+    for flags in (cpkv.FLAG_CONSUME_STAGING, 4):
+        rc = lib.cpkv_compose_fused(1, 2, 1, 64, cl.ctypes.data, ctypes.cast(tbl, ctypes.c_void_p), tcaps.ctypes.data,
+                                    ctypes.cast(rows, ctypes.c_void_p), rcap.ctypes.data, 64, 64, 64, 4, 64, flags,
+                                    64, null)
+        assert rc == cpkv.CPKV_ERR_ARG, flags
     # ragged: bad chunk / k_align
     rc = lib.cpkv_ragged_plan_build(1, 0, 1, pl.ctypes.data, cl.ctypes.data, null, 0, null, 0, *([null] * 7), 0,
                                     null, null, null)

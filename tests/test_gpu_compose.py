@@ -250,7 +250,7 @@ def test_host_argument_errors_raise():
 # fused single-GPU compose (no staging round trip): same output as fill + gather
 # ---------------------------------------------------------------------------
 
-def _run_fused(batch, dense_extra=2, layer=0):
+def _run_fused(batch, dense_extra=2, layer=0, early=False):
     plan, want = _plan_pair(batch, dense_extra)
     layers = ComposeLayers(plan, batch.row_bytes)
     slabs = wl.host_pool(batch, layer)
@@ -259,15 +259,18 @@ def _run_fused(batch, dense_extra=2, layer=0):
     d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
     dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
                        device="cuda")
-    layers.compose_fused(d_slabs, d_rows, dense)
+    layers.compose_fused(d_slabs, d_rows, dense, early_inputs=early)
+    if early:  # a second, dependent launch right behind the first (its inputs were complete before either)
+        layers.compose_fused(d_slabs, d_rows, dense, early_inputs=True)
     torch.cuda.synchronize()
     assert int(plan.d_status.item()) == 0
     return dense.cpu().numpy(), plan, slabs, rows
 
 
+@pytest.mark.parametrize("early", [False, True], ids=["plain", "early-inputs"])
 @pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
-def test_fused_matches_oracle_edge_cases(batch):
-    dense, plan, slabs, rows = _run_fused(batch)
+def test_fused_matches_oracle_edge_cases(batch, early):
+    dense, plan, slabs, rows = _run_fused(batch, early=early)
     want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
                                 page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
     assert np.array_equal(dense, want)
@@ -326,7 +329,7 @@ def test_fused_bad_descriptor_is_zeroed_and_flagged():
 # one-launch layer compose: fill + gather in one kernel, same stagings and dense
 # ---------------------------------------------------------------------------
 
-def _run_one_launch(batch, dense_extra=2, layer=0, guard=0x5A):
+def _run_one_launch(batch, dense_extra=2, layer=0, guard=0x5A, early=False):
     plan, want_plan = _plan_pair(batch, dense_extra)
     layers = ComposeLayers(plan, batch.row_bytes)
     slabs = wl.host_pool(batch, layer)
@@ -337,7 +340,9 @@ def _run_one_launch(batch, dense_extra=2, layer=0, guard=0x5A):
         s.fill_(guard)
     dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
                        device="cuda")
-    layers.compose_one_launch(d_slabs, d_rows, dense)
+    layers.compose_one_launch(d_slabs, d_rows, dense, early_inputs=early)
+    if early:  # a second, dependent launch right behind the first (its inputs were complete before either)
+        layers.compose_one_launch(d_slabs, d_rows, dense, early_inputs=True)
     torch.cuda.synchronize()
     assert int(plan.d_status.item()) == 0
     want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
@@ -349,9 +354,10 @@ def _run_one_launch(batch, dense_extra=2, layer=0, guard=0x5A):
         assert np.array_equal(s.cpu().numpy(), want_stg[w]), w
 
 
+@pytest.mark.parametrize("early", [False, True], ids=["plain", "early-inputs"])
 @pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
-def test_one_launch_matches_oracle_edge_cases(batch):
-    _run_one_launch(batch)
+def test_one_launch_matches_oracle_edge_cases(batch, early):
+    _run_one_launch(batch, early=early)
 
 
 @pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (3, 48), (128, 1152), (64, 4096), (7, 16), (1, 16)])
@@ -550,7 +556,7 @@ def test_one_launch_consuming_staging_matches_oracle(batch):
     dense = torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
                        device="cuda")
     for _ in range(2):  # the second layer restages what the first consumed
-        layers.compose_one_launch(d_slabs, d_rows, dense, consume_staging=True)
+        layers.compose_one_launch(d_slabs, d_rows, dense, consume_staging=True, early_inputs=True)
     torch.cuda.synchronize()
     assert int(plan.d_status.item()) == 0
     want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,

@@ -114,7 +114,7 @@ def test_planar_rejects_bad_planes():
 # one-launch layer compose of planar pages: same stagings and dense buffer
 # ---------------------------------------------------------------------------
 
-def _one_launch(batch, dense_extra=1, guard=0x3C, fused=False):
+def _one_launch(batch, dense_extra=1, guard=0x3C, fused=False, early=False):
     """The one-launch layer compose (fused=False: the stagings are checked
     too) or the planar fused compose (fused=True: the stagings must keep
     their guard bytes)."""
@@ -130,10 +130,11 @@ def _one_launch(batch, dense_extra=1, guard=0x3C, fused=False):
     d_planes = [[torch.from_numpy(x).cuda() for x in pw] for pw in per_writer]
     dense = torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
     pools = [torch.from_numpy(s).cuda() for s in slabs]
-    if fused:
-        layers.compose_fused(pools, d_planes, dense, plane_bytes=list(batch.planes))
-    else:
-        layers.compose_one_launch(pools, d_planes, dense, plane_bytes=list(batch.planes))
+    for _ in range(2 if early else 1):  # early: a second, dependent launch right behind the first
+        if fused:
+            layers.compose_fused(pools, d_planes, dense, plane_bytes=list(batch.planes), early_inputs=early)
+        else:
+            layers.compose_one_launch(pools, d_planes, dense, plane_bytes=list(batch.planes), early_inputs=early)
     torch.cuda.synchronize()
     assert int(plan.d_status.item()) == 0
     want = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, planes,
@@ -151,9 +152,10 @@ def _one_launch(batch, dense_extra=1, guard=0x3C, fused=False):
         assert np.array_equal(got, want_stg[w]), w
 
 
+@pytest.mark.parametrize("early", [False, True], ids=["plain", "early-inputs"])
 @pytest.mark.parametrize("batch", _edge_planar(), ids=lambda b: b.name)
-def test_planar_one_launch_matches_oracle(batch):
-    _one_launch(batch)
+def test_planar_one_launch_matches_oracle(batch, early):
+    _one_launch(batch, early=early)
 
 
 @pytest.mark.parametrize("ps,planes", [(16, (16,)), (16, (64, 4)), (16, (4, 4, 8)), (16, (128, 4)),
@@ -198,9 +200,10 @@ def test_planar_one_launch_fuzz(seed):
 # planar fused compose (no stagings): same dense buffer, stagings untouched
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("early", [False, True], ids=["plain", "early-inputs"])
 @pytest.mark.parametrize("batch", _edge_planar(), ids=lambda b: b.name)
-def test_planar_fused_matches_oracle(batch):
-    _one_launch(batch, fused=True)
+def test_planar_fused_matches_oracle(batch, early):
+    _one_launch(batch, fused=True, early=early)
 
 
 @pytest.mark.parametrize("ps,planes", [(16, (64, 4)), (16, (4, 4, 8)), (16, (128, 4)), (16, (32, 16, 4, 12)),
