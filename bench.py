@@ -312,8 +312,10 @@ class ComposeWorkload:
         """Launch one layer's work: ``all`` of it, or one kernel of it."""
         dense = self.layers.dense[layer % 2]
         # Every input of a layer's compose (plan, pools, rows) is complete before
-        # the step's layer loop starts, and no kernel of the loop writes one, so
-        # the one-launch forms may read them early (cpkv.FLAG_EARLY_INPUTS).
+        # the step's layer loop starts (or, end to end, is joined to the layer
+        # by an event wait on its upload), and no kernel of the loop writes
+        # one, so the fills and the one-launch forms may read them early
+        # (cpkv.FLAG_EARLY_INPUTS).
         if self.variant == "fused":
             self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream,
                                       plane_bytes=list(self.batch.planes) if self.batch.planes else None,
@@ -326,9 +328,9 @@ class ComposeWorkload:
             return
         if kind in ("all", "fill"):
             if self.batch.planes:
-                self.layers.fill_planes(self.rows[layer], list(self.batch.planes), stream)
+                self.layers.fill_planes(self.rows[layer], list(self.batch.planes), stream, early_inputs=True)
             else:
-                self.layers.fill(self.rows[layer], stream)
+                self.layers.fill(self.rows[layer], stream, early_inputs=True)
         if kind in ("all", "gather"):
             self.layers.gather(self.pools_of(layer), dense, stream, consume_staging=self.consume_staging)
 
@@ -760,14 +762,15 @@ def main(argv=None):
     return 0 if (status | st0) == 0 else 3
 
 
-def run_e2e(work, a, ws):
-    """Same metric through the public API with host buffers.  Every step
-    uploads the batch metadata and all layers' current rows from pinned host
-    memory, runs the step, and reads the status word and the ragged counts
+def build_e2e(work):
+    """The end-to-end step through the public API with host buffers, as one
+    CUDA graph.  Every replay uploads the batch metadata and all layers'
+    current rows from pinned host memory (a copy of the workload's rows taken
+    now), runs the step, and reads the status word and the ragged counts
     back.  The uploads run on a copy stream, one layer at a time, and layer
-    l's compose waits only for layer l's rows, so the copies overlap the
-    compose of earlier layers.  The whole step is one CUDA graph; the host
-    synchronises on the result every step."""
+    l's compose waits (an event wait) only for layer l's rows, so the copies
+    overlap the compose of earlier layers.  Returns (one, h2d, d2h): one()
+    replays the graph, synchronises and raises on a non-zero status word."""
     torch = work.torch
     b = work.batch
     h_meta = [torch.from_numpy(np.ascontiguousarray(x, np.int32)).pin_memory()
@@ -818,6 +821,13 @@ def run_e2e(work, a, ws):
         if int(h_out[0]) != 0:
             raise RuntimeError(f"status word {int(h_out[0])}")
 
+    return one, h2d, d2h
+
+
+def run_e2e(work, a, ws):
+    """Same metric through the public API with host buffers (build_e2e);
+    the host synchronises on the result every step."""
+    one, h2d, d2h = build_e2e(work)
     for _ in range(2):
         one()
     steps = max(3, a.steps // 4)

@@ -145,6 +145,29 @@ int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
                     int32_t *d_staging_page_inverse, int64_t *d_mixed_locs, int64_t *d_staging_rows,
                     int32_t *d_token_writer_row, int32_t *d_status, cpkv_stream_t stream);
 
+/* Flags of cpkv_fill_current(_planes), cpkv_compose_layer(_planes) and
+ * cpkv_compose_fused(_planes). */
+/* The stagings are consumed, as with CPKV_GATHER_CONSUME_STAGING (layer
+ * compose only): each staged piece's L2 lines are dropped once it has been
+ * read back, and the staging bytes are undefined after the call. */
+#define CPKV_FLAG_CONSUME_STAGING 1
+/* Early inputs: the caller promises that nothing the call reads (the plan
+ * arrays, the pools, the current rows) or raises bits in (the status word) is
+ * written by the kernel launched just before it on the stream, and that
+ * every other writer of those inputs had
+ * finished before that kernel started or is joined to this call by an event
+ * wait on the stream after that kernel (an event wait stays a full
+ * dependency; in a CUDA graph it is a full edge).  The call is then launched
+ * as a programmatic dependent of the previous kernel: its CTAs may start
+ * while that kernel still runs (in SM slots it leaves free or its tail frees)
+ * and read inputs at once, and each thread waits for that kernel to complete
+ * (griddepcontrol.wait) before its first global store, so every write stays
+ * ordered after it.  In a per-layer loop whose inputs were produced before
+ * the loop this holds; directly after the kernel that writes the current
+ * rows or the plan it does not.  The fused and layer composes take the early
+ * launch only for pages of several pieces. */
+#define CPKV_FLAG_EARLY_INPUTS 2
+
 /*
  * cpkv_fill_current — per layer: write every current row into its writer's
  * staging.  In the "staging-direct compose" message this is one index copy
@@ -166,13 +189,15 @@ int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
  *                     staging_cap_pages >= C + 1
  *   d_staging_rows, d_token_writer_row: from cpkv_plan_build; d_writer [C]
  *   row_bytes         R, a multiple of 16
+ *   flags             CPKV_FLAG_EARLY_INPUTS or 0; other bits return
+ *                     CPKV_ERR_ARG
  * Status bits: ROW_OOB / WRITER_OOB (that row is skipped).
  */
 int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,
                       const void *const *h_cur_rows, const int64_t *h_cur_rows_cap,
                       void *const *h_staging, int64_t staging_cap_pages,
                       const int64_t *d_staging_rows, const int32_t *d_token_writer_row,
-                      const int32_t *d_writer, int64_t num_cur_pages, int32_t *d_status,
+                      const int32_t *d_writer, int64_t num_cur_pages, int flags, int32_t *d_status,
                       cpkv_stream_t stream);
 
 /*
@@ -199,6 +224,8 @@ int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_bytes, cons
  *                     16-byte aligned
  *   h_staging         host array [cp] of device pointers, each
  *                     [staging_cap_pages][ps * sum(plane_bytes)] bytes
+ *   flags             CPKV_FLAG_EARLY_INPUTS or 0; other bits return
+ *                     CPKV_ERR_ARG
  * The gather of planar pages is cpkv_compose_gather with
  * row_bytes = sum(plane_bytes) (pages are copied as opaque bytes).
  * Status bits: ROW_OOB / WRITER_OOB (that token is skipped).
@@ -207,7 +234,7 @@ int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n_planes, co
                              const int32_t *h_cur_lens, const void *const *h_cur_planes,
                              const int64_t *h_cur_rows_cap, void *const *h_staging, int64_t staging_cap_pages,
                              const int64_t *d_staging_rows, const int32_t *d_token_writer_row,
-                             const int32_t *d_writer, int64_t num_cur_pages, int32_t *d_status,
+                             const int32_t *d_writer, int64_t num_cur_pages, int flags, int32_t *d_status,
                              cpkv_stream_t stream);
 
 /*
@@ -263,22 +290,6 @@ int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
                               const void *const *h_src_table, const int64_t *h_src_cap_pages,
                               const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages, int kinds,
                               void *d_dense, int32_t *d_status, cpkv_stream_t stream);
-
-/* Flags of cpkv_compose_layer(_planes) and cpkv_compose_fused(_planes). */
-/* The stagings are consumed, as with CPKV_GATHER_CONSUME_STAGING (layer
- * compose only): each staged piece's L2 lines are dropped once it has been
- * read back, and the staging bytes are undefined after the call. */
-#define CPKV_FLAG_CONSUME_STAGING 1
-/* Early inputs: the caller promises that everything the call reads (the plan
- * arrays, the pools and the current rows) was complete before the previous
- * kernel on the stream started, and that nothing still running writes it.
- * The kernel is then launched as a programmatic dependent of the previous
- * kernel (for pages of several pieces): its CTAs may start in the SM slots
- * that launch's tail frees and read inputs at once, and they wait for it
- * only before their first store.  In a per-layer loop whose inputs were
- * produced before the loop this holds; directly after the kernel that writes
- * the current rows or the plan it does not. */
-#define CPKV_FLAG_EARLY_INPUTS 2
 
 /*
  * cpkv_compose_layer — per layer: cpkv_fill_current followed by

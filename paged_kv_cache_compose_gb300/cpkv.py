@@ -78,9 +78,9 @@ def _declare(lib):
     lib.cpkv_plan_sizes.argtypes = [_I, _I, _P, _P, ctypes.POINTER(_Sizes)]
     lib.cpkv_writer_token_counts.argtypes = [_I, _I, _I, _P, _P, _L, _P]
     lib.cpkv_plan_build.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _L] + [_P] * 11
-    lib.cpkv_fill_current.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
+    lib.cpkv_fill_current.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _I, _P, _P]
     lib.cpkv_compose_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P]
-    lib.cpkv_fill_current_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P, _P]
+    lib.cpkv_fill_current_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _I, _P, _P]
     lib.cpkv_compose_gather_kinds.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _I, _P, _P, _P]
     lib.cpkv_compose_layer.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P, _P]
     lib.cpkv_compose_layer_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P,
@@ -204,9 +204,9 @@ def cpkv_plan_build(prefix_lens, cur_lens, d_prefix_pages, d_cur_pages, d_writer
 
 def cpkv_fill_current(cur_lens, cur_rows: Sequence, staging: Sequence, *, page_size, cp_size, row_bytes,
                       staging_cap_pages, d_staging_rows, d_token_writer_row, d_writer, num_cur_pages,
-                      d_status, cur_rows_cap=None, stream=None):
+                      d_status, cur_rows_cap=None, early_inputs=False, stream=None):
     """Per-layer fill.  ``cur_rows[w]`` / ``staging[w]``: uint8 CUDA tensors (or raw pointers with
-    ``cur_rows_cap`` given)."""
+    ``cur_rows_cap`` given).  ``early_inputs``: FLAG_EARLY_INPUTS (its contract is the caller's)."""
     cl = _host_i32(cur_lens)
     if cur_rows_cap is None:
         cur_rows_cap = [t.numel() // row_bytes for t in cur_rows]
@@ -216,14 +216,15 @@ def cpkv_fill_current(cur_lens, cur_rows: Sequence, staging: Sequence, *, page_s
     rc = load().cpkv_fill_current(
         len(cl), page_size, cp_size, row_bytes, _hp(cl), ctypes.cast(rows_arr, _P), _hp(caps),
         ctypes.cast(stg_arr, _P), staging_cap_pages, _dp(d_staging_rows), _dp(d_token_writer_row),
-        _dp(d_writer), num_cur_pages, _dp(d_status), _stream(stream))
+        _dp(d_writer), num_cur_pages, compose_flags(early_inputs=early_inputs), _dp(d_status), _stream(stream))
     _check("cpkv_fill_current", rc)
 
 
 def cpkv_fill_current_planes(cur_lens, cur_planes: Sequence, staging: Sequence, *, page_size, cp_size, plane_bytes,
                              staging_cap_pages, d_staging_rows, d_token_writer_row, d_writer, num_cur_pages,
-                             d_status, cur_rows_cap=None, stream=None):
-    """Planar-page fill.  ``cur_planes[p][w]``: writer w's rows of plane p (uint8 CUDA tensors)."""
+                             d_status, cur_rows_cap=None, early_inputs=False, stream=None):
+    """Planar-page fill.  ``cur_planes[p][w]``: writer w's rows of plane p (uint8 CUDA tensors).
+    ``early_inputs``: FLAG_EARLY_INPUTS (its contract is the caller's)."""
     cl, pb = _host_i32(cur_lens), _host_i32(plane_bytes)
     n_planes = len(pb)
     if cur_rows_cap is None:
@@ -234,7 +235,7 @@ def cpkv_fill_current_planes(cur_lens, cur_planes: Sequence, staging: Sequence, 
     rc = load().cpkv_fill_current_planes(len(cl), page_size, cp_size, n_planes, _hp(pb), _hp(cl),
                                          ctypes.cast(flat, _P), _hp(caps), ctypes.cast(stg, _P), staging_cap_pages,
                                          _dp(d_staging_rows), _dp(d_token_writer_row), _dp(d_writer), num_cur_pages,
-                                         _dp(d_status), _stream(stream))
+                                         compose_flags(early_inputs=early_inputs), _dp(d_status), _stream(stream))
     _check("cpkv_fill_current_planes", rc)
 
 

@@ -178,6 +178,29 @@ CPKV_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "
 CPKV_DEV int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// A kernel launched with programmatic stream serialization (launch_kernel
+// with dependent = true) may start before the previous kernel on the stream
+// has finished: as soon as every CTA of that kernel has run
+// release_dependents() or exited.  wait_prerequisite() returns once the
+// previous kernel has completed and its memory writes are visible; in a
+// kernel not launched that way it returns at once.
+CPKV_DEV void release_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+CPKV_DEV void wait_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Once per thread (`open` starts false): wait_prerequisite() before the
+// thread's first global store, so that an early-launched kernel orders every
+// write after the previous kernel while its loads may run ahead.
+CPKV_DEV void store_gate(bool *open) {
+  if (!*open) {
+    wait_prerequisite();
+    *open = true;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // scans
 // ---------------------------------------------------------------------------
 template <typename T>
@@ -246,6 +269,29 @@ int persistent_grid(const void *kernel, int threads, size_t smem, int cap_per_sm
 inline int launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? CPKV_OK : CPKV_ERR_CUDA;
+}
+
+// Launch a kernel that takes one parameter block by value, as a programmatic
+// dependent of the previous kernel on `s` when `dependent` is set (see
+// release_dependents / wait_prerequisite).  CPKV_OK or CPKV_ERR_CUDA.
+template <typename Params>
+int launch_kernel(void (*kernel)(Params), dim3 grid, dim3 block, size_t smem, bool dependent, cudaStream_t s,
+                  const Params &prm) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, prm) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CPKV_ERR_CUDA;
+  }
+  return launch_status();
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

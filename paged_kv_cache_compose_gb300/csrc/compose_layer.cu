@@ -70,16 +70,10 @@ __device__ __forceinline__ void bulk_wait_complete_dyn(int64_t n) {
   }
 }
 
-// Wait, once per thread, for the previous kernel on the stream before the
-// first global store.  A no-op unless the launch is a programmatic dependent
-// (pages of several pieces, as for the fused compose: the CTAs may start in
-// the slots the previous launch's tail frees and issue loads first).
-__device__ __forceinline__ void store_gate(bool *open) {
-  if (!*open) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    *open = true;
-  }
-}
+// Every thread passes store_gate (common.cuh) before its first global store.
+// It waits only when the launch is a programmatic dependent (pages of several
+// pieces, as for the fused compose: the CTAs may start in the slots the
+// previous launch's tail frees and issue loads first).
 
 struct Readback {
   const uint8_t *src;  // staging piece
@@ -268,7 +262,7 @@ __global__ void __launch_bounds__(64, 1)
   // Row layout (one warp): the same warp does both.
   const bool copy_role = copy_warp, store_role = PLANAR ? !copy_warp : true;
   const uint64_t keep = l2_policy_evict_last();  // staging stores
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  release_dependents();
   bool stores_open = false;  // plain stores of this warp wait for the previous launch once
 
   if (copy_warp) {  // request-level exclusive scans, 32 requests per step
@@ -394,21 +388,7 @@ int launch_layer(void (*kernel)(Params), int threads, int64_t units, size_t smem
   const void *fn = reinterpret_cast<const void *>(kernel);
   if (ensure_dynamic_smem(fn, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
   const int grid = persistent_grid(fn, threads, smem, cap_per_sm, units);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kernel, prm) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return CPKV_ERR_CUDA;
-  }
-  return launch_status();
+  return launch_kernel(kernel, dim3(grid), dim3(threads), smem, dependent, s, prm);
 }
 
 // staged: h_src_table / h_src_cap_pages hold 2*cp entries (pools, then

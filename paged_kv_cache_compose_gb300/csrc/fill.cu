@@ -13,6 +13,16 @@
 // read once (L2 evict_first); staging rows are written with evict_last
 // because the gather that follows reads them back.
 //
+// With CPKV_FLAG_EARLY_INPUTS the fill is launched as a programmatic
+// dependent of the previous kernel on the stream (the previous layer's
+// gather, which releases its dependents at its start).  The fill's blocks
+// then take the SM room the gather's one-warp CTAs leave free, resolve their
+// indices and load their first rows while the gather runs, and each thread
+// waits for the gather (store_gate) before its first store: the staging the
+// fill overwrites is what that gather reads.  Measured per 78-layer traced
+// step: 4.451 -> 4.290 ms; one-token pages 5.457 -> 5.192 ms; fp8 unchanged
+// (19.99 ms).  In a plain launch the gate returns at once.
+//
 // (A variant that moves whole pages with bulk copies when a page's indices
 // form a run was slower here: each page first needs a round trip of index
 // loads, and a layer has only a few pages per CTA to overlap them with.)
@@ -84,6 +94,7 @@ __device__ void copy_rows_unrolled(const FillParams<MAXB> &p, uint64_t read_once
   const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t stride = (int64_t)p.nRow * kWarpsPerBlock * RIF;
   const int vpr = p.vpr;
+  bool stores_open = false;
   for (int64_t tb = warp_id * RIF; tb < p.T; tb += kIters * stride) {
     const int64_t tl = tb + (int64_t)(lane / RIF) * stride + (lane % RIF);
     const RowJob mine = tl < p.T ? resolve_row(p, tl) : RowJob{nullptr, nullptr};
@@ -108,6 +119,7 @@ __device__ void copy_rows_unrolled(const FillParams<MAXB> &p, uint64_t read_once
           if (job[r].src != nullptr && c < vpr) v[r][k] = ld_stream16_hint(job[r].src + 16 * (int64_t)c, read_once);
         }
       }
+      store_gate(&stores_open);
 #pragma unroll
       for (int r = 0; r < RIF; ++r) {
 #pragma unroll
@@ -126,9 +138,11 @@ __device__ void copy_rows_wide(const FillParams<MAXB> &p, uint64_t read_once, ui
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)p.nRow * kWarpsPerBlock;
+  bool stores_open = false;
   for (int64_t t = warp_id; t < p.T; t += nwarps) {
     const RowJob job = resolve_row(p, t);
     if (job.src == nullptr) continue;
+    store_gate(&stores_open);
     for (int c = lane; c < p.vpr; c += 32)
       st16_hint(job.dst + 16 * (int64_t)c, ld_stream16_hint(job.src + 16 * (int64_t)c, read_once), keep);
   }
@@ -158,6 +172,7 @@ __device__ void zero_pad_rows(const FillParams<MAXB> &p, int b) {
     if (threadIdx.x == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
     return;
   }
+  wait_prerequisite();
   const int64_t first = sr + 1, end = (slot + 1) * p.ps;  // [first, end) rows to zero
   uint8_t *base = p.staging[w] + first * p.R;
   const int64_t nvec = (end - first) * p.vpr;
@@ -180,13 +195,14 @@ __global__ void __launch_bounds__(kFillThreads, kBlocksPerSm) fill_current_kerne
 }
 
 template <int MAXB>
-int launch_fill(const FillParams<MAXB> &prm, int grid, cudaStream_t s) {
-  if (prm.vpr <= 32) fill_current_kernel<MAXB, 4, 1><<<grid, kFillThreads, 0, s>>>(prm);
-  else if (prm.vpr <= 64) fill_current_kernel<MAXB, 4, 2><<<grid, kFillThreads, 0, s>>>(prm);
-  else if (prm.vpr <= 96) fill_current_kernel<MAXB, 2, 3><<<grid, kFillThreads, 0, s>>>(prm);
-  else if (prm.vpr <= 128) fill_current_kernel<MAXB, 2, 4><<<grid, kFillThreads, 0, s>>>(prm);
-  else fill_current_kernel<MAXB, 0, 0><<<grid, kFillThreads, 0, s>>>(prm);
-  return launch_status();
+int launch_fill(const FillParams<MAXB> &prm, int grid, bool early, cudaStream_t s) {
+  void (*kernel)(FillParams<MAXB>);
+  if (prm.vpr <= 32) kernel = fill_current_kernel<MAXB, 4, 1>;
+  else if (prm.vpr <= 64) kernel = fill_current_kernel<MAXB, 4, 2>;
+  else if (prm.vpr <= 96) kernel = fill_current_kernel<MAXB, 2, 3>;
+  else if (prm.vpr <= 128) kernel = fill_current_kernel<MAXB, 2, 4>;
+  else kernel = fill_current_kernel<MAXB, 0, 0>;
+  return launch_kernel(kernel, dim3(grid), dim3(kFillThreads), 0, early, s, prm);
 }
 
 }  // namespace
@@ -197,9 +213,11 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
                                  const int64_t *h_cur_rows_cap, void *const *h_staging,
                                  int64_t staging_cap_pages, const int64_t *d_staging_rows,
                                  const int32_t *d_token_writer_row, const int32_t *d_writer,
-                                 int64_t num_cur_pages, int32_t *d_status, cpkv_stream_t stream) {
+                                 int64_t num_cur_pages, int flags, int32_t *d_status, cpkv_stream_t stream) {
   using namespace cpkv;
   if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
+  if ((flags & ~CPKV_FLAG_EARLY_INPUTS) != 0) return CPKV_ERR_ARG;
+  const bool early = (flags & CPKV_FLAG_EARLY_INPUTS) != 0;
   if (row_bytes <= 0 || row_bytes % 16 != 0) return CPKV_ERR_ARG;
   if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
   if (h_cur_rows == nullptr || h_cur_rows_cap == nullptr || h_staging == nullptr || d_status == nullptr)
@@ -244,10 +262,10 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
   if (B <= 64) {
     FillParams<64> prm;
     CPKV_FILL_FILL(prm)
-    return launch_fill(prm, nRow + B, s);
+    return launch_fill(prm, nRow + B, early, s);
   }
   FillParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_FILL(prm)
 #undef CPKV_FILL_FILL
-  return launch_fill(prm, nRow + B, s);
+  return launch_fill(prm, nRow + B, early, s);
 }

@@ -20,6 +20,11 @@
 // (token, unit) with consecutive threads on consecutive units, so a warp
 // reads and writes contiguous bytes (a unit is 16 bytes when the plane allows
 // it, else 4).  Blocks [nTile, nTile + B) zero the pad slices.
+//
+// With CPKV_FLAG_EARLY_INPUTS the fill is launched as a programmatic
+// dependent of the previous kernel on the stream (the previous layer's
+// gather) and each thread waits for it (store_gate) before its first store,
+// as in cpkv_fill_current.
 #include <stdint.h>
 
 #include "common.cuh"
@@ -46,7 +51,7 @@ struct PlaneParams {
 };
 
 template <int MAXB>
-__device__ void copy_tile(const PlaneParams<MAXB> &p, int64_t t0) {
+__device__ void copy_tile(const PlaneParams<MAXB> &p, int64_t t0, bool *stores_open) {
   __shared__ uint8_t *dst_page[kThreads];  // staging page base of each token (nullptr: skip)
   __shared__ int32_t dst_off[kThreads];    // token slot inside the page
   __shared__ int32_t src_row[kThreads];
@@ -103,6 +108,7 @@ __device__ void copy_tile(const PlaneParams<MAXB> &p, int64_t t0) {
           }
         }
       }
+      store_gate(stores_open);
 #pragma unroll
       for (int r = 0; r < kUnroll; ++r) {
         if (dst[r] == nullptr) continue;
@@ -137,6 +143,7 @@ __device__ void zero_pad(const PlaneParams<MAXB> &p, int b) {
     if (threadIdx.x == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
     return;
   }
+  wait_prerequisite();
   uint8_t *page = p.staging[w] + slot * p.page_bytes;
   const int64_t first = sr - slot * p.ps + 1;  // first pad token slot
   for (int pl = 0; pl < p.n_planes; ++pl) {
@@ -149,8 +156,9 @@ __device__ void zero_pad(const PlaneParams<MAXB> &p, int b) {
 template <int MAXB>
 __global__ void __launch_bounds__(kThreads) fill_planes_kernel(const __grid_constant__ PlaneParams<MAXB> p) {
   if ((int)blockIdx.x < p.nTile) {
+    bool stores_open = false;
     for (int64_t t0 = (int64_t)blockIdx.x * kThreads; t0 < p.T; t0 += (int64_t)p.nTile * kThreads) {
-      copy_tile(p, t0);
+      copy_tile(p, t0, &stores_open);
       __syncthreads();  // the tile's shared indices are reused by the next tile
     }
   } else {
@@ -166,9 +174,12 @@ extern "C" int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n
                                         const int64_t *h_cur_rows_cap, void *const *h_staging,
                                         int64_t staging_cap_pages, const int64_t *d_staging_rows,
                                         const int32_t *d_token_writer_row, const int32_t *d_writer,
-                                        int64_t num_cur_pages, int32_t *d_status, cpkv_stream_t stream) {
+                                        int64_t num_cur_pages, int flags, int32_t *d_status,
+                                        cpkv_stream_t stream) {
   using namespace cpkv;
   if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
+  if ((flags & ~CPKV_FLAG_EARLY_INPUTS) != 0) return CPKV_ERR_ARG;
+  const bool early = (flags & CPKV_FLAG_EARLY_INPUTS) != 0;
   if (n_planes < 1 || n_planes > kMaxPlanes || h_plane_bytes == nullptr) return CPKV_ERR_ARG;
   if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
   if (h_cur_planes == nullptr || h_cur_rows_cap == nullptr || h_staging == nullptr || d_status == nullptr)
@@ -234,12 +245,10 @@ extern "C" int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n
   if (B <= 64) {
     PlaneParams<64> prm;
     CPKV_FILL_PLANES(prm)
-    fill_planes_kernel<64><<<nTile + B, kThreads, 0, s>>>(prm);
-    return launch_status();
+    return launch_kernel(fill_planes_kernel<64>, dim3(nTile + B), dim3(kThreads), 0, early, s, prm);
   }
   PlaneParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_PLANES(prm)
 #undef CPKV_FILL_PLANES
-  fill_planes_kernel<CPKV_MAX_BATCH><<<nTile + B, kThreads, 0, s>>>(prm);
-  return launch_status();
+  return launch_kernel(fill_planes_kernel<CPKV_MAX_BATCH>, dim3(nTile + B), dim3(kThreads), 0, early, s, prm);
 }

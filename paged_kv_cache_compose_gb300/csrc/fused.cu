@@ -35,22 +35,13 @@ constexpr int kMaxCtasPerSm = 3;  // one-warp CTAs per SM, at most; fewer when t
 // With CPKV_FLAG_EARLY_INPUTS and pages of several pieces, the kernel is
 // launched as a programmatic dependent of the previous kernel on the stream:
 // its CTAs may start in SM slots that the previous launch's tail frees, read
-// their inputs at once, and wait for that launch (griddepcontrol.wait) only
-// before their first global store.  Measured per 78-layer step: traced
+// their inputs at once, and wait for that launch (store_gate) only before
+// their first global store.  Measured per 78-layer step: traced
 // 4.045 -> 3.807 ms, fp8 17.99 -> 17.64 ms; waiting before the first load
 // instead kept only 4.045 -> 3.993 ms.  Pages of one piece run many small
 // CTAs per SM, where the next launch's CTAs would sit beside the current ones
 // from the start (one-token pages: 4.27 -> 4.70 ms), so they launch plainly.
 // In a plain launch the waits return at once.
-
-// Wait, once, for the previous kernel on the stream (programmatic dependent
-// launch) before the first global store (warp-uniform).
-__device__ __forceinline__ void store_gate(bool *open) {
-  if (!*open) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    *open = true;
-  }
-}
 constexpr int kMaxPieceBytes = 24 * 1024;
 
 template <int MAXB>
@@ -77,8 +68,8 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
   __shared__ int32_t cur_page_start[MAXB + 1];  // first batch current page of request b
   __shared__ int64_t token_start[MAXB + 1];     // first batch token of request b
   const int lane = threadIdx.x;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  bool stores_open = false;
+  release_dependents();
+  bool stores_open = false;  // store_gate: warp-uniform here
 
   // request-level exclusive scans, 32 requests per step
   {
@@ -181,21 +172,7 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
 template <typename Params>
 int launch_fused(void (*kernel)(Params), int grid, size_t smem, bool dependent, cudaStream_t s,
                  const Params &prm) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(32);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kernel, prm) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return CPKV_ERR_CUDA;
-  }
-  return launch_status();
+  return launch_kernel(kernel, dim3(grid), dim3(32), smem, dependent, s, prm);
 }
 
 }  // namespace

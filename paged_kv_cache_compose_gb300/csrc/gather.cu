@@ -87,6 +87,9 @@ __device__ __forceinline__ Unit resolve_unit(const GatherParams &p, int64_t u, i
 // loaded its L2 lines are dropped without write-back.
 template <bool kConsume>
 __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant__ GatherParams p) {
+  // A fill launched after this gather with CPKV_FLAG_EARLY_INPUTS may start
+  // its loads now; its stores wait for this kernel to complete.
+  release_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ uint8_t *ring_dst[kStages];

@@ -43,7 +43,7 @@ __global__ void plan_init_inverses(int32_t *__restrict__ pi, int32_t *__restrict
                                    bool vec) {
   // plan_main may start now: it waits for this grid only before its first
   // access to the inverses.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  release_dependents();
   const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if (vec) {
@@ -161,7 +161,7 @@ __device__ void plan_dense_slots(const PlanParams<MAXB> &p, const RequestScan &r
     const int32_t i = is_prefix ? 0 : rs.cur_page_start[b] + (k - npp);
     const int32_t lp = is_prefix ? p.prefix_pages[rs.prefix_page_start[b] + k] : p.cur_pages[i];
     const int32_t w = is_prefix ? 0 : p.writer[i];
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    wait_prerequisite();
     if (is_prefix) {
       if (lp < 1 || lp >= p.P) {
         raise_status(p.status, CPKV_STATUS_PAGE_OOB);
@@ -288,26 +288,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_main(const __grid_constant_
 
 // plan_main is a programmatic dependent of plan_init_inverses: its request
 // scans, page-table loads, descriptors and token arrays overlap the init;
-// only the inverse scatters wait for it (griddepcontrol.wait).
+// only the inverse scatters wait for it (wait_prerequisite).
 template <int MAXB>
 int launch_plan(const PlanParams<MAXB> &prm, int nB, cudaStream_t s) {
   const int grid = prm.nA + nB;
   if (grid == 0) return CPKV_OK;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kPlanThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, plan_main<MAXB>, prm) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return CPKV_ERR_CUDA;
-  }
-  return launch_status();
+  return launch_kernel(plan_main<MAXB>, dim3(grid), dim3(kPlanThreads), 0, true, s, prm);
 }
 
 template <int MAXB>

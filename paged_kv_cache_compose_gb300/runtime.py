@@ -66,14 +66,17 @@ class ComposeLayers:
         self.dense = [torch.empty((plan.dense_cap_pages * ps, row_bytes), dtype=torch.uint8, device=plan.device)
                       for _ in range(num_dense)]
 
-    def fill(self, cur_rows_per_writer, stream=None):
+    def fill(self, cur_rows_per_writer, stream=None, early_inputs=False):
+        """``early_inputs``: the rows and the plan were complete before the
+        previous kernel on the stream started (cpkv.FLAG_EARLY_INPUTS)."""
         p = self.plan
         cpkv.cpkv_fill_current(p.cur_lens, cur_rows_per_writer, self.staging, page_size=p.page_size,
                                cp_size=p.cp_size, row_bytes=self.row_bytes, staging_cap_pages=p.staging_cap_pages,
                                d_staging_rows=p["staging_rows"], d_token_writer_row=p["token_writer_row"],
-                               d_writer=p.d_writer, num_cur_pages=p.C, d_status=p.d_status, stream=stream)
+                               d_writer=p.d_writer, num_cur_pages=p.C, d_status=p.d_status,
+                               early_inputs=early_inputs, stream=stream)
 
-    def fill_planes(self, cur_planes_per_writer, plane_bytes, stream=None):
+    def fill_planes(self, cur_planes_per_writer, plane_bytes, stream=None, early_inputs=False):
         """Planar-page fill (``cur_planes_per_writer[p][w]``); the row width of
         these buffers must be ``sum(plane_bytes)``."""
         p = self.plan
@@ -81,7 +84,8 @@ class ComposeLayers:
                                       cp_size=p.cp_size, plane_bytes=plane_bytes,
                                       staging_cap_pages=p.staging_cap_pages, d_staging_rows=p["staging_rows"],
                                       d_token_writer_row=p["token_writer_row"], d_writer=p.d_writer,
-                                      num_cur_pages=p.C, d_status=p.d_status, stream=stream)
+                                      num_cur_pages=p.C, d_status=p.d_status, early_inputs=early_inputs,
+                                      stream=stream)
 
     def gather(self, pools, dense, stream=None, consume_staging=False):
         """``pools``: the cp owner slabs [slab_pages, ps, R] of this layer.

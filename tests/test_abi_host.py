@@ -86,8 +86,23 @@ def test_host_errors_before_any_launch(lib):
     rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
     assert rc == cpkv.CPKV_ERR_ARG
     # fill: row width must be a multiple of 16
-    rc = lib.cpkv_fill_current(1, 2, 1, 100, cl.ctypes.data, *([null] * 3), 5, *([null] * 3), 2, null, null)
+    rc = lib.cpkv_fill_current(1, 2, 1, 100, cl.ctypes.data, *([null] * 3), 5, *([null] * 3), 2, 0, null, null)
     assert rc == cpkv.CPKV_ERR_ARG
+    # fill flags: an empty batch returns before any launch, so only the flag word decides
+    empty = np.zeros(1, np.int32)
+    fake = (ctypes.c_void_p * 1)(16)  # never dereferenced: nothing to copy
+    zero_cap = np.zeros(1, np.int64)
+    pb = np.array([16], np.int32)
+    for flags, want in ((0, cpkv.CPKV_OK), (cpkv.FLAG_EARLY_INPUTS, cpkv.CPKV_OK), (cpkv.FLAG_CONSUME_STAGING, cpkv.CPKV_ERR_ARG),
+                        (4, cpkv.CPKV_ERR_ARG), (-1, cpkv.CPKV_ERR_ARG)):
+        rc = lib.cpkv_fill_current(1, 2, 1, 64, empty.ctypes.data, ctypes.cast(fake, ctypes.c_void_p),
+                                   zero_cap.ctypes.data, ctypes.cast(fake, ctypes.c_void_p), 1, null, null, null, 0,
+                                   flags, 64, null)
+        assert rc == want, ("fill", flags)
+        rc = lib.cpkv_fill_current_planes(1, 2, 1, 1, pb.ctypes.data, empty.ctypes.data,
+                                          ctypes.cast(fake, ctypes.c_void_p), zero_cap.ctypes.data,
+                                          ctypes.cast(fake, ctypes.c_void_p), 1, null, null, null, 0, flags, 64, null)
+        assert rc == want, ("fill_planes", flags)
     # gather: unaligned dense pointer
     tbl = (ctypes.c_void_p * 2)(16, 32)
     caps = np.array([1, 1], np.int64)

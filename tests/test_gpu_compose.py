@@ -565,6 +565,45 @@ def test_one_launch_consuming_staging_matches_oracle(batch):
 
 
 # ---------------------------------------------------------------------------
+# fill launched early behind the previous layer's gather (FLAG_EARLY_INPUTS)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("consume", [False, True], ids=["kept", "consumed"])
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_fill_early_behind_gather_matches_oracle(batch, consume):
+    """Three layers of distinct rows and pools, uploaded before the loop; each
+    fill starts while the previous layer's gather still reads the stagings it
+    overwrites.  Every layer has its own dense buffer and is checked, so a
+    store that ran ahead of that gather would show in the earlier layer."""
+    n_layers = 3
+    plan, _ = _plan_pair(batch, dense_extra=1)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    for s in layers.staging:
+        s.fill_(0xA5)
+    host = [(wl.host_pool(batch, l), wl.host_current_rows(batch, l)) for l in range(n_layers)]
+    dev = [([torch.from_numpy(s).cuda() for s in slabs],
+            [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]) for slabs, rows in host]
+    dense = [torch.full((plan.dense_cap_pages * batch.page_size, batch.row_bytes), 0xCD, dtype=torch.uint8,
+                        device="cuda") for _ in range(n_layers)]
+    torch.cuda.synchronize()
+    for l in range(n_layers):
+        layers.fill(dev[l][1], early_inputs=True)
+        layers.gather(dev[l][0], dense[l], consume_staging=consume)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    for l, (slabs, rows) in enumerate(host):
+        want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                    page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+        assert np.array_equal(dense[l].cpu().numpy(), want), l
+    if not consume:
+        stg_want = [np.full(tuple(s.shape), 0xA5, np.uint8) for s in layers.staging]
+        oracle.staging(batch.cur_lens, batch.writer, host[-1][1], stg_want, page_size=batch.page_size,
+                       cp_size=batch.cp_size)
+        for w, s in enumerate(layers.staging):
+            assert np.array_equal(s.cpu().numpy(), stg_want[w]), w
+
+
+# ---------------------------------------------------------------------------
 # failure detection on the GPU without a fault: a copy that never lands
 # ---------------------------------------------------------------------------
 

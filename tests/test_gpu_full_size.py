@@ -110,6 +110,31 @@ def test_benchmark_workload_matches_oracle(config, variant):
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("variant", ["staging", "fused", "layer"])
+def test_end_to_end_graph_matches_oracle(variant):
+    """The end-to-end step (rows uploaded from pinned host memory on a copy
+    stream, each layer joined to its upload by an event wait, fills and
+    one-launch composes launched early behind the previous kernel).  The
+    device rows are poisoned first, so a compose that read its rows before
+    their upload landed would differ from the oracle."""
+    work = bench.ComposeWorkload("traced_78", variant=variant, consume_staging=variant != "fused")
+    try:
+        one, h2d, d2h = bench.build_e2e(work)
+        assert h2d >= work.rows_all.numel() and d2h == 20
+        work.rows_all.fill_(0xEE)
+        for d in work.layers.dense:
+            d.fill_(0xCD)
+        one()
+        assert work.status() == 0
+        _check_plan(work)
+        _check_layer(work, work.num_layers - 2)
+        _check_layer(work, work.num_layers - 1)
+    finally:
+        del work
+        gc.collect()
+        torch.cuda.empty_cache()
+
+
 def test_traced_single_layer_full_pool():
     """The traced batch against its 200 000-page pool (one layer)."""
     from paged_kv_cache_compose_gb300.runtime import ComposeLayers, ComposePlan

@@ -83,6 +83,32 @@ def test_planar_compose_matches_oracle(batch):
     assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, batch.page_size * batch.row_bytes), want)
 
 
+@pytest.mark.parametrize("batch", _edge_planar(), ids=lambda b: b.name)
+def test_planar_fill_early_behind_gather(batch):
+    """Three layers of distinct planar rows and pools, uploaded first; each
+    planar fill starts while the previous gather still reads the stagings.
+    Every layer has its own dense buffer and is checked."""
+    ps, cp, n_layers = batch.page_size, batch.cp_size, 3
+    plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                       page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages, dense_cap_pages=None).build()
+    layers = ComposeLayers(plan, batch.row_bytes)
+    host = [_inputs(batch, seed=l) for l in range(n_layers)]
+    dev = [([torch.from_numpy(s).cuda() for s in slabs], [[torch.from_numpy(x).cuda() for x in pw] for pw in per_writer])
+           for slabs, _, per_writer in host]
+    dense = [torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
+             for _ in range(n_layers)]
+    torch.cuda.synchronize()
+    for l in range(n_layers):
+        layers.fill_planes(dev[l][1], list(batch.planes), early_inputs=True)
+        layers.gather(dev[l][0], dense[l])
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    for l, (slabs, planes, _) in enumerate(host):
+        want = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, planes,
+                                           page_size=ps, cp_size=cp, plane_bytes=list(batch.planes))
+        assert np.array_equal(dense[l].cpu().numpy().reshape(plan.dense_cap_pages, ps * batch.row_bytes), want), l
+
+
 @pytest.mark.parametrize("batch", _edge_planar()[:4], ids=lambda b: b.name)
 def test_planar_fill_reversed_rows(batch):
     _compose(batch, reverse_rows=True)
