@@ -36,6 +36,7 @@ import workloads as wl  # noqa: E402
 
 METRIC = "compose GB/s and % of HBM peak; ms per 78-layer compose at bs=12/44.6K tokens"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (reported beside the measured or fallback peak)
 
 
 # ---------------------------------------------------------------------------
@@ -700,6 +701,7 @@ def main(argv=None):
                               "max": round(step_ms[-1], 4), "steps_timed": len(step_ms)},
         "ms_per_78_layer_compose": round(ms_step * 78 / work.num_layers, 4),
         "pct_of_hbm_peak": round(100 * value_gbs / ws / hbm_peak, 2),
+        "pct_of_nominal_hbm": round(100 * value_gbs / ws / NOMINAL_HBM_GBS, 2),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
