@@ -252,6 +252,9 @@ int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n_planes, co
  * dense page d <- page d_src[d] of table[d_owner[d]] (ps*R contiguous bytes);
  * owner -1 -> zeros.  A descriptor outside the table or the source's capacity
  * raises DESC_OOB and its page is zero-filled.
+ * The gather releases its programmatic dependents when it starts: a kernel
+ * launched after it with CPKV_FLAG_EARLY_INPUTS (the next layer's fill) may
+ * start while it runs and waits for it before storing.
  */
 int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
                         const void *const *h_src_table, const int64_t *h_src_cap_pages,
