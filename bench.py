@@ -315,25 +315,29 @@ class ComposeWorkload:
         # Every input of a layer's compose (plan, pools, rows) is complete before
         # the step's layer loop starts (or, end to end, is joined to the layer
         # by an event wait on its upload), and no kernel of the loop writes
-        # one, so the fills and the one-launch forms may read them early
-        # (cpkv.FLAG_EARLY_INPUTS).
+        # one, so the step launches its kernels early behind the previous one
+        # (cpkv.FLAG_EARLY_INPUTS, cpkv.GATHER_EARLY_INPUTS).  The graphs that
+        # time one kind of kernel alone launch plainly, so that their launches
+        # never overlap and each one's duration is measured whole.
+        early = kind == "all"
         if self.variant == "fused":
             self.layers.compose_fused(self.pools_of(layer), self.rows[layer], dense, stream,
                                       plane_bytes=list(self.batch.planes) if self.batch.planes else None,
-                                      early_inputs=True)
+                                      early_inputs=early)
             return
         if self.variant == "layer":
             self.layers.compose_one_launch(self.pools_of(layer), self.rows[layer], dense, stream,
                                            plane_bytes=list(self.batch.planes) if self.batch.planes else None,
-                                           consume_staging=self.consume_staging, early_inputs=True)
+                                           consume_staging=self.consume_staging, early_inputs=early)
             return
         if kind in ("all", "fill"):
             if self.batch.planes:
-                self.layers.fill_planes(self.rows[layer], list(self.batch.planes), stream, early_inputs=True)
+                self.layers.fill_planes(self.rows[layer], list(self.batch.planes), stream, early_inputs=early)
             else:
-                self.layers.fill(self.rows[layer], stream, early_inputs=True)
+                self.layers.fill(self.rows[layer], stream, early_inputs=early)
         if kind in ("all", "gather"):
-            self.layers.gather(self.pools_of(layer), dense, stream, consume_staging=self.consume_staging)
+            self.layers.gather(self.pools_of(layer), dense, stream, consume_staging=self.consume_staging,
+                               early_inputs=early)
 
     def kernel_graphs(self):
         """Two more CUDA graphs: the step's fills alone and its gathers alone
@@ -664,7 +668,8 @@ def main(argv=None):
         k1.record()
         torch.cuda.synchronize()
         kern[kind] = k0.elapsed_time(k1) / (reps * work.num_layers)
-    kernel_timing = "alone: a CUDA graph of the step's launches of that kernel only, replayed"
+    kernel_timing = ("alone: a CUDA graph of the step's launches of that kernel only, replayed, launched plainly "
+                     "(in the step they launch early behind the previous kernel; here launches never overlap)")
     if work.consume_staging and work.variant == "staging":
         kernel_timing += (" (the gather consumes the stagings, so when replayed alone it reads them from DRAM: "
                           "all its algorithmic bytes cross DRAM; inside the step they are read from L2)")

@@ -275,6 +275,18 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
  * cpkv_plan_build name each staging slot once); a second read of a consumed
  * page would see undefined bytes. */
 #define CPKV_GATHER_CONSUME_STAGING 8
+/* Flag for cpkv_compose_gather_kinds: early inputs, as CPKV_FLAG_EARLY_INPUTS
+ * but for the gather behind its fill.  The caller promises that the plan
+ * arrays and the pools were complete before the previous kernel on the
+ * stream started and that nothing still running writes them; that previous
+ * kernel may write the stagings (the fill).  For pages of several pieces the
+ * gather is then launched as a programmatic dependent of that kernel (the
+ * fills release their dependents when they finish): its CTAs may start as
+ * the fill's blocks retire and load descriptors and pool pages at once, and
+ * each waits for the previous kernel to complete (griddepcontrol.wait) before
+ * its first staging load and before its first store.  Pages of one piece are
+ * launched plainly. */
+#define CPKV_GATHER_EARLY_INPUTS 16
 
 /*
  * cpkv_compose_gather_kinds — the gather restricted to some slot kinds;
@@ -286,7 +298,8 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
  * is then the fill followed by the current pages only
  * (kinds = CPKV_GATHER_STAGING).  The two calls together write exactly what
  * one cpkv_compose_gather writes.  kinds may also carry
- * CPKV_GATHER_CONSUME_STAGING; any other value returns CPKV_ERR_ARG.  Other
+ * CPKV_GATHER_CONSUME_STAGING and CPKV_GATHER_EARLY_INPUTS; any other value
+ * returns CPKV_ERR_ARG.  Other
  * arguments as cpkv_compose_gather.
  */
 int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,

@@ -39,6 +39,7 @@ GATHER_STAGING = 2
 GATHER_ZERO = 4
 GATHER_ALL = 7
 GATHER_CONSUME_STAGING = 8  # flag: staging bytes are undefined after the gather (L2 lines dropped)
+GATHER_EARLY_INPUTS = 16  # flag: launched early behind the fill (its contract is the caller's)
 FLAG_CONSUME_STAGING = 1    # layer compose: the stagings are consumed
 FLAG_EARLY_INPUTS = 2       # layer / fused compose: inputs complete before the previous kernel started
 

@@ -21,7 +21,9 @@
 // waits for the gather (store_gate) before its first store: the staging the
 // fill overwrites is what that gather reads.  Measured per 78-layer traced
 // step: 4.451 -> 4.290 ms; one-token pages 5.457 -> 5.192 ms; fp8 unchanged
-// (19.99 ms).  In a plain launch the gate returns at once.
+// (19.99 ms).  In a plain launch the gate returns at once.  The fill itself
+// releases its dependents as each block finishes, for a gather launched with
+// CPKV_GATHER_EARLY_INPUTS.
 //
 // (A variant that moves whole pages with bulk copies when a page's indices
 // form a run was slower here: each page first needs a round trip of index
@@ -192,6 +194,9 @@ __global__ void __launch_bounds__(kFillThreads, kBlocksPerSm) fill_current_kerne
   } else {
     zero_pad_rows(p, blockIdx.x - p.nRow);
   }
+  // the gather of these stagings (CPKV_GATHER_EARLY_INPUTS) may launch once
+  // every block is here; it waits for this kernel before reading a staging
+  release_dependents();
 }
 
 template <int MAXB>

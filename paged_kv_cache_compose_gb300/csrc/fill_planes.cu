@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(kThreads) fill_planes_kernel(const __grid_cons
   } else {
     zero_pad(p, blockIdx.x - p.nTile);
   }
+  release_dependents();  // as in cpkv_fill_current
 }
 
 }  // namespace

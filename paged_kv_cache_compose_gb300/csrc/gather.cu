@@ -23,6 +23,17 @@
 // stagings are consumed: once a staging piece has landed in shared memory
 // its L2 lines are dropped, so the fill's dirty staging lines are never
 // written back to DRAM.
+//
+// With CPKV_GATHER_EARLY_INPUTS and pages of several pieces the gather is
+// launched as a programmatic dependent of the previous kernel (its fill, which
+// releases its dependents as its blocks finish).  Its CTAs start as the
+// fill's blocks retire, load descriptors and pool pieces at once, and each
+// waits for the fill (store_gate) before its first staging load and before
+// its first store.  Measured per 78-layer traced step: 4.284 -> 4.200 ms;
+// fp8 unchanged (19.77 ms); one-token pages, where the ring runs many small
+// CTAs per SM, 5.195 -> 5.555 ms, so pages of one piece launch plainly.
+// The gather itself releases its dependents at its start (the next layer's
+// fill, launched with CPKV_FLAG_EARLY_INPUTS, may start while it runs).
 #include <stdint.h>
 
 #include "bulk_ring.cuh"
@@ -103,6 +114,7 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
   // no copy waits on a descriptor load of its own.
   const int lane = threadIdx.x;
   const int64_t step = gridDim.x;
+  bool open = false;  // store_gate: warp-uniform here
   for (int64_t base = blockIdx.x; base < p.units; base += 32 * step) {
     const int64_t mine = base + lane * step;
     int32_t my_o = -1, my_s = 0;
@@ -118,10 +130,14 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
       bool skip;
       const Unit x = resolve_unit(p, u, o, sr, lane == 0, &skip);
       if (skip) continue;
+      // staging loads and stores (a zero unit, or a push that stores the
+      // oldest stage) wait for the previous kernel when launched early
+      if (x.src == nullptr || o >= p.n_pool || ring.tail - ring.head == kLoadsInFlight) store_gate(&open);
       if (x.src == nullptr) warp_zero(x.dst, x.bytes);
       else ring.push(x.src, x.dst, x.bytes, kConsume && o >= p.n_pool);
     }
   }
+  store_gate(&open);
   ring.drain();
 }
 
@@ -133,8 +149,10 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
                                          const int32_t *d_owner, const int32_t *d_src, int64_t dense_cap_pages,
                                          int kinds, void *d_dense, int32_t *d_status, cpkv_stream_t stream) {
   using namespace cpkv;
-  if (kinds < 0 || kinds > (CPKV_GATHER_ALL | CPKV_GATHER_CONSUME_STAGING)) return CPKV_ERR_ARG;
+  if (kinds < 0 || kinds > (CPKV_GATHER_ALL | CPKV_GATHER_CONSUME_STAGING | CPKV_GATHER_EARLY_INPUTS))
+    return CPKV_ERR_ARG;
   const bool consume = (kinds & CPKV_GATHER_CONSUME_STAGING) != 0;
+  const bool early = (kinds & CPKV_GATHER_EARLY_INPUTS) != 0;
   kinds &= CPKV_GATHER_ALL;
   if (page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
   if (row_bytes <= 0 || ((int64_t)page_size * row_bytes) % 16 != 0 || dense_cap_pages < 0) return CPKV_ERR_ARG;
@@ -179,9 +197,9 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
                                  : ring_cap_one_piece(piece_bytes, kLoadsInFlight, kMaxCtasPerSmOnePiece),
                       prm.units);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (consume) gather_pages_kernel<true><<<grid, 32, smem, s>>>(prm);
-  else gather_pages_kernel<false><<<grid, 32, smem, s>>>(prm);
-  return launch_status();
+  const bool dependent = early && pieces > 1;
+  if (consume) return launch_kernel(gather_pages_kernel<true>, dim3(grid), dim3(32), smem, dependent, s, prm);
+  return launch_kernel(gather_pages_kernel<false>, dim3(grid), dim3(32), smem, dependent, s, prm);
 }
 
 extern "C" int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,

@@ -87,13 +87,16 @@ class ComposeLayers:
                                       num_cur_pages=p.C, d_status=p.d_status, early_inputs=early_inputs,
                                       stream=stream)
 
-    def gather(self, pools, dense, stream=None, consume_staging=False):
+    def gather(self, pools, dense, stream=None, consume_staging=False, early_inputs=False):
         """``pools``: the cp owner slabs [slab_pages, ps, R] of this layer.
         ``consume_staging``: the stagings are refilled before their next read,
         so their L2 lines are dropped after the gather reads them (their bytes
-        are undefined afterwards)."""
-        if consume_staging:
-            self.gather_kinds(pools, dense, cpkv.GATHER_ALL | cpkv.GATHER_CONSUME_STAGING, stream)
+        are undefined afterwards).  ``early_inputs``: the plan and the pools
+        were complete before the previous kernel on the stream (the fill)
+        started (cpkv.GATHER_EARLY_INPUTS)."""
+        if consume_staging or early_inputs:
+            kinds = cpkv.GATHER_ALL | (cpkv.GATHER_CONSUME_STAGING if consume_staging else 0)
+            self.gather_kinds(pools, dense, kinds | (cpkv.GATHER_EARLY_INPUTS if early_inputs else 0), stream)
             return
         p = self.plan
         table = list(pools) + list(self.staging)

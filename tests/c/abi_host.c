@@ -57,7 +57,7 @@ int main(void) {
         "plan_build: dense capacity below D rejected");
   CHECK(cpkv_fill_current(2, 4, 2, 100, cur, NULL, NULL, NULL, 4, NULL, NULL, NULL, 3, 0, NULL, 0) == CPKV_ERR_ARG,
         "fill_current: row width not a multiple of 16 rejected");
-  CHECK(cpkv_compose_gather_kinds(4, 1, 16, NULL, NULL, NULL, NULL, 1, 9, NULL, NULL, 0) == CPKV_ERR_ARG,
+  CHECK(cpkv_compose_gather_kinds(4, 1, 16, NULL, NULL, NULL, NULL, 1, 32, NULL, NULL, 0) == CPKV_ERR_ARG,
         "gather_kinds: bad kind mask rejected");
   CHECK(cpkv_compose_layer(2, 4, 2, 16, cur, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 4, NULL, 0, NULL, 0) ==
             CPKV_ERR_ARG,

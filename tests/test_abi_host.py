@@ -88,6 +88,15 @@ def test_host_errors_before_any_launch(lib):
     # fill: row width must be a multiple of 16
     rc = lib.cpkv_fill_current(1, 2, 1, 100, cl.ctypes.data, *([null] * 3), 5, *([null] * 3), 2, 0, null, null)
     assert rc == cpkv.CPKV_ERR_ARG
+    # gather kinds: with no dense pages the call returns before any launch, so only the mask decides
+    tbl2 = (ctypes.c_void_p * 2)(16, 32)
+    caps2 = np.zeros(2, np.int64)
+    for kinds, want in ((cpkv.GATHER_ALL, cpkv.CPKV_OK), (cpkv.GATHER_ALL | cpkv.GATHER_EARLY_INPUTS, cpkv.CPKV_OK),
+                        (cpkv.GATHER_ALL | cpkv.GATHER_CONSUME_STAGING | cpkv.GATHER_EARLY_INPUTS, cpkv.CPKV_OK),
+                        (32, cpkv.CPKV_ERR_ARG), (cpkv.GATHER_ALL | 32, cpkv.CPKV_ERR_ARG), (-1, cpkv.CPKV_ERR_ARG)):
+        rc = lib.cpkv_compose_gather_kinds(16, 1, 64, ctypes.cast(tbl2, ctypes.c_void_p), caps2.ctypes.data, null,
+                                           null, 0, kinds, null, 64, null)
+        assert rc == want, kinds
     # fill flags: an empty batch returns before any launch, so only the flag word decides
     empty = np.zeros(1, np.int32)
     fake = (ctypes.c_void_p * 1)(16)  # never dereferenced: nothing to copy

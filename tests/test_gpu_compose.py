@@ -512,11 +512,39 @@ def test_prefetch_then_consume_equals_compose(batch):
     assert np.array_equal(dense.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("ps,R", [(16, 1152), (64, 1152), (64, 656), (3, 48)])
+def test_gather_early_behind_fill_page_geometries(ps, R):
+    """Early gathers (several pieces per page, and one piece: launched
+    plainly) behind early fills, three layers, every layer checked."""
+    rng = np.random.default_rng(ps * 13 + R)
+    B = 7
+    pfx = (rng.integers(0, 8 * ps, B) // ps) * ps
+    cur = rng.integers(1, 6 * ps, B)
+    batch = wl.make_compose_batch("geo-early", 41, page_size=ps, cp_size=3, num_pool_pages=500, row_bytes=R,
+                                  prefix_lens=pfx, cur_lens=cur, row_kind="bytes")
+    plan, _ = _plan_pair(batch, dense_extra=1)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    host = [(wl.host_pool(batch, l), wl.host_current_rows(batch, l)) for l in range(3)]
+    dev = [([torch.from_numpy(s).cuda() for s in slabs],
+            [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]) for slabs, rows in host]
+    dense = [torch.full((plan.dense_cap_pages * ps, R), 0xCD, dtype=torch.uint8, device="cuda") for _ in range(3)]
+    torch.cuda.synchronize()
+    for l in range(3):
+        layers.fill(dev[l][1], early_inputs=True)
+        layers.gather(dev[l][0], dense[l], consume_staging=True, early_inputs=True)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    for l, (slabs, rows) in enumerate(host):
+        want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                    page_size=ps, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+        assert np.array_equal(dense[l].cpu().numpy(), want), l
+
+
 def test_gather_kinds_rejects_bad_mask():
     batch = wl.tiny_batch()
     plan, _ = _plan_pair(batch)
     layers = ComposeLayers(plan, batch.row_bytes)
-    for bad in (-1, 16, 31):
+    for bad in (-1, 32, 63):
         with pytest.raises(cpkv.CpkvError):
             layers.gather_kinds([torch.from_numpy(s).cuda() for s in wl.host_pool(batch)], layers.dense[0], bad)
 
@@ -568,13 +596,15 @@ def test_one_launch_consuming_staging_matches_oracle(batch):
 # fill launched early behind the previous layer's gather (FLAG_EARLY_INPUTS)
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("early_gather", [False, True], ids=["gather-plain", "gather-early"])
 @pytest.mark.parametrize("consume", [False, True], ids=["kept", "consumed"])
 @pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
-def test_fill_early_behind_gather_matches_oracle(batch, consume):
+def test_fill_early_behind_gather_matches_oracle(batch, consume, early_gather):
     """Three layers of distinct rows and pools, uploaded before the loop; each
     fill starts while the previous layer's gather still reads the stagings it
-    overwrites.  Every layer has its own dense buffer and is checked, so a
-    store that ran ahead of that gather would show in the earlier layer."""
+    overwrites, and (gather-early) each gather starts while its fill still
+    writes them.  Every layer has its own dense buffer and is checked, so a
+    store or a staging read that ran ahead would show."""
     n_layers = 3
     plan, _ = _plan_pair(batch, dense_extra=1)
     layers = ComposeLayers(plan, batch.row_bytes)
@@ -588,7 +618,7 @@ def test_fill_early_behind_gather_matches_oracle(batch, consume):
     torch.cuda.synchronize()
     for l in range(n_layers):
         layers.fill(dev[l][1], early_inputs=True)
-        layers.gather(dev[l][0], dense[l], consume_staging=consume)
+        layers.gather(dev[l][0], dense[l], consume_staging=consume, early_inputs=early_gather)
     torch.cuda.synchronize()
     assert int(plan.d_status.item()) == 0
     for l, (slabs, rows) in enumerate(host):
