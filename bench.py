@@ -340,8 +340,10 @@ class ComposeWorkload:
                                early_inputs=early)
 
     def kernel_graphs(self):
-        """Two more CUDA graphs: the step's fills alone and its gathers alone
-        (same inputs, same launch shapes), to time each kernel's launches."""
+        """One more CUDA graph per kernel of the step (fills alone and gathers
+        alone; the fused or layer kernel alone): the step's launches of that
+        kernel, same inputs and launch shapes, launched plainly so that no two
+        launches overlap, to time each kernel's launches."""
         torch = self.torch
         graphs = {}
         for kind in self.kernels:
