@@ -165,7 +165,10 @@ int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
  * ordered after it.  In a per-layer loop whose inputs were produced before
  * the loop this holds; directly after the kernel that writes the current
  * rows or the plan it does not.  The fused and layer composes take the early
- * launch only for pages of several pieces. */
+ * launch only for pages of several pieces.  Chains of early launches stay
+ * ordered: every early-launched kernel of this library has at least one
+ * thread pass that wait before it can finish, so it completes only after its
+ * predecessor, and no store runs ahead of a kernel two launches back. */
 #define CPKV_FLAG_EARLY_INPUTS 2
 
 /*

@@ -192,13 +192,7 @@ CPKV_DEV void wait_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "mem
 
 // Once per thread (`open` starts false): wait_prerequisite() before the
 // thread's first global store, so that an early-launched kernel orders every
-// write after the previous kernel while its loads may run ahead.  Every
-// early-launched kernel of this library has at least one thread pass this
-// wait before the kernel can finish (each CTA of the gather and the one-launch
-// composes gates before its final drain; the fills store whenever they have
-// rows), so a kernel completes only after its predecessor has, and a chain
-// of early launches never lets a store run ahead of a kernel two or more
-// launches back.
+// write after the previous kernel while its loads may run ahead.
 CPKV_DEV void store_gate(bool *open) {
   if (!*open) {
     wait_prerequisite();
