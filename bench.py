@@ -556,6 +556,69 @@ def time_oracle(b, pools, rows, min_seconds=10.0, max_seconds=30.0):
     return moved / el / 1e9, el, steps
 
 
+def _all_cores_worker(config, n_layers, shared_pool, seconds, barrier, out):
+    """One process of the all-cores oracle baseline: host inputs generated
+    from the workload's seeds, one untimed step, then oracle steps from the
+    common start (a barrier) for ``seconds``.  Puts (bytes, t0, t1, steps),
+    or an error string."""
+    try:
+        import oracle
+
+        b, pools, rows = oracle_sample(wl.CONFIGS[config](), n_layers, shared_pool=shared_pool)
+        lib = oracle.load()
+        oracle_step(b, pools, rows, lib)
+        barrier.wait(timeout=600)
+        t0 = time.time()
+        moved, steps = 0, 0
+        while True:
+            moved += oracle_step(b, pools, rows, lib)
+            steps += 1
+            t1 = time.time()
+            if t1 - t0 >= seconds:
+                break
+        out.put((moved, t0, t1, steps))
+    except Exception as e:  # reported by the parent, which then gives no number
+        barrier.abort()
+        out.put(f"{type(e).__name__}: {e}")
+
+
+def time_oracle_all_cores(config, n_layers, shared_pool=False, seconds=10.0, workers=None):
+    """The labelled all-cores variant of the CPU baseline: one single-threaded
+    oracle process per host core, each running the same bounded sample on its
+    own host-generated copy of the inputs, started together.  Returns
+    (GB/s over the common wall-clock window, processes, seconds, steps), or
+    None with the reason when a worker failed."""
+    import multiprocessing as mp
+    import queue
+
+    ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
+    n = workers or os.cpu_count() or 1
+    barrier, out = ctx.Barrier(n), ctx.Queue()
+    procs = [ctx.Process(target=_all_cores_worker, args=(config, n_layers, shared_pool, seconds, barrier, out))
+             for _ in range(n)]
+    for p in procs:
+        p.start()
+    res, err = [], None
+    try:
+        for _ in range(n):
+            r = out.get(timeout=900)
+            if isinstance(r, str):
+                err = err or r
+            else:
+                res.append(r)
+    except queue.Empty:
+        err = err or "a worker did not report within 900 s"
+    for p in procs:
+        p.join(timeout=60)
+        if p.is_alive():
+            p.terminate()
+    if err is not None or len(res) != n:
+        return None, err or "missing worker results"
+    moved = sum(r[0] for r in res)
+    t0, t1 = min(r[1] for r in res), max(r[2] for r in res)
+    return (moved / (t1 - t0) / 1e9, n, t1 - t0, sum(r[3] for r in res)), None
+
+
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
@@ -579,6 +642,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's bounded sample")
+    ap.add_argument("--no-cpu-all-cores", action="store_true",
+                    help="skip the all-cores variant of the CPU baseline (one oracle process per core)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small cases for profiling; the headline uses all 78)")
     ap.add_argument("--consume-staging", choices=["auto", "on", "off"], default="auto",
@@ -694,6 +759,19 @@ def main(argv=None):
                "sample": f"plan + ragged plan + {len(pools)} of {work.num_layers} layers (staging + gather) of "
                          f"the same batch and inputs, repeated {steps}x over {secs:.1f}s, single-threaded C",
                "host": host_cpu()}
+    cpu_all = None
+    if not a.no_cpu_baseline and not a.no_cpu_all_cores and rank == 0 and ws == 1:
+        n_layers = min(a.cpu_layers, work.num_layers)
+        got, why = time_oracle_all_cores(a.config, n_layers, shared_pool=work.shared_pool)
+        if got is None:
+            cpu_all = {"value": None, "unavailable": why}
+        else:
+            gbs_all, procs, secs, steps = got
+            cpu_all = {"value": round(gbs_all, 3), "unit": "GB/s", "cores": procs, "kind": "oracle",
+                       "sample": f"{procs} single-threaded oracle processes (one per host core) started together, "
+                                 f"each running plan + ragged plan + {n_layers} of {work.num_layers} layers "
+                                 f"(staging + gather) on its own host-generated inputs of the same batch; "
+                                 f"{steps} steps in {secs:.1f}s in all"}
 
     b = work.batch
     line = {
@@ -759,6 +837,7 @@ def main(argv=None):
                for k in kern if k != top},
         },
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
         "gpu_launches": work.launches_per_step * a.steps,
         "clocks": clk,

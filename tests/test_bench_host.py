@@ -67,3 +67,15 @@ def test_layer_bytes_planar_unstaged_planes():
 def test_pool_pages_only_for_shared_pool_workloads():
     with pytest.raises(ValueError):
         bench.ComposeWorkload("traced_78", device="cpu", pool_pages=4096)
+
+
+def test_all_cores_oracle_baseline_runs_and_aggregates():
+    got, why = bench.time_oracle_all_cores("tiny", 1, seconds=0.3, workers=2)
+    assert why is None
+    gbs, procs, secs, steps = got
+    assert procs == 2 and gbs > 0 and secs >= 0.3 and steps >= 2
+
+
+def test_all_cores_oracle_baseline_reports_a_failed_worker():
+    got, why = bench.time_oracle_all_cores("no such workload", 1, seconds=0.1, workers=2)
+    assert got is None and "KeyError" in why
