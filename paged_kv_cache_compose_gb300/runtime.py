@@ -162,9 +162,14 @@ class ComposeLayers:
                                 row_bytes=self.row_bytes, dense_cap_pages=p.dense_cap_pages, d_status=p.d_status,
                                 consume_staging=consume_staging, early_inputs=early_inputs, stream=stream)
 
-    def compose_layer(self, layer: int, pools, cur_rows_per_writer, stream=None):
-        """Fill + gather of one layer into the dense buffer of its parity."""
+    def compose_layer(self, layer: int, pools, cur_rows_per_writer, stream=None, consume_staging=False,
+                      early_inputs=False):
+        """Fill + gather of one layer into the dense buffer of its parity.
+        ``early_inputs``: both kernels launch early (the fill behind the
+        previous kernel, the gather behind the fill); the caller promises that
+        the plan, pools and rows were complete before the previous kernel on
+        the stream started."""
         dense = self.dense[layer % len(self.dense)]
-        self.fill(cur_rows_per_writer, stream)
-        self.gather(pools, dense, stream)
+        self.fill(cur_rows_per_writer, stream, early_inputs=early_inputs)
+        self.gather(pools, dense, stream, consume_staging=consume_staging, early_inputs=early_inputs)
         return dense
