@@ -3,9 +3,11 @@
 Each case draws a batch (requests, page size, cp, row width, prefix/current
 lengths, writer assignment, shared prefix pages, capacity padding) from a
 fixed seed, runs the plan, the fill + gather, the one-launch layer compose, the fused
-compose and the prefix/current split on the GPU, and the ragged plan for every rank, and
-compares everything with the CPU oracle.
+compose and the prefix/current split on the GPU, plain and as chains of early launches,
+and the ragged plan for every rank, and compares everything with the CPU oracle.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -103,6 +105,48 @@ def test_fuzz_compose(seed):
     assert np.array_equal(one.cpu().numpy(), want)
     for w in range(cp):
         assert np.array_equal(layers.staging[w].cpu().numpy(), want_stg[w]), w
+
+
+@pytest.mark.parametrize("seed", range(100, 120))
+def test_fuzz_early_launch_chains(seed):
+    """Three layers of distinct inputs, uploaded first, through each chain of
+    early launches (CPKV_FLAG_EARLY_INPUTS, CPKV_GATHER_EARLY_INPUTS): fill +
+    gather, the fused compose and the one-launch layer compose.  Every
+    layer has its own dense buffer and is checked against the oracle.  Odd
+    seeds widen the rows to pages of about 40 KB, several pieces for every
+    kernel, so the early launches are taken (one-piece pages launch the
+    gather and the one-launch kernels plainly)."""
+    batch, extra = random_batch(seed)
+    if seed % 2:
+        batch = dataclasses.replace(batch, row_bytes=16 * -(-40960 // (batch.page_size * 16)))
+    ps, cp, R = batch.page_size, batch.cp_size, batch.row_bytes
+    T, C, D = oracle.sizes(batch.prefix_lens, batch.cur_lens, ps)
+    cap = D + extra
+    plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                       page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages, dense_cap_pages=cap).build()
+    layers = ComposeLayers(plan, R)
+    n_layers, consume = 3, seed % 2 == 0
+    host = [(wl.host_pool(batch, l), wl.host_current_rows(batch, l)) for l in range(n_layers)]
+    dev = [([torch.from_numpy(s).cuda() for s in slabs],
+            [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]) for slabs, rows in host]
+    out = {k: [torch.full((cap * ps, R), 0xCD, dtype=torch.uint8, device="cuda") for _ in range(n_layers)]
+           for k in ("staging", "fused", "layer")}
+    torch.cuda.synchronize()
+    for l in range(n_layers):
+        layers.fill(dev[l][1], early_inputs=True)
+        layers.gather(dev[l][0], out["staging"][l], consume_staging=consume, early_inputs=True)
+    for l in range(n_layers):
+        layers.compose_fused(dev[l][0], dev[l][1], out["fused"][l], early_inputs=True)
+    for l in range(n_layers):
+        layers.compose_one_launch(dev[l][0], dev[l][1], out["layer"][l], consume_staging=consume,
+                                  early_inputs=True)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    for l, (slabs, rows) in enumerate(host):
+        want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                    page_size=ps, cp_size=cp, dense_cap=cap)
+        for k, bufs in out.items():
+            assert np.array_equal(bufs[l].cpu().numpy(), want), (k, l)
 
 
 @pytest.mark.parametrize("seed", range(30))
