@@ -66,9 +66,24 @@ def compile_oracle(src: str = _SRC, out: str = _LIB_PATH, extra_flags=()) -> str
     return out
 
 
+def _foreign_elf(path: str) -> bool:
+    """True when ``path`` is a shared object built for another CPU than this
+    host's (ELF e_machine: 62 x86-64, 183 AArch64)."""
+    import platform
+
+    want = {"x86_64": 62, "aarch64": 183}.get(platform.machine())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return True
+    return want is not None and (head[:4] != b"\x7fELF" or int.from_bytes(head[18:20], "little") != want)
+
+
 def build() -> str:
     with _lock:
-        if (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        if (not os.path.exists(_LIB_PATH)) or _foreign_elf(_LIB_PATH) or \
+                os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
             tmp = _LIB_PATH + f".{os.getpid()}.tmp"
             compile_oracle(out=tmp)
             os.replace(tmp, _LIB_PATH)

@@ -43,8 +43,27 @@ def _deps() -> list[str]:
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
+_ELF_MACHINE = {"x86_64": 62, "aarch64": 183}  # ELF e_machine of this host's shared objects
+
+
+def _built_for_other_machine(path: str) -> bool:
+    """True when ``path`` is an ELF object for another CPU than this host's
+    (a library copied over from a machine of another architecture)."""
+    import platform
+
+    want = _ELF_MACHINE.get(platform.machine())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return True
+    if want is None or len(head) < 20 or head[:4] != b"\x7fELF":
+        return want is not None
+    return int.from_bytes(head[18:20], "little") != want
+
+
 def stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+    if not os.path.exists(LIB_PATH) or _built_for_other_machine(LIB_PATH):
         return True
     t = os.path.getmtime(LIB_PATH)
     return any(os.path.getmtime(p) > t for p in _deps())
