@@ -181,3 +181,22 @@ def test_missing_library_fails_loudly(tmp_path):
             cpkv.load(str(tmp_path / "absent.so"))
     finally:
         cpkv._lib = saved
+
+
+def test_build_rebuilds_a_library_compiled_for_another_cpu(tmp_path):
+    import platform
+
+    from paged_kv_cache_compose_gb300 import build as cuda_build
+
+    mine = cuda_build._ELF_MACHINE.get(platform.machine())
+    if mine is None:
+        pytest.skip("host CPU not in the ELF table")
+    other = 183 if mine == 62 else 62
+    for machine, foreign in ((mine, False), (other, True)):
+        f = tmp_path / f"lib{machine}.so"
+        f.write_bytes(b"\x7fELF" + bytes(14) + machine.to_bytes(2, "little") + bytes(44))
+        assert cuda_build._built_for_other_machine(str(f)) is foreign
+    junk = tmp_path / "junk.so"
+    junk.write_bytes(b"not an elf file at all")
+    assert cuda_build._built_for_other_machine(str(junk))
+    assert not cuda_build._built_for_other_machine(cuda_build.LIB_PATH)
