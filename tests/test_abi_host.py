@@ -183,7 +183,7 @@ def test_missing_library_fails_loudly(tmp_path):
         cpkv._lib = saved
 
 
-def test_build_rebuilds_a_library_compiled_for_another_cpu(tmp_path):
+def test_build_rebuilds_a_library_compiled_for_another_cpu(tmp_path, lib):
     import platform
 
     from paged_kv_cache_compose_gb300 import build as cuda_build
