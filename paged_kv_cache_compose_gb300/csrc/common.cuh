@@ -311,4 +311,13 @@ inline int ring_cap_one_piece(int64_t piece_bytes, int loads_in_flight, int floo
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Whether an early (programmatic dependent) launch of a persistent grid of
+// `grid` one-warp CTAs pays: only when it runs at most 4 CTAs per SM.  There
+// its CTAs start in the room the previous kernel leaves and overlap that
+// kernel's tail (traced pages, 3-4 per SM: fused 4.05 -> 3.81 ms per step;
+// index-key pages, 3 per SM: fused 3.947 -> 3.700 ms).  With many small CTAs
+// per SM (one-token pages, 24) the early CTAs crowd the previous kernel's
+// tail and the step got slower (fused 4.27 -> 4.70 ms).
+inline bool early_launch_pays(int grid) { return grid <= 4 * device_sm_count(); }
+
 }  // namespace cpkv

@@ -32,15 +32,17 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kLoadsInFlight = 2;
 constexpr int kMaxCtasPerSm = 3;  // one-warp CTAs per SM, at most; fewer when their rings do not fit
-// With CPKV_FLAG_EARLY_INPUTS and pages of several pieces, the kernel is
+// With CPKV_FLAG_EARLY_INPUTS and a grid of at most 4 CTAs per SM
+// (early_launch_pays), the kernel is
 // launched as a programmatic dependent of the previous kernel on the stream:
 // its CTAs may start in SM slots that the previous launch's tail frees, read
 // their inputs at once, and wait for that launch (store_gate) only before
 // their first global store.  Measured per 78-layer step: traced
 // 4.045 -> 3.807 ms, fp8 17.99 -> 17.64 ms; waiting before the first load
-// instead kept only 4.045 -> 3.993 ms.  Pages of one piece run many small
-// CTAs per SM, where the next launch's CTAs would sit beside the current ones
-// from the start (one-token pages: 4.27 -> 4.70 ms), so they launch plainly.
+// instead kept only 4.045 -> 3.993 ms.  Index-key pages (one 8448-byte
+// piece, 3 CTAs per SM): 3.947 -> 3.700 ms.  One-token pages run 24 small
+// CTAs per SM, where the next launch's CTAs would sit beside the current
+// ones from the start (4.27 -> 4.70 ms), so that grid launches plainly.
 // In a plain launch the waits return at once.
 constexpr int kMaxPieceBytes = 24 * 1024;
 
@@ -237,7 +239,7 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
     const int grid = persistent_grid(kernel, 32, smem, cap_per_sm, units);
     FusedParams<64> prm;
     CPKV_FILL_FUSED(prm)
-    return launch_fused(compose_fused_kernel<64>, grid, smem, early && pieces > 1, s, prm);
+    return launch_fused(compose_fused_kernel<64>, grid, smem, early && early_launch_pays(grid), s, prm);
   }
   const void *kernel = reinterpret_cast<const void *>(compose_fused_kernel<CPKV_MAX_BATCH>);
   if (ensure_dynamic_smem(kernel, kStages * kMaxPieceBytes) != CPKV_OK) return CPKV_ERR_CUDA;
@@ -245,5 +247,5 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
   FusedParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_FUSED(prm)
 #undef CPKV_FILL_FUSED
-  return launch_fused(compose_fused_kernel<CPKV_MAX_BATCH>, grid, smem, early && pieces > 1, s, prm);
+  return launch_fused(compose_fused_kernel<CPKV_MAX_BATCH>, grid, smem, early && early_launch_pays(grid), s, prm);
 }

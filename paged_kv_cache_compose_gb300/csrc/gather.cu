@@ -24,14 +24,16 @@
 // its L2 lines are dropped, so the fill's dirty staging lines are never
 // written back to DRAM.
 //
-// With CPKV_GATHER_EARLY_INPUTS and pages of several pieces the gather is
+// With CPKV_GATHER_EARLY_INPUTS and a grid of at most 4 CTAs per SM
+// (early_launch_pays: pages of several pieces, index-key pages) the gather is
 // launched as a programmatic dependent of the previous kernel (its fill, which
 // releases its dependents as its blocks finish).  Its CTAs start as the
 // fill's blocks retire, load descriptors and pool pieces at once, and each
 // waits for the fill (store_gate) before its first staging load and before
-// its first store.  Measured per 78-layer traced step: 4.284 -> 4.200 ms;
-// fp8 unchanged (19.77 ms); one-token pages, where the ring runs many small
-// CTAs per SM, 5.195 -> 5.555 ms, so pages of one piece launch plainly.
+// its first store.  Measured per 78-layer step: traced 4.284 -> 4.200 ms;
+// fp8 unchanged (19.77 ms); index keys 4.143 -> 4.128 ms; one-token pages,
+// where the ring runs 24 small CTAs per SM, 5.195 -> 5.555 ms, so that grid
+// launches plainly.
 // The gather itself releases its dependents at its start (the next layer's
 // fill, launched with CPKV_FLAG_EARLY_INPUTS, may start while it runs).
 #include <stdint.h>
@@ -197,7 +199,7 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
                                  : ring_cap_one_piece(piece_bytes, kLoadsInFlight, kMaxCtasPerSmOnePiece),
                       prm.units);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool dependent = early && pieces > 1;
+  const bool dependent = early && early_launch_pays(grid);
   if (consume) return launch_kernel(gather_pages_kernel<true>, dim3(grid), dim3(32), smem, dependent, s, prm);
   return launch_kernel(gather_pages_kernel<false>, dim3(grid), dim3(32), smem, dependent, s, prm);
 }
