@@ -540,6 +540,57 @@ def test_gather_early_behind_fill_page_geometries(ps, R):
         assert np.array_equal(dense[l].cpu().numpy(), want), l
 
 
+def _page_run_batch(seed=77, cp=4, ps=1, R=1152, B=5):
+    """Small pages whose sources form runs: each request's prefix pages are
+    consecutive local pages of one owner (ids r + cp * k for consecutive k),
+    and its current pages go to contiguous writers, so consecutive dense
+    current pages have consecutive staging slots of one writer."""
+    rng = np.random.default_rng(seed)
+    pfx = rng.integers(5, 40, B) * ps
+    cur = rng.integers(3, 30, B)
+    next_local = [1] * cp
+    prefix_pages = []
+    for b in range(B):
+        r = int(rng.integers(0, cp))
+        n = int(pfx[b] // ps)
+        prefix_pages += [r + cp * (next_local[r] + k) for k in range(n)]
+        next_local[r] += n + int(rng.integers(0, 3))  # a gap between requests now and then
+    first_cur = cp * (max(next_local) + 1)
+    C = int(((cur + ps - 1) // ps).sum())
+    cur_pages = first_cur + np.arange(C)
+    P = int(first_cur + C + 1)
+    return wl.make_compose_batch("page-runs", seed, page_size=ps, cp_size=cp, num_pool_pages=P, row_bytes=R,
+                                 prefix_lens=pfx, cur_lens=cur, prefix_pages=np.array(prefix_pages),
+                                 cur_pages=cur_pages, writer=wl.contiguous_writers(cur, ps, cp),
+                                 row_kind="bytes")
+
+
+@pytest.mark.parametrize("early", [False, True], ids=["plain", "early"])
+@pytest.mark.parametrize("consume", [False, True], ids=["kept", "consumed"])
+@pytest.mark.parametrize("ps,R", [(1, 1152), (4, 272), (2, 16)])
+def test_gather_merges_page_runs(ps, R, consume, early):
+    """Page-run merging in the grouped small-page gather: pool and staging
+    runs are loaded as single copies, zero slots fill the group's tail; two
+    layers of distinct inputs, each checked."""
+    batch = _page_run_batch(ps=ps, R=R)
+    plan, _ = _plan_pair(batch, dense_extra=9)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    host = [(wl.host_pool(batch, l), wl.host_current_rows(batch, l)) for l in range(2)]
+    dev = [([torch.from_numpy(s).cuda() for s in slabs],
+            [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]) for slabs, rows in host]
+    dense = [torch.full((plan.dense_cap_pages * ps, R), 0xCD, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for l in range(2):
+        layers.fill(dev[l][1], early_inputs=early)
+        layers.gather(dev[l][0], dense[l], consume_staging=consume, early_inputs=early)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    for l, (slabs, rows) in enumerate(host):
+        want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                    page_size=ps, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+        assert np.array_equal(dense[l].cpu().numpy(), want), l
+
+
 def test_gather_kinds_rejects_bad_mask():
     batch = wl.tiny_batch()
     plan, _ = _plan_pair(batch)
