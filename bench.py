@@ -818,7 +818,8 @@ def main(argv=None):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": {"gather": "gather_pages_kernel (cpkv_compose_gather)",
+            "kernel": {"gather": ("gather_groups_kernel" if work.batch.page_size * work.batch.row_bytes <= 4096
+                                  else "gather_pages_kernel") + " (cpkv_compose_gather_kinds)",
                        "fused": ("compose_layer_kernel (cpkv_compose_fused_planes)" if work.batch.planes
                                  else "compose_fused_kernel (cpkv_compose_fused)"),
                        "layer": ("compose_layer_kernel (cpkv_compose_layer_planes)" if work.batch.planes
