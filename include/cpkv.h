@@ -260,6 +260,9 @@ int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n_planes, co
  * The gather releases its programmatic dependents when it starts: a kernel
  * launched after it with CPKV_FLAG_EARLY_INPUTS (the next layer's fill) may
  * start while it runs and waits for it before storing.
+ * Pages of at most 4 KB are moved a group of consecutive dense pages at a
+ * time, and a run of consecutive source pages within one table entry is one
+ * copy (page-run merging); the result is the same bytes.
  */
 int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
                         const void *const *h_src_table, const int64_t *h_src_cap_pages,
