@@ -79,3 +79,20 @@ def test_all_cores_oracle_baseline_runs_and_aggregates():
 def test_all_cores_oracle_baseline_reports_a_failed_worker():
     got, why = bench.time_oracle_all_cores("no such workload", 1, seconds=0.1, workers=2)
     assert got is None and "KeyError" in why
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the CPU oracle arm) runs without a GPU and
+    prints one JSON line with the keys the contract asks for."""
+    import json
+    import subprocess
+    import sys
+
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config", "traced", "--steps", "1",
+                          "--cpu-layers", "1"], cwd=bench.ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["warmup"] >= 3
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
