@@ -453,12 +453,17 @@ int cpkv_ragged_plan_sizes(int B, int chunk, const int32_t *h_q_lens, const int3
  *   kv_lens = prefix_b + q_starts + q_lens;
  *   k_bases = sum_{b' < b} align_up(prefix_b' + q_b', k_align);
  *   current_bases = k_bases + prefix_b; q_bases = exclusive sum of q_lens.
- * d_topk_offsets[j] = k_bases of the segment holding this rank's j-th token.
+ * d_topk_offsets[j] = k_bases of the segment holding this rank's j-th token:
+ * the base that turns the j-th query's topk key indices, which count from the
+ * start of its request's keys, into rows of the ragged key buffer.
+ * topk is the indexer's keys per query (2048 in the ragged config).  It is
+ * the width of the consumer's index matrix [Q_r][topk]; no plan array depends
+ * on it, and topk <= 0 returns CPKV_ERR_ARG.
  * Capacities: seg_cap >= S, topk_cap >= Q_r (S <= n_owned and
  * Q_r <= n_owned * chunk always hold).  d_counts (device int64 [2]) receives
  * (S, Q_r).  Status bits: CHUNK_OOB (bad cp_index), OUT_CAPACITY.
  */
-int cpkv_ragged_plan_build(int B, int chunk, int k_align, const int32_t *h_prefix_lens,
+int cpkv_ragged_plan_build(int B, int chunk, int k_align, int topk, const int32_t *h_prefix_lens,
                            const int32_t *h_q_lens, const int32_t *d_cp_index, int64_t n_owned,
                            int32_t *d_topk_offsets, int64_t topk_cap, int32_t *d_seg_req,
                            int32_t *d_kv_lens, int32_t *d_q_starts, int32_t *d_q_lens,

@@ -91,7 +91,7 @@ def _declare(lib):
     lib.cpkv_compose_fused_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _I, _P,
                                               _P]
     lib.cpkv_ragged_plan_sizes.argtypes = [_I, _I, _P, _P, _L, _P, _P]
-    lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
+    lib.cpkv_ragged_plan_build.argtypes = [_I, _I, _I, _I, _P, _P, _P, _L, _P, _L] + [_P] * 7 + [_L, _P, _P, _P]
     for name in EXPORTED:
         getattr(lib, name).restype = _I
     lib.cpkv_error_string.argtypes = [_I]
@@ -348,12 +348,13 @@ def cpkv_selftest_ring_timeout(d_dst16, d_status, stream=None):
            load().cpkv_selftest_ring_timeout(_dp(d_dst16), _dp(d_status), _stream(stream)))
 
 
-def cpkv_ragged_plan_build(prefix_lens, q_lens, d_cp_index, n_owned: int, *, chunk, k_align, out, d_counts,
+def cpkv_ragged_plan_build(prefix_lens, q_lens, d_cp_index, n_owned: int, *, chunk, k_align, topk, out, d_counts,
                            d_status, stream=None):
-    """Ragged index plan of one rank into the tensors of ``out`` (see ``ragged_buffers``)."""
+    """Ragged index plan of one rank into the tensors of ``out`` (see ``ragged_buffers``);
+    ``topk``: the indexer's keys per query (validated > 0)."""
     pl, ql = _host_i32(prefix_lens), _host_i32(q_lens)
     rc = load().cpkv_ragged_plan_build(
-        len(pl), chunk, k_align, _hp(pl), _hp(ql), _dp(d_cp_index), n_owned, _dp(out["topk_offsets"]),
+        len(pl), chunk, k_align, topk, _hp(pl), _hp(ql), _dp(d_cp_index), n_owned, _dp(out["topk_offsets"]),
         out["topk_offsets"].numel(), _dp(out["seg_req"]), _dp(out["kv_lens"]), _dp(out["q_starts"]),
         _dp(out["q_lens"]), _dp(out["k_bases"]), _dp(out["q_bases"]), _dp(out["current_bases"]),
         out["seg_req"].numel(), _dp(d_counts), _dp(d_status), _stream(stream))

@@ -27,6 +27,12 @@ constexpr uint64_t kRingWaitLimitNs = 2000000000ull;  // 2 s; a piece lands in m
 
 // Drop the L2 lines that lie wholly inside [src, src + bytes) without
 // writing them back (warp-uniform call; the bytes become undefined).
+// Invariant of every consuming caller: a discarded staging line reverts to
+// whatever DRAM last held, so each staging byte that a later read sees (a
+// staged row, a pad row, a lane-copied plane slice) must be rewritten before
+// that read.  The fills write every row of a current page and zero every pad
+// row after a request's last token; a fill that skipped any of them would
+// leak stale DRAM bytes into the next dense buffer.
 CPKV_DEV void warp_discard_l2(const uint8_t *src, uint32_t bytes) {
   const uintptr_t first = (reinterpret_cast<uintptr_t>(src) + 127) & ~static_cast<uintptr_t>(127);
   const uintptr_t end = (reinterpret_cast<uintptr_t>(src) + bytes) & ~static_cast<uintptr_t>(127);

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kRaggedThreads) ragged_plan_kernel(const __gri
 }  // namespace
 }  // namespace cpkv
 
-extern "C" int cpkv_ragged_plan_build(int B, int chunk, int k_align, const int32_t *h_prefix_lens,
+extern "C" int cpkv_ragged_plan_build(int B, int chunk, int k_align, int topk, const int32_t *h_prefix_lens,
                                       const int32_t *h_q_lens, const int32_t *d_cp_index, int64_t n_owned,
                                       int32_t *d_topk_offsets, int64_t topk_cap, int32_t *d_seg_req,
                                       int32_t *d_kv_lens, int32_t *d_q_starts, int32_t *d_q_lens,
@@ -156,7 +156,10 @@ extern "C" int cpkv_ragged_plan_build(int B, int chunk, int k_align, const int32
                                       int64_t seg_cap, int64_t *d_counts, int32_t *d_status,
                                       cpkv_stream_t stream) {
   using namespace cpkv;
-  if (B < 0 || chunk <= 0 || k_align <= 0 || n_owned < 0 || topk_cap < 0 || seg_cap < 0) return CPKV_ERR_ARG;
+  // topk is the consumer's index width: no plan array depends on it, but a
+  // plan for a non-positive width is a caller error
+  if (B < 0 || chunk <= 0 || k_align <= 0 || topk <= 0 || n_owned < 0 || topk_cap < 0 || seg_cap < 0)
+    return CPKV_ERR_ARG;
   if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
   if (d_status == nullptr || d_counts == nullptr) return CPKV_ERR_ARG;
   if (B > 0 && (h_prefix_lens == nullptr || h_q_lens == nullptr)) return CPKV_ERR_ARG;

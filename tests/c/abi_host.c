@@ -63,6 +63,14 @@ int main(void) {
             CPKV_ERR_ARG,
         "layer compose without pointer tables rejected");
 
+  {
+    int32_t *fake = (int32_t *)(uintptr_t)256;
+    int64_t *fake64 = (int64_t *)(uintptr_t)256;
+    CHECK(cpkv_ragged_plan_build(2, 4, 1, 0, pfx, q, fake, 2, fake, 8, fake, fake, fake, fake, fake, fake, fake, 2,
+                                 fake64, fake, 0) == CPKV_ERR_ARG,
+          "ragged_plan_build: topk of 0 rejected");
+  }
+
   CHECK(strncmp(cpkv_error_string(CPKV_ERR_CAPACITY), "CPKV_ERR_CAPACITY", 17) == 0, "error strings");
   CHECK(cpkv_version() == CPKV_VERSION, "library version matches the header");
   return fails ? 1 : 0;

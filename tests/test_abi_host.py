@@ -157,9 +157,15 @@ def test_host_errors_before_any_launch(lib):
                                     64, null)
         assert rc == cpkv.CPKV_ERR_ARG, flags
     # ragged: bad chunk / k_align
-    rc = lib.cpkv_ragged_plan_build(1, 0, 1, pl.ctypes.data, cl.ctypes.data, null, 0, null, 0, *([null] * 7), 0,
-                                    null, null, null)
+    rc = lib.cpkv_ragged_plan_build(1, 0, 1, 2048, pl.ctypes.data, cl.ctypes.data, null, 0, null, 0,
+                                    *([null] * 7), 0, null, null, null)
     assert rc == cpkv.CPKV_ERR_ARG
+    # ragged: a topk that is not positive, every other argument well formed
+    fake = ctypes.c_void_p(256)
+    for topk in (0, -2048):
+        rc = lib.cpkv_ragged_plan_build(1, 4, 1, topk, pl.ctypes.data, cl.ctypes.data, fake, 1, fake, 8,
+                                        *([fake] * 7), 2, fake, fake, null)
+        assert rc == cpkv.CPKV_ERR_ARG, topk
 
 
 def test_unaligned_prefix_raises_in_binding(lib):

@@ -27,9 +27,26 @@ def _batch_order_rows(batch, rows_per_writer):
     return g
 
 
-def _check_layer(work, layer):
+_COMPACT = {}
+
+
+def _compact(work, layer):
+    """The layer's pool compacted to the referenced pages (cached for a pool
+    that all layers share)."""
+    if not work.shared_pool:
+        return bench.compact_pool(work.batch, work.pools_of(layer))
+    key = id(work)
+    if key not in _COMPACT:
+        _COMPACT.clear()
+        _COMPACT[key] = bench.compact_pool(work.batch, work.pools_of(layer))
+    return _COMPACT[key]
+
+
+def _check_layer(work, layer, got=None):
+    """Layer ``layer``'s dense buffer (or the host copy ``got``) against the
+    oracle's definition; returns the batch-ordered rows of row-major pages."""
     b = work.batch
-    nb, slabs = bench.compact_pool(b, work.pools_of(layer))
+    nb, slabs = _compact(work, layer)
     if b.planes:
         tw = wl.token_writer(b)
         planes = []
@@ -42,13 +59,13 @@ def _check_layer(work, layer):
                                            [s.reshape(s.shape[0], -1) for s in slabs], planes,
                                            page_size=b.page_size, cp_size=b.cp_size, plane_bytes=list(b.planes),
                                            dense_cap=work.plan.dense_cap_pages)
-        got = work.layers.dense[layer % 2].cpu().numpy().reshape(work.plan.dense_cap_pages, -1)
+        got = (work.dense_of(layer) if got is None else got).cpu().numpy().reshape(work.plan.dense_cap_pages, -1)
         assert np.array_equal(got, want), f"layer {layer}"
         return None
     g = _batch_order_rows(b, work.rows[layer])
     want = oracle.compose_dense(nb.prefix_lens, nb.cur_lens, nb.prefix_pages, slabs, g, page_size=b.page_size,
                                 cp_size=b.cp_size, dense_cap=work.plan.dense_cap_pages)
-    got = work.layers.dense[layer % 2].cpu().numpy()
+    got = (work.dense_of(layer) if got is None else got).cpu().numpy()
     assert np.array_equal(got, want), f"layer {layer}"
     return g
 
@@ -105,6 +122,39 @@ def test_benchmark_workload_matches_oracle(config, variant):
         if variant in ("staging", "prefetch", "layer") and g is not None and not consume:
             _check_staging(work, g)
     finally:
+        _COMPACT.clear()
+        del work
+        gc.collect()
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("config,variant,early", [
+    ("traced_78", "staging-consume", True), ("traced_78", "staging-consume", False), ("traced_78", "staging", True),
+    ("traced_78", "fused", True), ("traced_78", "layer-consume", True), ("fp8_nsa", "staging-consume", True)])
+def test_every_layer_of_the_78_layer_graph_matches_oracle(config, variant, early):
+    """The benchmark's 78-layer step over the traced batch, replayed from its
+    CUDA graph, with one dense buffer per layer so that every layer's output
+    survives the step: all 78 dense layers byte-exact against the oracle.
+    With early launches (the benchmark's form) a layer's fill starts behind
+    the previous layer's gather and its gather behind the fill; a store that
+    ran ahead of its predecessor in any layer would show up here."""
+    consume = variant.endswith("-consume")
+    variant = variant.removesuffix("-consume")
+    work = bench.ComposeWorkload(config, variant=variant, consume_staging=consume, num_dense=78, early=early)
+    try:
+        for d in work.layers.dense:
+            d.fill_(0xCD)
+        work.capture()
+        for d in work.layers.dense:
+            d.fill_(0xCD)
+        work.run()
+        torch.cuda.synchronize()
+        assert work.status() == 0
+        _check_plan(work)
+        for layer in range(work.num_layers):
+            _check_layer(work, layer)
+    finally:
+        _COMPACT.clear()
         del work
         gc.collect()
         torch.cuda.empty_cache()
@@ -114,22 +164,28 @@ def test_benchmark_workload_matches_oracle(config, variant):
 def test_end_to_end_graph_matches_oracle(variant):
     """The end-to-end step (rows uploaded from pinned host memory on a copy
     stream, each layer joined to its upload by an event wait, fills and
-    one-launch composes launched early behind the previous kernel).  The
-    device rows are poisoned first, so a compose that read its rows before
-    their upload landed would differ from the oracle."""
-    work = bench.ComposeWorkload("traced_78", variant=variant, consume_staging=variant != "fused")
+    one-launch composes launched early behind the previous kernel, the last
+    layer's dense buffer read back to pinned host memory).  One dense buffer
+    per layer, so every layer is checked.  The device rows are poisoned first,
+    so a compose that read its rows before their upload landed would differ
+    from the oracle."""
+    work = bench.ComposeWorkload("traced_78", variant=variant, consume_staging=variant != "fused", num_dense=78)
     try:
-        one, h2d, d2h = bench.build_e2e(work)
-        assert h2d >= work.rows_all.numel() and d2h == 20
+        one, h2d, d2h, h_dense = bench.build_e2e(work)
+        dense_bytes = work.dense_of(work.num_layers - 1).numel()
+        assert h2d >= work.rows_all.numel() and d2h == 20 + dense_bytes
         work.rows_all.fill_(0xEE)
         for d in work.layers.dense:
             d.fill_(0xCD)
+        h_dense.fill_(0xAB)
         one()
         assert work.status() == 0
         _check_plan(work)
-        _check_layer(work, work.num_layers - 2)
-        _check_layer(work, work.num_layers - 1)
+        for layer in range(work.num_layers):
+            _check_layer(work, layer)
+        _check_layer(work, work.num_layers - 1, got=h_dense)
     finally:
+        _COMPACT.clear()
         del work
         gc.collect()
         torch.cuda.empty_cache()

@@ -168,7 +168,7 @@ def test_fuzz_ragged(seed):
         counts = torch.zeros(2, dtype=torch.int64, device="cuda")
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         cpkv.cpkv_ragged_plan_build(rb.prefix_lens, rb.q_lens, torch.from_numpy(ci).cuda(), len(ci), chunk=chunk,
-                                    k_align=rb.k_align, out=out, d_counts=counts, d_status=status)
+                                    k_align=rb.k_align, topk=rb.topk, out=out, d_counts=counts, d_status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == want["status"] == 0
         assert counts.cpu().tolist() == [S, Q]

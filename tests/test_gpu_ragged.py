@@ -22,7 +22,7 @@ def _gpu_ragged(rb, rank, cp_index=None, seg_extra=3, topk_extra=5):
     counts = torch.full((2,), -1, dtype=torch.int64, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     d_ci = torch.from_numpy(ci.astype(np.int32)).cuda()
-    cpkv.cpkv_ragged_plan_build(rb.prefix_lens, rb.q_lens, d_ci, len(ci), chunk=rb.chunk, k_align=rb.k_align,
+    cpkv.cpkv_ragged_plan_build(rb.prefix_lens, rb.q_lens, d_ci, len(ci), chunk=rb.chunk, k_align=rb.k_align, topk=rb.topk,
                                 out=out, d_counts=counts, d_status=status)
     torch.cuda.synchronize()
     return out, counts.cpu().numpy(), int(status.item()), (S, Q)
@@ -88,7 +88,7 @@ def test_ragged_empty_rank_and_bad_index():
     bad = torch.from_numpy(np.array([1, 0], np.int32)).cuda()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
-    cpkv.cpkv_ragged_plan_build(rb.prefix_lens, rb.q_lens, bad, 2, chunk=8, k_align=1, out=out, d_counts=cnt,
+    cpkv.cpkv_ragged_plan_build(rb.prefix_lens, rb.q_lens, bad, 2, chunk=8, k_align=1, topk=2048, out=out, d_counts=cnt,
                                 d_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & cpkv.STATUS_CHUNK_OOB

@@ -328,6 +328,7 @@ class RaggedBatch:
         return int(pages_per_len(self.q_lens, self.chunk).sum())
 
     split: str = "interleaved"
+    topk: int = 2048  # the NSA indexer's selected keys per query (the consumer's index width)
 
     def cp_index(self, rank: int) -> np.ndarray:
         """Chunk ids owned by ``rank``, ascending, under the batch's split:
