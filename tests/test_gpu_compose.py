@@ -540,6 +540,33 @@ def test_gather_early_behind_fill_page_geometries(ps, R):
         assert np.array_equal(dense[l].cpu().numpy(), want), l
 
 
+@pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
+def test_consumed_stagings_are_rewritten_before_every_read(batch):
+    """After a consuming gather a staging holds whatever DRAM last saw (here a
+    0xA5 poison written before the first layer): three layers of row fill +
+    consuming gather with distinct inputs, each dense buffer against the
+    oracle.  Exact only if every fill rewrites every staged row and every pad
+    row that the gather reads."""
+    plan, _ = _plan_pair(batch, dense_extra=2)
+    layers = ComposeLayers(plan, batch.row_bytes)
+    for st in layers.staging:
+        st.fill_(0xA5)
+    ps = batch.page_size
+    host = [(wl.host_pool(batch, l), wl.host_current_rows(batch, l)) for l in range(3)]
+    dense = [torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
+             for _ in range(3)]
+    torch.cuda.synchronize()
+    for l, (slabs, rows) in enumerate(host):
+        layers.fill([torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)])
+        layers.gather([torch.from_numpy(s).cuda() for s in slabs], dense[l], consume_staging=True)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    for l, (slabs, rows) in enumerate(host):
+        want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                    page_size=ps, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+        assert np.array_equal(dense[l].cpu().numpy(), want), l
+
+
 def _page_run_batch(seed=77, cp=4, ps=1, R=1152, B=5):
     """Small pages whose sources form runs: each request's prefix pages are
     consecutive local pages of one owner (ids r + cp * k for consecutive k),

@@ -279,9 +279,9 @@ def test_consumed_stagings_are_rewritten_before_every_read(batch):
     """A consuming gather drops the stagings' L2 lines, so afterwards a
     staging holds whatever DRAM last saw (here a 0xA5 poison).  The dense
     output stays exact only if the next fill rewrites every staging byte the
-    gather reads, pad slices included.  Stagings poisoned, then: row-major
-    fill + consuming gather, and twice planar fill + consuming gather, with
-    distinct inputs; every layer's dense buffer against the oracle."""
+    gather reads, pad slices included.  Stagings poisoned, then three layers
+    of planar fill + consuming gather with distinct inputs; every layer's
+    dense buffer against the oracle."""
     ps, cp = batch.page_size, batch.cp_size
     plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
                        page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages, dense_cap_pages=None).build()
@@ -289,29 +289,16 @@ def test_consumed_stagings_are_rewritten_before_every_read(batch):
     for st in layers.staging:
         st.fill_(0xA5)
     torch.cuda.synchronize()
-    dense = []
-    wants = []
-    # layer 0: the row fill over the same page geometry (rows of sum(planes) bytes)
-    row_batch = dataclasses.replace(batch, planes=None, row_kind="bytes")
-    slabs0 = wl.host_pool(row_batch, 0)
-    rows0 = wl.host_current_rows(row_batch, 0)
-    d0 = torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
-    layers.fill([torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(row_batch, rows0)])
-    layers.gather([torch.from_numpy(s).cuda() for s in slabs0], d0, consume_staging=True)
-    dense.append(d0)
-    wants.append(oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs0, rows0,
-                                      page_size=ps, cp_size=cp, dense_cap=plan.dense_cap_pages)
-                 .reshape(plan.dense_cap_pages, -1))
-    for layer in (1, 2):
+    dense, wants = [], []
+    for layer in range(3):
         slabs, planes, per_writer = _inputs(batch, seed=layer)
         d = torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
         layers.fill_planes([[torch.from_numpy(x).cuda() for x in pw] for pw in per_writer], list(batch.planes))
-        layers.gather([torch.from_numpy(s.reshape(s.shape[0], ps, -1)).cuda() for s in slabs], d,
-                      consume_staging=True)
+        layers.gather([torch.from_numpy(s).cuda() for s in slabs], d, consume_staging=True)
         dense.append(d)
         wants.append(oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs,
                                                  planes, page_size=ps, cp_size=cp, plane_bytes=list(batch.planes)))
     torch.cuda.synchronize()
     assert int(plan.d_status.item()) == 0
     for layer, (d, want) in enumerate(zip(dense, wants)):
-        assert np.array_equal(d.cpu().numpy().reshape(plan.dense_cap_pages, -1), want), layer
+        assert np.array_equal(d.cpu().numpy().reshape(plan.dense_cap_pages, ps * batch.row_bytes), want), layer
