@@ -134,8 +134,16 @@ int cpkv_writer_token_counts(int B, int page_size, int cp_size, const int32_t *h
  *   d_staging_rows   int64 [T]: staging row (i + 1) * ps + offset
  *   d_token_writer_row int32 [T]: row of the token in its writer's
  *                    current-row buffer (batch order within each writer)
+ * Workspace (device, caller-allocated, at least the bytes that
+ * cpkv_plan_workspace_bytes gives, 4-byte aligned; may be NULL when that is
+ * 0): the per-writer row totals of each block of current pages, written by
+ * the call's first kernel and read by its second.  Its contents between
+ * calls are irrelevant (every entry read is written first in the same call),
+ * and two calls whose kernels overlap on the GPU must not share one.
  * Status bits: PAGE_OOB / WRITER_OOB (the slot gets owner -1), DUP_CURRENT_PAGE,
  * CURRENT_IN_PREFIX.
+ * Errors: ARG (bad sizes, null or unaligned pointers), UNALIGNED_PREFIX,
+ * CAPACITY (dense_cap_pages < D, workspace_bytes too small), LIMIT, CUDA.
  */
 int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
                     const int32_t *h_prefix_lens, const int32_t *h_cur_lens,
@@ -143,7 +151,19 @@ int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
                     int64_t dense_cap_pages, int32_t *d_prefix_spans, int32_t *d_cur_spans,
                     int32_t *d_owner, int32_t *d_src, int32_t *d_page_inverse,
                     int32_t *d_staging_page_inverse, int64_t *d_mixed_locs, int64_t *d_staging_rows,
-                    int32_t *d_token_writer_row, int32_t *d_status, cpkv_stream_t stream);
+                    int32_t *d_token_writer_row, void *d_workspace, int64_t workspace_bytes, int32_t *d_status,
+                    cpkv_stream_t stream);
+
+/*
+ * cpkv_plan_workspace_bytes — device workspace that cpkv_plan_build needs for
+ * a batch (host only): 4 * cp_size bytes per block of current pages, a block
+ * being about 2048 current tokens (32 to 1024 pages; so a few KB for batches
+ * of a few hundred thousand tokens).  0 when the batch has no current page.
+ * Errors: ARG (B < 0, page_size <= 0, cp_size outside [1, CPKV_MAX_CP], a
+ * negative length, a null pointer), LIMIT (B > CPKV_MAX_BATCH, too many
+ * current pages for int32 indices).
+ */
+int cpkv_plan_workspace_bytes(int B, int page_size, int cp_size, const int32_t *h_cur_lens, int64_t *h_bytes);
 
 /* Flags of cpkv_fill_current(_planes), cpkv_compose_layer(_planes) and
  * cpkv_compose_fused(_planes). */

@@ -18,6 +18,7 @@ from .cpkv import (  # noqa: F401
     cpkv_fill_current_planes,
     cpkv_plan_build,
     cpkv_plan_sizes,
+    cpkv_plan_workspace_bytes,
     cpkv_ragged_plan_build,
     cpkv_ragged_plan_sizes,
     cpkv_version,
@@ -28,6 +29,6 @@ from .cpkv import (  # noqa: F401
 
 __all__ = [
     "cpkv", "CpkvError", "cpkv_compose_fused", "cpkv_compose_fused_planes", "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_layer_planes", "cpkv_fill_current", "cpkv_fill_current_planes", "cpkv_plan_build", "cpkv_plan_sizes",
-    "cpkv_ragged_plan_build", "cpkv_ragged_plan_sizes", "cpkv_version", "cpkv_writer_token_counts",
+    "cpkv_plan_workspace_bytes",    "cpkv_ragged_plan_build", "cpkv_ragged_plan_sizes", "cpkv_version", "cpkv_writer_token_counts",
     "plan_buffers", "ragged_buffers",
 ]

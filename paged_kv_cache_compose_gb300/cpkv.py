@@ -51,7 +51,8 @@ MAX_CP = 64
 MAX_BATCH = 1024
 
 EXPORTED = (
-    "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_fill_current",
+    "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_plan_workspace_bytes",
+    "cpkv_fill_current",
     "cpkv_fill_current_planes",
     "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_layer_planes",
     "cpkv_compose_fused", "cpkv_compose_fused_planes", "cpkv_selftest_ring_timeout", "cpkv_ragged_plan_sizes",
@@ -78,7 +79,8 @@ _lib = None
 def _declare(lib):
     lib.cpkv_plan_sizes.argtypes = [_I, _I, _P, _P, ctypes.POINTER(_Sizes)]
     lib.cpkv_writer_token_counts.argtypes = [_I, _I, _I, _P, _P, _L, _P]
-    lib.cpkv_plan_build.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _L] + [_P] * 11
+    lib.cpkv_plan_build.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _L] + [_P] * 10 + [_L, _P, _P]
+    lib.cpkv_plan_workspace_bytes.argtypes = [_I, _I, _I, _P, _P]
     lib.cpkv_fill_current.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _I, _P, _P]
     lib.cpkv_compose_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_fill_current_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _I, _P, _P]
@@ -191,15 +193,27 @@ def cpkv_ragged_plan_sizes(q_lens, cp_index, chunk: int):
 # device entry points (stream-ordered, asynchronous)
 # ---------------------------------------------------------------------------
 
+def cpkv_plan_workspace_bytes(cur_lens, page_size: int, cp_size: int) -> int:
+    """Device workspace bytes that ``cpkv_plan_build`` needs for this batch."""
+    cl = _host_i32(cur_lens)
+    out = ctypes.c_int64(0)
+    _check("cpkv_plan_workspace_bytes",
+           load().cpkv_plan_workspace_bytes(len(cl), page_size, cp_size, _hp(cl), ctypes.byref(out)))
+    return int(out.value)
+
+
 def cpkv_plan_build(prefix_lens, cur_lens, d_prefix_pages, d_cur_pages, d_writer, *, page_size, cp_size,
                     num_pool_pages, dense_cap_pages, out, d_status, stream=None):
-    """Build the compose plan into the tensors of ``out`` (see ``plan_buffers``)."""
+    """Build the compose plan into the tensors of ``out`` (see ``plan_buffers``;
+    ``out["workspace"]`` is the call's device workspace)."""
     pl, cl = _host_i32(prefix_lens), _host_i32(cur_lens)
+    ws = out["workspace"]
     rc = load().cpkv_plan_build(
         len(pl), page_size, cp_size, num_pool_pages, _hp(pl), _hp(cl), _dp(d_prefix_pages), _dp(d_cur_pages),
         _dp(d_writer), dense_cap_pages, _dp(out["prefix_spans"]), _dp(out["cur_spans"]), _dp(out["owner"]),
         _dp(out["src"]), _dp(out["page_inverse"]), _dp(out["staging_page_inverse"]), _dp(out["mixed_locs"]),
-        _dp(out["staging_rows"]), _dp(out["token_writer_row"]), _dp(d_status), _stream(stream))
+        _dp(out["staging_rows"]), _dp(out["token_writer_row"]), _dp(ws), ws.numel() * ws.element_size(),
+        _dp(d_status), _stream(stream))
     _check("cpkv_plan_build", rc)
 
 
@@ -369,11 +383,13 @@ def cpkv_version() -> int:
 # allocation helpers (torch device memory; no computation)
 # ---------------------------------------------------------------------------
 
-def plan_buffers(B: int, T: int, dense_cap_pages: int, num_pool_pages: int, device="cuda") -> dict:
+def plan_buffers(B: int, T: int, dense_cap_pages: int, num_pool_pages: int, device="cuda",
+                 workspace_bytes: int = 0) -> dict:
     import torch
 
     i32, i64 = torch.int32, torch.int64
     return {
+        "workspace": torch.empty(-(-workspace_bytes // 4), dtype=i32, device=device),
         "prefix_spans": torch.empty((B, 2), dtype=i32, device=device),
         "cur_spans": torch.empty((B, 2), dtype=i32, device=device),
         "owner": torch.empty(dense_cap_pages, dtype=i32, device=device),

@@ -1,17 +1,28 @@
 // cpkv_plan_build: the per-batch compose plan on the device.
 //
 // Two launches on the caller's stream, the second a programmatic dependent
-// of the first (it starts early and waits only before the inverse scatters):
-//   1. plan_init_inverses  — page_inverse[:] = -1, staging_page_inverse[:] = 0
-//                            (P entries each; the only P-sized work).
-//   2. plan_main           — blocks [0, nA): one thread per dense slot:
-//                            descriptors (owner, src) and the inverse
-//                            scatters, plus the spans (block 0);
-//                            blocks [nA, nA + nB): 32 current pages per block:
-//                            per-writer row bases and the per-token arrays.
+// of the first (it starts early and waits for the first only before it
+// touches what the first writes):
+//   1. plan_init   — blocks [0, nInit): page_inverse[:] = -1,
+//                    staging_page_inverse[:] = 0 (P entries each, the only
+//                    P-sized work); blocks [nInit, nInit + NB): per token
+//                    block j, the rows of each writer in its K current pages
+//                    (workspace[j][w]).
+//   2. plan_main   — blocks [0, nA): one thread per dense slot: descriptors
+//                    (owner, src) and the inverse scatters, plus the spans
+//                    (block 0); blocks [nA, nA + NB): K current pages per
+//                    block: per-writer row bases and the per-token arrays.
+// The per-writer row base of a current page (the row of its first token in
+// its writer's current-row buffer) is an exclusive sum over earlier pages of
+// the same writer.  It is taken in two levels: across token blocks from the
+// workspace (a block adds the totals of the blocks before it, cp values
+// each), inside a block by warp matching and a scan over its warps.  So the
+// work is linear in the number of current pages; K grows as the page size
+// shrinks (about 2048 tokens per block, 32 to 1024 pages), which keeps
+// blocks few and full on one-token pages.
 // Host lengths travel as kernel parameters (__grid_constant__), so nothing
-// is copied host-to-device and nothing syncs.  Every block rebuilds the
-// request-level exclusive scans in shared memory (B <= 1024, one block scan).
+// is copied host-to-device and nothing syncs.  Every block that needs them
+// rebuilds the request-level exclusive scans in shared memory (B <= 1024).
 //
 // Method: "staging-direct compose" message of commits d63fbd4 (spans,
 // descriptors, staging-remapped inverse, mixed_locs / staging rows built once
@@ -25,58 +36,35 @@ namespace cpkv {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kPagesPerBlock = 32;  // current pages handled by one token block (one warp lane each)
+constexpr int kTokensPerBlock = 2048;    // tokens a token block writes, about
+constexpr int kMaxPagesPerBlock = 1024;  // one current page per thread
 
 template <int MAXB>
 struct PlanParams {
-  int B, ps, cp, nA;
+  int B, ps, cp, nA, nInit, K, NB;  // K current pages per token block, NB token blocks
+  bool vec;                         // the inverses are 16-byte aligned
   int64_t P, dense_cap, D, C, T;
   const int32_t *prefix_pages, *cur_pages, *writer;
   int32_t *prefix_spans, *cur_spans, *owner, *src, *page_inverse, *staging_page_inverse;
   int64_t *mixed_locs, *staging_rows;
   int32_t *token_writer_row, *status;
+  int32_t *block_rows;  // workspace [NB][cp]: rows of writer w in token block j's pages
   int32_t prefix_lens[MAXB];
   int32_t cur_lens[MAXB];
 };
 
-__global__ void plan_init_inverses(int32_t *__restrict__ pi, int32_t *__restrict__ spi, int64_t P,
-                                   bool vec) {
-  // plan_main may start now: it waits for this grid only before its first
-  // access to the inverses.
-  release_dependents();
-  const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  if (vec) {
-    const int64_t n4 = P >> 2;
-    int4 *pi4 = reinterpret_cast<int4 *>(pi);
-    int4 *spi4 = reinterpret_cast<int4 *>(spi);
-    for (int64_t i = tid; i < n4; i += stride) {
-      pi4[i] = make_int4(-1, -1, -1, -1);
-      spi4[i] = make_int4(0, 0, 0, 0);
-    }
-    for (int64_t i = (n4 << 2) + tid; i < P; i += stride) {
-      pi[i] = -1;
-      spi[i] = 0;
-    }
-  } else {
-    for (int64_t i = tid; i < P; i += stride) {
-      pi[i] = -1;
-      spi[i] = 0;
-    }
-  }
-}
-
 // Request-level exclusive scans, one request per thread (B <= 1024).
+template <int MAXB>
 struct RequestScan {
-  int32_t dense_start[CPKV_MAX_BATCH + 1];   // first dense slot of request b
-  int32_t cur_page_start[CPKV_MAX_BATCH + 1];  // first batch current page index
-  int32_t prefix_page_start[CPKV_MAX_BATCH + 1];  // CSR offset into prefix_pages
-  int64_t token_start[CPKV_MAX_BATCH + 1];   // first batch token
+  int32_t dense_start[MAXB + 1];        // first dense slot of request b
+  int32_t cur_page_start[MAXB + 1];     // first batch current page index
+  int32_t prefix_page_start[MAXB + 1];  // CSR offset into prefix_pages
+  int64_t token_start[MAXB + 1];        // first batch token
   int64_t scratch64[33];
 };
 
 template <int MAXB>
-__device__ void build_request_scan(const PlanParams<MAXB> &p, RequestScan &rs) {
+__device__ void build_request_scan(const PlanParams<MAXB> &p, RequestScan<MAXB> &rs) {
   if (p.B <= 32) {  // one warp: shuffle scans and a single barrier
     if (threadIdx.x < 32) {
       const int b = threadIdx.x;
@@ -131,7 +119,7 @@ __device__ void build_request_scan(const PlanParams<MAXB> &p, RequestScan &rs) {
 }
 
 template <int MAXB>
-__device__ bool slot_is_prefix(const PlanParams<MAXB> &p, const RequestScan &rs, int32_t slot) {
+__device__ bool slot_is_prefix(const PlanParams<MAXB> &p, const RequestScan<MAXB> &rs, int32_t slot) {
   if (slot < 0 || slot >= p.D || p.B == 0) return false;
   const int b = upper_index<int32_t>(rs.dense_start, p.B, slot);
   return slot - rs.dense_start[b] < p.prefix_lens[b] / p.ps;
@@ -139,7 +127,7 @@ __device__ bool slot_is_prefix(const PlanParams<MAXB> &p, const RequestScan &rs,
 
 // One thread per dense slot: descriptors and inverse scatters.
 template <int MAXB>
-__device__ void plan_dense_slots(const PlanParams<MAXB> &p, const RequestScan &rs) {
+__device__ void plan_dense_slots(const PlanParams<MAXB> &p, const RequestScan<MAXB> &rs) {
   const int64_t d = (int64_t)blockIdx.x * kPlanThreads + threadIdx.x;
   if (blockIdx.x == 0 && threadIdx.x < p.B) {
     const int b = threadIdx.x;
@@ -156,7 +144,7 @@ __device__ void plan_dense_slots(const PlanParams<MAXB> &p, const RequestScan &r
     const int32_t k = (int32_t)d - rs.dense_start[b];
     const int32_t npp = p.prefix_lens[b] / p.ps;
     const unsigned int slot = (unsigned int)d;
-    // the page tables are loaded before waiting for plan_init_inverses
+    // the page tables are loaded before waiting for plan_init
     const bool is_prefix = k < npp;
     const int32_t i = is_prefix ? 0 : rs.cur_page_start[b] + (k - npp);
     const int32_t lp = is_prefix ? p.prefix_pages[rs.prefix_page_start[b] + k] : p.cur_pages[i];
@@ -193,91 +181,168 @@ __device__ void plan_dense_slots(const PlanParams<MAXB> &p, const RequestScan &r
   p.src[d] = src;
 }
 
-// 32 current pages per block: per-writer token row bases, then per-token
-// mixed_locs / staging_rows / token_writer_row.
+// Current page i of the batch: its rows n (ps, or fewer on a request's last
+// page), its first token, its dense slot, and its writer (-1 when out of
+// range).
 template <int MAXB>
-__device__ void plan_current_tokens(const PlanParams<MAXB> &p, const RequestScan &rs, int blk) {
-  __shared__ int32_t full_pages[CPKV_MAX_CP];  // pages of writer w before this block
-  __shared__ int64_t short_rows[CPKV_MAX_CP];  // missing rows of w's partial pages before this block
-  __shared__ int64_t page_tok0[kPagesPerBlock];
-  __shared__ int32_t page_slot[kPagesPerBlock];
-  __shared__ int32_t page_rows[kPagesPerBlock];
-  __shared__ int32_t page_row_base[kPagesPerBlock];
+struct CurPage {
+  int32_t n, w, slot;
+  int64_t tok0;
+};
+
+template <int MAXB>
+__device__ CurPage<MAXB> current_page(const PlanParams<MAXB> &p, const RequestScan<MAXB> &rs, int64_t i) {
+  CurPage<MAXB> c;
+  const int b = upper_index<int32_t>(rs.cur_page_start, p.B, (int32_t)i);
+  const int32_t kp = (int32_t)i - rs.cur_page_start[b];  // page index inside the request
+  c.n = min(p.ps, p.cur_lens[b] - kp * p.ps);
+  c.tok0 = rs.token_start[b] + (int64_t)kp * p.ps;
+  c.slot = rs.dense_start[b] + p.prefix_lens[b] / p.ps + kp;
+  c.w = p.writer[i];
+  if (c.w < 0 || c.w >= p.cp) c.w = -1;
+  return c;
+}
+
+// Rows of the lanes below this one whose writer is the same (`peers`, from
+// __match_any_sync), and the group's total.
+__device__ __forceinline__ void same_writer_rows(unsigned int peers, int32_t n, int32_t *before, int32_t *total) {
+  const int lane = threadIdx.x & 31;
+  int32_t b = 0, t = 0;
+#pragma unroll
+  for (int l = 0; l < 32; ++l) {
+    const int32_t nl = __shfl_sync(0xffffffffu, n, l);
+    if ((peers >> l) & 1u) {
+      t += nl;
+      if (l < lane) b += nl;
+    }
+  }
+  *before = b;
+  *total = t;
+}
+
+// Token block j of plan_init: rows of each writer in current pages
+// [j K, (j + 1) K), to the workspace.
+template <int MAXB>
+__device__ void plan_block_rows(const PlanParams<MAXB> &p, int j) {
+  __shared__ RequestScan<MAXB> rs;
+  __shared__ int32_t rows[CPKV_MAX_CP];
+  if (threadIdx.x < CPKV_MAX_CP) rows[threadIdx.x] = 0;
+  build_request_scan(p, rs);  // ends with __syncthreads()
+  const int64_t i = (int64_t)j * p.K + threadIdx.x;
+  int32_t w = -1, n = 0;
+  if ((int)threadIdx.x < p.K && i < p.C) {
+    const CurPage<MAXB> c = current_page(p, rs, i);
+    w = c.w;
+    n = w < 0 ? 0 : c.n;
+  }
+  const unsigned int peers = __match_any_sync(0xffffffffu, w);
+  int32_t before, total;
+  same_writer_rows(peers, n, &before, &total);
+  if (w >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&rows[w], total);
+  __syncthreads();
+  if ((int)threadIdx.x < p.cp) p.block_rows[(int64_t)j * p.cp + threadIdx.x] = rows[threadIdx.x];
+}
+
+template <int MAXB>
+__global__ void __launch_bounds__(kPlanThreads) plan_init(const __grid_constant__ PlanParams<MAXB> p) {
+  // plan_main may start now: it waits for this grid only before its first
+  // access to the inverses or the workspace.
+  release_dependents();
+  if ((int)blockIdx.x >= p.nInit) {
+    plan_block_rows(p, blockIdx.x - p.nInit);
+    return;
+  }
+  const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)p.nInit * blockDim.x;
+  int32_t *pi = p.page_inverse, *spi = p.staging_page_inverse;
+  int64_t done = 0;
+  if (p.vec) {
+    const int64_t n4 = p.P >> 2;
+    int4 *pi4 = reinterpret_cast<int4 *>(pi);
+    int4 *spi4 = reinterpret_cast<int4 *>(spi);
+    for (int64_t i = tid; i < n4; i += stride) {
+      pi4[i] = make_int4(-1, -1, -1, -1);
+      spi4[i] = make_int4(0, 0, 0, 0);
+    }
+    done = n4 << 2;
+  }
+  for (int64_t i = done + tid; i < p.P; i += stride) {
+    pi[i] = -1;
+    spi[i] = 0;
+  }
+}
+
+// Token block j of plan_main: per-writer row bases of current pages
+// [i0, i0 + K), i0 = j K, then their tokens' mixed_locs / staging_rows /
+// token_writer_row.
+template <int MAXB>
+__device__ void plan_current_tokens(const PlanParams<MAXB> &p, const RequestScan<MAXB> &rs, int j) {
+  __shared__ int32_t base_rows[CPKV_MAX_CP];          // rows of writer w before i0
+  __shared__ int32_t warp_rows[kPlanThreads / 32][CPKV_MAX_CP];  // per warp, then scanned over warps
+  __shared__ int32_t page_tok0[kMaxPagesPerBlock];
+  __shared__ int32_t page_slot[kMaxPagesPerBlock];
+  __shared__ int32_t page_rows[kMaxPagesPerBlock];
+  __shared__ int32_t page_row_base[kMaxPagesPerBlock];
 
   const int ps = p.ps, cp = p.cp;
-  const int64_t i0 = (int64_t)blk * kPagesPerBlock;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x < CPKV_MAX_CP) {
-    full_pages[threadIdx.x] = 0;
-    short_rows[threadIdx.x] = 0;
-  }
+  constexpr int kWarps = kPlanThreads / 32;
+  const int64_t i0 = (int64_t)j * p.K;
+  const int npages = (int)min64(p.K, p.C - i0);
+  if (threadIdx.x < CPKV_MAX_CP) base_rows[threadIdx.x] = 0;
+  for (int k = threadIdx.x; k < kWarps * CPKV_MAX_CP; k += kPlanThreads) (&warp_rows[0][0])[k] = 0;
   __syncthreads();
 
-  // pages of each writer before i0 (warp-aggregated shared atomics)
-  for (int64_t base = 0; base < i0; base += kPlanThreads) {  // uniform trip count: full warps in match
-    const int64_t i = base + threadIdx.x;
-    int32_t w = -1;
-    if (i < i0) {
-      w = p.writer[i];
-      if (w < 0 || w >= cp) w = -1;
-    }
-    const unsigned int peers = __match_any_sync(0xffffffffu, w);
-    if (w >= 0 && lane == __ffs(peers) - 1) atomicAdd(&full_pages[w], __popc(peers));
+  // this block's pages, one per thread; the rows of same-writer pages below
+  // it in the warp, and each writer's total per warp
+  const int t = threadIdx.x;
+  int32_t w = -1, n = 0;
+  if (t < npages) {
+    const CurPage<MAXB> c = current_page(p, rs, i0 + t);
+    w = c.w;
+    n = c.n;
+    page_tok0[t] = (int32_t)c.tok0;
+    page_slot[t] = c.slot;
+    page_rows[t] = c.n;
   }
-  // each request's last page, if partial and before i0, holds fewer rows
-  for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
-    const int32_t rem = p.cur_lens[b] % ps;
-    const int32_t last = rs.cur_page_start[b + 1] - 1;
-    if (rem != 0 && last < i0) {
-      const int32_t w = p.writer[last];
-      if (w >= 0 && w < cp) atomicAdd(reinterpret_cast<unsigned long long *>(&short_rows[w]),
-                                      (unsigned long long)(ps - rem));
-    }
+  const unsigned int peers = __match_any_sync(0xffffffffu, w);
+  int32_t before, total;
+  same_writer_rows(peers, w < 0 ? 0 : n, &before, &total);
+  if (w >= 0 && lane == __ffs(peers) - 1) warp_rows[warp][w] = total;
+
+  // rows of each writer in the token blocks before this one (plan_init)
+  wait_prerequisite();
+  for (int64_t k = threadIdx.x; k < (int64_t)j * cp; k += kPlanThreads) {
+    const int32_t v = p.block_rows[k];
+    if (v != 0) atomicAdd(&base_rows[(int)(k % cp)], v);
   }
   __syncthreads();
-
-  if (warp == 0) {
-    const int64_t i = i0 + lane;
-    int32_t w = -1, n = 0;
-    if (i < p.C) {
-      const int b = upper_index<int32_t>(rs.cur_page_start, p.B, (int32_t)i);
-      const int32_t kp = (int32_t)i - rs.cur_page_start[b];  // page index inside the request
-      n = min(ps, p.cur_lens[b] - kp * ps);
-      w = p.writer[i];
-      page_tok0[lane] = rs.token_start[b] + (int64_t)kp * ps;
-      page_slot[lane] = rs.dense_start[b] + p.prefix_lens[b] / ps + kp;
-      page_rows[lane] = n;
-      if (w < 0 || w >= cp) w = -1;
-    }
-    // rows of same-writer pages earlier in this block
-    int32_t before = 0;
-#pragma unroll
-    for (int l = 0; l < 32; ++l) {
-      const int32_t wl = __shfl_sync(0xffffffffu, w, l);
-      const int32_t nl = __shfl_sync(0xffffffffu, n, l);
-      if (l < lane && wl == w) before += nl;
-    }
-    if (i < p.C) {
-      page_row_base[lane] =
-          w < 0 ? -1 : (int32_t)((int64_t)full_pages[w] * ps - short_rows[w] + before);
+  // exclusive scan of each writer's rows over the warps of this block
+  if (threadIdx.x < cp) {
+    int32_t run = base_rows[threadIdx.x];
+    for (int k = 0; k < kWarps; ++k) {
+      const int32_t v = warp_rows[k][threadIdx.x];
+      warp_rows[k][threadIdx.x] = run;
+      run += v;
     }
   }
   __syncthreads();
+  if (t < npages) page_row_base[t] = w < 0 ? -1 : warp_rows[warp][w] + before;
+  __syncthreads();
 
-  const int npages = (int)min64(kPagesPerBlock, p.C - i0);
   for (int u = threadIdx.x; u < npages * ps; u += kPlanThreads) {
-    const int j = u / ps, off = u - j * ps;
-    if (off >= page_rows[j]) continue;
-    const int64_t t = page_tok0[j] + off;
-    p.mixed_locs[t] = (int64_t)page_slot[j] * ps + off;
-    p.staging_rows[t] = (i0 + j + 1) * ps + off;
-    p.token_writer_row[t] = page_row_base[j] < 0 ? -1 : page_row_base[j] + off;
+    const int jj = u / ps, off = u - jj * ps;
+    if (off >= page_rows[jj]) continue;
+    const int64_t tok = (int64_t)page_tok0[jj] + off;
+    p.mixed_locs[tok] = (int64_t)page_slot[jj] * ps + off;
+    p.staging_rows[tok] = (i0 + jj + 1) * ps + off;
+    p.token_writer_row[tok] = page_row_base[jj] < 0 ? -1 : page_row_base[jj] + off;
   }
 }
 
 template <int MAXB>
 __global__ void __launch_bounds__(kPlanThreads) plan_main(const __grid_constant__ PlanParams<MAXB> p) {
-  __shared__ RequestScan rs;
+  __shared__ RequestScan<MAXB> rs;
   build_request_scan(p, rs);
   if ((int)blockIdx.x < p.nA) {
     plan_dense_slots(p, rs);
@@ -286,12 +351,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_main(const __grid_constant_
   }
 }
 
-// plan_main is a programmatic dependent of plan_init_inverses: its request
-// scans, page-table loads, descriptors and token arrays overlap the init;
-// only the inverse scatters wait for it (wait_prerequisite).
+// Current pages per token block for page size ps: about kTokensPerBlock
+// tokens, a multiple of 32 between 32 and kMaxPagesPerBlock.
+inline int pages_per_token_block(int ps) {
+  int64_t k = kTokensPerBlock / ps;
+  k = (k + 31) / 32 * 32;
+  if (k < 32) k = 32;
+  if (k > kMaxPagesPerBlock) k = kMaxPagesPerBlock;
+  return (int)k;
+}
+
+inline int64_t workspace_bytes_for(int64_t C, int ps, int cp) {
+  return ceil_div(C, pages_per_token_block(ps)) * cp * (int64_t)sizeof(int32_t);
+}
+
+// plan_init is launched plainly; plan_main is its programmatic dependent:
+// its request scans, page-table loads, descriptors and page walks overlap the
+// init, and only the inverse scatters and the reads of the workspace wait for
+// it (wait_prerequisite).
 template <int MAXB>
-int launch_plan(const PlanParams<MAXB> &prm, int nB, cudaStream_t s) {
-  const int grid = prm.nA + nB;
+int launch_plan(const PlanParams<MAXB> &prm, cudaStream_t s) {
+  if (prm.nInit + prm.NB > 0) {
+    const int rc = launch_kernel(plan_init<MAXB>, dim3(prm.nInit + prm.NB), dim3(kPlanThreads), 0, false, s, prm);
+    if (rc != CPKV_OK) return rc;
+  }
+  const int grid = prm.nA + prm.NB;
   if (grid == 0) return CPKV_OK;
   return launch_kernel(plan_main<MAXB>, dim3(grid), dim3(kPlanThreads), 0, true, s, prm);
 }
@@ -307,6 +391,22 @@ void fill_common(PlanParams<MAXB> &prm, int B, const int32_t *pl, const int32_t 
 }  // namespace
 }  // namespace cpkv
 
+extern "C" int cpkv_plan_workspace_bytes(int B, int page_size, int cp_size, const int32_t *h_cur_lens,
+                                         int64_t *h_bytes) {
+  using namespace cpkv;
+  if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP || h_bytes == nullptr) return CPKV_ERR_ARG;
+  if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
+  if (B > 0 && h_cur_lens == nullptr) return CPKV_ERR_ARG;
+  int64_t C = 0;
+  for (int b = 0; b < B; ++b) {
+    if (h_cur_lens[b] < 0) return CPKV_ERR_ARG;
+    C += ceil_div(h_cur_lens[b], page_size);
+  }
+  if (C > INT32_MAX - 2) return CPKV_ERR_LIMIT;
+  *h_bytes = workspace_bytes_for(C, page_size, cp_size);
+  return CPKV_OK;
+}
+
 extern "C" int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
                                const int32_t *h_prefix_lens, const int32_t *h_cur_lens,
                                const int32_t *d_prefix_pages, const int32_t *d_cur_pages,
@@ -314,7 +414,8 @@ extern "C" int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_po
                                int32_t *d_cur_spans, int32_t *d_owner, int32_t *d_src,
                                int32_t *d_page_inverse, int32_t *d_staging_page_inverse,
                                int64_t *d_mixed_locs, int64_t *d_staging_rows, int32_t *d_token_writer_row,
-                               int32_t *d_status, cpkv_stream_t stream) {
+                               void *d_workspace, int64_t workspace_bytes, int32_t *d_status,
+                               cpkv_stream_t stream) {
   using namespace cpkv;
   if (cp_size < 1 || cp_size > CPKV_MAX_CP || num_pool_pages < 1 || dense_cap_pages < 0) return CPKV_ERR_ARG;
   if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
@@ -331,39 +432,42 @@ extern "C" int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_po
   if (sz.C > 0 && (d_cur_pages == nullptr || d_writer == nullptr)) return CPKV_ERR_ARG;
   if (sz.T > 0 && (d_mixed_locs == nullptr || d_staging_rows == nullptr || d_token_writer_row == nullptr))
     return CPKV_ERR_ARG;
+  const int K = pages_per_token_block(page_size);
+  const int64_t NB = ceil_div(sz.C, K);
+  const int64_t need = workspace_bytes_for(sz.C, page_size, cp_size);
+  if (workspace_bytes < 0) return CPKV_ERR_ARG;
+  if (need > 0 && (d_workspace == nullptr || (reinterpret_cast<uintptr_t>(d_workspace) & 3u) != 0))
+    return CPKV_ERR_ARG;
+  if (workspace_bytes < need) return CPKV_ERR_CAPACITY;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  {
-    const bool vec = aligned16(d_page_inverse) && aligned16(d_staging_page_inverse);
-    const int64_t work = vec ? (num_pool_pages >> 2) + 3 : num_pool_pages;
-    const int64_t blocks = ceil_div(work, 256);
-    const int grid = (int)(blocks < 4 * device_sm_count() ? (blocks > 0 ? blocks : 1) : 4 * device_sm_count());
-    plan_init_inverses<<<grid, 256, 0, s>>>(d_page_inverse, d_staging_page_inverse, num_pool_pages, vec);
-    rc = launch_status();
-    if (rc != CPKV_OK) return rc;
-  }
-
+  const bool vec = aligned16(d_page_inverse) && aligned16(d_staging_page_inverse);
+  const int64_t init_work = vec ? (num_pool_pages >> 2) + 3 : num_pool_pages;
+  const int64_t init_blocks = ceil_div(init_work, kPlanThreads);
+  const int nInit = (int)(init_blocks < 2 * device_sm_count() ? (init_blocks > 0 ? init_blocks : 1)
+                                                              : 2 * device_sm_count());
   int nA = (int)ceil_div(dense_cap_pages, kPlanThreads);
   if (nA == 0 && B > 0) nA = 1;  // block 0 writes the spans
-  const int nB = (int)ceil_div(sz.C, kPagesPerBlock);
 
 #define CPKV_FILL_PLAN(prm)                                                                        \
-  prm.B = B; prm.ps = page_size; prm.cp = cp_size; prm.nA = nA; prm.P = num_pool_pages;           \
+  prm.B = B; prm.ps = page_size; prm.cp = cp_size; prm.nA = nA; prm.nInit = nInit; prm.K = K;     \
+  prm.NB = (int)NB; prm.vec = vec; prm.P = num_pool_pages;                                         \
   prm.dense_cap = dense_cap_pages; prm.D = sz.D; prm.C = sz.C; prm.T = sz.T;                       \
   prm.prefix_pages = d_prefix_pages; prm.cur_pages = d_cur_pages; prm.writer = d_writer;           \
   prm.prefix_spans = d_prefix_spans; prm.cur_spans = d_cur_spans; prm.owner = d_owner;             \
   prm.src = d_src; prm.page_inverse = d_page_inverse; prm.staging_page_inverse = d_staging_page_inverse; \
   prm.mixed_locs = d_mixed_locs; prm.staging_rows = d_staging_rows;                                \
   prm.token_writer_row = d_token_writer_row; prm.status = d_status;                                \
+  prm.block_rows = static_cast<int32_t *>(d_workspace);                                            \
   fill_common(prm, B, h_prefix_lens, h_cur_lens);
 
   if (B <= 64) {
     PlanParams<64> prm;
     CPKV_FILL_PLAN(prm)
-    return launch_plan(prm, nB, s);
+    return launch_plan(prm, s);
   }
   PlanParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_PLAN(prm)
 #undef CPKV_FILL_PLAN
-  return launch_plan(prm, nB, s);
+  return launch_plan(prm, s);
 }

@@ -30,7 +30,9 @@ class ComposePlan:
         self.d_prefix_pages = torch.as_tensor(np.ascontiguousarray(prefix_pages, dtype=np.int32)).to(self.device)
         self.d_cur_pages = torch.as_tensor(np.ascontiguousarray(cur_pages, dtype=np.int32)).to(self.device)
         self.d_writer = torch.as_tensor(host_writer).to(self.device)
-        self.bufs = cpkv.plan_buffers(self.B, self.T, self.dense_cap_pages, num_pool_pages, self.device)
+        self.bufs = cpkv.plan_buffers(self.B, self.T, self.dense_cap_pages, num_pool_pages, self.device,
+                                      workspace_bytes=cpkv.cpkv_plan_workspace_bytes(self.cur_lens, page_size,
+                                                                                     cp_size))
         self.d_status = torch.zeros(1, dtype=torch.int32, device=self.device)
 
     @property

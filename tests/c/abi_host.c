@@ -50,10 +50,10 @@ int main(void) {
 
   /* device entry points reject bad arguments on the host, before any launch */
   CHECK(cpkv_plan_build(2, 4, 65, 16, pfx, cur, NULL, NULL, NULL, 8, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
-                        NULL, NULL, NULL, 0) == CPKV_ERR_ARG,
+                        NULL, NULL, NULL, 0, NULL, 0) == CPKV_ERR_ARG,
         "plan_build: cp_size above the limit rejected");
   CHECK(cpkv_plan_build(2, 4, 2, 16, pfx, cur, NULL, NULL, NULL, 4, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
-                        NULL, NULL, NULL, 0) == CPKV_ERR_CAPACITY,
+                        NULL, NULL, NULL, 0, NULL, 0) == CPKV_ERR_CAPACITY,
         "plan_build: dense capacity below D rejected");
   CHECK(cpkv_fill_current(2, 4, 2, 100, cur, NULL, NULL, NULL, 4, NULL, NULL, NULL, 3, 0, NULL, 0) == CPKV_ERR_ARG,
         "fill_current: row width not a multiple of 16 rejected");

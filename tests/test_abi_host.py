@@ -72,18 +72,18 @@ def test_host_errors_before_any_launch(lib):
     pl = np.array([3], np.int32)
     cl = np.array([4], np.int32)
     null = None
-    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
+    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), 0, null, null)
     assert rc == cpkv.CPKV_ERR_UNALIGNED_PREFIX
     pl = np.array([2], np.int32)
-    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 2, *([null] * 10), null)
+    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 2, *([null] * 10), 0, null, null)
     assert rc == cpkv.CPKV_ERR_CAPACITY
-    rc = lib.cpkv_plan_build(1, 2, 65, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
+    rc = lib.cpkv_plan_build(1, 2, 65, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), 0, null, null)
     assert rc == cpkv.CPKV_ERR_ARG
     big = np.zeros(1025, np.int32)
-    rc = lib.cpkv_plan_build(1025, 2, 1, 8, big.ctypes.data, big.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
+    rc = lib.cpkv_plan_build(1025, 2, 1, 8, big.ctypes.data, big.ctypes.data, *([null] * 3), 10, *([null] * 10), 0, null, null)
     assert rc == cpkv.CPKV_ERR_LIMIT
     # missing output pointers are reported, not dereferenced
-    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), null)
+    rc = lib.cpkv_plan_build(1, 2, 1, 8, pl.ctypes.data, cl.ctypes.data, *([null] * 3), 10, *([null] * 10), 0, null, null)
     assert rc == cpkv.CPKV_ERR_ARG
     # fill: row width must be a multiple of 16
     rc = lib.cpkv_fill_current(1, 2, 1, 100, cl.ctypes.data, *([null] * 3), 5, *([null] * 3), 2, 0, null, null)
