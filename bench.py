@@ -1091,7 +1091,11 @@ def run_e2e(work, a, ws):
                       "host memory every step (the other layers' dense buffers stay on the device for attention)"}
 
 
-def _graph_us(torch, fn, reps, per):
+def _graph_us(torch, fn, reps, per, inner=1):
+    """µs per unit of ``fn`` (``per`` units per call), from CUDA events around
+    ``reps`` replays of a graph that holds ``inner`` calls back to back.  With
+    inner = 1 every replay also pays the graph launch from the host; with
+    more, consecutive calls follow each other on the device."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -1100,7 +1104,8 @@ def _graph_us(torch, fn, reps, per):
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        fn()
+        for _ in range(inner):
+            fn()
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
@@ -1110,13 +1115,15 @@ def _graph_us(torch, fn, reps, per):
         g.replay()
     e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) * 1e3 / (reps * per)
+    return e0.elapsed_time(e1) * 1e3 / (reps * per * inner)
 
 
 def ragged_plan_latency(reps: int, splits=("interleaved", "contiguous", "zigzag")):
     """µs per ragged index plan build of the ragged config (B=64, 131 072 q
-    tokens, cp=8, topk=2048), per CP rank and for all ranks back to back, one
-    CUDA graph per measured set (the launch inside the graph is included)."""
+    tokens, cp=8, topk=2048): one CUDA graph per measured set, replayed
+    (``us_per_rank``: a graph holding one rank's build, so each replay also
+    pays its launch from the host; ``us_all_ranks``: all 8 ranks in one graph;
+    ``us_per_build_back_to_back``: 10 x all ranks in one graph, per build)."""
     import torch
 
     from paged_kv_cache_compose_gb300 import cpkv
@@ -1140,7 +1147,9 @@ def ragged_plan_latency(reps: int, splits=("interleaved", "contiguous", "zigzag"
                                             topk=rb.topk, out=buf, d_counts=cnt, d_status=status)
         per_rank = [_graph_us(torch, lambda j=j: build([j]), reps, 1) for j in jobs]
         all_ranks = _graph_us(torch, lambda: build(jobs), reps, 1)
+        back_to_back = _graph_us(torch, lambda: build(jobs), reps, len(jobs), inner=10)
         out[split] = {"us_per_rank": [round(x, 2) for x in per_rank], "us_all_ranks": round(all_ranks, 2),
+                      "us_per_build_back_to_back": round(back_to_back, 2),
                       "B": rb.B, "q_tokens": int(rb.q_lens.sum()), "cp": rb.cp_size, "topk": rb.topk,
                       "status_word": int(status.item())}
     return out
@@ -1152,7 +1161,9 @@ COMPOSE_PLAN_BATCHES = {"traced": wl.traced_batch, "traced_78_slab": wl.traced_7
 
 def compose_plan_latency(reps: int, names=tuple(COMPOSE_PLAN_BATCHES)):
     """µs per compose plan build (cpkv_plan_build: inverses over the whole
-    pool, descriptors, per-token arrays), one CUDA graph per batch."""
+    pool, descriptors, per-token arrays): ``us`` from a graph holding one
+    build (each replay also pays its launch from the host), ``us_back_to_back``
+    from a graph holding 10 builds in a row."""
     import torch
 
     from paged_kv_cache_compose_gb300.runtime import ComposePlan
@@ -1162,7 +1173,9 @@ def compose_plan_latency(reps: int, names=tuple(COMPOSE_PLAN_BATCHES)):
         b = COMPOSE_PLAN_BATCHES[name]()
         plan = ComposePlan(b.prefix_lens, b.cur_lens, b.prefix_pages, b.cur_pages, b.writer, page_size=b.page_size,
                            cp_size=b.cp_size, num_pool_pages=b.num_pool_pages)
-        out[name] = {"us": round(_graph_us(torch, lambda: plan.build(), reps, 1), 2), "B": b.B, "T": b.T,
+        out[name] = {"us": round(_graph_us(torch, lambda: plan.build(), reps, 1), 2),
+                     "us_back_to_back": round(_graph_us(torch, lambda: plan.build(), reps, 1, inner=10), 2),
+                     "B": b.B, "T": b.T,
                      "C": plan.C, "D": plan.D, "page_size": b.page_size, "num_pool_pages": b.num_pool_pages,
                      "status_word": int(plan.d_status.item())}
     return out

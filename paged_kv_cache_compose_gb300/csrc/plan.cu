@@ -5,8 +5,9 @@
 // touches what the first writes):
 //   1. plan_init   — blocks [0, nInit): page_inverse[:] = -1,
 //                    staging_page_inverse[:] = 0 (P entries each, the only
-//                    P-sized work); blocks [nInit, nInit + NB): per token
-//                    block j, the rows of each writer in its K current pages
+//                    P-sized work); for batches of more than 4096 current
+//                    pages, blocks [nInit, nInit + NB): per token block j,
+//                    the rows of each writer in its K current pages
 //                    (workspace[j][w]).
 //   2. plan_main   — blocks [0, nA): one thread per dense slot: descriptors
 //                    (owner, src) and the inverse scatters, plus the spans
@@ -14,12 +15,14 @@
 //                    block: per-writer row bases and the per-token arrays.
 // The per-writer row base of a current page (the row of its first token in
 // its writer's current-row buffer) is an exclusive sum over earlier pages of
-// the same writer.  It is taken in two levels: across token blocks from the
-// workspace (a block adds the totals of the blocks before it, cp values
-// each), inside a block by warp matching and a scan over its warps.  So the
-// work is linear in the number of current pages; K grows as the page size
-// shrinks (about 2048 tokens per block, 32 to 1024 pages), which keeps
-// blocks few and full on one-token pages.
+// the same writer.  It is taken in two levels: across token blocks, inside a
+// block by warp matching and a scan over its warps.  Across blocks, a batch
+// of at most 4096 current pages is counted by each block directly (a few load
+// rounds, no wait for plan_init); a larger one goes through the workspace (a
+// block adds the totals of the blocks before it, cp values each, after
+// waiting for plan_init).  So the work is linear in the number of current
+// pages; K grows as the page size shrinks (about 2048 tokens per block, 32 to
+// 1024 pages), which keeps blocks few and full on one-token pages.
 // Host lengths travel as kernel parameters (__grid_constant__), so nothing
 // is copied host-to-device and nothing syncs.  Every block that needs them
 // rebuilds the request-level exclusive scans in shared memory (B <= 1024).
@@ -38,6 +41,9 @@ namespace {
 constexpr int kPlanThreads = 1024;
 constexpr int kTokensPerBlock = 2048;    // tokens a token block writes, about
 constexpr int kMaxPagesPerBlock = 1024;  // one current page per thread
+// Batches of at most this many current pages need no workspace: a token
+// block counts the pages before it itself (at most 4 rounds of 1024 loads).
+constexpr int64_t kDirectMaxPages = 4096;
 
 template <int MAXB>
 struct PlanParams {
@@ -220,25 +226,37 @@ __device__ __forceinline__ void same_writer_rows(unsigned int peers, int32_t n, 
   *total = t;
 }
 
-// Token block j of plan_init: rows of each writer in current pages
-// [j K, (j + 1) K), to the workspace.
+// Add the rows of each writer in current pages [first, last) to rows[w]
+// (shared, block-wide call: one page per thread per round, lanes of one
+// writer summed in the warp, one shared atomic per writer and warp).
+template <int MAXB>
+__device__ void add_writer_rows(const PlanParams<MAXB> &p, const RequestScan<MAXB> &rs, int64_t first,
+                                int64_t last, int32_t *rows) {
+  for (int64_t base = first; base < last; base += kPlanThreads) {  // uniform trip count: full warps in match
+    const int64_t i = base + threadIdx.x;
+    int32_t w = -1, n = 0;
+    if (i < last) {
+      const CurPage<MAXB> c = current_page(p, rs, i);
+      w = c.w;
+      n = w < 0 ? 0 : c.n;
+    }
+    const unsigned int peers = __match_any_sync(0xffffffffu, w);
+    int32_t before, total;
+    same_writer_rows(peers, n, &before, &total);
+    if (w >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&rows[w], total);
+  }
+}
+
+// Token block j of plan_init (batches of more than kDirectMaxPages current
+// pages): rows of each writer in current pages [j K, (j + 1) K), to the
+// workspace.
 template <int MAXB>
 __device__ void plan_block_rows(const PlanParams<MAXB> &p, int j) {
   __shared__ RequestScan<MAXB> rs;
   __shared__ int32_t rows[CPKV_MAX_CP];
   if (threadIdx.x < CPKV_MAX_CP) rows[threadIdx.x] = 0;
   build_request_scan(p, rs);  // ends with __syncthreads()
-  const int64_t i = (int64_t)j * p.K + threadIdx.x;
-  int32_t w = -1, n = 0;
-  if ((int)threadIdx.x < p.K && i < p.C) {
-    const CurPage<MAXB> c = current_page(p, rs, i);
-    w = c.w;
-    n = w < 0 ? 0 : c.n;
-  }
-  const unsigned int peers = __match_any_sync(0xffffffffu, w);
-  int32_t before, total;
-  same_writer_rows(peers, n, &before, &total);
-  if (w >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&rows[w], total);
+  add_writer_rows(p, rs, (int64_t)j * p.K, min64((int64_t)(j + 1) * p.K, p.C), rows);
   __syncthreads();
   if ((int)threadIdx.x < p.cp) p.block_rows[(int64_t)j * p.cp + threadIdx.x] = rows[threadIdx.x];
 }
@@ -287,7 +305,7 @@ __device__ void plan_current_tokens(const PlanParams<MAXB> &p, const RequestScan
   const int ps = p.ps, cp = p.cp;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int kWarps = kPlanThreads / 32;
-  const int64_t i0 = (int64_t)j * p.K;
+  const int64_t i0 = (int64_t)j * p.K;  // this block's first current page
   const int npages = (int)min64(p.K, p.C - i0);
   if (threadIdx.x < CPKV_MAX_CP) base_rows[threadIdx.x] = 0;
   for (int k = threadIdx.x; k < kWarps * CPKV_MAX_CP; k += kPlanThreads) (&warp_rows[0][0])[k] = 0;
@@ -309,18 +327,36 @@ __device__ void plan_current_tokens(const PlanParams<MAXB> &p, const RequestScan
   int32_t before, total;
   same_writer_rows(peers, w < 0 ? 0 : n, &before, &total);
   if (w >= 0 && lane == __ffs(peers) - 1) warp_rows[warp][w] = total;
+  __syncthreads();
 
-  // rows of each writer in the token blocks before this one (plan_init)
-  wait_prerequisite();
-  for (int64_t k = threadIdx.x; k < (int64_t)j * cp; k += kPlanThreads) {
-    const int32_t v = p.block_rows[k];
-    if (v != 0) atomicAdd(&base_rows[(int)(k % cp)], v);
+  // the token locations that need no row base, while plan_init still runs
+  for (int u = threadIdx.x; u < npages * ps; u += kPlanThreads) {
+    const int jj = u / ps, off = u - jj * ps;
+    if (off >= page_rows[jj]) continue;
+    const int64_t tok = (int64_t)page_tok0[jj] + off;
+    p.mixed_locs[tok] = (int64_t)page_slot[jj] * ps + off;
+    p.staging_rows[tok] = (i0 + jj + 1) * ps + off;
+  }
+
+  // rows of each writer in the pages before this block: counted here when
+  // the batch is small (at most kDirectMaxPages pages, a few load rounds, no
+  // wait), else the totals of the blocks before this one from the workspace
+  // (plan_init)
+  if (p.block_rows == nullptr) {
+    add_writer_rows(p, rs, 0, i0, base_rows);
+  } else {
+    wait_prerequisite();
+    for (int64_t k = threadIdx.x; k < (int64_t)j * cp; k += kPlanThreads) {
+      const int32_t v = p.block_rows[k];
+      if (v != 0) atomicAdd(&base_rows[(int)(k % cp)], v);
+    }
   }
   __syncthreads();
-  // exclusive scan of each writer's rows over the warps of this block
+  // exclusive scan of each writer's rows over the warps that hold pages
   if (threadIdx.x < cp) {
+    const int used = (npages + 31) / 32;
     int32_t run = base_rows[threadIdx.x];
-    for (int k = 0; k < kWarps; ++k) {
+    for (int k = 0; k < used; ++k) {
       const int32_t v = warp_rows[k][threadIdx.x];
       warp_rows[k][threadIdx.x] = run;
       run += v;
@@ -333,10 +369,7 @@ __device__ void plan_current_tokens(const PlanParams<MAXB> &p, const RequestScan
   for (int u = threadIdx.x; u < npages * ps; u += kPlanThreads) {
     const int jj = u / ps, off = u - jj * ps;
     if (off >= page_rows[jj]) continue;
-    const int64_t tok = (int64_t)page_tok0[jj] + off;
-    p.mixed_locs[tok] = (int64_t)page_slot[jj] * ps + off;
-    p.staging_rows[tok] = (i0 + jj + 1) * ps + off;
-    p.token_writer_row[tok] = page_row_base[jj] < 0 ? -1 : page_row_base[jj] + off;
+    p.token_writer_row[(int64_t)page_tok0[jj] + off] = page_row_base[jj] < 0 ? -1 : page_row_base[jj] + off;
   }
 }
 
@@ -362,6 +395,7 @@ inline int pages_per_token_block(int ps) {
 }
 
 inline int64_t workspace_bytes_for(int64_t C, int ps, int cp) {
+  if (C <= kDirectMaxPages) return 0;
   return ceil_div(C, pages_per_token_block(ps)) * cp * (int64_t)sizeof(int32_t);
 }
 
@@ -371,8 +405,10 @@ inline int64_t workspace_bytes_for(int64_t C, int ps, int cp) {
 // it (wait_prerequisite).
 template <int MAXB>
 int launch_plan(const PlanParams<MAXB> &prm, cudaStream_t s) {
-  if (prm.nInit + prm.NB > 0) {
-    const int rc = launch_kernel(plan_init<MAXB>, dim3(prm.nInit + prm.NB), dim3(kPlanThreads), 0, false, s, prm);
+  const int nRowBlocks = prm.block_rows != nullptr ? prm.NB : 0;
+  {
+    const int rc = launch_kernel(plan_init<MAXB>, dim3(prm.nInit + nRowBlocks), dim3(kPlanThreads), 0, false, s,
+                                 prm);
     if (rc != CPKV_OK) return rc;
   }
   const int grid = prm.nA + prm.NB;
@@ -458,7 +494,7 @@ extern "C" int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_po
   prm.src = d_src; prm.page_inverse = d_page_inverse; prm.staging_page_inverse = d_staging_page_inverse; \
   prm.mixed_locs = d_mixed_locs; prm.staging_rows = d_staging_rows;                                \
   prm.token_writer_row = d_token_writer_row; prm.status = d_status;                                \
-  prm.block_rows = static_cast<int32_t *>(d_workspace);                                            \
+  prm.block_rows = need > 0 ? static_cast<int32_t *>(d_workspace) : nullptr;                      \
   fill_common(prm, B, h_prefix_lens, h_cur_lens);
 
   if (B <= 64) {

@@ -62,6 +62,43 @@ def test_plan_matches_oracle_fp8_full_size():
     _assert_plan_equal(plan, want)
 
 
+def _many_pages_batch(name, seed, ps, cp, B, cur_hi, writers="random"):
+    rng = np.random.default_rng(seed)
+    cur = rng.integers(1, cur_hi, B)
+    pfx = (rng.integers(0, 4 * cur_hi, B) // ps) * ps
+    C = int(((cur + ps - 1) // ps).sum())
+    writer = rng.integers(0, cp, C) if writers == "random" else None
+    P = int((pfx // ps).sum() + C + 10)
+    return wl.make_compose_batch(name, seed, page_size=ps, cp_size=cp, num_pool_pages=P, row_bytes=16,
+                                 prefix_lens=pfx, cur_lens=cur, writer=writer, row_kind="bytes", rng=rng)
+
+
+def _exact_pages_batch(C, ps=1, cp=5, seed=9):
+    """A batch of exactly C current pages (the workspace threshold sits at 4096)."""
+    rng = np.random.default_rng(seed)
+    cur = np.full(4, (C // 4) * ps)
+    cur[0] += (C - int(cur.sum()) // ps) * ps
+    return wl.make_compose_batch(f"C{C}", seed, page_size=ps, cp_size=cp, num_pool_pages=C + 64, row_bytes=16,
+                                 prefix_lens=np.array([0, ps, 0, 2 * ps]), cur_lens=cur,
+                                 writer=rng.integers(0, cp, C), row_kind="bytes", rng=rng)
+
+
+@pytest.mark.parametrize("batch", [
+    _exact_pages_batch(4096), _exact_pages_batch(4097), _exact_pages_batch(5000, ps=2),
+    _many_pages_batch("ps1-random", 31, 1, 8, 12, 7000),
+    _many_pages_batch("ps3-random", 32, 3, 7, 40, 2000),
+    _many_pages_batch("ps16-b300", 33, 16, 5, 300, 600),
+    _many_pages_batch("ps1-b1000-rr", 34, 1, 12, 1000, 60, writers="round-robin"),
+], ids=lambda b: b.name)
+def test_plan_matches_oracle_many_current_pages(batch):
+    """Batches of more than 4096 current pages take their per-writer row
+    bases from per-block totals in the workspace (random and round-robin
+    writers, partial pages, the B > 64 parameter block); at most 4096, each
+    block counts the pages before it directly."""
+    plan, want = _plan_pair(batch, dense_extra=2)
+    _assert_plan_equal(plan, want)
+
+
 def test_plan_large_batch_template():
     """B > 64 takes the 1024-request parameter block."""
     rng = np.random.default_rng(5)
