@@ -156,10 +156,9 @@ int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
 
 /*
  * cpkv_plan_workspace_bytes — device workspace that cpkv_plan_build needs for
- * a batch (host only).  0 for batches of at most 4096 current pages, which
- * the plan counts without one; else 4 * cp_size bytes per block of current
- * pages, a block being about 2048 current tokens (32 to 1024 pages; so a few
- * KB for batches of a few hundred thousand tokens).
+ * a batch (host only): 4 * cp_size bytes per block of current pages, a block
+ * being about 2048 current tokens (32 to 1024 pages; so a few KB for batches
+ * of a few hundred thousand tokens).  0 when the batch has no current page.
  * Errors: ARG (B < 0, page_size <= 0, cp_size outside [1, CPKV_MAX_CP], a
  * negative length, a null pointer), LIMIT (B > CPKV_MAX_BATCH, too many
  * current pages for int32 indices).

@@ -5,9 +5,8 @@
 // touches what the first writes):
 //   1. plan_init   — blocks [0, nInit): page_inverse[:] = -1,
 //                    staging_page_inverse[:] = 0 (P entries each, the only
-//                    P-sized work); for batches of more than 4096 current
-//                    pages, blocks [nInit, nInit + NB): per token block j,
-//                    the rows of each writer in its K current pages
+//                    P-sized work); blocks [nInit, nInit + NB): per token
+//                    block j, the rows of each writer in its K current pages
 //                    (workspace[j][w]).
 //   2. plan_main   — blocks [0, nA): one thread per dense slot: descriptors
 //                    (owner, src) and the inverse scatters, plus the spans
@@ -15,14 +14,19 @@
 //                    block: per-writer row bases and the per-token arrays.
 // The per-writer row base of a current page (the row of its first token in
 // its writer's current-row buffer) is an exclusive sum over earlier pages of
-// the same writer.  It is taken in two levels: across token blocks, inside a
-// block by warp matching and a scan over its warps.  Across blocks, a batch
-// of at most 4096 current pages is counted by each block directly (a few load
-// rounds, no wait for plan_init); a larger one goes through the workspace (a
-// block adds the totals of the blocks before it, cp values each, after
-// waiting for plan_init).  So the work is linear in the number of current
-// pages; K grows as the page size shrinks (about 2048 tokens per block, 32 to
-// 1024 pages), which keeps blocks few and full on one-token pages.
+// the same writer.  It is taken in two levels: across token blocks from the
+// workspace (a block adds the totals of the blocks before it, cp values
+// each), inside a block by warp matching and a scan over its warps.  So the
+// work is linear in the number of current pages; K grows as the page size
+// shrinks (about 2048 tokens per block, 32 to 1024 pages), which keeps
+// blocks few and full on one-token pages.  Measured per build, 10 builds back
+// to back in a CUDA graph: traced batch 6.36 us, fp8 batch 8.0 us, traced
+// lengths on one-token pages 8.2 us.  Each block counting the pages before it
+// itself (no workspace, no wait for plan_init) measured slower: 6.77, 9.5 and
+// 8.2 us.  The first form, each 32-page block rescanning all earlier pages,
+// took 78 us per build on one-token pages.
+// (Token blocks that hold only part of a warp's pages, and warps without a
+// short page, skip the per-lane row sums: a full page holds ps rows.)
 // Host lengths travel as kernel parameters (__grid_constant__), so nothing
 // is copied host-to-device and nothing syncs.  Every block that needs them
 // rebuilds the request-level exclusive scans in shared memory (B <= 1024).
@@ -41,9 +45,6 @@ namespace {
 constexpr int kPlanThreads = 1024;
 constexpr int kTokensPerBlock = 2048;    // tokens a token block writes, about
 constexpr int kMaxPagesPerBlock = 1024;  // one current page per thread
-// Batches of at most this many current pages need no workspace: a token
-// block counts the pages before it itself (at most 4 rounds of 1024 loads).
-constexpr int64_t kDirectMaxPages = 4096;
 
 template <int MAXB>
 struct PlanParams {
@@ -210,9 +211,19 @@ __device__ CurPage<MAXB> current_page(const PlanParams<MAXB> &p, const RequestSc
 }
 
 // Rows of the lanes below this one whose writer is the same (`peers`, from
-// __match_any_sync), and the group's total.
-__device__ __forceinline__ void same_writer_rows(unsigned int peers, int32_t n, int32_t *before, int32_t *total) {
+// __match_any_sync), and the group's total (warp-uniform call).  A lane
+// whose page is full holds ps rows, so a warp without short pages (only a
+// request's last page can be short) counts lanes; otherwise the rows are
+// summed over the lanes by shuffles.
+__device__ __forceinline__ void same_writer_rows(unsigned int peers, int32_t n, bool valid, int ps, int32_t *before,
+                                                 int32_t *total) {
   const int lane = threadIdx.x & 31;
+  const unsigned int below = (1u << lane) - 1u;
+  if (__ballot_sync(0xffffffffu, valid && n != ps) == 0u) {
+    *before = ps * __popc(peers & below);
+    *total = ps * __popc(peers);
+    return;
+  }
   int32_t b = 0, t = 0;
 #pragma unroll
   for (int l = 0; l < 32; ++l) {
@@ -229,21 +240,29 @@ __device__ __forceinline__ void same_writer_rows(unsigned int peers, int32_t n, 
 // Add the rows of each writer in current pages [first, last) to rows[w]
 // (shared, block-wide call: one page per thread per round, lanes of one
 // writer summed in the warp, one shared atomic per writer and warp).
+// Every page counts ps rows (one coalesced load of the writers per round,
+// lanes of one writer counted by the warp); then each request whose last
+// page is short and in the range takes back the rows that page lacks.
 template <int MAXB>
 __device__ void add_writer_rows(const PlanParams<MAXB> &p, const RequestScan<MAXB> &rs, int64_t first,
                                 int64_t last, int32_t *rows) {
   for (int64_t base = first; base < last; base += kPlanThreads) {  // uniform trip count: full warps in match
     const int64_t i = base + threadIdx.x;
-    int32_t w = -1, n = 0;
+    int32_t w = -1;
     if (i < last) {
-      const CurPage<MAXB> c = current_page(p, rs, i);
-      w = c.w;
-      n = w < 0 ? 0 : c.n;
+      w = p.writer[i];
+      if (w < 0 || w >= p.cp) w = -1;
     }
     const unsigned int peers = __match_any_sync(0xffffffffu, w);
-    int32_t before, total;
-    same_writer_rows(peers, n, &before, &total);
-    if (w >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&rows[w], total);
+    if (w >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&rows[w], p.ps * __popc(peers));
+  }
+  for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
+    const int32_t rem = p.cur_lens[b] % p.ps;
+    const int64_t lastp = rs.cur_page_start[b + 1] - 1;
+    if (rem != 0 && lastp >= first && lastp < last) {
+      const int32_t w = p.writer[lastp];
+      if (w >= 0 && w < p.cp) atomicAdd(&rows[w], rem - p.ps);
+    }
   }
 }
 
@@ -323,10 +342,13 @@ __device__ void plan_current_tokens(const PlanParams<MAXB> &p, const RequestScan
     page_slot[t] = c.slot;
     page_rows[t] = c.n;
   }
-  const unsigned int peers = __match_any_sync(0xffffffffu, w);
-  int32_t before, total;
-  same_writer_rows(peers, w < 0 ? 0 : n, &before, &total);
-  if (w >= 0 && lane == __ffs(peers) - 1) warp_rows[warp][w] = total;
+  int32_t before = 0;
+  if (warp * 32 < npages) {  // warps that hold pages
+    const unsigned int peers = __match_any_sync(0xffffffffu, w);
+    int32_t total;
+    same_writer_rows(peers, n, w >= 0, ps, &before, &total);
+    if (w >= 0 && lane == __ffs(peers) - 1) warp_rows[warp][w] = total;
+  }
   __syncthreads();
 
   // the token locations that need no row base, while plan_init still runs
@@ -338,18 +360,12 @@ __device__ void plan_current_tokens(const PlanParams<MAXB> &p, const RequestScan
     p.staging_rows[tok] = (i0 + jj + 1) * ps + off;
   }
 
-  // rows of each writer in the pages before this block: counted here when
-  // the batch is small (at most kDirectMaxPages pages, a few load rounds, no
-  // wait), else the totals of the blocks before this one from the workspace
-  // (plan_init)
-  if (p.block_rows == nullptr) {
-    add_writer_rows(p, rs, 0, i0, base_rows);
-  } else {
-    wait_prerequisite();
-    for (int64_t k = threadIdx.x; k < (int64_t)j * cp; k += kPlanThreads) {
-      const int32_t v = p.block_rows[k];
-      if (v != 0) atomicAdd(&base_rows[(int)(k % cp)], v);
-    }
+  // rows of each writer in the pages before this block: the totals of the
+  // token blocks before this one, from the workspace (plan_init)
+  wait_prerequisite();
+  for (int64_t k = threadIdx.x; k < (int64_t)j * cp; k += kPlanThreads) {
+    const int32_t v = p.block_rows[k];
+    if (v != 0) atomicAdd(&base_rows[(int)(k % cp)], v);
   }
   __syncthreads();
   // exclusive scan of each writer's rows over the warps that hold pages
@@ -395,7 +411,6 @@ inline int pages_per_token_block(int ps) {
 }
 
 inline int64_t workspace_bytes_for(int64_t C, int ps, int cp) {
-  if (C <= kDirectMaxPages) return 0;
   return ceil_div(C, pages_per_token_block(ps)) * cp * (int64_t)sizeof(int32_t);
 }
 
@@ -405,10 +420,8 @@ inline int64_t workspace_bytes_for(int64_t C, int ps, int cp) {
 // it (wait_prerequisite).
 template <int MAXB>
 int launch_plan(const PlanParams<MAXB> &prm, cudaStream_t s) {
-  const int nRowBlocks = prm.block_rows != nullptr ? prm.NB : 0;
   {
-    const int rc = launch_kernel(plan_init<MAXB>, dim3(prm.nInit + nRowBlocks), dim3(kPlanThreads), 0, false, s,
-                                 prm);
+    const int rc = launch_kernel(plan_init<MAXB>, dim3(prm.nInit + prm.NB), dim3(kPlanThreads), 0, false, s, prm);
     if (rc != CPKV_OK) return rc;
   }
   const int grid = prm.nA + prm.NB;
@@ -494,7 +507,7 @@ extern "C" int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_po
   prm.src = d_src; prm.page_inverse = d_page_inverse; prm.staging_page_inverse = d_staging_page_inverse; \
   prm.mixed_locs = d_mixed_locs; prm.staging_rows = d_staging_rows;                                \
   prm.token_writer_row = d_token_writer_row; prm.status = d_status;                                \
-  prm.block_rows = need > 0 ? static_cast<int32_t *>(d_workspace) : nullptr;                      \
+  prm.block_rows = static_cast<int32_t *>(d_workspace);                                            \
   fill_common(prm, B, h_prefix_lens, h_cur_lens);
 
   if (B <= 64) {

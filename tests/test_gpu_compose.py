@@ -91,10 +91,10 @@ def _exact_pages_batch(C, ps=1, cp=5, seed=9):
     _many_pages_batch("ps1-b1000-rr", 34, 1, 12, 1000, 60, writers="round-robin"),
 ], ids=lambda b: b.name)
 def test_plan_matches_oracle_many_current_pages(batch):
-    """Batches of more than 4096 current pages take their per-writer row
-    bases from per-block totals in the workspace (random and round-robin
-    writers, partial pages, the B > 64 parameter block); at most 4096, each
-    block counts the pages before it directly."""
+    """Batches of thousands of current pages in many token blocks: per-writer
+    row bases from per-block totals in the workspace (random and round-robin
+    writers, partial pages, blocks of 1024 one-token pages, the B > 64
+    parameter block)."""
     plan, want = _plan_pair(batch, dense_extra=2)
     _assert_plan_equal(plan, want)
 

@@ -88,16 +88,13 @@ def test_two_level_row_bases_match_oracle(batch):
     got, NB = model_token_writer_row(batch)
     assert np.array_equal(got, want)
     cuda_build.build()
-    C = int(((np.asarray(batch.cur_lens) + batch.page_size - 1) // batch.page_size).sum())
-    # batches of at most 4096 current pages are counted without a workspace
-    assert cpkv.cpkv_plan_workspace_bytes(batch.cur_lens, batch.page_size, batch.cp_size) == \
-        (NB * batch.cp_size * 4 if C > 4096 else 0)
+    assert cpkv.cpkv_plan_workspace_bytes(batch.cur_lens, batch.page_size, batch.cp_size) == NB * batch.cp_size * 4
 
 
 def test_short_workspace_is_refused_before_any_launch():
     cuda_build.build()
     lib = cpkv.load()
-    b = wl.traced_78_token_pages_batch()  # 44 600 current pages: the workspace path
+    b = wl.traced_78_token_pages_batch()  # 44 600 current pages in 44 blocks
     need = cpkv.cpkv_plan_workspace_bytes(b.cur_lens, b.page_size, b.cp_size)
     assert need > 0
     pl = np.ascontiguousarray(b.prefix_lens, np.int32)
@@ -112,9 +109,9 @@ def test_short_workspace_is_refused_before_any_launch():
 
 def test_workspace_is_small():
     cuda_build.build()
-    for batch in (wl.traced_batch(), wl.fp8_nsa_batch()):  # 703 and 2065 current pages: none
-        assert cpkv.cpkv_plan_workspace_bytes(batch.cur_lens, batch.page_size, batch.cp_size) == 0, batch.name
-    b = wl.traced_78_token_pages_batch()  # 44 600 one-token pages: 44 blocks x 8 writers
-    assert cpkv.cpkv_plan_workspace_bytes(b.cur_lens, b.page_size, b.cp_size) == 44 * 8 * 4
+    # traced: 703 pages in blocks of 32; fp8: 2065 in blocks of 32; one-token
+    # pages: 44 600 in blocks of 1024; 8 writers, 4 bytes each
+    for batch, blocks in ((wl.traced_batch(), 22), (wl.fp8_nsa_batch(), 65), (wl.traced_78_token_pages_batch(), 44)):
+        assert cpkv.cpkv_plan_workspace_bytes(batch.cur_lens, batch.page_size, batch.cp_size) == blocks * 8 * 4
     assert cpkv.cpkv_plan_workspace_bytes([0, 0], 16, 4) == 0
     assert cpkv.cpkv_plan_workspace_bytes([4097], 1, 4) == 5 * 4 * 4
