@@ -165,6 +165,38 @@ int cpkv_plan_build(int B, int page_size, int cp_size, int64_t num_pool_pages,
  */
 int cpkv_plan_workspace_bytes(int B, int page_size, int cp_size, const int32_t *h_cur_lens, int64_t *h_bytes);
 
+/*
+ * cpkv_plan_build_noalloc — cpkv_plan_build for callers that cannot allocate
+ * device memory, not even the small workspace: a plugin inside a framework
+ * whose caching allocator owns all device memory (a raw cudaMalloc would
+ * bypass it, and cudaMalloc / cudaFree synchronise the device), or a server
+ * that reserved nearly all of HBM for its KV cache pool up front.  The pages
+ * have no counterpart of this call; it exists for such callers only.
+ *
+ * Same arguments, outputs, status bits and errors as cpkv_plan_build, minus
+ * the workspace: the call uses a fixed 64 KiB array in device memory that the
+ * library holds on every GPU it is loaded on until the process exits, and
+ * allocates nothing.  The caller still passes every input and output.
+ *   - Limit: batches whose cpkv_plan_workspace_bytes exceeds 65536 bytes
+ *     (more than 16384 / cp_size blocks of current pages, e.g. about 4M
+ *     current tokens at cp_size 8) return CPKV_ERR_LIMIT, nothing launched.
+ *   - Set-up: the first call on a device, with that device current, looks up
+ *     the array's device address (cudaGetSymbolAddress) and keeps it; make
+ *     that first call before any stream capture on the device.  A failed
+ *     look-up returns CPKV_ERR_CUDA.
+ *   - Sharing: all calls on a device use the one array, which keeps the last
+ *     call's contents (no entry needs clearing: a call reads only what it
+ *     wrote).  Calls whose kernels overlap on the GPU race on it; order them
+ *     on one stream or with events.
+ */
+int cpkv_plan_build_noalloc(int B, int page_size, int cp_size, int64_t num_pool_pages,
+                            const int32_t *h_prefix_lens, const int32_t *h_cur_lens,
+                            const int32_t *d_prefix_pages, const int32_t *d_cur_pages, const int32_t *d_writer,
+                            int64_t dense_cap_pages, int32_t *d_prefix_spans, int32_t *d_cur_spans,
+                            int32_t *d_owner, int32_t *d_src, int32_t *d_page_inverse,
+                            int32_t *d_staging_page_inverse, int64_t *d_mixed_locs, int64_t *d_staging_rows,
+                            int32_t *d_token_writer_row, int32_t *d_status, cpkv_stream_t stream);
+
 /* Flags of cpkv_fill_current(_planes), cpkv_compose_layer(_planes) and
  * cpkv_compose_fused(_planes). */
 /* The stagings are consumed, as with CPKV_GATHER_CONSUME_STAGING (layer

@@ -52,6 +52,7 @@ MAX_BATCH = 1024
 
 EXPORTED = (
     "cpkv_plan_sizes", "cpkv_writer_token_counts", "cpkv_plan_build", "cpkv_plan_workspace_bytes",
+    "cpkv_plan_build_noalloc",
     "cpkv_fill_current",
     "cpkv_fill_current_planes",
     "cpkv_compose_gather", "cpkv_compose_gather_kinds", "cpkv_compose_layer", "cpkv_compose_layer_planes",
@@ -81,6 +82,7 @@ def _declare(lib):
     lib.cpkv_writer_token_counts.argtypes = [_I, _I, _I, _P, _P, _L, _P]
     lib.cpkv_plan_build.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _L] + [_P] * 10 + [_L, _P, _P]
     lib.cpkv_plan_workspace_bytes.argtypes = [_I, _I, _I, _P, _P]
+    lib.cpkv_plan_build_noalloc.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _P, _L] + [_P] * 11
     lib.cpkv_fill_current.argtypes = [_I, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _L, _I, _P, _P]
     lib.cpkv_compose_gather.argtypes = [_I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P]
     lib.cpkv_fill_current_planes.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _I, _P, _P]
@@ -215,6 +217,21 @@ def cpkv_plan_build(prefix_lens, cur_lens, d_prefix_pages, d_cur_pages, d_writer
         _dp(out["staging_rows"]), _dp(out["token_writer_row"]), _dp(ws), ws.numel() * ws.element_size(),
         _dp(d_status), _stream(stream))
     _check("cpkv_plan_build", rc)
+
+
+def cpkv_plan_build_noalloc(prefix_lens, cur_lens, d_prefix_pages, d_cur_pages, d_writer, *, page_size, cp_size,
+                            num_pool_pages, dense_cap_pages, out, d_status, stream=None):
+    """``cpkv_plan_build`` without a caller workspace: the library's fixed
+    device array serves instead (for callers that cannot allocate; see
+    include/cpkv.h for its size limit and sharing rules).  ``out`` as for
+    ``cpkv_plan_build``; its "workspace" entry, if any, is not used."""
+    pl, cl = _host_i32(prefix_lens), _host_i32(cur_lens)
+    rc = load().cpkv_plan_build_noalloc(
+        len(pl), page_size, cp_size, num_pool_pages, _hp(pl), _hp(cl), _dp(d_prefix_pages), _dp(d_cur_pages),
+        _dp(d_writer), dense_cap_pages, _dp(out["prefix_spans"]), _dp(out["cur_spans"]), _dp(out["owner"]),
+        _dp(out["src"]), _dp(out["page_inverse"]), _dp(out["staging_page_inverse"]), _dp(out["mixed_locs"]),
+        _dp(out["staging_rows"]), _dp(out["token_writer_row"]), _dp(d_status), _stream(stream))
+    _check("cpkv_plan_build_noalloc", rc)
 
 
 def cpkv_fill_current(cur_lens, cur_rows: Sequence, staging: Sequence, *, page_size, cp_size, row_bytes,
