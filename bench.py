@@ -205,7 +205,7 @@ class ComposeWorkload:
 
     def __init__(self, config: str = "traced_78", device="cuda", num_layers: int | None = None,
                  variant: str = "staging", pool_pages: int | None = None, consume_staging: bool | None = None,
-                 num_dense: int = 2, early: bool = True):
+                 num_dense: int = 2, early: bool = True, fill_mode: str = "pages"):
         import torch
 
         from paged_kv_cache_compose_gb300 import cpkv
@@ -226,6 +226,10 @@ class ComposeWorkload:
         # per layer keeps every layer's output for a full parity check)
         self.layers = ComposeLayers(self.plan, b.row_bytes, num_dense=num_dense)
         self.early = bool(early)
+        # the fill moves each current page as one run (its plan is cpkv_plan_build's), or row by row
+        if fill_mode not in ("pages", "rows"):
+            raise ValueError(fill_mode)
+        self.fill_mode = fill_mode
         # pools: one per layer (own slab) unless the config shares one pool over its layers
         self.shared_pool = config in ("fp8_nsa", "index_k")
         n_pools = 1 if self.shared_pool else self.num_layers
@@ -364,7 +368,7 @@ class ComposeWorkload:
             if self.batch.planes:
                 self.layers.fill_planes(self.rows[layer], list(self.batch.planes), stream, early_inputs=early)
             else:
-                self.layers.fill(self.rows[layer], stream, early_inputs=early)
+                self.layers.fill(self.rows[layer], stream, early_inputs=early, page_runs=self.fill_mode == "pages")
         if kind in ("all", "gather"):
             self.layers.gather(self.pools_of(layer), dense, stream, consume_staging=self.consume_staging,
                                early_inputs=early)
@@ -757,7 +761,7 @@ def extra_configs(a, device, hbm_peak):
     out = {}
     steps = max(5, min(a.steps, 20))
     t0 = time.perf_counter()
-    work = ComposeWorkload("fp8_nsa", device=device, variant=a.variant)
+    work = ComposeWorkload("fp8_nsa", device=device, variant=a.variant, fill_mode=a.fill_mode)
     setup_s = time.perf_counter() - t0
     warm_and_capture(work, 3)
     st0 = work.status()
@@ -817,6 +821,9 @@ def main(argv=None):
     ap.add_argument("--consume-staging", choices=["auto", "on", "off"], default="auto",
                     help="staging variant: the gather drops each staging piece's L2 lines after reading it "
                          "(the stagings are refilled before their next read); auto = on for row-major pages")
+    ap.add_argument("--fill-mode", choices=["pages", "rows"], default="pages",
+                    help="staging variant: the fill moves each current page as one run (the plan's pages are "
+                         "runs) or copies row by row through the index arrays")
     ap.add_argument("--pool-pages", type=int, default=None,
                     help="pool size of the shared-pool workloads (fp8_nsa, index_k): small device footprints for "
                          "profiling; every launch still moves the same pages")
@@ -843,7 +850,8 @@ def main(argv=None):
 
     cpkv_build.build()
     work = ComposeWorkload(a.config, device=device, num_layers=a.layers, variant=a.variant, pool_pages=a.pool_pages,
-                           consume_staging={"auto": None, "on": True, "off": False}[a.consume_staging])
+                           consume_staging={"auto": None, "on": True, "off": False}[a.consume_staging],
+                           fill_mode=a.fill_mode)
     hbm_peak, peak_src, _ = read_peaks()
 
     warm_and_capture(work, a.warmup, graph=not a.no_graph)
@@ -927,6 +935,7 @@ def main(argv=None):
         "page_size": b.page_size, "cp_size": b.cp_size, "row_bytes": b.row_bytes,
         "variant": work.variant,
         "consume_staging": work.consume_staging,
+        "fill_mode": work.fill_mode if work.variant in ("staging", "prefetch") else None,
         "bytes_per_layer": work.layer_bytes,
         "dram_bytes_per_layer": work.bytes["dram_min"],
         "l2": ("L2 flushed between steps (a 512 MB write outside the per-step events)" if work.num_layers == 1

@@ -224,6 +224,19 @@ int cpkv_plan_build_noalloc(int B, int page_size, int cp_size, int64_t num_pool_
  * thread pass that wait before it can finish, so it completes only after its
  * predecessor, and no store runs ahead of a kernel two launches back. */
 #define CPKV_FLAG_EARLY_INPUTS 2
+/* Page runs (cpkv_fill_current only): the caller promises that the index
+ * arrays are those of cpkv_plan_build for this batch, so that current page i
+ * (n_i tokens, batch order) is staged at rows (i + 1) * ps .. (i + 1) * ps +
+ * n_i - 1 of its writer's staging and read from n_i consecutive rows of that
+ * writer's buffer, starting at d_token_writer_row of the page's first token.
+ * The fill then moves each page as one run in 4 KB chunks (one index lookup
+ * per page instead of per row) and zeroes the pad rows of short pages in the
+ * same pass; the stagings end up byte-identical.  Each page's first staging
+ * row and its first and last source rows are checked against the run: a
+ * page that does not fit raises ROW_OOB and is not written (other
+ * violations inside the run are not detected).  Pages under 4 KB take the
+ * row fill, which needs no promise. */
+#define CPKV_FILL_PAGE_RUNS 4
 
 /*
  * cpkv_fill_current — per layer: write every current row into its writer's
@@ -246,8 +259,8 @@ int cpkv_plan_build_noalloc(int B, int page_size, int cp_size, int64_t num_pool_
  *                     staging_cap_pages >= C + 1
  *   d_staging_rows, d_token_writer_row: from cpkv_plan_build; d_writer [C]
  *   row_bytes         R, a multiple of 16
- *   flags             CPKV_FLAG_EARLY_INPUTS or 0; other bits return
- *                     CPKV_ERR_ARG
+ *   flags             CPKV_FLAG_EARLY_INPUTS, CPKV_FILL_PAGE_RUNS (or 0);
+ *                     other bits return CPKV_ERR_ARG
  * Status bits: ROW_OOB / WRITER_OOB (that row is skipped).
  */
 int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_bytes, const int32_t *h_cur_lens,

@@ -42,6 +42,7 @@ GATHER_CONSUME_STAGING = 8  # flag: staging bytes are undefined after the gather
 GATHER_EARLY_INPUTS = 16  # flag: launched early behind the fill (its contract is the caller's)
 FLAG_CONSUME_STAGING = 1    # layer compose: the stagings are consumed
 FLAG_EARLY_INPUTS = 2       # layer / fused compose: inputs complete before the previous kernel started
+FILL_PAGE_RUNS = 4          # fill: the index arrays are a plan of cpkv_plan_build (pages move as runs)
 
 
 def compose_flags(consume_staging=False, early_inputs=False) -> int:
@@ -236,9 +237,10 @@ def cpkv_plan_build_noalloc(prefix_lens, cur_lens, d_prefix_pages, d_cur_pages, 
 
 def cpkv_fill_current(cur_lens, cur_rows: Sequence, staging: Sequence, *, page_size, cp_size, row_bytes,
                       staging_cap_pages, d_staging_rows, d_token_writer_row, d_writer, num_cur_pages,
-                      d_status, cur_rows_cap=None, early_inputs=False, stream=None):
+                      d_status, cur_rows_cap=None, early_inputs=False, page_runs=False, stream=None):
     """Per-layer fill.  ``cur_rows[w]`` / ``staging[w]``: uint8 CUDA tensors (or raw pointers with
-    ``cur_rows_cap`` given).  ``early_inputs``: FLAG_EARLY_INPUTS (its contract is the caller's)."""
+    ``cur_rows_cap`` given).  ``early_inputs``: FLAG_EARLY_INPUTS; ``page_runs``: FILL_PAGE_RUNS (the
+    index arrays are a plan of cpkv_plan_build for this batch); both contracts are the caller's."""
     cl = _host_i32(cur_lens)
     if cur_rows_cap is None:
         cur_rows_cap = [t.numel() // row_bytes for t in cur_rows]
@@ -248,7 +250,8 @@ def cpkv_fill_current(cur_lens, cur_rows: Sequence, staging: Sequence, *, page_s
     rc = load().cpkv_fill_current(
         len(cl), page_size, cp_size, row_bytes, _hp(cl), ctypes.cast(rows_arr, _P), _hp(caps),
         ctypes.cast(stg_arr, _P), staging_cap_pages, _dp(d_staging_rows), _dp(d_token_writer_row),
-        _dp(d_writer), num_cur_pages, compose_flags(early_inputs=early_inputs), _dp(d_status), _stream(stream))
+        _dp(d_writer), num_cur_pages, compose_flags(early_inputs=early_inputs) | (FILL_PAGE_RUNS if page_runs else 0),
+        _dp(d_status), _stream(stream))
     _check("cpkv_fill_current", rc)
 
 

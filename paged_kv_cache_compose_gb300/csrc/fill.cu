@@ -28,6 +28,9 @@
 // (A variant that moves whole pages with bulk copies when a page's indices
 // form a run was slower here: each page first needs a round trip of index
 // loads, and a layer has only a few pages per CTA to overlap them with.)
+//
+// With CPKV_FILL_PAGE_RUNS the caller promises the plan's page runs, and
+// fill_pages_kernel below moves each current page as one run instead.
 #include <stdint.h>
 
 #include "common.cuh"
@@ -49,6 +52,8 @@ struct FillParams {
   int32_t *status;
   int64_t T, C, staging_cap_rows, R;
   int ps, cp, B, nRow, vpr;  // vpr = R / 16
+  int64_t units;             // page mode: chunks of current pages (C * upp)
+  int32_t upp;               // page mode: chunks per page
   int32_t cur_lens[MAXB];
 };
 
@@ -183,6 +188,140 @@ __device__ void zero_pad_rows(const FillParams<MAXB> &p, int b) {
   for (int64_t i = threadIdx.x; i < nvec; i += kFillThreads) st16_hint(base + 16 * i, z, keep);
 }
 
+// ---------------------------------------------------------------------------
+// Page mode (CPKV_FILL_PAGE_RUNS): the plan of cpkv_plan_build stages current
+// page i's n_i tokens at rows (i + 1) ps .. (i + 1) ps + n_i - 1 of its
+// writer's staging and reads them from n_i consecutive rows of the writer's
+// buffer, from token_writer_row of the page's first token.  So a page is one
+// contiguous run on both sides, and the fill moves it in chunks of
+// 4 KB (32 lanes x 8 16-byte vectors): a unit is one chunk of
+// one page (the last chunks of a short page are partly or wholly pad, zeroed
+// in the same pass).  A warp resolves the pages of 32 units at once, one
+// unit per lane: the page's writer and first source row are two independent
+// loads (no per-row index chain), plus the first staging row and the last
+// source row, which must fit the run (a page that does not is skipped and
+// raises ROW_OOB).  Each unit then issues all its loads before its stores, so
+// a warp keeps 4 KB in flight.  Units u = warp + k * warps: consecutive
+// warps stream consecutive chunks.
+// Measured (same box, two runs each): traced 78-layer step 4.183 ms against
+// 4.202 with the row fill, fp8 19.70-19.80 against 19.90.  Alone the kernel
+// is no faster than the row fill (15.5 against 14.3 us): both are bound by
+// the rounds of load latency of a 51 MB copy, not by index loads.  Shapes
+// tried: 2 KB chunks with 8 blocks of 256 or 4 of 512 threads per SM (32
+// registers, spills) 4.63-4.68 ms; 8 blocks of 128 threads 4.226 ms; the
+// pages through the gather's bulk-copy ring (one-warp CTAs, 16 KB pieces)
+// 4.175 ms traced but 20.10 ms fp8.
+constexpr int kPageChunkVecs = 256;  // 4 KB chunks
+constexpr int kPageVpl = kPageChunkVecs / 32;
+constexpr int kPageThreads = 256;
+constexpr int kPageWarps = kPageThreads / 32;
+constexpr int kPageBlocksPerSm = 4;  // one resident wave
+
+struct PageUnit {
+  const uint8_t *src;  // nullptr: skip
+  uint8_t *dst;
+  int32_t copy, total;  // bytes copied from src, bytes written (the rest zero)
+};
+
+template <int MAXB>
+__device__ PageUnit resolve_page_unit(const FillParams<MAXB> &p, const int32_t *cur_page_start,
+                                      const int64_t *token_start, int64_t u) {
+  PageUnit x{nullptr, nullptr, 0, 0};
+  if (u >= p.units) return x;
+  const int64_t i = u / p.upp;
+  const int32_t c = (int32_t)(u - i * p.upp);
+  const int b = upper_index<int32_t>(cur_page_start, p.B, (int32_t)i);
+  const int32_t kp = (int32_t)i - cur_page_start[b];
+  const int32_t n = min(p.ps, p.cur_lens[b] - kp * p.ps);
+  const int64_t tok0 = token_start[b] + (int64_t)kp * p.ps;
+  // independent loads: writer, first and last source rows, first staging row
+  const int32_t w = p.writer[i];
+  const int32_t r0 = p.token_writer_row[tok0];
+  const int32_t r1 = p.token_writer_row[tok0 + n - 1];
+  const int64_t s0 = p.staging_rows[tok0];
+  if (w < 0 || w >= p.cp) {
+    if (c == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
+    return x;
+  }
+  if (r0 < 0 || r1 != r0 + n - 1 || (int64_t)r0 + n > p.cur_cap[w] || s0 != (i + 1) * p.ps) {
+    if (c == 0) raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    return x;
+  }
+  const int64_t page_bytes = (int64_t)p.ps * p.R;
+  const int64_t off = (int64_t)c * (kPageChunkVecs * 16);
+  x.total = (int32_t)min64(kPageChunkVecs * 16, page_bytes - off);
+  const int64_t rows_bytes = (int64_t)n * p.R;
+  x.copy = (int32_t)(off < rows_bytes ? min64(x.total, rows_bytes - off) : 0);
+  x.src = p.cur_rows[w] + (int64_t)r0 * p.R + off;
+  x.dst = p.staging[w] + (i + 1) * page_bytes + off;
+  return x;
+}
+
+template <int MAXB>
+__global__ void __launch_bounds__(kPageThreads, kPageBlocksPerSm) fill_pages_kernel(const __grid_constant__ FillParams<MAXB> p) {
+  __shared__ int32_t cur_page_start[MAXB + 1];
+  __shared__ int64_t token_start[MAXB + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {  // request-level exclusive scans, 32 requests per step
+    int32_t carry_pages = 0;
+    int64_t carry_tok = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      const int32_t n = b < p.B ? p.cur_lens[b] : 0;
+      const int32_t np = (n + p.ps - 1) / p.ps;
+      const int32_t inc_p = warp_inclusive_scan<int32_t>(np);
+      const int64_t inc_t = warp_inclusive_scan<int64_t>((int64_t)n);
+      if (b < p.B) {
+        cur_page_start[b] = carry_pages + inc_p - np;
+        token_start[b] = carry_tok + inc_t - n;
+      }
+      carry_pages += __shfl_sync(0xffffffffu, inc_p, 31);
+      carry_tok += __shfl_sync(0xffffffffu, inc_t, 31);
+    }
+    if (lane == 0) {
+      cur_page_start[p.B] = carry_pages;
+      token_start[p.B] = carry_tok;
+    }
+  }
+  __syncthreads();
+  const uint64_t read_once = l2_policy_evict_first();
+  const uint64_t keep = l2_policy_evict_last();
+  const int64_t nw = (int64_t)gridDim.x * kPageWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kPageWarps + warp;
+  bool stores_open = false;
+  for (int64_t base = gw; base < p.units; base += 32 * nw) {
+    const PageUnit mine = resolve_page_unit(p, cur_page_start, token_start, base + lane * nw);
+    for (int j = 0; j < 32; ++j) {
+      if (base + j * nw >= p.units) break;  // uniform across the warp
+      const uint8_t *src = reinterpret_cast<const uint8_t *>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine.src), j));
+      uint8_t *dst = reinterpret_cast<uint8_t *>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine.dst), j));
+      const int32_t copy = __shfl_sync(0xffffffffu, mine.copy, j);
+      const int32_t total = __shfl_sync(0xffffffffu, mine.total, j);
+      if (src == nullptr) continue;  // uniform
+      uint4 v[kPageVpl];
+#pragma unroll
+      for (int k = 0; k < kPageVpl; ++k) {
+        const int32_t off = 16 * (lane + 32 * k);
+        v[k] = off < copy ? ld_stream16_hint(src + off, read_once) : make_uint4(0, 0, 0, 0);
+      }
+      store_gate(&stores_open);
+#pragma unroll
+      for (int k = 0; k < kPageVpl; ++k) {
+        const int32_t off = 16 * (lane + 32 * k);
+        if (off < total) st16_hint(dst + off, v[k], keep);
+      }
+    }
+  }
+  // an early-launched fill finishes only after the kernel before it, even if
+  // it stored nothing (chains of early launches stay ordered)
+  if (threadIdx.x == 0) store_gate(&stores_open);
+  // the gather of these stagings (CPKV_GATHER_EARLY_INPUTS) may launch once
+  // every block is here; it waits for this kernel before reading a staging
+  release_dependents();
+}
+
 // RIF = 0 selects the wide-row loop.
 template <int MAXB, int RIF, int VPL>
 __global__ void __launch_bounds__(kFillThreads, kBlocksPerSm) fill_current_kernel(const __grid_constant__ FillParams<MAXB> p) {
@@ -221,7 +360,7 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
                                  int64_t num_cur_pages, int flags, int32_t *d_status, cpkv_stream_t stream) {
   using namespace cpkv;
   if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
-  if ((flags & ~CPKV_FLAG_EARLY_INPUTS) != 0) return CPKV_ERR_ARG;
+  if ((flags & ~(CPKV_FLAG_EARLY_INPUTS | CPKV_FILL_PAGE_RUNS)) != 0) return CPKV_ERR_ARG;
   const bool early = (flags & CPKV_FLAG_EARLY_INPUTS) != 0;
   if (row_bytes <= 0 || row_bytes % 16 != 0) return CPKV_ERR_ARG;
   if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
@@ -246,11 +385,6 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
   if (T == 0 && C == 0) return CPKV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  const int64_t row_warps = ceil_div(T, 2);
-  const int64_t row_blocks_needed = ceil_div(row_warps, kWarpsPerBlock);
-  const int64_t row_blocks_cap = (int64_t)device_sm_count() * kBlocksPerSm;
-  const int nRow = (int)(row_blocks_needed < row_blocks_cap ? row_blocks_needed : row_blocks_cap);
-
 #define CPKV_FILL_FILL(prm)                                                                  \
   for (int w = 0; w < CPKV_MAX_CP; ++w) {                                                    \
     prm.cur_rows[w] = w < cp_size ? static_cast<const uint8_t *>(h_cur_rows[w]) : nullptr;   \
@@ -261,16 +395,29 @@ extern "C" int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_
   prm.writer = d_writer; prm.status = d_status; prm.T = T; prm.C = C;                        \
   prm.staging_cap_rows = staging_cap_pages * page_size; prm.R = row_bytes;                   \
   prm.ps = page_size; prm.cp = cp_size; prm.B = B; prm.nRow = nRow;                          \
-  prm.vpr = (int)(row_bytes / 16);                                                           \
+  prm.vpr = (int)(row_bytes / 16); prm.units = C * upp; prm.upp = (int32_t)upp;              \
   for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
+
+  // page mode for pages of at least one chunk (smaller pages are rows: the
+  // row kernel moves the same bytes)
+  const int64_t page_bytes = (int64_t)page_size * row_bytes;
+  const bool pages = (flags & CPKV_FILL_PAGE_RUNS) != 0 && page_bytes >= kPageChunkVecs * 16;
+  const int64_t upp = ceil_div(page_bytes, kPageChunkVecs * 16);
+  const int64_t row_warps = pages ? ceil_div(C * upp, 2) : ceil_div(T, 2);
+  const int64_t row_blocks_needed = ceil_div(row_warps, pages ? kPageWarps : kWarpsPerBlock);
+  const int64_t row_blocks_cap = (int64_t)device_sm_count() * (pages ? kPageBlocksPerSm : kBlocksPerSm);
+  const int nRow = (int)(row_blocks_needed < row_blocks_cap ? row_blocks_needed : row_blocks_cap);
 
   if (B <= 64) {
     FillParams<64> prm;
     CPKV_FILL_FILL(prm)
+    if (pages) return launch_kernel(fill_pages_kernel<64>, dim3(nRow), dim3(kPageThreads), 0, early, s, prm);
     return launch_fill(prm, nRow + B, early, s);
   }
   FillParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_FILL(prm)
 #undef CPKV_FILL_FILL
+  if (pages)
+    return launch_kernel(fill_pages_kernel<CPKV_MAX_BATCH>, dim3(nRow), dim3(kPageThreads), 0, early, s, prm);
   return launch_fill(prm, nRow + B, early, s);
 }

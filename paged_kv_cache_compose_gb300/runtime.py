@@ -68,15 +68,17 @@ class ComposeLayers:
         self.dense = [torch.empty((plan.dense_cap_pages * ps, row_bytes), dtype=torch.uint8, device=plan.device)
                       for _ in range(num_dense)]
 
-    def fill(self, cur_rows_per_writer, stream=None, early_inputs=False):
+    def fill(self, cur_rows_per_writer, stream=None, early_inputs=False, page_runs=True):
         """``early_inputs``: the rows and the plan were complete before the
-        previous kernel on the stream started (cpkv.FLAG_EARLY_INPUTS)."""
+        previous kernel on the stream started (cpkv.FLAG_EARLY_INPUTS).
+        ``page_runs``: the plan's index arrays move each current page as one
+        run (cpkv.FILL_PAGE_RUNS; they are this plan's own, so it holds)."""
         p = self.plan
         cpkv.cpkv_fill_current(p.cur_lens, cur_rows_per_writer, self.staging, page_size=p.page_size,
                                cp_size=p.cp_size, row_bytes=self.row_bytes, staging_cap_pages=p.staging_cap_pages,
                                d_staging_rows=p["staging_rows"], d_token_writer_row=p["token_writer_row"],
                                d_writer=p.d_writer, num_cur_pages=p.C, d_status=p.d_status,
-                               early_inputs=early_inputs, stream=stream)
+                               early_inputs=early_inputs, page_runs=page_runs, stream=stream)
 
     def fill_planes(self, cur_planes_per_writer, plane_bytes, stream=None, early_inputs=False):
         """Planar-page fill (``cur_planes_per_writer[p][w]``); the row width of
@@ -165,13 +167,13 @@ class ComposeLayers:
                                 consume_staging=consume_staging, early_inputs=early_inputs, stream=stream)
 
     def compose_layer(self, layer: int, pools, cur_rows_per_writer, stream=None, consume_staging=False,
-                      early_inputs=False):
+                      early_inputs=False, page_runs=True):
         """Fill + gather of one layer into the dense buffer of its parity.
         ``early_inputs``: both kernels launch early (the fill behind the
         previous kernel, the gather behind the fill); the caller promises that
         the plan, pools and rows were complete before the previous kernel on
         the stream started."""
         dense = self.dense[layer % len(self.dense)]
-        self.fill(cur_rows_per_writer, stream, early_inputs=early_inputs)
+        self.fill(cur_rows_per_writer, stream, early_inputs=early_inputs, page_runs=page_runs)
         self.gather(pools, dense, stream, consume_staging=consume_staging, early_inputs=early_inputs)
         return dense

@@ -110,9 +110,11 @@ def test_plan_large_batch_template():
     _assert_plan_equal(plan, want)
 
 
-def _run_compose(batch, dense_extra=1, guard=0xA5, num_layers=1):
+def _run_compose(batch, dense_extra=1, guard=0xA5, num_layers=1, page_runs=True):
     """Plan + fill + gather on the GPU with host-generated inputs; returns
-    (dense [host], staging list [host], plan, slabs, rows) for the last layer."""
+    (dense [host], staging list [host], plan, slabs, rows) for the last layer.
+    ``page_runs``: the fill moves pages as runs (pages of 4 KB and more) or
+    takes the row-by-row index copy."""
     plan, want = _plan_pair(batch, dense_extra)
     _assert_plan_equal(plan, want)
     layers = ComposeLayers(plan, batch.row_bytes)
@@ -126,7 +128,7 @@ def _run_compose(batch, dense_extra=1, guard=0xA5, num_layers=1):
         rows = wl.host_current_rows(batch, layer)
         d_slabs = [torch.from_numpy(s).cuda() for s in slabs]
         d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
-        dense = layers.compose_layer(layer, d_slabs, d_rows)
+        dense = layers.compose_layer(layer, d_slabs, d_rows, page_runs=page_runs)
         out = (dense, slabs, rows)
     torch.cuda.synchronize()
     assert int(plan.d_status.item()) == 0
@@ -134,9 +136,10 @@ def _run_compose(batch, dense_extra=1, guard=0xA5, num_layers=1):
     return dense.cpu().numpy(), [s.cpu().numpy() for s in layers.staging], plan, slabs, rows
 
 
+@pytest.mark.parametrize("page_runs", [True, False], ids=["page-runs", "rows"])
 @pytest.mark.parametrize("batch", pins.edge_batches(), ids=lambda b: b.name)
-def test_compose_matches_oracle_edge_cases(batch):
-    dense, staging, plan, slabs, rows = _run_compose(batch, dense_extra=2)
+def test_compose_matches_oracle_edge_cases(batch, page_runs):
+    dense, staging, plan, slabs, rows = _run_compose(batch, dense_extra=2, page_runs=page_runs)
     want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
                                 page_size=batch.page_size, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
     assert np.array_equal(dense, want)
@@ -146,6 +149,64 @@ def test_compose_matches_oracle_edge_cases(batch):
     oracle.staging(batch.cur_lens, batch.writer, rows, stg_want, page_size=ps, cp_size=batch.cp_size)
     for w in range(batch.cp_size):
         assert np.array_equal(staging[w], stg_want[w]), w
+
+
+@pytest.mark.parametrize("ps,R", [(64, 656), (5, 1024), (64, 64), (16, 1152), (4, 1152), (3, 1152), (128, 48),
+                                  (2, 4096), (1, 8192)])
+def test_page_run_fill_geometries(ps, R):
+    """The page-run fill on pages of one, several and partial 4 KB chunks
+    (41 984-byte fp8 pages end in a 1024-byte chunk; 5 x 1024 = 4 KB + 1 KB;
+    exactly one chunk; 18 chunks; one-token pages of 4 and 8 KB) and below
+    one chunk (the row fill), three layers each with short pages: stagings
+    (guard bytes elsewhere) and dense against the oracle."""
+    rng = np.random.default_rng(ps * 7 + R)
+    B = 9
+    pfx = (rng.integers(0, 6 * ps, B) // ps) * ps
+    cur = rng.integers(1, 5 * ps + 3, B)
+    batch = wl.make_compose_batch("geo-runs", 53, page_size=ps, cp_size=3, num_pool_pages=400, row_bytes=R,
+                                  prefix_lens=pfx, cur_lens=cur, row_kind="bytes")
+    dense, staging, plan, slabs, rows = _run_compose(batch, dense_extra=1, num_layers=3)
+    want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                page_size=ps, cp_size=batch.cp_size, dense_cap=plan.dense_cap_pages)
+    assert np.array_equal(dense, want)
+    stg_want = [np.full_like(s, 0xA5) for s in staging]
+    oracle.staging(batch.cur_lens, batch.writer, rows, stg_want, page_size=ps, cp_size=batch.cp_size)
+    for w in range(batch.cp_size):
+        assert np.array_equal(staging[w], stg_want[w]), w
+
+
+def test_page_run_fill_flags_indices_that_are_not_runs():
+    """With FILL_PAGE_RUNS, a page whose source rows are reversed, or whose
+    first staging row is moved, breaks the promised run: that page raises
+    ROW_OOB and keeps its guard bytes; every other page is filled."""
+    batch = wl.make_compose_batch("runs-check", 57, page_size=8, cp_size=4, num_pool_pages=64, row_bytes=1152,
+                                  prefix_lens=np.array([16, 0]), cur_lens=np.array([20, 13]), row_kind="bytes")
+    ps, R = batch.page_size, batch.row_bytes
+    plan, _ = _plan_pair(batch)
+    layers = ComposeLayers(plan, R)
+    rows = wl.host_current_rows(batch, 0)
+    d_rows = [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]
+    tw = plan["token_writer_row"].cpu().numpy().copy()
+    sr = plan["staging_rows"].cpu().numpy().copy()
+    assert plan.C >= 3 and ps * R >= 4096
+    tw[0:ps] = tw[0:ps][::-1]  # page 0: reversed source rows
+    sr[ps] += 1                 # page 1: first staging row moved
+    for s_ in layers.staging:
+        s_.fill_(0xA5)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cpkv.cpkv_fill_current(plan.cur_lens, d_rows, layers.staging, page_size=ps, cp_size=plan.cp_size, row_bytes=R,
+                           staging_cap_pages=plan.staging_cap_pages, d_staging_rows=torch.from_numpy(sr).cuda(),
+                           d_token_writer_row=torch.from_numpy(tw).cuda(), d_writer=plan.d_writer,
+                           num_cur_pages=plan.C, d_status=status, page_runs=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == cpkv.STATUS_ROW_OOB
+    stg_want = [np.full(((plan.C + 1) * ps, R), 0xA5, np.uint8) for _ in range(plan.cp_size)]
+    oracle.staging(batch.cur_lens, batch.writer, rows, stg_want, page_size=ps, cp_size=plan.cp_size)
+    for i in (0, 1):  # the broken pages keep their guard bytes
+        w = int(batch.writer[i])
+        stg_want[w][(i + 1) * ps:(i + 2) * ps] = 0xA5
+    for w in range(plan.cp_size):
+        assert np.array_equal(layers.staging[w].cpu().numpy(), stg_want[w]), w
 
 
 def test_compose_tiny_78_layers():
