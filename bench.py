@@ -944,11 +944,11 @@ def main(argv=None):
         "cuda_graph": not a.no_graph,
         "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
     }
+    small = b.page_size * b.row_bytes <= 4096  # pages moved a group of consecutive dense pages at a time
     kernel_name = {
-        "gather": ("gather_groups_kernel" if b.page_size * b.row_bytes <= 4096 else "gather_pages_kernel")
-        + " (cpkv_compose_gather_kinds)",
+        "gather": ("gather_groups_kernel" if small else "gather_pages_kernel") + " (cpkv_compose_gather_kinds)",
         "fused": ("compose_layer_kernel (cpkv_compose_fused_planes)" if b.planes
-                  else "compose_fused_kernel (cpkv_compose_fused)"),
+                  else ("compose_fused_groups_kernel" if small else "compose_fused_kernel") + " (cpkv_compose_fused)"),
         "layer": ("compose_layer_kernel (cpkv_compose_layer_planes)" if b.planes
                   else "compose_layer_kernel (cpkv_compose_layer)")}[top]
     roofline = {

@@ -38,7 +38,7 @@
 // fill, launched with CPKV_FLAG_EARLY_INPUTS, may start while it runs).
 #include <stdint.h>
 
-#include "bulk_ring.cuh"
+#include "group_ring.cuh"
 
 namespace cpkv {
 namespace {
@@ -164,132 +164,6 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
 // cross table entries or mix pools with stagings, so a consumed staging run
 // never covers pool bytes.  Used only when every slot kind is written (a
 // skipped slot must keep its bytes).
-constexpr int kGroupStages = 4;
-constexpr int kGroupLoads = 2;          // stages with loads in flight per CTA
-constexpr int kGroupBytes = 8 * 1024;   // stage size
-constexpr int kMaxCtasPerSmGroups = 6;
-
-template <bool kConsume>
-struct GroupRing {
-  uint8_t *smem;        // kGroupStages * stage_bytes (dynamic shared memory)
-  uint64_t *full;       // kGroupStages mbarriers
-  uint8_t **dst;        // kGroupStages dense destinations (shared)
-  uint32_t *bytes;      // kGroupStages group sizes (shared)
-  int *live;            // kGroupStages: the stage was armed (shared)
-  const uint8_t *(*drop_src)[32];  // kConsume: staging runs to drop once loaded (shared)
-  uint32_t (*drop_bytes)[32];
-  int *drop_n;
-  int32_t *status;
-  uint32_t stage_bytes;
-  uint64_t pol;
-  int64_t head, tail;   // consumed / issued (warp-uniform)
-  bool dead;            // a bounded wait gave up (warp-uniform)
-  bool open;            // store_gate
-
-  // Wait for the oldest group and store it (warp-uniform call).
-  CPKV_DEV void consume() {
-    const int s = (int)(head % kGroupStages);
-    store_gate(&open);
-    int ok = 0, dead_now = dead ? 1 : 0;
-    if ((threadIdx.x & 31) == 0) {
-      bool landed = false;
-      if (live[s]) {
-        landed = mbar_wait_bounded(&full[s], (uint32_t)((head / kGroupStages) & 1), kRingWaitLimitNs);
-        if (!landed && !dead_now) {
-          dead_now = 1;
-          raise_status(status, CPKV_STATUS_TIMEOUT);
-        }
-      }
-      if (landed && !dead_now) bulk_store_s2g_hint(dst[s], smem + (size_t)s * stage_bytes, bytes[s], pol);
-      bulk_commit();
-      ok = landed && !dead_now;
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    dead = __shfl_sync(0xffffffffu, dead_now, 0) != 0;
-    if (kConsume && ok)
-      for (int k = 0; k < drop_n[s]; ++k) warp_discard_l2(drop_src[s][k], drop_bytes[s][k]);
-    ++head;
-  }
-
-  // Issue group [d0, d0 + n): lane j < n holds page j's descriptor (o, sr).
-  CPKV_DEV void push_group(const GatherParams &p, int64_t d0, int n, int32_t o, int32_t sr) {
-    const unsigned all = 0xffffffffu;
-    const int lane = threadIdx.x & 31;
-    if (tail - head == kGroupLoads) consume();
-    const int s = (int)(tail % kGroupStages);
-    uint8_t *stage = smem + (size_t)s * stage_bytes;
-    const uint32_t pb = (uint32_t)p.page_bytes;
-    // my page: 0 none, 1 zero-fill, 2 copy
-    int kind = 0;
-    const uint8_t *src = nullptr;
-    if (lane < n) {
-      if (o == -1) {
-        kind = 1;
-      } else if (o < -1 || o >= p.n_table || sr < 0 || sr >= p.cap_pages[o]) {
-        kind = 1;
-        raise_status(p.status, CPKV_STATUS_DESC_OOB);
-      } else {
-        kind = 2;
-        src = p.table[o] + (int64_t)sr * p.page_bytes;
-      }
-    }
-    // runs: page j continues page j - 1 when both are copies from one table
-    // entry with consecutive source pages
-    const int32_t o_prev = __shfl_up_sync(all, o, 1);
-    const int32_t s_prev = __shfl_up_sync(all, sr, 1);
-    const int kind_prev = __shfl_up_sync(all, kind, 1);
-    const bool cont = lane > 0 && kind == 2 && kind_prev == 2 && o == o_prev && sr == s_prev + 1;
-    const uint64_t cont_mask = __ballot_sync(all, cont);
-    const bool start = kind == 2 && !cont;
-    // run length: this page plus the continuing pages right after it
-    const uint64_t after = cont_mask >> (lane + 1);
-    const int run = start ? __ffsll((long long)~after) : 0;  // trailing ones of `after`, plus one
-    const bool staging = kind == 2 && o >= p.n_pool;
-    const int copies = __popc(__ballot_sync(all, kind == 2));
-    const unsigned zero_mask = __ballot_sync(all, kind == 1);
-    const unsigned drop_mask = __ballot_sync(all, kConsume && start && staging);
-    // the stage's previous store must have finished reading shared memory
-    if (lane == 0 && tail >= kGroupStages) bulk_wait_read_dyn((int)(head - tail + kGroupStages - 1));
-    __syncwarp();
-    if (zero_mask != 0) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (unsigned m = zero_mask; m != 0; m &= m - 1) {
-        uint4 *page = reinterpret_cast<uint4 *>(stage + (size_t)(__ffs(m) - 1) * pb);
-        for (uint32_t i = lane; i < pb / 16; i += 32) page[i] = z;
-      }
-      fence_proxy_async_smem();  // the zeros are read by the bulk store (async proxy)
-    }
-    if (__any_sync(all, staging)) store_gate(&open);  // staging rows only after the fill
-    if (lane == 0) {
-      live[s] = 0;
-      if (!dead) {
-        dst[s] = p.dense + d0 * p.page_bytes;
-        bytes[s] = (uint32_t)n * pb;
-        live[s] = 1;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)copies * pb);  // 0 bytes: the phase completes now
-      }
-      if (kConsume) drop_n[s] = dead ? 0 : __popc(drop_mask);
-    }
-    if (kConsume && (drop_mask >> lane) & 1u) {
-      const int k = __popc(drop_mask & ((1u << lane) - 1u));
-      drop_src[s][k] = src;
-      drop_bytes[s][k] = (uint32_t)run * pb;
-    }
-    __syncwarp();
-    if (start && !dead) bulk_load_g2s_hint(stage + (size_t)lane * pb, src, (uint32_t)run * pb, &full[s], pol);
-    ++tail;
-    __syncwarp();
-  }
-
-  // Store everything in flight and wait until the stores are complete.
-  CPKV_DEV void drain() {
-    store_gate(&open);
-    while (head < tail) consume();
-    if ((threadIdx.x & 31) == 0) bulk_wait_all();
-    __syncwarp();
-  }
-};
-
 template <bool kConsume>
 __global__ void __launch_bounds__(32) gather_groups_kernel(const __grid_constant__ GatherParams p) {
   release_dependents();  // as in gather_pages_kernel
@@ -302,26 +176,10 @@ __global__ void __launch_bounds__(32) gather_groups_kernel(const __grid_constant
   __shared__ uint32_t st_drop_bytes[kGroupStages][32];
   __shared__ int st_drop_n[kGroupStages];
   const int lane = threadIdx.x;
+  const uint32_t pb = (uint32_t)p.page_bytes;
   GroupRing<kConsume> ring;
-  ring.smem = smem;
-  ring.full = full;
-  ring.dst = st_dst;
-  ring.bytes = st_bytes;
-  ring.live = st_live;
-  ring.drop_src = st_drop_src;
-  ring.drop_bytes = st_drop_bytes;
-  ring.drop_n = st_drop_n;
-  ring.status = p.status;
-  ring.stage_bytes = (uint32_t)(p.group * p.page_bytes);
-  ring.pol = l2_policy_evict_first();
-  ring.head = ring.tail = 0;
-  ring.dead = false;
-  ring.open = false;
-  if (lane == 0) {
-    for (int s = 0; s < kGroupStages; ++s) mbar_init(&full[s], 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
+  ring.init(smem, full, st_dst, st_bytes, st_live, st_drop_src, st_drop_bytes, st_drop_n, p.status,
+            (uint32_t)(p.group * p.page_bytes));
   // Group u covers dense pages [u * G, min(u * G + G, dense_cap)).  The next
   // group's descriptors are loaded before the current group is issued.
   const int G = p.group;
@@ -341,7 +199,20 @@ __global__ void __launch_bounds__(32) gather_groups_kernel(const __grid_constant
       o_next = p.owner[v * G + lane];
       s_next = p.src[v * G + lane];
     }
-    ring.push_group(p, d0, n, o, sr);
+    // my page: a whole-page copy from its table entry, or zeros (owner -1,
+    // invalid descriptors)
+    GroupPage pg{nullptr, 0, -1, false};
+    if (lane < n && o != -1) {
+      if (o < -1 || o >= p.n_table || sr < 0 || sr >= p.cap_pages[o]) {
+        raise_status(p.status, CPKV_STATUS_DESC_OOB);
+      } else {
+        pg.src = p.table[o] + (int64_t)sr * p.page_bytes;
+        pg.copy = pb;
+        pg.entry = o;
+        pg.staging = o >= p.n_pool;
+      }
+    }
+    ring.push_group(p.dense + d0 * p.page_bytes, n, pb, pg);
     o = o_next;
     sr = s_next;
   }

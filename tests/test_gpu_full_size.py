@@ -102,7 +102,8 @@ def _check_plan(work):
                                             ("index_k", "fused"), ("traced_78", "staging-consume"),
                                             ("fp8_nsa", "staging-consume"), ("traced_78", "layer-consume"),
                                             ("index_k", "layer-consume"), ("traced_78_ps1", "staging"),
-                                            ("traced_78_ps1", "fused"), ("traced_78_ps1", "staging-consume")])
+                                            ("traced_78_ps1", "fused"), ("traced_78_ps1", "staging-consume"),
+                                            ("traced_78_ps1", "layer"), ("traced_78_ps1", "layer-consume")])
 def test_benchmark_workload_matches_oracle(config, variant):
     consume = variant.endswith("-consume")  # plain variants keep their stagings, which are checked
     variant = variant.removesuffix("-consume")
@@ -130,7 +131,8 @@ def test_benchmark_workload_matches_oracle(config, variant):
 
 @pytest.mark.parametrize("config,variant,early", [
     ("traced_78", "staging-consume", True), ("traced_78", "staging-consume", False), ("traced_78", "staging", True),
-    ("traced_78", "fused", True), ("traced_78", "layer-consume", True), ("fp8_nsa", "staging-consume", True)])
+    ("traced_78", "fused", True), ("traced_78", "layer-consume", True), ("fp8_nsa", "staging-consume", True),
+    ("traced_78_ps1", "layer-consume", True), ("traced_78_ps1", "fused", True)])
 def test_every_layer_of_the_78_layer_graph_matches_oracle(config, variant, early):
     """The benchmark's 78-layer step over the traced batch, replayed from its
     CUDA graph, with one dense buffer per layer so that every layer's output
