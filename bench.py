@@ -714,7 +714,9 @@ def time_kernels(work, steps: int):
 
 def kernel_rooflines(work, kern, hbm_peak):
     """Per kernel: algorithmic bytes per launch over its average launch time,
-    and the bytes of it that cross DRAM (kernel_dram_bytes) over the same time."""
+    the bytes of it that cross DRAM (kernel_dram_bytes) over the same time,
+    and the DRAM bytes ncu measured per launch (kernel_traffic; None without
+    a capture of the current sources)."""
     out = {}
     for k, ms in kern.items():
         alg = work.kernels[k]
@@ -722,7 +724,8 @@ def kernel_rooflines(work, kern, hbm_peak):
         out[k] = {"avg_launch_ms": round(ms, 5), "algorithmic_bytes_per_launch": alg,
                   "achieved": round(alg / (ms / 1e3) / 1e9, 1), "frac": round(alg / (ms / 1e3) / 1e9 / hbm_peak, 4),
                   "dram_bytes_per_launch": dram, "dram_achieved": round(dram / (ms / 1e3) / 1e9, 1),
-                  "dram_frac": round(dram / (ms / 1e3) / 1e9 / hbm_peak, 4)}
+                  "dram_frac": round(dram / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                  "traffic": kernel_traffic(k, work.config)}
     return out
 
 
@@ -886,7 +889,7 @@ def main(argv=None):
     top = {"fused": "fused", "layer": "layer"}.get(work.variant, "gather")
     status = work.status()
 
-    traffic = kernel_traffic(top, a.config)
+    traffic = kroof[top]["traffic"]
 
     # end to end through the public API with host buffers
     e2e = None
