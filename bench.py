@@ -366,7 +366,8 @@ class ComposeWorkload:
             return
         if kind in ("all", "fill"):
             if self.batch.planes:
-                self.layers.fill_planes(self.rows[layer], list(self.batch.planes), stream, early_inputs=early)
+                self.layers.fill_planes(self.rows[layer], list(self.batch.planes), stream, early_inputs=early,
+                                        page_runs=self.fill_mode == "pages")
             else:
                 self.layers.fill(self.rows[layer], stream, early_inputs=early, page_runs=self.fill_mode == "pages")
         if kind in ("all", "gather"):

@@ -224,7 +224,7 @@ int cpkv_plan_build_noalloc(int B, int page_size, int cp_size, int64_t num_pool_
  * thread pass that wait before it can finish, so it completes only after its
  * predecessor, and no store runs ahead of a kernel two launches back. */
 #define CPKV_FLAG_EARLY_INPUTS 2
-/* Page runs (cpkv_fill_current only): the caller promises that the index
+/* Page runs (cpkv_fill_current, cpkv_fill_current_planes): the caller promises that the index
  * arrays are those of cpkv_plan_build for this batch, so that current page i
  * (n_i tokens, batch order) is staged at rows (i + 1) * ps .. (i + 1) * ps +
  * n_i - 1 of its writer's staging and read from n_i consecutive rows of that
@@ -235,7 +235,10 @@ int cpkv_plan_build_noalloc(int B, int page_size, int cp_size, int64_t num_pool_
  * row and its first and last source rows are checked against the run: a
  * page that does not fit raises ROW_OOB and is not written (other
  * violations inside the run are not detected).  Pages under 4 KB take the
- * row fill, which needs no promise. */
+ * row fill, which needs no promise.  For planar pages each plane of a page
+ * is a run (n_i consecutive slices of the writer's plane rows into the page's
+ * plane), moved in chunks of up to 4 KB with 16-byte vectors where source,
+ * destination and sizes allow, else 4-byte words. */
 #define CPKV_FILL_PAGE_RUNS 4
 
 /*
@@ -294,8 +297,8 @@ int cpkv_fill_current(int B, int page_size, int cp_size, int64_t row_bytes, cons
  *                     16-byte aligned
  *   h_staging         host array [cp] of device pointers, each
  *                     [staging_cap_pages][ps * sum(plane_bytes)] bytes
- *   flags             CPKV_FLAG_EARLY_INPUTS or 0; other bits return
- *                     CPKV_ERR_ARG
+ *   flags             CPKV_FLAG_EARLY_INPUTS, CPKV_FILL_PAGE_RUNS (or 0);
+ *                     other bits return CPKV_ERR_ARG
  * The gather of planar pages is cpkv_compose_gather with
  * row_bytes = sum(plane_bytes) (pages are copied as opaque bytes).
  * Status bits: ROW_OOB / WRITER_OOB (that token is skipped).

@@ -257,9 +257,9 @@ def cpkv_fill_current(cur_lens, cur_rows: Sequence, staging: Sequence, *, page_s
 
 def cpkv_fill_current_planes(cur_lens, cur_planes: Sequence, staging: Sequence, *, page_size, cp_size, plane_bytes,
                              staging_cap_pages, d_staging_rows, d_token_writer_row, d_writer, num_cur_pages,
-                             d_status, cur_rows_cap=None, early_inputs=False, stream=None):
+                             d_status, cur_rows_cap=None, early_inputs=False, page_runs=False, stream=None):
     """Planar-page fill.  ``cur_planes[p][w]``: writer w's rows of plane p (uint8 CUDA tensors).
-    ``early_inputs``: FLAG_EARLY_INPUTS (its contract is the caller's)."""
+    ``early_inputs``: FLAG_EARLY_INPUTS; ``page_runs``: FILL_PAGE_RUNS; both contracts are the caller's."""
     cl, pb = _host_i32(cur_lens), _host_i32(plane_bytes)
     n_planes = len(pb)
     if cur_rows_cap is None:
@@ -270,7 +270,7 @@ def cpkv_fill_current_planes(cur_lens, cur_planes: Sequence, staging: Sequence, 
     rc = load().cpkv_fill_current_planes(len(cl), page_size, cp_size, n_planes, _hp(pb), _hp(cl),
                                          ctypes.cast(flat, _P), _hp(caps), ctypes.cast(stg, _P), staging_cap_pages,
                                          _dp(d_staging_rows), _dp(d_token_writer_row), _dp(d_writer), num_cur_pages,
-                                         compose_flags(early_inputs=early_inputs), _dp(d_status), _stream(stream))
+                                         compose_flags(early_inputs=early_inputs) | (FILL_PAGE_RUNS if page_runs else 0), _dp(d_status), _stream(stream))
     _check("cpkv_fill_current_planes", rc)
 
 

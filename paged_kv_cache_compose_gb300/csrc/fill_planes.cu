@@ -46,6 +46,8 @@ struct PlaneParams {
   int32_t *status;
   int64_t T, C, staging_cap_rows, page_bytes;
   int32_t plane_bytes[kMaxPlanes], plane_start[kMaxPlanes], plane_unit[kMaxPlanes];
+  int32_t chunk_start[kMaxPlanes + 1];  // page mode: first chunk of plane p within a page (last: chunks per page)
+  int64_t units;                        // page mode: C * chunks per page
   int32_t n_planes, ps, cp, B, nTile;
   int32_t cur_lens[MAXB];
 };
@@ -153,6 +155,149 @@ __device__ void zero_pad(const PlaneParams<MAXB> &p, int b) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Page mode (CPKV_FILL_PAGE_RUNS): with the plan of cpkv_plan_build, current
+// page i's n_i tokens are consecutive rows of each plane of their writer,
+// from token_writer_row of the page's first token, and their slices are
+// consecutive in each plane of staging slot i + 1.  So each plane of a page
+// is one contiguous run on both sides: a unit is one chunk of at most 4 KB of
+// one plane of one page, moved with 16-byte vectors when its source,
+// destination and sizes allow it, else with 4-byte words, the pad slices of a
+// short page zeroed in the same pass.  A warp resolves the pages of 32 units
+// at once with independent loads (writer, first and last source row, first
+// staging row; a page that does not fit the run is skipped and raises
+// ROW_OOB), as in the row page fill.  The index keys: two 4 KB key chunks and
+// one 256-byte scale chunk per page.
+constexpr int kPageThreads = 256;
+constexpr int kPageWarps = kPageThreads / 32;
+constexpr int kPageBlocksPerSm = 4;
+constexpr int kChunkBytes = 4096;
+constexpr int kChunkVpl = kChunkBytes / 16 / 32;  // 16-byte vectors per lane and chunk
+constexpr int kWordVpl = 8;                       // 4-byte words per lane and pass
+
+struct PlaneUnit {
+  const uint8_t *src;  // nullptr: skip
+  uint8_t *dst;
+  int32_t copy, total;
+};
+
+template <int MAXB>
+__device__ PlaneUnit resolve_plane_unit(const PlaneParams<MAXB> &p, const int32_t *cur_page_start,
+                                        const int64_t *token_start, int64_t u) {
+  PlaneUnit x{nullptr, nullptr, 0, 0};
+  if (u >= p.units) return x;
+  const int32_t upp = p.chunk_start[p.n_planes];
+  const int64_t i = u / upp;
+  const int32_t c = (int32_t)(u - i * upp);
+  int q = 0;
+  while (q + 1 < p.n_planes && p.chunk_start[q + 1] <= c) ++q;
+  const int32_t k = c - p.chunk_start[q];
+  const int b = upper_index<int32_t>(cur_page_start, p.B, (int32_t)i);
+  const int32_t kp = (int32_t)i - cur_page_start[b];
+  const int32_t n = min(p.ps, p.cur_lens[b] - kp * p.ps);
+  const int64_t tok0 = token_start[b] + (int64_t)kp * p.ps;
+  const int32_t w = p.writer[i];
+  const int32_t r0 = p.token_writer_row[tok0];
+  const int32_t r1 = p.token_writer_row[tok0 + n - 1];
+  const int64_t s0 = p.staging_rows[tok0];
+  if (w < 0 || w >= p.cp) {
+    if (c == 0) raise_status(p.status, CPKV_STATUS_WRITER_OOB);
+    return x;
+  }
+  if (r0 < 0 || r1 != r0 + n - 1 || (int64_t)r0 + n > p.cur_cap[w] || s0 != (i + 1) * p.ps) {
+    if (c == 0) raise_status(p.status, CPKV_STATUS_ROW_OOB);
+    return x;
+  }
+  const int32_t wp = p.plane_bytes[q];
+  const int64_t seg = (int64_t)p.ps * wp, off = (int64_t)k * kChunkBytes;
+  x.total = (int32_t)min64(kChunkBytes, seg - off);
+  const int64_t rows_bytes = (int64_t)n * wp;
+  x.copy = (int32_t)(off < rows_bytes ? min64(x.total, rows_bytes - off) : 0);
+  x.src = p.planes[q][w] + (int64_t)r0 * wp + off;
+  x.dst = p.staging[w] + (i + 1) * p.page_bytes + p.plane_start[q] + off;
+  return x;
+}
+
+template <int MAXB>
+__global__ void __launch_bounds__(kPageThreads, kPageBlocksPerSm)
+    fill_planes_pages_kernel(const __grid_constant__ PlaneParams<MAXB> p) {
+  __shared__ int32_t cur_page_start[MAXB + 1];
+  __shared__ int64_t token_start[MAXB + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {  // request-level exclusive scans, 32 requests per step
+    int32_t carry_pages = 0;
+    int64_t carry_tok = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      const int32_t n = b < p.B ? p.cur_lens[b] : 0;
+      const int32_t np = (n + p.ps - 1) / p.ps;
+      const int32_t inc_p = warp_inclusive_scan<int32_t>(np);
+      const int64_t inc_t = warp_inclusive_scan<int64_t>((int64_t)n);
+      if (b < p.B) {
+        cur_page_start[b] = carry_pages + inc_p - np;
+        token_start[b] = carry_tok + inc_t - n;
+      }
+      carry_pages += __shfl_sync(0xffffffffu, inc_p, 31);
+      carry_tok += __shfl_sync(0xffffffffu, inc_t, 31);
+    }
+    if (lane == 0) {
+      cur_page_start[p.B] = carry_pages;
+      token_start[p.B] = carry_tok;
+    }
+  }
+  __syncthreads();
+  const uint64_t read_once = l2_policy_evict_first(), keep = l2_policy_evict_last();
+  const int64_t nw = (int64_t)gridDim.x * kPageWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kPageWarps + warp;
+  bool stores_open = false;
+  for (int64_t base = gw; base < p.units; base += 32 * nw) {
+    const PlaneUnit mine = resolve_plane_unit(p, cur_page_start, token_start, base + lane * nw);
+    for (int j = 0; j < 32; ++j) {
+      if (base + j * nw >= p.units) break;  // uniform across the warp
+      const uint8_t *src = reinterpret_cast<const uint8_t *>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine.src), j));
+      uint8_t *dst = reinterpret_cast<uint8_t *>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine.dst), j));
+      const int32_t copy = __shfl_sync(0xffffffffu, mine.copy, j);
+      const int32_t total = __shfl_sync(0xffffffffu, mine.total, j);
+      if (src == nullptr) continue;  // uniform
+      if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) | (uint32_t)copy |
+            (uint32_t)total) & 15u) == 0) {
+        uint4 v[kChunkVpl];
+#pragma unroll
+        for (int r = 0; r < kChunkVpl; ++r) {
+          const int32_t off = 16 * (lane + 32 * r);
+          v[r] = off < copy ? ld_stream16_hint(src + off, read_once) : make_uint4(0, 0, 0, 0);
+        }
+        store_gate(&stores_open);
+#pragma unroll
+        for (int r = 0; r < kChunkVpl; ++r) {
+          const int32_t off = 16 * (lane + 32 * r);
+          if (off < total) st16_hint(dst + off, v[r], keep);
+        }
+      } else {  // 4-byte slices at an offset that is not a 16-byte multiple
+        for (int32_t w0 = 0; w0 < total / 4; w0 += 32 * kWordVpl) {
+          uint32_t v[kWordVpl];
+#pragma unroll
+          for (int r = 0; r < kWordVpl; ++r) {
+            const int32_t i = w0 + lane + 32 * r;
+            v[r] = 4 * i < copy ? __ldg(reinterpret_cast<const uint32_t *>(src) + i) : 0u;
+          }
+          store_gate(&stores_open);
+#pragma unroll
+          for (int r = 0; r < kWordVpl; ++r) {
+            const int32_t i = w0 + lane + 32 * r;
+            if (4 * i < total) reinterpret_cast<uint32_t *>(dst)[i] = v[r];
+          }
+        }
+      }
+    }
+  }
+  // an early-launched fill finishes only after the kernel before it
+  if (threadIdx.x == 0) store_gate(&stores_open);
+  release_dependents();  // as in cpkv_fill_current
+}
+
 template <int MAXB>
 __global__ void __launch_bounds__(kThreads) fill_planes_kernel(const __grid_constant__ PlaneParams<MAXB> p) {
   if ((int)blockIdx.x < p.nTile) {
@@ -179,8 +324,9 @@ extern "C" int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n
                                         cpkv_stream_t stream) {
   using namespace cpkv;
   if (B < 0 || page_size <= 0 || cp_size < 1 || cp_size > CPKV_MAX_CP) return CPKV_ERR_ARG;
-  if ((flags & ~CPKV_FLAG_EARLY_INPUTS) != 0) return CPKV_ERR_ARG;
+  if ((flags & ~(CPKV_FLAG_EARLY_INPUTS | CPKV_FILL_PAGE_RUNS)) != 0) return CPKV_ERR_ARG;
   const bool early = (flags & CPKV_FLAG_EARLY_INPUTS) != 0;
+  const bool pages = (flags & CPKV_FILL_PAGE_RUNS) != 0;
   if (n_planes < 1 || n_planes > kMaxPlanes || h_plane_bytes == nullptr) return CPKV_ERR_ARG;
   if (B > CPKV_MAX_BATCH) return CPKV_ERR_LIMIT;
   if (h_cur_planes == nullptr || h_cur_rows_cap == nullptr || h_staging == nullptr || d_status == nullptr)
@@ -241,15 +387,34 @@ extern "C" int cpkv_fill_current_planes(int B, int page_size, int cp_size, int n
   prm.status = d_status; prm.T = T; prm.C = C; prm.staging_cap_rows = staging_cap_pages * page_size;  \
   prm.page_bytes = page_bytes; prm.n_planes = n_planes; prm.ps = page_size; prm.cp = cp_size;         \
   prm.B = B; prm.nTile = nTile;                                                                        \
+  {                                                                                                    \
+    int32_t cs = 0;                                                                                    \
+    for (int p = 0; p <= kMaxPlanes; ++p) {                                                            \
+      prm.chunk_start[p] = cs;                                                                         \
+      if (p < n_planes) cs += (int32_t)ceil_div((int64_t)page_size * h_plane_bytes[p], kChunkBytes);   \
+    }                                                                                                  \
+    prm.chunk_start[n_planes] = cs;                                                                    \
+    prm.units = C * cs;                                                                                \
+  }                                                                                                    \
   for (int b = 0; b < B; ++b) prm.cur_lens[b] = h_cur_lens[b];
+
+  // page mode: one resident wave of 4 blocks per SM, about 2 units per warp
+  int64_t upp = 0;
+  for (int p = 0; p < n_planes; ++p) upp += ceil_div((int64_t)page_size * h_plane_bytes[p], kChunkBytes);
+  const int64_t pblocks = ceil_div(ceil_div(C * upp, 2), kPageWarps);
+  const int64_t pcap = (int64_t)device_sm_count() * kPageBlocksPerSm;
+  const int nPage = (int)(pblocks < pcap ? (pblocks > 0 ? pblocks : 1) : pcap);
 
   if (B <= 64) {
     PlaneParams<64> prm;
     CPKV_FILL_PLANES(prm)
+    if (pages) return launch_kernel(fill_planes_pages_kernel<64>, dim3(nPage), dim3(kPageThreads), 0, early, s, prm);
     return launch_kernel(fill_planes_kernel<64>, dim3(nTile + B), dim3(kThreads), 0, early, s, prm);
   }
   PlaneParams<CPKV_MAX_BATCH> prm;
   CPKV_FILL_PLANES(prm)
 #undef CPKV_FILL_PLANES
+  if (pages)
+    return launch_kernel(fill_planes_pages_kernel<CPKV_MAX_BATCH>, dim3(nPage), dim3(kPageThreads), 0, early, s, prm);
   return launch_kernel(fill_planes_kernel<CPKV_MAX_BATCH>, dim3(nTile + B), dim3(kThreads), 0, early, s, prm);
 }

@@ -80,16 +80,17 @@ class ComposeLayers:
                                d_writer=p.d_writer, num_cur_pages=p.C, d_status=p.d_status,
                                early_inputs=early_inputs, page_runs=page_runs, stream=stream)
 
-    def fill_planes(self, cur_planes_per_writer, plane_bytes, stream=None, early_inputs=False):
+    def fill_planes(self, cur_planes_per_writer, plane_bytes, stream=None, early_inputs=False, page_runs=True):
         """Planar-page fill (``cur_planes_per_writer[p][w]``); the row width of
-        these buffers must be ``sum(plane_bytes)``."""
+        these buffers must be ``sum(plane_bytes)``.  ``page_runs``: each plane
+        of a current page moves as one run (cpkv.FILL_PAGE_RUNS)."""
         p = self.plan
         cpkv.cpkv_fill_current_planes(p.cur_lens, cur_planes_per_writer, self.staging, page_size=p.page_size,
                                       cp_size=p.cp_size, plane_bytes=plane_bytes,
                                       staging_cap_pages=p.staging_cap_pages, d_staging_rows=p["staging_rows"],
                                       d_token_writer_row=p["token_writer_row"], d_writer=p.d_writer,
                                       num_cur_pages=p.C, d_status=p.d_status, early_inputs=early_inputs,
-                                      stream=stream)
+                                      page_runs=page_runs, stream=stream)
 
     def gather(self, pools, dense, stream=None, consume_staging=False, early_inputs=False):
         """``pools``: the cp owner slabs [slab_pages, ps, R] of this layer.

@@ -110,7 +110,7 @@ def test_host_errors_before_any_launch(lib):
                                    flags, 64, null)
         assert rc == want, ("fill", flags)
     for flags, want in ((0, cpkv.CPKV_OK), (cpkv.FLAG_EARLY_INPUTS, cpkv.CPKV_OK), (cpkv.FLAG_CONSUME_STAGING, cpkv.CPKV_ERR_ARG),
-                        (4, cpkv.CPKV_ERR_ARG), (-1, cpkv.CPKV_ERR_ARG)):
+                        (cpkv.FILL_PAGE_RUNS, cpkv.CPKV_OK), (8, cpkv.CPKV_ERR_ARG), (-1, cpkv.CPKV_ERR_ARG)):
         rc = lib.cpkv_fill_current_planes(1, 2, 1, 1, pb.ctypes.data, empty.ctypes.data,
                                           ctypes.cast(fake, ctypes.c_void_p), zero_cap.ctypes.data,
                                           ctypes.cast(fake, ctypes.c_void_p), 1, null, null, null, 0, flags, 64, null)

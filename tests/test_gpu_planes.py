@@ -35,7 +35,7 @@ def _edge_planar():
     return [_planar(b) for b in pins.edge_batches() if (b.page_size * 132) % 16 == 0]
 
 
-def _compose(batch, per_writer_mut=None, reverse_rows=False):
+def _compose(batch, per_writer_mut=None, reverse_rows=False, page_runs=False):
     ps, cp = batch.page_size, batch.cp_size
     plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
                        page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages,
@@ -59,7 +59,7 @@ def _compose(batch, per_writer_mut=None, reverse_rows=False):
     cpkv.cpkv_fill_current_planes(batch.cur_lens, d_planes, layers.staging, page_size=ps, cp_size=cp,
                                   plane_bytes=list(batch.planes), staging_cap_pages=plan.staging_cap_pages,
                                   d_staging_rows=plan["staging_rows"], d_token_writer_row=tw, d_writer=plan.d_writer,
-                                  num_cur_pages=plan.C, d_status=status)
+                                  num_cur_pages=plan.C, d_status=status, page_runs=page_runs)
     dense = torch.full((plan.dense_cap_pages * ps, batch.row_bytes), 0xCD, dtype=torch.uint8, device="cuda")
     layers.gather([torch.from_numpy(s).cuda() for s in slabs], dense)
     torch.cuda.synchronize()
@@ -74,9 +74,10 @@ def _compose(batch, per_writer_mut=None, reverse_rows=False):
     return dense, plan, slabs, planes
 
 
+@pytest.mark.parametrize("page_runs", [False, True], ids=["rows", "page-runs"])
 @pytest.mark.parametrize("batch", _edge_planar(), ids=lambda b: b.name)
-def test_planar_compose_matches_oracle(batch):
-    dense, plan, slabs, planes = _compose(batch)
+def test_planar_compose_matches_oracle(batch, page_runs):
+    dense, plan, slabs, planes = _compose(batch, page_runs=page_runs)
     want = oracle.compose_dense_planes(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, planes,
                                        page_size=batch.page_size, cp_size=batch.cp_size,
                                        plane_bytes=list(batch.planes))
@@ -114,10 +115,14 @@ def test_planar_fill_reversed_rows(batch):
     _compose(batch, reverse_rows=True)
 
 
-@pytest.mark.parametrize("planes", [(16,), (64, 4), (4, 4, 8), (128, 4), (32, 16, 4, 12)])
-def test_planar_plane_shapes(planes):
+@pytest.mark.parametrize("page_runs", [False, True], ids=["rows", "page-runs"])
+@pytest.mark.parametrize("planes", [(16,), (64, 4), (4, 4, 8), (128, 4), (32, 16, 4, 12), (4096, 4), (4, 260)])
+def test_planar_plane_shapes(planes, page_runs):
+    """Plane widths 4 to 4096 bytes (a plane of several 4 KB chunks per page;
+    4-byte planes at offsets that are not 16-byte multiples), tiny batch
+    (ps 16, short pages), both fills."""
     b = _planar(wl.tiny_batch(), planes)
-    dense, plan, slabs, cur = _compose(b)
+    dense, plan, slabs, cur = _compose(b, page_runs=page_runs)
     want = oracle.compose_dense_planes(b.prefix_lens, b.cur_lens, b.prefix_pages, slabs, cur, page_size=b.page_size,
                                        cp_size=b.cp_size, plane_bytes=list(planes))
     assert np.array_equal(dense.cpu().numpy().reshape(plan.dense_cap_pages, b.page_size * b.row_bytes), want)
