@@ -765,7 +765,8 @@ def extra_configs(a, device, hbm_peak):
     out = {}
     steps = max(5, min(a.steps, 20))
     t0 = time.perf_counter()
-    work = ComposeWorkload("fp8_nsa", device=device, variant=a.variant, fill_mode=a.fill_mode)
+    work = ComposeWorkload("fp8_nsa", device=device, variant=a.variant, fill_mode=a.fill_mode,
+                           early=a.launch == "early")
     setup_s = time.perf_counter() - t0
     warm_and_capture(work, 3)
     st0 = work.status()
@@ -825,6 +826,9 @@ def main(argv=None):
     ap.add_argument("--consume-staging", choices=["auto", "on", "off"], default="auto",
                     help="staging variant: the gather drops each staging piece's L2 lines after reading it "
                          "(the stagings are refilled before their next read); auto = on for row-major pages")
+    ap.add_argument("--launch", choices=["early", "plain"], default="early",
+                    help="early: each kernel of the layer loop launches as a programmatic dependent of the previous "
+                         "one (all inputs exist before the loop); plain: ordinary launches")
     ap.add_argument("--fill-mode", choices=["pages", "rows"], default="pages",
                     help="staging variant: the fill moves each current page as one run (the plan's pages are "
                          "runs) or copies row by row through the index arrays")
@@ -855,7 +859,7 @@ def main(argv=None):
     cpkv_build.build()
     work = ComposeWorkload(a.config, device=device, num_layers=a.layers, variant=a.variant, pool_pages=a.pool_pages,
                            consume_staging={"auto": None, "on": True, "off": False}[a.consume_staging],
-                           fill_mode=a.fill_mode)
+                           fill_mode=a.fill_mode, early=a.launch == "early")
     hbm_peak, peak_src, _ = read_peaks()
 
     warm_and_capture(work, a.warmup, graph=not a.no_graph)
@@ -940,6 +944,7 @@ def main(argv=None):
         "variant": work.variant,
         "consume_staging": work.consume_staging,
         "fill_mode": work.fill_mode if work.variant in ("staging", "prefetch") else None,
+        "launch": "early" if work.early else "plain",
         "bytes_per_layer": work.layer_bytes,
         "dram_bytes_per_layer": work.bytes["dram_min"],
         "l2": ("L2 flushed between steps (a 512 MB write outside the per-step events)" if work.num_layers == 1
