@@ -147,10 +147,12 @@ __global__ void __launch_bounds__(32) gather_pages_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------
 // Small pages: groups of consecutive dense pages, with page-run merging
 // ---------------------------------------------------------------------------
-// Pages of at most 4 KB are moved a group at a time: a unit is G consecutive
-// dense pages (G = 8 KB / page bytes, at most 32), and lane j resolves the
-// group's page j.  Consecutive pages whose sources are consecutive pages of
-// one table entry form a run, loaded into the stage with ONE bulk copy (page-
+// Pages of at most 4 KB are moved a group at a time through the group ring
+// (group_ring.cuh, shared with the fused compose on small pages): a unit is
+// G consecutive dense pages (G = 8 KB / page bytes, at most 32), and lane j
+// resolves the group's page j.  Consecutive pages whose sources are
+// consecutive pages of one table entry form a run, loaded into the stage with
+// ONE bulk copy (page-
 // run merging: a contiguous stretch of a pool or a staging is one copy); zero
 // pages (owner -1, invalid descriptors) are zero-filled in shared memory by
 // the warp; the whole group is stored with ONE bulk copy, since dense pages
