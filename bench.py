@@ -103,12 +103,18 @@ def kernel_dram_bytes(lb, kernel, consume_staging):
 
 
 def kernel_source_sha(files) -> str:
+    """Hash of the code of the kernel sources (comments and blank space
+    removed, so that an edited comment keeps a capture valid)."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "paged_kv_cache_compose_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_compose_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
