@@ -276,10 +276,13 @@ class ComposeWorkload:
         self.graph = None
         self.variant = variant
         # the gather consumes the stagings (drops their L2 lines after reading
-        # them): by default for row-major pages, where it measured faster
-        # (traced -6%, fp8 -1%); the planar index-key pages measured 1.5% slower
+        # them): by default for row-major pages above 4 KB, where it measured
+        # faster (traced -6%, fp8 -1%); the planar index-key pages measured
+        # 1.5% slower, and one-token 1152-byte pages 5% (fill + group gather,
+        # 4.74 against 4.49 ms) and 11% (one launch, 5.62 against 5.03 ms)
         if consume_staging is None:
-            consume_staging = variant in ("staging", "layer") and not b.planes
+            consume_staging = (variant in ("staging", "layer") and not b.planes
+                               and b.page_size * b.row_bytes > 4096)
         self.consume_staging = bool(consume_staging) and variant in ("staging", "layer")
         if variant == "staging":
             self.launches_per_step = 3 + 2 * self.num_layers  # plan (2) + ragged (1) + (fill + gather) per layer
@@ -965,7 +968,7 @@ def main(argv=None):
         "fused": ("compose_layer_kernel (cpkv_compose_fused_planes)" if b.planes
                   else ("compose_fused_groups_kernel" if small else "compose_fused_kernel") + " (cpkv_compose_fused)"),
         "layer": ("compose_layer_kernel (cpkv_compose_layer_planes)" if b.planes
-                  else "compose_layer_kernel (cpkv_compose_layer)")}[top]
+                  else ("compose_layer_groups_kernel" if small else "compose_layer_kernel") + " (cpkv_compose_layer)")}[top]
     roofline = {
         "bound": "hbm",
         "kernel": kernel_name,

@@ -458,9 +458,12 @@ def test_one_launch_matches_oracle_edge_cases(batch, early):
     _run_one_launch(batch, early=early)
 
 
-@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (3, 48), (128, 1152), (64, 4096), (7, 16), (1, 16)])
+@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (3, 48), (128, 1152), (64, 4096), (7, 16), (1, 16),
+                                  (1, 1152), (2, 2048), (5, 64), (1, 4096)])
 def test_one_launch_page_geometries(ps, R):
-    """Pieces that straddle the end of a partial page's rows, several pieces per page."""
+    """Pieces that straddle the end of a partial page's rows, several pieces
+    per page; pages of at most 4 KB go in groups of consecutive dense pages
+    (32 pages of 16 bytes, 7 of 1152, 25 of 320, 2 of 4096)."""
     rng = np.random.default_rng(ps * 11 + R)
     B = 7
     pfx = (rng.integers(0, 6 * ps, B) // ps) * ps
