@@ -401,7 +401,10 @@ __global__ void __launch_bounds__(64, 1)
 // Measured on the traced lengths with one-token pages (78 layers, 1152-byte
 // pages, round-robin writers; ms per step, stagings kept / consumed; the
 // stage count S, groups loading L and groups reading back K):
-//   8 KB groups, S 3, L 2, K 1, 8 CTAs per SM (the form here)  4.80 / 5.57
+//   8 KB groups, S 3, L 2, K 1, 8 CTAs per SM (the form here)  4.69 / 5.41
+//     with every bulk copy issued by lane 0 in a loop over runs 4.80 / 5.57
+//     with the group loads also issued by their runs' lanes      4.85 / 5.26
+//   (the rows below with lane 0 issuing every copy)
 //   8 KB, S 2, L 1, K 1, 12 CTAs per SM                        5.04 / 4.95
 //   8 KB, S 4, 6 CTAs per SM (L, K of 2 and 1, 2 and 2, 3 and 1) 5.67 / 6.73-6.78
 //   the same with a full proxy fence (shared and global)       5.97 / 6.77
@@ -413,8 +416,9 @@ __global__ void __launch_bounds__(64, 1)
 //   8 KB groups, S 4                                           8.20-8.52 / 8.89-9.35
 // against 4.49 / 4.74 ms for the row fill followed by the group gather.  A
 // warp waits on its loads, its staging stores' fence and its read-backs in
-// turn and spends about 700 instructions per 4 KB group (ncu), so the
-// throughput follows the number of warps per SM and the bytes each handles.
+// turn and spends about 940 instructions per 8 KB group (700 per 4 KB
+// group, ncu), so the throughput follows the number of warps per SM and the
+// bytes each handles.
 constexpr int kLayerGroupBytes = 8 * 1024;  // stage size
 constexpr int kMaxCtasPerSmLayerGroups = 8;
 constexpr int kLayerGroupStages = 3;
@@ -520,7 +524,6 @@ struct LayerGroupRing {
   // Consume the oldest loading group: stage its current pages out to their
   // staging slots and start their read-back.
   CPKV_DEV void consume() {
-    const unsigned all = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     store_gate(&open);
     while (head - stored >= kLayerGroupBacks) finish_oldest();
@@ -549,13 +552,9 @@ struct LayerGroupRing {
     const PageRun pr = page_runs(cur, stg[s][lane], cur ? pb : 0u, entry[s][lane], pb);
     if (lane == 0) mbar_arrive_expect_tx(&back[s], (uint32_t)__popc(cm) * pb);
     __syncwarp();
-    for (unsigned m = __ballot_sync(all, pr.start); m != 0; m &= m - 1) {
-      const int j = __ffs(m) - 1;
-      const unsigned long long src = __shfl_sync(all, reinterpret_cast<unsigned long long>(stg[s][lane]), j);
-      const uint32_t b = __shfl_sync(all, pr.bytes, j);
-      if (lane == 0)
-        bulk_load_g2s_hint(stage + (size_t)j * pb, reinterpret_cast<const uint8_t *>(src), b, &back[s], stream_pol);
-    }
+    // each run's first lane issues its read-back (the group loads below go
+    // through lane 0, which measured faster there)
+    if (pr.start) bulk_load_g2s_hint(stage + (size_t)lane * pb, stg[s][lane], pr.bytes, &back[s], stream_pol);
     __syncwarp();
   }
 
