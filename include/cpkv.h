@@ -217,9 +217,11 @@ int cpkv_plan_build_noalloc(int B, int page_size, int cp_size, int64_t num_pool_
  * ordered after it.  In a per-layer loop whose inputs were produced before
  * the loop this holds; directly after the kernel that writes the current
  * rows or the plan it does not.  The fused and layer composes take the early
- * launch only when their grid runs at most 4 CTAs per SM (pages of several
- * pieces, 8448-byte index-key pages); one-token pages run 24 and launch
- * plainly, where the early launch measured slower.  Chains of early launches stay
+ * launch when their grid runs at most 4 CTAs per SM (pages of several
+ * pieces, 8448-byte index-key pages) and for row pages of at most 4 KB, which
+ * go in groups of consecutive dense pages at 6 or 8 CTAs per SM; other grids
+ * of more CTAs per SM launch plainly, where the early launch measured
+ * slower.  Chains of early launches stay
  * ordered: every early-launched kernel of this library has at least one
  * thread pass that wait before it can finish, so it completes only after its
  * predecessor, and no store runs ahead of a kernel two launches back. */
@@ -356,13 +358,14 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
  * arrays and the pools were complete before the previous kernel on the
  * stream started and that nothing still running writes them; that previous
  * kernel may write the stagings (the fill).  When its grid runs at most 4
- * CTAs per SM (pages of several pieces, index-key pages) the
- * gather is then launched as a programmatic dependent of that kernel (the
+ * CTAs per SM (pages of several pieces, index-key pages), and for pages of
+ * at most 4 KB (moved in groups of consecutive dense pages), the gather is
+ * then launched as a programmatic dependent of that kernel (the
  * fills release their dependents when they finish): its CTAs may start as
  * the fill's blocks retire and load descriptors and pool pages at once, and
  * each waits for the previous kernel to complete (griddepcontrol.wait) before
- * its first staging load and before its first store.  A grid of more CTAs
- * per SM (one-token pages) is launched plainly. */
+ * its first staging load and before its first store.  Any other grid of
+ * more CTAs per SM is launched plainly. */
 #define CPKV_GATHER_EARLY_INPUTS 16
 
 /*

@@ -317,7 +317,9 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // kernel's tail (traced pages, 3-4 per SM: fused 4.05 -> 3.81 ms per step;
 // index-key pages, 3 per SM: fused 3.947 -> 3.700 ms).  With many small CTAs
 // per SM (one-token pages, 24) the early CTAs crowd the previous kernel's
-// tail and the step got slower (fused 4.27 -> 4.70 ms).
+// tail and the step got slower (fused 4.27 -> 4.70 ms).  The grouped
+// small-page kernels (8 KB groups, 6-8 CTAs per SM) do not ask: they launch
+// early whenever the caller allows it, which measured faster for all three.
 inline bool early_launch_pays(int grid) { return grid <= 4 * device_sm_count(); }
 
 }  // namespace cpkv

@@ -399,8 +399,8 @@ __global__ void __launch_bounds__(64, 1)
 // page is written and read back, and each dense page is written once.
 //
 // Measured on the traced lengths with one-token pages (78 layers, 1152-byte
-// pages, round-robin writers; ms per step, stagings kept / consumed; the
-// stage count S, groups loading L and groups reading back K):
+// pages, round-robin writers, launched plainly; ms per step, stagings kept /
+// consumed; the stage count S, groups loading L and groups reading back K):
 //   8 KB groups, S 3, L 2, K 1, 8 CTAs per SM (the form here)  4.69 / 5.41
 //     with every bulk copy issued by lane 0 in a loop over runs 4.80 / 5.57
 //     with the group loads also issued by their runs' lanes      4.85 / 5.26
@@ -414,7 +414,8 @@ __global__ void __launch_bounds__(64, 1)
 //   4 KB groups, S 4, 8 CTAs per SM; 2 KB, 24                  6.90; 7.03 (kept)
 //   read-back by the lanes (coherent loads of their own stores, no fence),
 //   8 KB groups, S 4                                           8.20-8.52 / 8.89-9.35
-// against 4.49 / 4.74 ms for the row fill followed by the group gather.  A
+// against 4.49 / 4.74 ms for the row fill followed by the group gather
+// (launched early: 4.35 / 5.05 here, 4.40 / 4.64 for fill + gather).  A
 // warp waits on its loads, its staging stores' fence and its read-backs in
 // turn and spends about 940 instructions per 8 KB group (700 per 4 KB
 // group, ncu), so the throughput follows the number of warps per SM and the
@@ -851,7 +852,9 @@ int compose_layer_impl(bool staged, bool consume_staging, bool early, int B, int
   const bool planar = !(n_planes == 1 && h_plane_bytes[0] % 16 == 0);
   if (!planar && !staged) return CPKV_ERR_ARG;
   if (!planar && pieces == 1 && page_bytes * 2 <= kGroupBytes) {
-    // small pages: groups of consecutive dense pages, staged and read back by the warp
+    // small pages: groups of consecutive dense pages, staged and read back by
+    // the warp; launched early whenever asked (8 CTAs per SM: 4.69 -> 4.36 ms
+    // per one-token step, where early_launch_pays would refuse)
     const int64_t G = kLayerGroupBytes / page_bytes < 1 ? 1 : (kLayerGroupBytes / page_bytes < 32 ? kLayerGroupBytes / page_bytes : 32);
     const int64_t gunits = ceil_div(dense_cap_pages, G);
     const size_t gsmem = (size_t)kLayerGroupStages * (size_t)(G * page_bytes);
@@ -863,8 +866,8 @@ int compose_layer_impl(bool staged, bool consume_staging, bool early, int B, int
     LayerParams<MB, 1> prm;                                                                         \
     CPKV_FILL_LAYER(prm)                                                                            \
     prm.units = gunits; prm.pieces = (int32_t)G; prm.piece_bytes = (int32_t)page_bytes;             \
-    return launch_kernel(compose_layer_groups_kernel<MB, CO>, dim3(grid), dim3(32), gsmem,          \
-                         early && early_launch_pays(grid), s, prm);                                 \
+    return launch_kernel(compose_layer_groups_kernel<MB, CO>, dim3(grid), dim3(32), gsmem, early, s, \
+                         prm);                                                                      \
   }
     if (B <= 64 && consume_staging) CPKV_LAYER_GROUPS(64, true)
     if (B <= 64) CPKV_LAYER_GROUPS(64, false)

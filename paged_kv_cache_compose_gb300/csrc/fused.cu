@@ -181,8 +181,9 @@ __global__ void __launch_bounds__(32) compose_fused_kernel(const __grid_constant
 // descriptor, so descriptors are loaded two groups ahead and first rows one
 // group ahead.  Measured per 78-layer step on one-token pages (1152 bytes):
 // 4.27 -> 4.055 ms against one page per ring slot at 24 CTAs per SM; the
-// kernel alone 0.85 -> 0.893 of the copy peak.  The grid runs 6 CTAs per SM,
-// so it launches plainly (early_launch_pays).
+// kernel alone 0.85 -> 0.893 of the copy peak.  The grid runs 6 CTAs per SM
+// and launches early whenever asked, unlike the one-page-per-slot ring at 24
+// CTAs per SM that early_launch_pays keeps plain: 4.05 -> 3.72 ms per step.
 template <int MAXB>
 __device__ __forceinline__ int32_t group_row0(const FusedParams<MAXB> &p, const int32_t *cur_page_start,
                                               const int64_t *token_start, int32_t o, int32_t s) {
@@ -355,7 +356,7 @@ extern "C" int cpkv_compose_fused(int B, int page_size, int cp_size, int64_t row
     FusedParams<MB> prm;                                                                            \
     CPKV_FILL_FUSED(prm)                                                                            \
     prm.units = gunits; prm.pieces = (int32_t)G; prm.piece_bytes = (int32_t)page_bytes;             \
-    return launch_fused(compose_fused_groups_kernel<MB>, grid, gsmem, early && early_launch_pays(grid), s, prm); \
+    return launch_fused(compose_fused_groups_kernel<MB>, grid, gsmem, early, s, prm); \
   }
     if (B <= 64) CPKV_FUSED_GROUPS(64)
     CPKV_FUSED_GROUPS(CPKV_MAX_BATCH)

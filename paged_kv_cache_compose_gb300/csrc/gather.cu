@@ -32,8 +32,9 @@
 // waits for the fill (store_gate) before its first staging load and before
 // its first store.  Measured per 78-layer step: traced 4.284 -> 4.200 ms;
 // fp8 unchanged (19.77 ms); index keys 4.143 -> 4.128 ms; one-token pages,
-// where the ring runs 24 small CTAs per SM, 5.195 -> 5.555 ms, so that grid
-// launches plainly.
+// where the per-page ring ran 24 small CTAs per SM, 5.195 -> 5.555 ms, so
+// such grids launch plainly.  The group gather of pages of at most 4 KB (6
+// CTAs per SM) launches early: 4.49 -> 4.41 ms per one-token step.
 // The gather itself releases its dependents at its start (the next layer's
 // fill, launched with CPKV_FLAG_EARLY_INPUTS, may start while it runs).
 #include <stdint.h>
@@ -279,7 +280,7 @@ extern "C" int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row
                                   : reinterpret_cast<const void *>(gather_groups_kernel<false>);
     if (ensure_dynamic_smem(gkernel, kGroupStages * kGroupBytes) != CPKV_OK) return CPKV_ERR_CUDA;
     const int ggrid = persistent_grid(gkernel, 32, gsmem, kMaxCtasPerSmGroups, prm.units);
-    const bool gdep = early && early_launch_pays(ggrid);
+    const bool gdep = early;  // 6 CTAs per SM of 8 KB groups: early pays (4.49 -> 4.41 ms per one-token step)
     if (consume) return launch_kernel(gather_groups_kernel<true>, dim3(ggrid), dim3(32), gsmem, gdep, s, prm);
     return launch_kernel(gather_groups_kernel<false>, dim3(ggrid), dim3(32), gsmem, gdep, s, prm);
   }

@@ -22,6 +22,11 @@
 
 namespace cpkv {
 
+// Ring shape, measured on one-token pages (78-layer traced lengths, ms per
+// step for the fill + gather with stagings kept / the fused compose): 4
+// stages, 2 loading, 6 CTAs per SM 4.50 / 4.03; 4 stages with 3 loading
+// 4.51 / 4.05; 3 stages with 2 or 1 loading and 8 CTAs per SM 4.77 / 4.21
+// and 5.07 / 4.04; 2 stages, 12 CTAs per SM 4.76 / 4.09.
 constexpr int kGroupStages = 4;
 constexpr int kGroupLoads = 2;         // stages with loads in flight per CTA
 constexpr int kGroupBytes = 8 * 1024;  // stage size
