@@ -279,7 +279,7 @@ class ComposeWorkload:
         # them): by default for row-major pages above 4 KB, where it measured
         # faster (traced -6%, fp8 -1%); the planar index-key pages measured
         # 1.5% slower, and one-token 1152-byte pages 5% (fill + group gather,
-        # 4.64 against 4.40 ms) and 16% (one launch, 5.05 against 4.35 ms)
+        # 4.64 against 4.40 ms) and 13% (one launch, 4.90 against 4.36 ms)
         if consume_staging is None:
             consume_staging = (variant in ("staging", "layer") and not b.planes
                                and b.page_size * b.row_bytes > 4096)
