@@ -134,9 +134,9 @@ struct LayerGroupRing {
     return !dead;
   }
 
-  // The oldest consumed group's read-back has landed: drop its staging lines
-  // (kConsume) and store it to the dense buffer (exactly one bulk group per
-  // group, in group order).
+  // The oldest consumed group's read-back has landed: store it to the dense
+  // buffer (exactly one bulk group per group, in group order), then drop its
+  // staging lines (kConsume).
   CPKV_DEV void finish_oldest() {
     const int64_t g = stored;
     const int s = (int)(g % S);
