@@ -149,6 +149,64 @@ def test_fuzz_early_launch_chains(seed):
             assert np.array_equal(bufs[l].cpu().numpy(), want), (k, l)
 
 
+def small_pages_large_batch(seed):
+    """B in [65, 300] (the 1024-request parameter block), pages of 1-3
+    tokens and at most 4 KB (the grouped kernels), random writers."""
+    rng = np.random.default_rng(20_000 + seed)
+    ps = int(rng.choice([1, 2, 3]))
+    cp = int(rng.integers(1, 9))
+    R = 16 * int(rng.integers(1, 4096 // (16 * ps) + 1))
+    B = int(rng.integers(65, 301))
+    pfx = rng.integers(0, 8, size=B) * ps
+    cur = rng.integers(0, 6 * ps + 1, size=B)
+    n_pfx = int((pfx // ps).sum())
+    C = int(((cur + ps - 1) // ps).sum())
+    P = n_pfx + C + 8
+    ids = rng.permutation(np.arange(1, P))
+    writer = rng.integers(0, cp, size=C).astype(np.int32)
+    return wl.make_compose_batch(f"big{seed}", seed, page_size=ps, cp_size=cp, num_pool_pages=P, row_bytes=R,
+                                 prefix_lens=pfx, cur_lens=cur, prefix_pages=ids[:n_pfx].copy(),
+                                 cur_pages=ids[n_pfx:n_pfx + C], writer=writer, row_kind="bytes")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_early_chains_small_pages_large_batch(seed):
+    """Three layers through each chain of early launches on pages of at most
+    4 KB with more than 64 requests: the row fill + group gather, the grouped
+    fused compose and the grouped one-launch compose (stagings consumed on
+    even seeds), every layer against the oracle."""
+    batch = small_pages_large_batch(seed)
+    ps, cp, R = batch.page_size, batch.cp_size, batch.row_bytes
+    assert ps * R <= 4096 and batch.B > 64
+    T, C, D = oracle.sizes(batch.prefix_lens, batch.cur_lens, ps)
+    cap = D + 3
+    plan = ComposePlan(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, batch.cur_pages, batch.writer,
+                       page_size=ps, cp_size=cp, num_pool_pages=batch.num_pool_pages, dense_cap_pages=cap).build()
+    layers = ComposeLayers(plan, R)
+    n_layers, consume = 3, seed % 2 == 0
+    host = [(wl.host_pool(batch, l), wl.host_current_rows(batch, l)) for l in range(n_layers)]
+    dev = [([torch.from_numpy(s).cuda() for s in slabs],
+            [torch.from_numpy(r).cuda() for r in wl.split_rows_by_writer(batch, rows)]) for slabs, rows in host]
+    out = {k: [torch.full((cap * ps, R), 0xCD, dtype=torch.uint8, device="cuda") for _ in range(n_layers)]
+           for k in ("staging", "fused", "layer")}
+    torch.cuda.synchronize()
+    for l in range(n_layers):
+        layers.fill(dev[l][1], early_inputs=True)
+        layers.gather(dev[l][0], out["staging"][l], consume_staging=consume, early_inputs=True)
+    for l in range(n_layers):
+        layers.compose_fused(dev[l][0], dev[l][1], out["fused"][l], early_inputs=True)
+    for l in range(n_layers):
+        layers.compose_one_launch(dev[l][0], dev[l][1], out["layer"][l], consume_staging=consume,
+                                  early_inputs=True)
+    torch.cuda.synchronize()
+    assert int(plan.d_status.item()) == 0
+    for l, (slabs, rows) in enumerate(host):
+        want = oracle.compose_dense(batch.prefix_lens, batch.cur_lens, batch.prefix_pages, slabs, rows,
+                                    page_size=ps, cp_size=cp, dense_cap=cap)
+        for k, bufs in out.items():
+            assert np.array_equal(bufs[l].cpu().numpy(), want), (k, l)
+
+
 @pytest.mark.parametrize("seed", range(30))
 def test_fuzz_ragged(seed):
     rng = np.random.default_rng(10_000 + seed)
