@@ -259,10 +259,12 @@ def test_gather_random_descriptors_and_sentinels():
     assert np.array_equal(dense.cpu().numpy(), want)
 
 
-@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (1, 16), (3, 48), (128, 1152), (64, 4096)])
+@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (1, 16), (3, 48), (128, 1152), (64, 4096),
+                                  (1, 1152), (2, 2048), (1, 4096), (5, 64)])
 def test_gather_page_geometries(ps, R):
     """Pages that split into one or several bulk-copy pieces, odd page sizes,
-    and the 656-byte fp8 row."""
+    and the 656-byte fp8 row; pages of at most 4 KB in groups (7 of 1152 B,
+    2 of 4096 B, 25 of 320 B, 32 of 16 B)."""
     rng = np.random.default_rng(ps * 1000 + R)
     cp = 2
     caps = [9, 7, 5, 6]
@@ -374,9 +376,11 @@ def test_fused_matches_oracle_edge_cases(batch, early):
     assert np.array_equal(dense, want)
 
 
-@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (3, 48), (128, 1152), (64, 4096), (7, 16)])
+@pytest.mark.parametrize("ps,R", [(64, 656), (16, 1152), (3, 48), (128, 1152), (64, 4096), (7, 16),
+                                  (1, 1152), (2, 2048), (1, 4096), (5, 64)])
 def test_fused_page_geometries(ps, R):
-    """Pieces that straddle the end of a partial page's rows, several pieces per page."""
+    """Pieces that straddle the end of a partial page's rows, several pieces
+    per page; pages of at most 4 KB in groups of consecutive dense pages."""
     rng = np.random.default_rng(ps * 7 + R)
     B = 6
     pfx = (rng.integers(0, 6 * ps, B) // ps) * ps
