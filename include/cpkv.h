@@ -395,7 +395,10 @@ int cpkv_compose_gather_kinds(int page_size, int cp_size, int64_t row_bytes,
  * and reads each staged piece back into the dense page once that store has
  * completed.  The stagings and the dense buffer end up byte-identical to the
  * two-call form; every staged row is written and read back (pad rows, zero
- * in both, are written to the dense page directly).
+ * in both, are written to the dense page directly).  Pages of at most 4 KB
+ * go in groups of consecutive dense pages: a group's current pages, pad
+ * rows included, are stored to their staging slots and read back whole
+ * before the group is stored to the dense buffer.
  *   h_cur_lens       host int32 [B]
  *   h_cur_rows       host array [cp] of device pointers, writer w's current
  *                    rows [h_cur_rows_cap[w]][R], 16-byte aligned
