@@ -47,6 +47,11 @@ namespace {
 //   4 KB groups, S 4, 8 CTAs per SM; 2 KB, 24                  6.90; 7.03 (kept)
 //   read-back by the lanes (coherent loads of their own stores, no fence),
 //   8 KB groups, S 4                                           8.20-8.52 / 8.89-9.35
+//   two warps per CTA, a producer (descriptors, zeros, loads) and a
+//   consumer (staging stores, read-backs, dense stores) handing stages over
+//   through mbarriers, launched early: 8 KB groups, S 3, 8 CTAs per SM
+//   4.71 / 6.76; S 4 with 8, 6 or 4 KB groups (6, 8, 12 CTAs per SM)
+//   4.60-4.64 (kept), against 4.36 / 4.91 for this one-warp form
 // against 4.49 / 4.74 ms for the row fill followed by the group gather
 // (4.40 / 4.64 launched early).  A
 // warp waits on its loads, its staging stores' fence and its read-backs in
