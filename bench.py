@@ -766,40 +766,56 @@ def _free(torch):
 def extra_configs(a, device, hbm_peak):
     """The scope table's other measured rows, in the same run as the headline:
     the fp8 NSA compose over 78 layers (the headline's variant, timed the same
-    way over fewer steps, with its kernels timed alone), the ragged index plan
-    of the ragged config (every CP rank) and the compose plan of the traced,
-    fp8 and one-token-page batches."""
+    way over fewer steps, with its kernels timed alone), the traced lengths on
+    one-token pages (the headline's variant and one launch per layer), the
+    ragged index plan of the ragged config (every CP rank) and the compose
+    plan of the traced, fp8 and one-token-page batches."""
     import torch
 
     out = {}
     steps = max(5, min(a.steps, 20))
-    t0 = time.perf_counter()
-    work = ComposeWorkload("fp8_nsa", device=device, variant=a.variant, fill_mode=a.fill_mode,
-                           early=a.launch == "early")
-    setup_s = time.perf_counter() - t0
-    warm_and_capture(work, 3)
-    st0 = work.status()
-    ms_total, step_ms = timed_steps(work, steps)
-    ms_step = ms_total / steps
-    kern = time_kernels(work, steps)
-    b = work.batch
-    out["fp8_nsa"] = {
-        "workload": "fp8 NSA compose, 78 layers: bs=32, 131072 current tokens (lognormal split), prefix U[0,64K] "
-                    "page-floored, page_size=64, cp=8, 656-byte rows, one 2^20-page pool shared by the layers",
-        "variant": work.variant, "consume_staging": work.consume_staging, "steps": steps,
-        "ms_per_78_layer_compose": round(ms_step * 78 / work.num_layers, 4),
-        "ms_per_step_stats": {"median": round(step_ms[len(step_ms) // 2], 4), "min": round(step_ms[0], 4),
-                              "max": round(step_ms[-1], 4)},
-        "value": round(work.layer_bytes * work.num_layers / (ms_step / 1e3) / 1e9, 2), "unit": "GB/s",
-        **step_fractions(work, ms_step, hbm_peak),
-        "bytes_per_layer": work.layer_bytes, "dram_bytes_per_layer": work.bytes["dram_min"],
-        "B": b.B, "T": b.T, "C": work.plan.C, "D": work.plan.D,
-        "kernels": kernel_rooflines(work, kern, hbm_peak),
-        "setup_s": round(setup_s, 1),
-        "status_word": work.status() | st0,
-    }
-    del work
-    _free(torch)
+
+    def measure(config, variant, workload):
+        t0 = time.perf_counter()
+        work = ComposeWorkload(config, device=device, variant=variant, fill_mode=a.fill_mode,
+                               early=a.launch == "early")
+        setup_s = time.perf_counter() - t0
+        warm_and_capture(work, 3)
+        st0 = work.status()
+        ms_total, step_ms = timed_steps(work, steps)
+        ms_step = ms_total / steps
+        kern = time_kernels(work, steps)
+        b = work.batch
+        res = {
+            "workload": workload,
+            "variant": work.variant, "consume_staging": work.consume_staging, "steps": steps,
+            "ms_per_78_layer_compose": round(ms_step * 78 / work.num_layers, 4),
+            "ms_per_step_stats": {"median": round(step_ms[len(step_ms) // 2], 4), "min": round(step_ms[0], 4),
+                                  "max": round(step_ms[-1], 4)},
+            "value": round(work.layer_bytes * work.num_layers / (ms_step / 1e3) / 1e9, 2), "unit": "GB/s",
+            **step_fractions(work, ms_step, hbm_peak),
+            "bytes_per_layer": work.layer_bytes, "dram_bytes_per_layer": work.bytes["dram_min"],
+            "B": b.B, "T": b.T, "C": work.plan.C, "D": work.plan.D,
+            "kernels": kernel_rooflines(work, kern, hbm_peak),
+            "setup_s": round(setup_s, 1),
+            "status_word": work.status() | st0,
+        }
+        del work
+        _free(torch)
+        return res
+
+    out["fp8_nsa"] = measure(
+        "fp8_nsa", a.variant,
+        "fp8 NSA compose, 78 layers: bs=32, 131072 current tokens (lognormal split), prefix U[0,64K] "
+        "page-floored, page_size=64, cp=8, 656-byte rows, one 2^20-page pool shared by the layers")
+    # the traced lengths on one-token pages, through the kernels that move
+    # groups of consecutive dense pages: the headline's variant and the
+    # one-launch form
+    ps1 = ("traced lengths on one-token pages, 78 layers: page_size=1, 88832 prefix + 44600 current pages "
+           "of 1152 bytes per layer, a 2^18-page pool slab per layer")
+    out["traced_78_ps1"] = measure("traced_78_ps1", a.variant, ps1)
+    if a.variant != "layer":
+        out["traced_78_ps1_layer"] = measure("traced_78_ps1", "layer", ps1)
     reps = max(20, a.steps)
     out["ragged_plan"] = ragged_plan_latency(reps, splits=("interleaved",))["interleaved"]
     out["compose_plan"] = compose_plan_latency(reps, ("traced", "fp8_nsa", "traced_78_ps1"))
@@ -825,8 +841,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra-configs", action="store_true",
-                    help="skip the fp8 NSA, ragged-plan and compose-plan measurements that the default "
-                         "(traced_78) run adds to its line")
+                    help="skip the fp8 NSA, one-token-page, ragged-plan and compose-plan measurements that the "
+                         "default (traced_78) run adds to its line")
     ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's bounded sample")
     ap.add_argument("--no-cpu-all-cores", action="store_true",
                     help="skip the all-cores variant of the CPU baseline (one oracle process per core)")
@@ -994,7 +1010,8 @@ def main(argv=None):
         del work
         _free(torch)
         extra = extra_configs(a, device, hbm_peak)
-        status |= extra["fp8_nsa"]["status_word"]
+        for k in ("fp8_nsa", "traced_78_ps1", "traced_78_ps1_layer"):
+            status |= extra.get(k, {}).get("status_word", 0)
 
     line = {
         "metric": METRIC,
