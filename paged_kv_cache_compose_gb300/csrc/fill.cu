@@ -288,9 +288,10 @@ __global__ void __launch_bounds__(kPageThreads, kPageBlocksPerSm) fill_pages_ker
   // its CTAs load pool pages beside this fill and wait for it to complete
   // before any staging load or store.  Releasing it here rather than as the
   // blocks finish measured faster with the page runs (traced 78-layer step
-  // 4.18 -> 4.09 ms, fp8 19.79 -> 19.82 ms; same box, two runs each); the
-  // row fill below keeps releasing at its end, where the start measured
-  // slower.
+  // 4.18 -> 4.09 ms, fp8 19.79 -> 19.82 ms; same box, two runs each).  The
+  // row fill below keeps releasing at its end: at its start the traced step
+  // with row fills went 4.19 -> 4.10 ms, but one-token pages, whose group
+  // gather runs 6 CTAs per SM beside it, 4.40 -> 4.98 ms.
   release_dependents();
   const uint64_t read_once = l2_policy_evict_first();
   const uint64_t keep = l2_policy_evict_last();
