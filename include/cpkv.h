@@ -360,9 +360,10 @@ int cpkv_compose_gather(int page_size, int cp_size, int64_t row_bytes,
  * kernel may write the stagings (the fill).  When its grid runs at most 4
  * CTAs per SM (pages of several pieces, index-key pages), and for pages of
  * at most 4 KB (moved in groups of consecutive dense pages), the gather is
- * then launched as a programmatic dependent of that kernel (the
- * fills release their dependents when they finish): its CTAs may start as
- * the fill's blocks retire and load descriptors and pool pages at once, and
+ * then launched as a programmatic dependent of that kernel (the page-run
+ * fills release it at their start, the row fills as their blocks finish):
+ * its CTAs may start beside or after the fill and load descriptors and pool
+ * pages at once, and
  * each waits for the previous kernel to complete (griddepcontrol.wait) before
  * its first staging load and before its first store.  Any other grid of
  * more CTAs per SM is launched plainly. */

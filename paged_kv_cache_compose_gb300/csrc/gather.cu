@@ -26,11 +26,11 @@
 //
 // With CPKV_GATHER_EARLY_INPUTS and a grid of at most 4 CTAs per SM
 // (early_launch_pays: pages of several pieces, index-key pages) the gather is
-// launched as a programmatic dependent of the previous kernel (its fill, which
-// releases its dependents as its blocks finish).  Its CTAs start as the
-// fill's blocks retire, load descriptors and pool pieces at once, and each
-// waits for the fill (store_gate) before its first staging load and before
-// its first store.  Measured per 78-layer step: traced 4.284 -> 4.200 ms;
+// launched as a programmatic dependent of the previous kernel (its fill: the
+// page-run fills release it at their start, the row fills as their blocks
+// finish).  Its CTAs start beside or after the fill, load descriptors and
+// pool pieces at once, and each waits for the fill (store_gate) before its
+// first staging load and before its first store.  Measured per 78-layer step: traced 4.284 -> 4.200 ms;
 // fp8 unchanged (19.77 ms); index keys 4.143 -> 4.128 ms; one-token pages,
 // where the per-page ring ran 24 small CTAs per SM, 5.195 -> 5.555 ms, so
 // such grids launch plainly.  The group gather of pages of at most 4 KB (6
