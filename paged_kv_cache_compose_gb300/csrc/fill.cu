@@ -21,9 +21,9 @@
 // waits for the gather (store_gate) before its first store: the staging the
 // fill overwrites is what that gather reads.  Measured per 78-layer traced
 // step: 4.451 -> 4.290 ms; one-token pages 5.457 -> 5.192 ms; fp8 unchanged
-// (19.99 ms).  In a plain launch the gate returns at once.  The fill itself
-// releases its dependents as each block finishes, for a gather launched with
-// CPKV_GATHER_EARLY_INPUTS.
+// (19.99 ms).  In a plain launch the gate returns at once.  The row fill
+// releases its dependents as each block finishes, the page-run fill below at
+// its start, for a gather launched with CPKV_GATHER_EARLY_INPUTS.
 //
 // (A variant that moves whole pages with bulk copies when a page's indices
 // form a run was slower here: each page first needs a round trip of index
