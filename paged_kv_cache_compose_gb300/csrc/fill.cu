@@ -223,8 +223,9 @@ constexpr int kPageBlocksPerSm = 4;  // one resident wave
 // runs.  Measured per 78-layer step (same box, two runs each): traced (12 654
 // chunks, 3.5 per warp at 3 per SM) 4.10 -> 3.99-4.00 ms; fp8 (22 715
 // chunks) unchanged at 19.86 ms with 4 per SM, where 3 per SM measured 20.96-
-// 23.04 ms and 2 per SM 19.63 ms (one run); the traced step at 2 per SM
-// 4.14 ms.
+// 23.04 ms and 2 per SM 19.63 ms (three runs, against 19.70-19.71 at 4 per
+// SM: too small a gain to extend the rule from two workloads); the traced
+// step at 2 per SM 4.14 ms.
 constexpr int64_t kPageUnitsPerWarp3 = 4;
 
 struct PageUnit {
